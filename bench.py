@@ -1,0 +1,409 @@
+"""Benchmark of the DCNv2 forward on one GB300 (or N independent replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+One step = the whole forward through the C ABI: x -> channels-last,
+weight repack, fused kernel (three of the library's kernels). Inputs are
+resident in device memory; L2 is flushed (a 256 MiB write, outside the
+timing events) before every timed step. Step time and the fused kernel's
+time are taken with CUDA events on the launching stream; the JSON line
+reports TFLOP/s of the contraction (2*N*Cout*Ho*Wo*Cin/group*kh*kw flops),
+microseconds per call, the fused kernel's roofline fraction, an end-to-end
+number through host buffers, and the CPU oracle timed on the host cores.
+
+--impl reference times the CPU oracle (the only other implementation of
+this operator available here) on the same workload; see the oracle package.
+Under torchrun (N > 1) every rank runs its own full replica of the workload
+(weak scaling, no collective on the data path); rank 0 prints the line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from modulated_deformable_convolution_gb300.workloads import CONFIGS, make_inputs  # noqa: E402
+
+METRIC = "modulated deform-conv fwd TFLOP/s & µs/call at 1 GB300; % of roofline"
+UNIT = "TFLOP/s"
+FLUSH_BYTES = 256 << 20
+FUSED_SOURCES = ["mdcn_fused.cu", "mdcn_ptx.cuh", "mdcn_layout.cuh", "mdcn_plan.h"]
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def describe(case) -> str:
+    Ho, Wo = case.out_hw
+    return (f"{case.name}: N={case.N} Cin={case.Cin} Cout={case.Cout} H={case.H} W={case.W} -> Ho={Ho} Wo={Wo} "
+            f"{case.kh}x{case.kw} stride={case.stride[0]} pad={case.padding[0]} dil={case.dilation[0]} "
+            f"group={case.group} dg={case.deformable_group} bias={'yes' if case.bias else 'no'} dtype={case.dtype}")
+
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, local):
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+        return dist
+    return None
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, v: float) -> float:
+    if dist is None:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            return json.load(open(p)), "measured"
+        except Exception:
+            pass
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [s.strip() for s in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), reasons=parts[4:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["active_mask", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for name, val in zip(names[1:], r["reasons"][1:]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows), "sm_max_mhz": max(r["smax"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def fused_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in FUSED_SOURCES:
+        h.update(open(os.path.join(ROOT, "modulated_deformable_convolution_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch of the fused kernel from a committed ncu summary,
+    or None when there is none or the kernel changed since it was taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        t = json.load(open(p))
+        e = t.get(workload)
+        if e and e.get("fused_source_hash") == fused_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+def cpu_oracle_time(case, inp, budget_s: float = 20.0):
+    """Times the oracle as it stands on a bounded slice (whole output rows of
+    every image and channel). Returns (flops of the slice, seconds, rows, threads)."""
+    import oracle
+
+    oracle.build()
+    import numpy as np
+
+    np64 = lambda t: None if t is None else t.detach().to("cpu", torch.float64).numpy()
+    args = [np64(inp[k]) for k in ("x", "offset", "mask", "weight", "bias")]
+    Ho, _ = case.out_hw
+    flops_row = case.flops / Ho
+    # one probe row to size the slice
+    t0 = time.perf_counter()
+    oracle.forward(*args, ho_range=(0, 1), **case.attrs())
+    per_row = max(time.perf_counter() - t0, 1e-6)
+    rows = int(max(1, min(Ho, budget_s / per_row)))
+    t0 = time.perf_counter()
+    oracle.forward(*args, ho_range=(0, rows), **case.attrs())
+    dt = time.perf_counter() - t0
+    return flops_row * rows, dt, rows, oracle.num_threads()
+
+
+def run_reference(args, case, world, rank, dist):
+    """The CPU oracle arm: K timed steps of a bounded slice of the workload."""
+    barrier(dist)
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.build()
+    inp = make_inputs(case)
+    np64 = lambda t: None if t is None else t.detach().to("cpu", torch.float64).numpy()
+    a = [np64(inp[k]) for k in ("x", "offset", "mask", "weight", "bias")]
+    Ho, _ = case.out_hw
+    t0 = time.perf_counter()
+    oracle.forward(*a, ho_range=(0, 1), **case.attrs())
+    per_row = max(time.perf_counter() - t0, 1e-6)
+    budget = 150.0 / max(1, args.steps + args.warmup)  # whole run within a few minutes
+    rows = int(max(1, min(Ho, budget / per_row)))
+    flops = case.flops / Ho * rows
+    for _ in range(args.warmup):
+        oracle.forward(*a, ho_range=(0, rows), **case.attrs())
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.forward(*a, ho_range=(0, rows), **case.attrs())
+        times.append(time.perf_counter() - t0)
+    sec = statistics.mean(times)
+    value = flops / sec / 1e12
+    sample = f"output rows 0..{rows - 1} of {Ho} (all images, all channels) of {case.name}"
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": describe(case)},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, case, world, rank, local, dist):
+    import modulated_deformable_convolution_gb300 as mdcn
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    inp_cpu = make_inputs(case)
+    d = {k: (None if v is None else v.to(dev)) for k, v in inp_cpu.items()}
+    h = mdcn.Handle(**case.attrs())
+    x, off, m, w, b = d["x"], d["offset"], d["mask"], d["weight"], d["bias"]
+    ws = torch.empty(mdcn.mdcn_workspace_size(h, x, off, m, w, b), dtype=torch.uint8, device=dev)
+    out = torch.empty(mdcn.mdcn_output_dims(h, x, off, m, w, b), dtype=x.dtype, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        mdcn.mdcn_prepare_input(h, x, off, m, w, b, ws, stream)
+        mdcn.mdcn_pack_weight(h, x, off, m, w, b, ws, stream)
+        if ev is not None:
+            ev[0].record(stream)
+        mdcn.mdcn_forward_prepared(h, x, off, m, w, b, out, ws, stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    s, bits = mdcn.mdcn_query_status(ws)
+    if s != mdcn.MDCN_OK:
+        raise RuntimeError(f"device status after warm-up: {bits:#x}")
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    fev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    barrier(dist)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    for i in range(args.steps):
+        flush.zero_()
+        evs[i][0].record(stream)
+        step(fev[i])
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(c) for a, c in evs]
+    fused_ms = [a.elapsed_time(c) for a, c in fev]
+    ms = statistics.mean(step_ms)
+    ms_max = max_over_ranks(dist, ms)
+    s, bits = mdcn.mdcn_query_status(ws)
+    if s != mdcn.MDCN_OK:
+        raise RuntimeError(f"device status after the timed steps: {bits:#x}")
+
+    # end to end through the public API with host buffers: H2D of the step's
+    # inputs from pinned memory, the forward, D2H of the output
+    pinned = {k: (None if v is None else v.pin_memory()) for k, v in inp_cpu.items()}
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in pinned.values() if v is not None)
+    d2h = out_host.numel() * out_host.element_size()
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        dd = {k: (None if v is None else v.to(dev, non_blocking=True)) for k, v in pinned.items()}
+        mdcn.mdcn_forward(h, dd["x"], dd["offset"], dd["mask"], dd["weight"], dd["bias"], out, ws, stream)
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1) / e2e_steps)
+
+    # ablation (two-stage im2col + cuBLAS design) for context, same flush rule
+    abl_ms = None
+    try:
+        aws = torch.empty(mdcn.mdcn_im2col_gemm_workspace_size(h, x, off, m, w, b), dtype=torch.uint8, device=dev)
+        a_out = torch.empty_like(out)
+        for _ in range(2):
+            mdcn.mdcn_forward_im2col_gemm(h, x, off, m, w, b, a_out, aws, stream)
+        at = []
+        for _ in range(min(args.steps, 10)):
+            flush.zero_()
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            mdcn.mdcn_forward_im2col_gemm(h, x, off, m, w, b, a_out, aws, stream)
+            a1.record(stream)
+            at.append((a0, a1))
+        torch.cuda.synchronize()
+        abl_ms = statistics.mean(a.elapsed_time(c) for a, c in at)
+        del aws, a_out
+    except Exception as e:  # the ablation is context only
+        log("ablation skipped:", e)
+
+    if rank != 0:
+        return
+    flops = case.flops
+    value = world * flops / (ms_max * 1e-3) / 1e12
+    peaks, peak_src = measured_peaks()
+    fused_mean_s = statistics.mean(fused_ms) * 1e-3
+    achieved = flops / fused_mean_s / 1e12
+    if case.dtype == "f32":
+        # split-TF32: 3 tf32 passes; tf32 dense rate = bf16 rate x (1.1 / 2.25) nominal
+        peak = peaks["bf16_tflops"] * (1.1 / 2.25) / 3.0
+        peak_note = f"{peak_src} bf16 burst x tf32/bf16 nominal ratio / 3 passes"
+    else:
+        peak = peaks["bf16_tflops"]
+        peak_note = f"{peak_src} bf16 burst (fp16 has the same dense rate)"
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "traffic": profiled_traffic(case.name), "kernel": "fused_kernel", "peak_source": peak_note,
+            "kernel_us": fused_mean_s * 1e6}
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        f, sec, rows, thr = cpu_oracle_time(case, inp_cpu)
+        Ho, _ = case.out_hw
+        cpu = {"value": f / sec / 1e12, "unit": UNIT, "cores": thr, "kind": "oracle",
+               "sample": f"output rows 0..{rows - 1} of {Ho} (all images, all channels), {sec:.1f} s"}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "us_per_call": ms_max * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": case.dtype,
+        "data": "synthetic",
+        "config": {"workload": describe(case), "global_batch": case.N * world,
+                   "l2": "flushed before every timed step (256 MiB write outside the events)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "step": "prepare_input + pack_weight + fused kernel"},
+        "step_ms": {"mean": ms, "p10": sorted(step_ms)[len(step_ms) // 10],
+                    "p90": sorted(step_ms)[(len(step_ms) * 9) // 10]},
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "ablation_im2col_gemm": None if abl_ms is None else {"ms_per_call": abl_ms,
+                                                             "tflops": flops / (abl_ms * 1e-3) / 1e12},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="neck_f16", choices=sorted(CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_info()
+    dist = init_dist(world, local)
+    case = CONFIGS[args.config]
+    try:
+        if args.impl == "reference":
+            run_reference(args, case, world, rank, dist)
+        else:
+            from modulated_deformable_convolution_gb300 import build
+
+            if not os.path.exists(os.path.join(ROOT, "modulated_deformable_convolution_gb300", "libmdcn.so")):
+                build.build()
+            run_ours(args, case, world, rank, local, dist)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,189 @@
+/*
+ * mdcn.h — C ABI of the GB300 (sm_103a) modulated deformable convolution
+ * (DCNv2) forward library, libmdcn.so.
+ *
+ * The operation is the one described in "TensorRT plugin walkthrough:
+ * modulatedDeformConvPlugin" (trdm.cn):
+ *   section 2  inputs x, offset, mask, weight, optional bias; one output;
+ *              NCHW; output dims (x.d0, weight.d0, offset.d2, offset.d3);
+ *   section 3  attributes stride, padding, dilation (int[2] each), group,
+ *              deformable_group; stride, dilation >= 1, padding >= 0,
+ *              group, deformable_group >= 1; all five required;
+ *   section 4  every tensor has the type of x; float32 or float16 (this
+ *              library adds bfloat16 with the same semantics); linear NCHW;
+ *              offset/mask batch = x batch, mask spatial = offset spatial,
+ *              bias length = weight.d0;
+ *   section 5  y[n,o,ho,wo] = bias[o] + sum over input channels c of the
+ *              group of o and taps (i,j) of
+ *                weight[o, c_l, i, j] * mask[n, gd*K + k, ho, wo]
+ *                  * bilinear(x[n, c], ho*sh - ph + i*dh + offset[n, gd*2K + 2k, ho, wo],
+ *                                      wo*sw - pw + j*dw + offset[n, gd*2K + 2k + 1, ho, wo])
+ *              with K = kh*kw, k = i*kw + j, gd = c / (Cin/deformable_group),
+ *              c_l = c - group_of(o)*(Cin/group); bilinear() is 0 outside the
+ *              open range (-1, H) x (-1, W) and reads 0 for corners outside
+ *              the image.
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers named x, offset, mask, weight, bias, out and workspace are
+ *     DEVICE pointers, owned and allocated by the caller; the library never
+ *     allocates, frees or keeps them. They must be 16-byte aligned
+ *     (MDCN_ERR_ALIGN otherwise). Tensors are dense (contiguous) NCHW.
+ *   - A call that fails validation launches nothing and writes nothing.
+ *   - Forward calls are asynchronous on the given stream (a cudaStream_t
+ *     passed as void*; NULL is the legacy default stream). No host
+ *     synchronisation happens inside them. A CUDA launch error is reported
+ *     as MDCN_ERR_CUDA (see mdcn_last_cuda_error).
+ *   - No C++ exception crosses this interface; every call returns a status.
+ *   - A handle is immutable after mdcn_create and may be used from several
+ *     threads at once; concurrent forwards must use distinct workspaces.
+ */
+#ifndef MDCN_H
+#define MDCN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum mdcn_status {
+    MDCN_OK = 0,
+    MDCN_ERR_NULL = 1,        /* a required pointer argument is NULL */
+    MDCN_ERR_ATTR = 2,        /* an attribute is out of its section-3 range */
+    MDCN_ERR_SHAPE = 3,       /* tensor dims break a section-2/4 binding */
+    MDCN_ERR_DTYPE = 4,       /* unknown mdcn_dtype value */
+    MDCN_ERR_ALIGN = 5,       /* a device pointer is not 16-byte aligned */
+    MDCN_ERR_WORKSPACE = 6,   /* workspace_bytes below mdcn_workspace_size() */
+    MDCN_ERR_ARCH = 7,        /* the current device is not compute capability 10.3 */
+    MDCN_ERR_CUDA = 8,        /* a CUDA runtime call or launch failed */
+    MDCN_ERR_TIMEOUT = 9,     /* a device-side pipeline wait gave up (mdcn_query_status) */
+    MDCN_ERR_UNSUPPORTED = 10 /* valid input beyond this library's limits (e.g. a dim >= 2^31) */
+} mdcn_status;
+
+/* Element type shared by x, offset, mask, weight, bias and out (section 4). */
+typedef enum mdcn_dtype {
+    MDCN_F32 = 0,  /* float32; contraction as split-TF32 (3 tensor-core passes), fp32 accumulate */
+    MDCN_F16 = 1,  /* float16; fp16 columns, fp32 accumulate */
+    MDCN_BF16 = 2  /* bfloat16; bf16 columns, fp32 accumulate (not on the page: an extension) */
+} mdcn_dtype;
+
+/* The five required attributes of section 3, index 0 = height, 1 = width. */
+typedef struct mdcn_attrs {
+    int64_t stride[2];
+    int64_t padding[2];
+    int64_t dilation[2];
+    int64_t group;
+    int64_t deformable_group;
+} mdcn_attrs;
+
+/* Dims of the inputs exactly as the tensors have them (section 2). */
+typedef struct mdcn_dims {
+    int64_t x[4];      /* N, Cin, H, W */
+    int64_t offset[4]; /* N, 2*deformable_group*kh*kw, Ho, Wo */
+    int64_t mask[4];   /* N, deformable_group*kh*kw, Ho, Wo */
+    int64_t weight[4]; /* Cout, Cin/group, kh, kw */
+    int64_t bias;      /* Cout when a bias is given, 0 when there is none */
+} mdcn_dims;
+
+typedef struct mdcn_handle_* mdcn_handle;
+
+/* Validates attrs (section 3 ranges) and returns a handle holding a copy of
+ * them in *out. Errors: MDCN_ERR_NULL (attrs or out NULL), MDCN_ERR_ATTR.
+ * On error *out is left unchanged. Host only; touches no GPU. */
+mdcn_status mdcn_create(const mdcn_attrs* attrs, mdcn_handle* out);
+
+/* Frees the handle (NULL is accepted). Nothing else is freed. */
+mdcn_status mdcn_destroy(mdcn_handle handle);
+
+/* Output dims by the section-2 rule: out_dims = {x[0], weight[0], offset[2],
+ * offset[3]}, after checking every section-2/4 binding: offset and mask batch
+ * = x batch; mask spatial = offset spatial; offset channels =
+ * 2*dg*kh*kw; mask channels = dg*kh*kw; weight.d1 = Cin/group with group
+ * dividing Cin and Cout; dg dividing Cin; bias = Cout or 0; every dim >= 1.
+ * Ho and Wo are NOT recomputed from the convolution formula. Host only.
+ * Errors: MDCN_ERR_NULL, MDCN_ERR_SHAPE, MDCN_ERR_UNSUPPORTED (a dim or an
+ * element count beyond 2^31-1 / 2^62). */
+mdcn_status mdcn_output_dims(mdcn_handle handle, const mdcn_dims* dims, int64_t out_dims[4]);
+
+/* Bytes of device workspace mdcn_forward needs for these dims and dtype
+ * (channels-last copy of x, the repacked weight and a status word). Host only. */
+mdcn_status mdcn_workspace_size(mdcn_handle handle, const mdcn_dims* dims, mdcn_dtype dtype,
+                                size_t* bytes);
+
+/* The forward pass (section 5, steps 1-3) as one fused implicit-GEMM kernel:
+ * producer warps sample and modulate the columns straight into shared
+ * memory, tcgen05 tensor-core MMAs accumulate in tensor memory, the epilogue
+ * adds the bias and writes NCHW. The im2col column matrix never reaches
+ * device memory. Two small layout kernels run first (x to channels-last,
+ * weight repack), into workspace.
+ *   x [N,Cin,H,W], offset [N,2*dg*kh*kw,Ho,Wo], mask [N,dg*kh*kw,Ho,Wo],
+ *   weight [Cout,Cin/group,kh,kw], bias_or_null [Cout] or NULL,
+ *   out [N,Cout,Ho,Wo] (written), workspace of workspace_bytes (scratch,
+ *   contents undefined afterwards except the status word).
+ * dims->bias must be 0 exactly when bias_or_null is NULL.
+ * stream: cudaStream_t as void*. Requires a compute capability 10.3 device
+ * current on the calling thread. */
+mdcn_status mdcn_forward(mdcn_handle handle, const void* x, const void* offset, const void* mask,
+                         const void* weight, const void* bias_or_null, void* out,
+                         void* workspace, size_t workspace_bytes,
+                         const mdcn_dims* dims, mdcn_dtype dtype, void* stream);
+
+/* The three steps of mdcn_forward as separate calls, for callers that
+ * pack a constant weight once or time the steps on their own. Same
+ * arguments, rules and workspace as mdcn_forward; run on one stream in this
+ * order with one workspace:
+ *   mdcn_prepare_input:   x -> channels-last copy in workspace; clears the
+ *                         workspace status word;
+ *   mdcn_pack_weight:     weight -> packed K-major copy in workspace;
+ *   mdcn_forward_prepared: the fused kernel, reading both copies. */
+mdcn_status mdcn_prepare_input(mdcn_handle handle, const void* x, void* workspace, size_t workspace_bytes,
+                               const mdcn_dims* dims, mdcn_dtype dtype, void* stream);
+mdcn_status mdcn_pack_weight(mdcn_handle handle, const void* weight, void* workspace, size_t workspace_bytes,
+                             const mdcn_dims* dims, mdcn_dtype dtype, void* stream);
+mdcn_status mdcn_forward_prepared(mdcn_handle handle, const void* offset, const void* mask,
+                                  const void* bias_or_null, void* out, void* workspace, size_t workspace_bytes,
+                                  const mdcn_dims* dims, mdcn_dtype dtype, void* stream);
+
+/* Workspace bytes for mdcn_forward_im2col_gemm (the column matrix of the
+ * whole batch plus a float32 GEMM output). Host only. */
+mdcn_status mdcn_im2col_gemm_workspace_size(mdcn_handle handle, const mdcn_dims* dims,
+                                            mdcn_dtype dtype, size_t* bytes);
+
+/* Ablation: the same forward as the page's own two-stage design, kept for
+ * comparison only — a deformable im2col kernel writes the column matrix
+ * [N][Cin*kh*kw][Ho*Wo] into workspace (in the I/O dtype), one strided-
+ * batched cuBLAS GEMM per group contracts it with the weight (fp32
+ * accumulate, no TF32) into a float32 buffer, and a third kernel adds the
+ * bias and writes the output. Same arguments and rules as mdcn_forward. */
+mdcn_status mdcn_forward_im2col_gemm(mdcn_handle handle, const void* x, const void* offset,
+                                     const void* mask, const void* weight, const void* bias_or_null,
+                                     void* out, void* workspace, size_t workspace_bytes,
+                                     const mdcn_dims* dims, mdcn_dtype dtype, void* stream);
+
+/* Reads the device status word that the last mdcn_forward on this workspace
+ * left (synchronising the stream), stores its raw bits in *device_bits (may
+ * be NULL) and clears it. Returns MDCN_ERR_TIMEOUT when a pipeline wait in
+ * the fused kernel gave up (its output is then unspecified), MDCN_OK when
+ * the word is clear, MDCN_ERR_CUDA when the copy fails. */
+mdcn_status mdcn_query_status(const void* workspace, void* stream, uint32_t* device_bits);
+
+/* Self-test of the bounded wait used by every pipeline wait of the fused
+ * kernel: launches one block that waits on a shared-memory barrier that
+ * nothing ever signals, with the given limit in microseconds (1..10^7),
+ * then synchronises the stream. Returns MDCN_ERR_TIMEOUT when the wait gave
+ * up as designed, MDCN_OK if it (wrongly) completed. The GPU stays usable.
+ * status_word: a caller-owned device buffer of at least 16 bytes. */
+mdcn_status mdcn_selftest_wait_timeout(void* status_word, uint32_t limit_us, void* stream);
+
+/* cudaError_t value behind the last MDCN_ERR_CUDA returned on this thread. */
+int mdcn_last_cuda_error(void);
+
+/* Static description of a status code. Never NULL. */
+const char* mdcn_status_string(mdcn_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MDCN_H */

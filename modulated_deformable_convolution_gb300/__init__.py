@@ -1,0 +1,263 @@
+"""GB300 (sm_103a) modulated deformable convolution (DCNv2) forward.
+
+Thin Python binding of libmdcn.so (C ABI in include/mdcn.h): the functions
+named ``mdcn_*`` here mirror the C entry points one to one and only marshal
+arguments (torch tensors -> device pointers, dims, dtype, the current CUDA
+stream). Every step of the computation runs in the library's CUDA kernels;
+there is no CPU or PyTorch fallback, and a missing library raises.
+
+The operator follows "TensorRT plugin walkthrough: modulatedDeformConvPlugin"
+(section 2 inputs/outputs, section 3 attributes, section 5 algorithm).
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _abi
+from ._abi import (MDCN_BF16, MDCN_ERR_ALIGN, MDCN_ERR_ARCH, MDCN_ERR_ATTR, MDCN_ERR_CUDA, MDCN_ERR_DTYPE,  # noqa: F401
+                   MDCN_ERR_NULL, MDCN_ERR_SHAPE, MDCN_ERR_TIMEOUT, MDCN_ERR_UNSUPPORTED, MDCN_ERR_WORKSPACE,
+                   MDCN_F16, MDCN_F32, MDCN_OK)
+
+__all__ = ["Handle", "MdcnError", "forward", "mdcn_create", "mdcn_destroy", "mdcn_output_dims",
+           "mdcn_workspace_size", "mdcn_forward", "mdcn_prepare_input", "mdcn_pack_weight",
+           "mdcn_forward_prepared", "mdcn_im2col_gemm_workspace_size", "mdcn_forward_im2col_gemm",
+           "mdcn_query_status", "mdcn_selftest_wait_timeout", "mdcn_status_string", "library_path"]
+
+_DTYPES = {torch.float32: MDCN_F32, torch.float16: MDCN_F16, torch.bfloat16: MDCN_BF16}
+
+
+def library_path() -> str:
+    return _abi.LIB_PATH
+
+
+def _lib():
+    return _abi.load()
+
+
+class MdcnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = int(status)
+        msg = _lib().mdcn_status_string(self.status).decode()
+        extra = ""
+        if self.status == MDCN_ERR_CUDA:
+            extra = f" (cudaError {_lib().mdcn_last_cuda_error()})"
+        super().__init__(f"{what}: status {self.status}: {msg}{extra}")
+
+
+def _check(status: int, what: str):
+    if status != MDCN_OK:
+        raise MdcnError(status, what)
+
+
+def mdcn_status_string(status: int) -> str:
+    return _lib().mdcn_status_string(int(status)).decode()
+
+
+def _pair(v):
+    if isinstance(v, int):
+        return (v, v)
+    v = tuple(int(t) for t in v)
+    assert len(v) == 2
+    return v
+
+
+def mdcn_create(stride=1, padding=0, dilation=1, group=1, deformable_group=1):
+    """mdcn_create: returns the opaque handle (an int) or raises MdcnError."""
+    a = _abi.mdcn_attrs()
+    a.stride[:] = _pair(stride)
+    a.padding[:] = _pair(padding)
+    a.dilation[:] = _pair(dilation)
+    a.group = int(group)
+    a.deformable_group = int(deformable_group)
+    h = ctypes.c_void_p()
+    _check(_lib().mdcn_create(ctypes.byref(a), ctypes.byref(h)), "mdcn_create")
+    return h.value
+
+
+def mdcn_destroy(handle) -> None:
+    _check(_lib().mdcn_destroy(handle), "mdcn_destroy")
+
+
+class Handle:
+    """Owns one library handle (the five section-3 attributes)."""
+
+    def __init__(self, stride=1, padding=0, dilation=1, group=1, deformable_group=1):
+        self.attrs = dict(stride=_pair(stride), padding=_pair(padding), dilation=_pair(dilation), group=int(group),
+                          deformable_group=int(deformable_group))
+        self.value = mdcn_create(**self.attrs)
+
+    def close(self):
+        if getattr(self, "value", None):
+            mdcn_destroy(self.value)
+            self.value = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def _hval(handle):
+    return handle.value if isinstance(handle, Handle) else handle
+
+
+def make_dims(x_shape, offset_shape, mask_shape, weight_shape, bias_len: int = 0):
+    d = _abi.mdcn_dims()
+    d.x[:] = tuple(int(t) for t in x_shape)
+    d.offset[:] = tuple(int(t) for t in offset_shape)
+    d.mask[:] = tuple(int(t) for t in mask_shape)
+    d.weight[:] = tuple(int(t) for t in weight_shape)
+    d.bias = int(bias_len)
+    return d
+
+
+def _dims(x, offset, mask, weight, bias):
+    for name, t in (("x", x), ("offset", offset), ("mask", mask), ("weight", weight)):
+        if t.dim() != 4:
+            raise ValueError(f"{name} must be 4-D")
+    if bias is not None and bias.dim() != 1:
+        raise ValueError("bias must be 1-D")
+    return make_dims(x.shape, offset.shape, mask.shape, weight.shape, 0 if bias is None else bias.shape[0])
+
+
+def _dtype(t: torch.Tensor) -> int:
+    if t.dtype not in _DTYPES:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    return _DTYPES[t.dtype]
+
+
+def mdcn_output_dims(handle, x, offset, mask, weight, bias=None):
+    out = (ctypes.c_int64 * 4)()
+    _check(_lib().mdcn_output_dims(_hval(handle), ctypes.byref(_dims(x, offset, mask, weight, bias)), out),
+           "mdcn_output_dims")
+    return tuple(int(v) for v in out)
+
+
+def mdcn_workspace_size(handle, x, offset, mask, weight, bias=None, dtype=None) -> int:
+    n = ctypes.c_size_t()
+    dt = _dtype(x) if dtype is None else dtype
+    _check(_lib().mdcn_workspace_size(_hval(handle), ctypes.byref(_dims(x, offset, mask, weight, bias)), dt,
+                                      ctypes.byref(n)), "mdcn_workspace_size")
+    return int(n.value)
+
+
+def mdcn_im2col_gemm_workspace_size(handle, x, offset, mask, weight, bias=None, dtype=None) -> int:
+    n = ctypes.c_size_t()
+    dt = _dtype(x) if dtype is None else dtype
+    _check(_lib().mdcn_im2col_gemm_workspace_size(_hval(handle), ctypes.byref(_dims(x, offset, mask, weight, bias)),
+                                                  dt, ctypes.byref(n)), "mdcn_im2col_gemm_workspace_size")
+    return int(n.value)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check_tensors(x, offset, mask, weight, bias, out):
+    ts = [x, offset, mask, weight, out] + ([bias] if bias is not None else [])
+    for t in ts:
+        if not t.is_cuda:
+            raise ValueError("every tensor must be on a CUDA device")
+        if not t.is_contiguous():
+            raise ValueError("every tensor must be contiguous (NCHW)")
+        if t.dtype != x.dtype:
+            raise TypeError("every tensor must have the dtype of x")
+
+
+def _stream(dev, stream):
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def mdcn_forward(handle, x, offset, mask, weight, bias, out, workspace, stream=None) -> None:
+    """mdcn_forward on torch tensors (device memory) and the current stream."""
+    _check_tensors(x, offset, mask, weight, bias, out)
+    d = _dims(x, offset, mask, weight, bias)
+    with torch.cuda.device(x.device):
+        st = _stream(x.device, stream)
+        _check(_lib().mdcn_forward(_hval(handle), _ptr(x), _ptr(offset), _ptr(mask), _ptr(weight), _ptr(bias),
+                                   _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                   ctypes.byref(d), _dtype(x), st), "mdcn_forward")
+
+
+def mdcn_prepare_input(handle, x, offset, mask, weight, bias, workspace, stream=None) -> None:
+    """Step 1 of mdcn_forward: x -> channels-last copy in workspace."""
+    d = _dims(x, offset, mask, weight, bias)
+    with torch.cuda.device(x.device):
+        _check(_lib().mdcn_prepare_input(_hval(handle), _ptr(x), _ptr(workspace),
+                                         workspace.numel() * workspace.element_size(), ctypes.byref(d), _dtype(x),
+                                         _stream(x.device, stream)), "mdcn_prepare_input")
+
+
+def mdcn_pack_weight(handle, x, offset, mask, weight, bias, workspace, stream=None) -> None:
+    """Step 2 of mdcn_forward: weight -> packed copy in workspace."""
+    d = _dims(x, offset, mask, weight, bias)
+    with torch.cuda.device(x.device):
+        _check(_lib().mdcn_pack_weight(_hval(handle), _ptr(weight), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), ctypes.byref(d), _dtype(x),
+                                       _stream(x.device, stream)), "mdcn_pack_weight")
+
+
+def mdcn_forward_prepared(handle, x, offset, mask, weight, bias, out, workspace, stream=None) -> None:
+    """Step 3 of mdcn_forward: the fused kernel on the prepared workspace
+    (x and weight only supply dims and dtype here)."""
+    _check_tensors(x, offset, mask, weight, bias, out)
+    d = _dims(x, offset, mask, weight, bias)
+    with torch.cuda.device(x.device):
+        _check(_lib().mdcn_forward_prepared(_hval(handle), _ptr(offset), _ptr(mask), _ptr(bias), _ptr(out),
+                                            _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                            ctypes.byref(d), _dtype(x), _stream(x.device, stream)),
+               "mdcn_forward_prepared")
+
+
+def mdcn_forward_im2col_gemm(handle, x, offset, mask, weight, bias, out, workspace, stream=None) -> None:
+    _check_tensors(x, offset, mask, weight, bias, out)
+    d = _dims(x, offset, mask, weight, bias)
+    with torch.cuda.device(x.device):
+        st = _stream(x.device, stream)
+        _check(_lib().mdcn_forward_im2col_gemm(_hval(handle), _ptr(x), _ptr(offset), _ptr(mask), _ptr(weight),
+                                               _ptr(bias), _ptr(out), _ptr(workspace),
+                                               workspace.numel() * workspace.element_size(), ctypes.byref(d),
+                                               _dtype(x), st), "mdcn_forward_im2col_gemm")
+
+
+def mdcn_query_status(workspace, stream=None):
+    """Returns (status, raw device bits) and clears the word."""
+    bits = ctypes.c_uint32()
+    with torch.cuda.device(workspace.device):
+        s = _lib().mdcn_query_status(_ptr(workspace), _stream(workspace.device, stream), ctypes.byref(bits))
+    return int(s), int(bits.value)
+
+
+def mdcn_selftest_wait_timeout(status_buf, limit_us: int, stream=None) -> int:
+    with torch.cuda.device(status_buf.device):
+        return int(_lib().mdcn_selftest_wait_timeout(_ptr(status_buf), int(limit_us),
+                                                     _stream(status_buf.device, stream)))
+
+
+def forward(x, offset, mask, weight, bias=None, stride=1, padding=0, dilation=1, group=1, deformable_group=1,
+            algo: str = "fused", out=None, workspace=None, handle=None):
+    """DCNv2 forward: allocates the output (and workspace) with torch and
+    runs the library on the current stream. ``algo`` = "fused" (default) or
+    "im2col_gemm" (the two-stage ablation)."""
+    h = handle if handle is not None else Handle(stride, padding, dilation, group, deformable_group)
+    dims = mdcn_output_dims(h, x, offset, mask, weight, bias)
+    if out is None:
+        out = torch.empty(dims, dtype=x.dtype, device=x.device)
+    if algo == "fused":
+        need = mdcn_workspace_size(h, x, offset, mask, weight, bias)
+        if workspace is None or workspace.numel() * workspace.element_size() < need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+        mdcn_forward(h, x, offset, mask, weight, bias, out, workspace)
+    elif algo == "im2col_gemm":
+        need = mdcn_im2col_gemm_workspace_size(h, x, offset, mask, weight, bias)
+        if workspace is None or workspace.numel() * workspace.element_size() < need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+        mdcn_forward_im2col_gemm(h, x, offset, mask, weight, bias, out, workspace)
+    else:
+        raise ValueError(f"unknown algo {algo!r}")
+    return out

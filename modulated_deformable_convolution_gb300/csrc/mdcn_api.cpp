@@ -1,0 +1,421 @@
+// C ABI of libmdcn (include/mdcn.h): argument validation following
+// "TensorRT plugin walkthrough: modulatedDeformConvPlugin" (section 2 shape
+// rule, section 3 attribute ranges, section 4 type and dimension bindings),
+// the execution plan, and dispatch to the kernels. No exception leaves this
+// file; every entry point returns an mdcn_status.
+#include "mdcn.h"
+
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "mdcn_launch.h"
+#include "mdcn_plan.h"
+
+struct mdcn_handle_ {
+    mdcn_attrs attrs;
+};
+
+namespace {
+
+using mdcn::Plan;
+
+thread_local int g_last_cuda_error = 0;
+
+mdcn_status cuda_fail(cudaError_t e) {
+    g_last_cuda_error = static_cast<int>(e);
+    return MDCN_ERR_CUDA;
+}
+
+constexpr int64_t kI31 = (int64_t(1) << 31) - 1;
+constexpr int64_t kI62 = int64_t(1) << 62;
+
+int64_t gcd64(int64_t a, int64_t b) {
+    while (b) {
+        const int64_t t = a % b;
+        a = b;
+        b = t;
+    }
+    return a;
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+// a*b*... with overflow detection against kI62
+bool mul_ok(int64_t& acc, int64_t v) {
+    if (v < 0 || (v != 0 && acc > kI62 / v)) return false;
+    acc *= v;
+    return true;
+}
+
+bool attrs_valid(const mdcn_attrs& a) {
+    for (int i = 0; i < 2; ++i) {
+        if (a.stride[i] < 1 || a.dilation[i] < 1 || a.padding[i] < 0) return false;
+        if (a.stride[i] > kI31 || a.dilation[i] > kI31 || a.padding[i] > kI31) return false;
+    }
+    return a.group >= 1 && a.deformable_group >= 1 && a.group <= kI31 && a.deformable_group <= kI31;
+}
+
+// Section 2/4 bindings and the section-2 output rule.
+mdcn_status check_dims(const mdcn_attrs& a, const mdcn_dims& d, int64_t out[4]) {
+    for (int i = 0; i < 4; ++i)
+        if (d.x[i] < 1 || d.offset[i] < 1 || d.mask[i] < 1 || d.weight[i] < 1) return MDCN_ERR_SHAPE;
+    const int64_t N = d.x[0], Cin = d.x[1];
+    const int64_t Cout = d.weight[0], Cg = d.weight[1], kh = d.weight[2], kw = d.weight[3];
+    const int64_t Ho = d.offset[2], Wo = d.offset[3];
+    for (int i = 0; i < 4; ++i)
+        if (d.x[i] > kI31 || d.offset[i] > kI31 || d.mask[i] > kI31 || d.weight[i] > kI31) return MDCN_ERR_UNSUPPORTED;
+    int64_t K = kh;
+    if (!mul_ok(K, kw)) return MDCN_ERR_UNSUPPORTED;
+    const int64_t dg = a.deformable_group, g = a.group;
+    if (d.offset[0] != N || d.mask[0] != N) return MDCN_ERR_SHAPE;          // offset_0 = mask_0 = x_0
+    if (d.mask[2] != Ho || d.mask[3] != Wo) return MDCN_ERR_SHAPE;          // mask_2 = offset_2, mask_3 = offset_3
+    int64_t oc = 2 * dg;
+    if (!mul_ok(oc, K)) return MDCN_ERR_UNSUPPORTED;
+    if (d.offset[1] != oc) return MDCN_ERR_SHAPE;                           // 2*dg*kh*kw offset channels
+    if (d.mask[1] != dg * K) return MDCN_ERR_SHAPE;                         // dg*kh*kw mask channels
+    if (Cin % g != 0 || Cout % g != 0 || Cg != Cin / g) return MDCN_ERR_SHAPE;  // weight [Cout, Cin/group, kh, kw]
+    if (Cin % dg != 0) return MDCN_ERR_SHAPE;
+    if (d.bias != 0 && d.bias != Cout) return MDCN_ERR_SHAPE;               // bias_0 = weight_0
+    // element counts
+    int64_t n;
+    n = N; if (!mul_ok(n, Cin) || !mul_ok(n, d.x[2]) || !mul_ok(n, d.x[3])) return MDCN_ERR_UNSUPPORTED;
+    n = N; if (!mul_ok(n, oc) || !mul_ok(n, Ho) || !mul_ok(n, Wo)) return MDCN_ERR_UNSUPPORTED;
+    n = N; if (!mul_ok(n, Cout) || !mul_ok(n, Ho) || !mul_ok(n, Wo)) return MDCN_ERR_UNSUPPORTED;
+    n = Cout; if (!mul_ok(n, Cg) || !mul_ok(n, K)) return MDCN_ERR_UNSUPPORTED;
+    out[0] = N;
+    out[1] = Cout;
+    out[2] = Ho;
+    out[3] = Wo;
+    return MDCN_OK;
+}
+
+mdcn_status make_plan(const mdcn_attrs& a, const mdcn_dims* d, mdcn_dtype dtype, Plan* pl) {
+    if (!d || !pl) return MDCN_ERR_NULL;
+    if (dtype != MDCN_F32 && dtype != MDCN_F16 && dtype != MDCN_BF16) return MDCN_ERR_DTYPE;
+    int64_t od[4];
+    mdcn_status s = check_dims(a, *d, od);
+    if (s != MDCN_OK) return s;
+    Plan p;
+    std::memset(&p, 0, sizeof(p));
+    p.N = d->x[0];
+    p.Cin = d->x[1];
+    p.H = d->x[2];
+    p.W = d->x[3];
+    p.Cout = d->weight[0];
+    p.kh = d->weight[2];
+    p.kw = d->weight[3];
+    p.Ho = d->offset[2];
+    p.Wo = d->offset[3];
+    p.sh = static_cast<int32_t>(a.stride[0]);
+    p.sw = static_cast<int32_t>(a.stride[1]);
+    p.ph = static_cast<int32_t>(a.padding[0]);
+    p.pw = static_cast<int32_t>(a.padding[1]);
+    p.dh = static_cast<int32_t>(a.dilation[0]);
+    p.dw = static_cast<int32_t>(a.dilation[1]);
+    p.group = static_cast<int32_t>(a.group);
+    p.dg = static_cast<int32_t>(a.deformable_group);
+    p.dtype = static_cast<int32_t>(dtype);
+    p.has_bias = d->bias != 0;
+    const int64_t K = p.kh * p.kw;
+    const int64_t Cg = p.Cin / a.group, Og = p.Cout / a.group, Cd = p.Cin / a.deformable_group;
+    // positions are compared in fp32: keep every coordinate exactly representable
+    if (p.H >= (1 << 24) || p.W >= (1 << 24)) return MDCN_ERR_UNSUPPORTED;
+    if ((p.Ho - 1) * a.stride[0] + (p.kh - 1) * a.dilation[0] >= (1 << 24) ||
+        (p.Wo - 1) * a.stride[1] + (p.kw - 1) * a.dilation[1] >= (1 << 24))
+        return MDCN_ERR_UNSUPPORTED;
+    if (K > kI31 || Cg > kI31 || Og > kI31) return MDCN_ERR_UNSUPPORTED;
+    p.K = static_cast<int32_t>(K);
+    p.Cg = static_cast<int32_t>(Cg);
+    p.Og = static_cast<int32_t>(Og);
+    p.Cd = static_cast<int32_t>(Cd);
+    p.P = p.Ho * p.Wo;
+    p.NP = p.N * p.P;
+
+    const int64_t elem = dtype == MDCN_F32 ? 4 : 2;
+    p.BKc = static_cast<int32_t>(128 / elem);
+    const int64_t U = gcd64(Cg, Cd);
+    const int64_t UP = round_up(U, p.BKc);
+    p.U = static_cast<int32_t>(U);
+    p.UP = static_cast<int32_t>(UP);
+    p.Ug = static_cast<int32_t>(Cg / U);
+    p.nch = static_cast<int32_t>(UP / p.BKc);
+    p.ntb = static_cast<int32_t>(ceil_div(K, mdcn::kTapBlock));
+    int64_t KT = Cg / U;
+    if (!mul_ok(KT, K) || !mul_ok(KT, p.nch) || KT * p.BKc > kI31) return MDCN_ERR_UNSUPPORTED;
+    p.KT = static_cast<int32_t>(KT);
+    p.KP = KT * p.BKc;
+    p.Cp = (p.Cin / U) * UP;
+    if (ceil_div(p.Cp, 32) > 65535) return MDCN_ERR_UNSUPPORTED;
+
+    // N tiling: up to 256 output channels per MMA, two MMAs (512 TMEM columns) per CTA
+    if (Og <= 256) {
+        p.nsub = 1;
+        p.ntiles_n = 1;
+        p.BNs = static_cast<int32_t>(round_up(Og, 16));
+    } else {
+        p.nsub = 2;
+        p.ntiles_n = static_cast<int32_t>(ceil_div(Og, 512));
+        const int64_t per = ceil_div(Og, p.ntiles_n);
+        p.BNs = static_cast<int32_t>(round_up(ceil_div(per, 2), 16));
+    }
+    if (p.ntiles_n > 65535 || p.group > 65535) return MDCN_ERR_UNSUPPORTED;
+    int32_t cols = 32;
+    while (cols < p.nsub * p.BNs) cols <<= 1;
+    p.tmem_cols = cols;
+    p.mtiles = ceil_div(p.NP, mdcn::kTileM);
+    if (p.mtiles > kI31) return MDCN_ERR_UNSUPPORTED;
+    const int64_t halves = dtype == MDCN_F32 ? 2 : 1;
+    p.a_bytes = static_cast<int32_t>(mdcn::kTileM * 128 * halves);
+    p.b_bytes = static_cast<int32_t>(p.nsub * p.BNs * 128 * halves);
+    p.desc_bytes = mdcn::kGatherWarps * mdcn::kRowsPerWarp * mdcn::kTapBlock * mdcn::kDescBytes;
+    const int32_t fixed = 1024 + p.desc_bytes + 512;
+    int32_t stages = (mdcn::kSmemLimit - fixed) / (p.a_bytes + p.b_bytes);
+    if (stages > 6) stages = 6;
+    if (stages < 2) return MDCN_ERR_UNSUPPORTED;
+    p.stages = stages;
+    p.smem_bytes = fixed + stages * (p.a_bytes + p.b_bytes);
+
+    // workspace: [status 256 B][x channels-last][packed weight]
+    const int64_t wtiles = ceil_div(p.W, 32);
+    if (p.N * p.H * wtiles > kI31) return MDCN_ERR_UNSUPPORTED;
+    int64_t xt = p.N * p.H;
+    if (!mul_ok(xt, p.W) || !mul_ok(xt, p.Cp) || !mul_ok(xt, elem)) return MDCN_ERR_UNSUPPORTED;
+    int64_t rows = p.Cout * halves;
+    if (rows < p.BNs) rows = p.BNs;
+    p.wp_rows = rows;
+    int64_t wpb = rows;
+    if (!mul_ok(wpb, p.KP) || !mul_ok(wpb, elem) || rows > kI31) return MDCN_ERR_UNSUPPORTED;
+    p.off_xt = mdcn::kStatusBytes;
+    p.off_wp = align256(p.off_xt + static_cast<size_t>(xt));
+    p.ws_bytes = align256(p.off_wp + static_cast<size_t>(wpb));
+    *pl = p;
+    return MDCN_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// compute capability 10.3 check, cached per device
+mdcn_status check_device() {
+    static std::atomic<int> cached[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= 64) return MDCN_ERR_UNSUPPORTED;
+    int v = cached[dev].load(std::memory_order_acquire);
+    if (v == 0) {
+        int major = 0, minor = 0;
+        e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        if (e != cudaSuccess) return cuda_fail(e);
+        e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (e != cudaSuccess) return cuda_fail(e);
+        v = (major == 10 && minor == 3) ? 1 : 2;
+        if (v == 1) {
+            for (int dt = 0; dt < 3; ++dt) {
+                e = mdcn::prepare_fused_attributes(dt, mdcn::kSmemLimit);
+                if (e != cudaSuccess) return cuda_fail(e);
+            }
+        }
+        cached[dev].store(v, std::memory_order_release);
+    }
+    return v == 1 ? MDCN_OK : MDCN_ERR_ARCH;
+}
+
+mdcn_status check_forward_args(mdcn_handle h, const void* x, const void* offset, const void* mask, const void* weight,
+                               const void* bias, void* out, void* ws, const mdcn_dims* dims) {
+    if (!h || !x || !offset || !mask || !weight || !out || !ws || !dims) return MDCN_ERR_NULL;
+    if ((bias == nullptr) != (dims->bias == 0)) return bias ? MDCN_ERR_SHAPE : MDCN_ERR_NULL;
+    if (!aligned16(x) || !aligned16(offset) || !aligned16(mask) || !aligned16(weight) || !aligned16(out) ||
+        !aligned16(ws) || (bias && !aligned16(bias)))
+        return MDCN_ERR_ALIGN;
+    return MDCN_OK;
+}
+
+// Plan + workspace-size + device checks shared by the fused-path entry points.
+mdcn_status plan_for_call(mdcn_handle h, const mdcn_dims* dims, mdcn_dtype dtype, size_t ws_bytes, Plan* p) {
+    mdcn_status s = make_plan(h->attrs, dims, dtype, p);
+    if (s != MDCN_OK) return s;
+    if (ws_bytes < p->ws_bytes) return MDCN_ERR_WORKSPACE;
+    return check_device();
+}
+
+}  // namespace
+
+extern "C" {
+
+mdcn_status mdcn_create(const mdcn_attrs* attrs, mdcn_handle* out) {
+    if (!attrs || !out) return MDCN_ERR_NULL;
+    if (!attrs_valid(*attrs)) return MDCN_ERR_ATTR;
+    mdcn_handle h = new (std::nothrow) mdcn_handle_;
+    if (!h) return MDCN_ERR_UNSUPPORTED;
+    h->attrs = *attrs;
+    *out = h;
+    return MDCN_OK;
+}
+
+mdcn_status mdcn_destroy(mdcn_handle handle) {
+    delete handle;
+    return MDCN_OK;
+}
+
+mdcn_status mdcn_output_dims(mdcn_handle handle, const mdcn_dims* dims, int64_t out_dims[4]) {
+    if (!handle || !dims || !out_dims) return MDCN_ERR_NULL;
+    int64_t od[4];
+    mdcn_status s = check_dims(handle->attrs, *dims, od);
+    if (s != MDCN_OK) return s;
+    for (int i = 0; i < 4; ++i) out_dims[i] = od[i];
+    return MDCN_OK;
+}
+
+mdcn_status mdcn_workspace_size(mdcn_handle handle, const mdcn_dims* dims, mdcn_dtype dtype, size_t* bytes) {
+    if (!handle || !dims || !bytes) return MDCN_ERR_NULL;
+    Plan p;
+    mdcn_status s = make_plan(handle->attrs, dims, dtype, &p);
+    if (s != MDCN_OK) return s;
+    *bytes = p.ws_bytes;
+    return MDCN_OK;
+}
+
+mdcn_status mdcn_forward(mdcn_handle handle, const void* x, const void* offset, const void* mask, const void* weight,
+                         const void* bias_or_null, void* out, void* workspace, size_t workspace_bytes,
+                         const mdcn_dims* dims, mdcn_dtype dtype, void* stream) {
+    mdcn_status s = check_forward_args(handle, x, offset, mask, weight, bias_or_null, out, workspace, dims);
+    if (s != MDCN_OK) return s;
+    Plan p;
+    s = plan_for_call(handle, dims, dtype, workspace_bytes, &p);
+    if (s != MDCN_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = mdcn::launch_prep_input(p, x, workspace, st);
+    if (e == cudaSuccess) e = mdcn::launch_pack_weight(p, weight, workspace, st);
+    if (e == cudaSuccess) e = mdcn::launch_fused(p, offset, mask, bias_or_null, out, workspace, st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return MDCN_OK;
+}
+
+mdcn_status mdcn_prepare_input(mdcn_handle handle, const void* x, void* workspace, size_t workspace_bytes,
+                               const mdcn_dims* dims, mdcn_dtype dtype, void* stream) {
+    if (!handle || !x || !workspace || !dims) return MDCN_ERR_NULL;
+    if (!aligned16(x) || !aligned16(workspace)) return MDCN_ERR_ALIGN;
+    Plan p;
+    mdcn_status s = plan_for_call(handle, dims, dtype, workspace_bytes, &p);
+    if (s != MDCN_OK) return s;
+    cudaError_t e = mdcn::launch_prep_input(p, x, workspace, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    return MDCN_OK;
+}
+
+mdcn_status mdcn_pack_weight(mdcn_handle handle, const void* weight, void* workspace, size_t workspace_bytes,
+                             const mdcn_dims* dims, mdcn_dtype dtype, void* stream) {
+    if (!handle || !weight || !workspace || !dims) return MDCN_ERR_NULL;
+    if (!aligned16(weight) || !aligned16(workspace)) return MDCN_ERR_ALIGN;
+    Plan p;
+    mdcn_status s = plan_for_call(handle, dims, dtype, workspace_bytes, &p);
+    if (s != MDCN_OK) return s;
+    cudaError_t e = mdcn::launch_pack_weight(p, weight, workspace, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    return MDCN_OK;
+}
+
+mdcn_status mdcn_forward_prepared(mdcn_handle handle, const void* offset, const void* mask, const void* bias_or_null,
+                                  void* out, void* workspace, size_t workspace_bytes, const mdcn_dims* dims,
+                                  mdcn_dtype dtype, void* stream) {
+    if (!handle || !offset || !mask || !out || !workspace || !dims) return MDCN_ERR_NULL;
+    if ((bias_or_null == nullptr) != (dims->bias == 0)) return bias_or_null ? MDCN_ERR_SHAPE : MDCN_ERR_NULL;
+    if (!aligned16(offset) || !aligned16(mask) || !aligned16(out) || !aligned16(workspace) ||
+        (bias_or_null && !aligned16(bias_or_null)))
+        return MDCN_ERR_ALIGN;
+    Plan p;
+    mdcn_status s = plan_for_call(handle, dims, dtype, workspace_bytes, &p);
+    if (s != MDCN_OK) return s;
+    cudaError_t e = mdcn::launch_fused(p, offset, mask, bias_or_null, out, workspace, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    return MDCN_OK;
+}
+
+mdcn_status mdcn_im2col_gemm_workspace_size(mdcn_handle handle, const mdcn_dims* dims, mdcn_dtype dtype,
+                                            size_t* bytes) {
+    if (!handle || !dims || !bytes) return MDCN_ERR_NULL;
+    Plan p;
+    mdcn_status s = make_plan(handle->attrs, dims, dtype, &p);
+    if (s != MDCN_OK) return s;
+    if (p.P > kI31 || static_cast<int64_t>(p.Cg) * p.K > kI31 || p.N > kI31) return MDCN_ERR_UNSUPPORTED;
+    *bytes = mdcn::im2col_workspace_bytes(p);
+    return MDCN_OK;
+}
+
+mdcn_status mdcn_forward_im2col_gemm(mdcn_handle handle, const void* x, const void* offset, const void* mask,
+                                     const void* weight, const void* bias_or_null, void* out, void* workspace,
+                                     size_t workspace_bytes, const mdcn_dims* dims, mdcn_dtype dtype, void* stream) {
+    mdcn_status s = check_forward_args(handle, x, offset, mask, weight, bias_or_null, out, workspace, dims);
+    if (s != MDCN_OK) return s;
+    size_t need = 0;
+    s = mdcn_im2col_gemm_workspace_size(handle, dims, dtype, &need);
+    if (s != MDCN_OK) return s;
+    if (workspace_bytes < need) return MDCN_ERR_WORKSPACE;
+    Plan p;
+    s = make_plan(handle->attrs, dims, dtype, &p);
+    if (s != MDCN_OK) return s;
+    s = check_device();
+    if (s != MDCN_OK) return s;
+    cudaError_t e = mdcn::launch_im2col_gemm(p, x, offset, mask, weight, bias_or_null, out, workspace,
+                                             static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    return MDCN_OK;
+}
+
+mdcn_status mdcn_query_status(const void* workspace, void* stream, uint32_t* device_bits) {
+    if (!workspace) return MDCN_ERR_NULL;
+    if (!aligned16(workspace)) return MDCN_ERR_ALIGN;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint32_t bits = 0;
+    cudaError_t e = cudaMemcpyAsync(&bits, workspace, sizeof(bits), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(const_cast<void*>(workspace), 0, sizeof(bits), st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (device_bits) *device_bits = bits;
+    return (bits & 1u) ? MDCN_ERR_TIMEOUT : MDCN_OK;
+}
+
+mdcn_status mdcn_selftest_wait_timeout(void* status_word, uint32_t limit_us, void* stream) {
+    if (!status_word) return MDCN_ERR_NULL;
+    if (!aligned16(status_word)) return MDCN_ERR_ALIGN;
+    if (limit_us < 1 || limit_us > 10000000u) return MDCN_ERR_ATTR;
+    mdcn_status s = check_device();
+    if (s != MDCN_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = mdcn::launch_wait_selftest(static_cast<uint32_t*>(status_word), uint64_t(limit_us) * 1000u, st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    uint32_t bits = 0;
+    e = cudaMemcpyAsync(&bits, status_word, sizeof(bits), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (bits & (1u << 31)) return MDCN_OK;  // the wait completed: the bound is broken
+    return (bits & 1u) ? MDCN_ERR_TIMEOUT : MDCN_OK;
+}
+
+int mdcn_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char* mdcn_status_string(mdcn_status status) {
+    switch (status) {
+        case MDCN_OK: return "ok";
+        case MDCN_ERR_NULL: return "a required pointer is NULL";
+        case MDCN_ERR_ATTR: return "attribute out of range (stride, dilation >= 1; padding >= 0; group, deformable_group >= 1)";
+        case MDCN_ERR_SHAPE: return "tensor dims are inconsistent";
+        case MDCN_ERR_DTYPE: return "unknown dtype";
+        case MDCN_ERR_ALIGN: return "device pointer not 16-byte aligned";
+        case MDCN_ERR_WORKSPACE: return "workspace too small";
+        case MDCN_ERR_ARCH: return "current device is not compute capability 10.3";
+        case MDCN_ERR_CUDA: return "CUDA runtime error";
+        case MDCN_ERR_TIMEOUT: return "device pipeline wait timed out";
+        case MDCN_ERR_UNSUPPORTED: return "size beyond the library's limits";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,30 @@
+// Kernel launchers of libmdcn (internal; the public interface is include/mdcn.h).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "mdcn_plan.h"
+
+namespace mdcn {
+
+// Layout prep of the fused path into the workspace: x -> channels-last
+// (also clears the workspace status word), weight -> packed K-major.
+cudaError_t launch_prep_input(const Plan& pl, const void* x, void* ws, cudaStream_t st);
+cudaError_t launch_pack_weight(const Plan& pl, const void* weight, void* ws, cudaStream_t st);
+
+// The fused implicit-GEMM kernel (after launch_prep on the same workspace).
+cudaError_t launch_fused(const Plan& pl, const void* offset, const void* mask, const void* bias, void* out,
+                         void* ws, cudaStream_t st);
+
+// Dynamic shared memory the fused kernel may use on this device (set once).
+cudaError_t prepare_fused_attributes(int dtype, int smem_bytes);
+
+// Ablation: deformable im2col -> cuBLAS GEMM per group -> bias/convert.
+size_t im2col_workspace_bytes(const Plan& pl);
+cudaError_t launch_im2col_gemm(const Plan& pl, const void* x, const void* offset, const void* mask,
+                               const void* weight, const void* bias, void* out, void* ws, cudaStream_t st);
+
+// Bounded-wait self-test kernel.
+cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t st);
+
+}  // namespace mdcn

@@ -1,0 +1,210 @@
+"""Host-side tests of the C ABI (no GPU needed): the library loads and
+exports everything include/mdcn.h declares, attribute validation (section 3),
+the output-shape rule and dimension bindings (sections 2 and 4), workspace
+sizing, and argument checks that must reject a call before anything is
+launched. Fake device pointers are only ever passed to calls that fail
+validation first."""
+import ctypes
+
+import pytest
+import torch
+
+from modulated_deformable_convolution_gb300 import _abi
+
+import modulated_deformable_convolution_gb300 as mdcn
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from modulated_deformable_convolution_gb300 import build
+
+    build.build()
+    return _abi.load()
+
+
+def attrs(stride=(1, 1), padding=(1, 1), dilation=(1, 1), group=1, dg=1):
+    a = _abi.mdcn_attrs()
+    a.stride[:] = stride
+    a.padding[:] = padding
+    a.dilation[:] = dilation
+    a.group = group
+    a.deformable_group = dg
+    return a
+
+
+def handle(lib, **kw):
+    h = ctypes.c_void_p()
+    assert lib.mdcn_create(ctypes.byref(attrs(**kw)), ctypes.byref(h)) == 0
+    return h
+
+
+def dims(N=2, Cin=8, H=10, W=12, Cout=6, kh=3, kw=3, Ho=10, Wo=12, dg=1, group=1, bias=True):
+    K = kh * kw
+    return mdcn.make_dims((N, Cin, H, W), (N, 2 * dg * K, Ho, Wo), (N, dg * K, Ho, Wo), (Cout, Cin // group, kh, kw),
+                          Cout if bias else 0)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _abi.declared_functions()
+    assert "mdcn_forward" in names and "mdcn_create" in names
+    raw = ctypes.CDLL(_abi.LIB_PATH)
+    for n in names:
+        assert hasattr(raw, n), n
+
+
+def test_status_strings(lib):
+    for s in range(0, 11):
+        assert lib.mdcn_status_string(s)
+    assert lib.mdcn_status_string(999) == b"unknown status"
+
+
+@pytest.mark.parametrize("bad", [
+    dict(stride=(0, 1)), dict(stride=(1, -2)), dict(dilation=(0, 1)), dict(padding=(0, -1)), dict(group=0),
+    dict(dg=0), dict(dg=-3),
+])
+def test_create_rejects_out_of_range_attrs(lib, bad):
+    h = ctypes.c_void_p(1234)
+    assert lib.mdcn_create(ctypes.byref(attrs(**bad)), ctypes.byref(h)) == _abi.MDCN_ERR_ATTR
+    assert h.value == 1234  # untouched on error
+
+
+def test_create_null(lib):
+    h = ctypes.c_void_p()
+    assert lib.mdcn_create(None, ctypes.byref(h)) == _abi.MDCN_ERR_NULL
+    assert lib.mdcn_create(ctypes.byref(attrs()), None) == _abi.MDCN_ERR_NULL
+    assert lib.mdcn_destroy(None) == 0
+
+
+def out_dims(lib, h, d):
+    o = (ctypes.c_int64 * 4)()
+    s = lib.mdcn_output_dims(h, ctypes.byref(d), o)
+    return s, tuple(o)
+
+
+def test_output_dims_rule(lib):
+    """N from x, Cout from weight, Ho and Wo from offset, even when they do
+    not follow the convolution formula."""
+    h = handle(lib)
+    s, o = out_dims(lib, h, dims(N=3, Cout=5, Ho=4, Wo=17))
+    assert s == 0 and o == (3, 5, 4, 17)
+    lib.mdcn_destroy(h)
+
+
+@pytest.mark.parametrize("mut", ["offset_batch", "mask_batch", "mask_spatial", "offset_channels", "mask_channels",
+                                 "weight_cg", "bias_len", "group_cout", "dg_cin", "zero_dim"])
+def test_output_dims_bindings(lib, mut):
+    h = handle(lib, group=2, dg=2)
+    d = dims(Cin=8, Cout=6, group=2, dg=2)
+    assert out_dims(lib, h, d)[0] == 0
+    if mut == "offset_batch":
+        d.offset[0] = 3
+    elif mut == "mask_batch":
+        d.mask[0] = 1
+    elif mut == "mask_spatial":
+        d.mask[3] = 11
+    elif mut == "offset_channels":
+        d.offset[1] = 2 * 9
+    elif mut == "mask_channels":
+        d.mask[1] = 9
+    elif mut == "weight_cg":
+        d.weight[1] = 8
+    elif mut == "bias_len":
+        d.bias = 5
+    elif mut == "group_cout":
+        d.weight[0] = 7
+    elif mut == "dg_cin":
+        h2 = handle(lib, group=1, dg=3)
+        d = dims(Cin=8, Cout=6, dg=3)
+        assert out_dims(lib, h2, d)[0] == _abi.MDCN_ERR_SHAPE
+        return
+    elif mut == "zero_dim":
+        d.x[2] = 0
+    assert out_dims(lib, h, d)[0] == _abi.MDCN_ERR_SHAPE
+    lib.mdcn_destroy(h)
+
+
+def test_output_dims_too_large(lib):
+    h = handle(lib)
+    d = dims()
+    d.x[2] = 1 << 31
+    assert out_dims(lib, h, d)[0] == _abi.MDCN_ERR_UNSUPPORTED
+
+
+def ws_size(lib, h, d, dt):
+    n = ctypes.c_size_t()
+    s = lib.mdcn_workspace_size(h, ctypes.byref(d), dt, ctypes.byref(n))
+    return s, n.value
+
+
+def test_workspace_size(lib):
+    h = handle(lib)
+    d = dims(N=4, Cin=128, H=80, W=80, Cout=128, Ho=80, Wo=80, bias=False)
+    s, n = ws_size(lib, h, d, _abi.MDCN_F16)
+    # status header + channels-last x + packed weight, each 256-aligned
+    assert s == 0 and n >= 256 + 4 * 80 * 80 * 128 * 2 + 128 * 128 * 9 * 2
+    s, n32 = ws_size(lib, h, d, _abi.MDCN_F32)
+    assert s == 0 and n32 >= 256 + 4 * 80 * 80 * 128 * 4 + 2 * 128 * 128 * 9 * 4
+    assert ws_size(lib, h, d, 7)[0] == _abi.MDCN_ERR_DTYPE
+
+
+def fwd(lib, h, ptrs, d, dt=_abi.MDCN_F16, ws_bytes=1 << 30):
+    x, off, m, w, b, out, ws = ptrs
+    return lib.mdcn_forward(h, x, off, m, w, b, out, ws, ws_bytes, ctypes.byref(d), dt, None)
+
+
+FAKE = 0x7f0000000000  # never dereferenced: each call below fails validation first
+
+
+def test_forward_rejects_before_launch(lib):
+    h = handle(lib)
+    d = dims(bias=True)
+    p = [FAKE + 256 * i for i in range(7)]
+    # NULL pointers
+    for i in (0, 1, 2, 3, 5, 6):
+        q = list(p)
+        q[i] = None
+        assert fwd(lib, h, q, d) == _abi.MDCN_ERR_NULL
+    # bias pointer given but dims say no bias, and the reverse
+    q = list(p)
+    q[4] = None
+    assert fwd(lib, h, q, d) == _abi.MDCN_ERR_NULL
+    d0 = dims(bias=False)
+    assert fwd(lib, h, p, d0) == _abi.MDCN_ERR_SHAPE
+    # misaligned pointer
+    q = list(p)
+    q[1] = FAKE + 8
+    assert fwd(lib, h, q, d) == _abi.MDCN_ERR_ALIGN
+    # inconsistent dims
+    bad = dims(bias=True)
+    bad.mask[1] = 3
+    assert fwd(lib, h, p, bad) == _abi.MDCN_ERR_SHAPE
+    # workspace too small
+    assert fwd(lib, h, p, d, ws_bytes=16) == _abi.MDCN_ERR_WORKSPACE
+    # dtype
+    assert fwd(lib, h, p, d, dt=5) == _abi.MDCN_ERR_DTYPE
+    assert lib.mdcn_forward(None, *p, 1 << 30, ctypes.byref(d), 1, None) == _abi.MDCN_ERR_NULL
+    lib.mdcn_destroy(h)
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_forward_without_device_reports_cuda_error(lib):
+    """With valid arguments and no usable GPU the call stops at the device
+    check (nothing is dereferenced) and reports a CUDA error."""
+    h = handle(lib)
+    d = dims(bias=True)
+    p = [FAKE + 256 * i for i in range(7)]
+    assert fwd(lib, h, p, d) in (_abi.MDCN_ERR_CUDA, _abi.MDCN_ERR_ARCH)
+    lib.mdcn_destroy(h)
+
+
+def test_python_binding_rejects_cpu_tensors(lib):
+    x = torch.zeros(1, 8, 4, 4)
+    off = torch.zeros(1, 18, 4, 4)
+    m = torch.zeros(1, 9, 4, 4)
+    w = torch.zeros(8, 8, 3, 3)
+    h = mdcn.Handle(1, 1, 1, 1, 1)
+    assert mdcn.mdcn_output_dims(h, x, off, m, w) == (1, 8, 4, 4)
+    with pytest.raises(ValueError):
+        mdcn.mdcn_forward(h, x, off, m, w, None, torch.zeros(1, 8, 4, 4), torch.zeros(16, dtype=torch.uint8))
+    with pytest.raises(mdcn.MdcnError):
+        mdcn.Handle(stride=0)

@@ -1,0 +1,170 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle
+on the same seeded inputs.
+
+Gate (per case): max |gpu - ref| <= tol * max |ref|, tol = 1e-4 for float32
+I/O and 2e-2 for float16 / bfloat16 I/O with fp32 accumulation. The oracle
+consumes the inputs already rounded to the I/O dtype, widened exactly to
+float64. Informational columns (printed): the per-element relative error
+|gpu - ref| / max(|ref|, 1e-6) (max, mean, share above 1e-5).
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import modulated_deformable_convolution_gb300 as mdcn
+from modulated_deformable_convolution_gb300.workloads import CONFIG_ORDER, CONFIGS, Case, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-4, "f16": 2e-2, "bf16": 2e-2}
+
+
+def np64(t):
+    return None if t is None else t.detach().to("cpu", torch.float64).numpy()
+
+
+def oracle_out(oracle_mod, case, inp, ho_range=None):
+    return oracle_mod.forward(np64(inp["x"]), np64(inp["offset"]), np64(inp["mask"]), np64(inp["weight"]),
+                              np64(inp["bias"]), ho_range=ho_range, **case.attrs())
+
+
+def gpu_out(case, inp, algo="fused", check_status=True):
+    dev = torch.device("cuda", 0)
+    d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+    h = mdcn.Handle(**case.attrs())
+    if algo == "fused":
+        need = mdcn.mdcn_workspace_size(h, d["x"], d["offset"], d["mask"], d["weight"], d["bias"])
+        ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    else:
+        need = mdcn.mdcn_im2col_gemm_workspace_size(h, d["x"], d["offset"], d["mask"], d["weight"], d["bias"])
+        ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    shape = mdcn.mdcn_output_dims(h, d["x"], d["offset"], d["mask"], d["weight"], d["bias"])
+    out = torch.full(shape, float("nan"), dtype=d["x"].dtype, device=dev)  # poison: every element must be written
+    if algo == "fused":
+        mdcn.mdcn_forward(h, d["x"], d["offset"], d["mask"], d["weight"], d["bias"], out, ws)
+        if check_status:
+            s, bits = mdcn.mdcn_query_status(ws)
+            assert s == mdcn.MDCN_OK, f"device status {bits:#x}"
+    else:
+        mdcn.mdcn_forward_im2col_gemm(h, d["x"], d["offset"], d["mask"], d["weight"], d["bias"], out, ws)
+    torch.cuda.synchronize()
+    return out
+
+
+def compare(gpu, ref, dtype, label):
+    g = gpu.astype(np.float64)
+    assert np.isfinite(g).all(), f"{label}: non-finite output"
+    err = np.abs(g - ref)
+    scale = np.abs(ref).max()
+    ratio = err.max() / max(scale, 1e-30)
+    rel = err / np.maximum(np.abs(ref), 1e-6)
+    print(f"[{label}] max|err|/max|ref| = {ratio:.3e} (tol {TOL[dtype]:.0e}); rel: max {rel.max():.2e} "
+          f"mean {rel.mean():.2e} >1e-5 {np.mean(rel > 1e-5) * 100:.1f}%")
+    assert ratio <= TOL[dtype], f"{label}: {ratio:.3e} > {TOL[dtype]}"
+
+
+def sample_rows(Ho):
+    return sorted({0, 1, Ho // 2, Ho - 1})
+
+
+@pytest.mark.parametrize("name", CONFIG_ORDER)
+def test_named_workloads(oracle_mod, name):
+    """The five named workloads at full size, in the launch configuration the
+    benchmark times; the oracle computes sampled output rows (first, second,
+    middle, last: every border) for all images and channels."""
+    case = CONFIGS[name]
+    inp = make_inputs(case)
+    gpu = np64(gpu_out(case, inp))
+    Ho, _ = case.out_hw
+    rows = sample_rows(Ho) if Ho > 4 else list(range(Ho))
+    for r in rows:
+        ref = oracle_out(oracle_mod, case, inp, ho_range=(r, r + 1))
+        compare(gpu[:, :, r], ref[:, :, r], case.dtype, f"{name} row {r}")
+
+
+SWEEP = [
+    Case("f16_ragged", "f16", N=3, Cin=64, Cout=48, H=13, W=13, bias=True, seed=10, offset_dist=("normal", 1.5)),
+    Case("bf16_g2_dg4_s2", "bf16", N=2, Cin=128, Cout=96, H=11, W=17, stride=(2, 2), group=2, deformable_group=4,
+         bias=True, seed=11, offset_dist=("normal", 2.0)),
+    Case("f32_k5x3_dg2", "f32", N=1, Cin=32, Cout=40, H=15, W=15, kh=5, kw=3, padding=(2, 1), deformable_group=2,
+         bias=True, seed=12, offset_dist=("uniform", -2.0, 2.0)),
+    Case("f16_depthwise", "f16", N=2, Cin=16, Cout=16, H=9, W=9, group=16, deformable_group=16, bias=True, seed=13),
+    Case("f16_cout320", "f16", N=1, Cin=64, Cout=320, H=12, W=12, bias=False, seed=14),
+    Case("bf16_cout544", "bf16", N=1, Cin=32, Cout=544, H=10, W=10, bias=True, seed=15),
+    Case("f32_1x1_dg3_far", "f32", N=2, Cin=24, Cout=20, H=7, W=9, kh=1, kw=1, padding=(0, 0), deformable_group=3,
+         bias=False, seed=16, offset_dist=("uniform", -8.0, 8.0), mask_dist="uniform"),
+    Case("f16_s2p2d2_g4_dg2", "f16", N=1, Cin=64, Cout=64, H=21, W=21, stride=(2, 2), padding=(2, 2),
+         dilation=(2, 2), group=4, deformable_group=2, bias=True, seed=17, offset_dist=("normal", 3.0)),
+    Case("bf16_1x5_free_hw", "bf16", N=3, Cin=48, Cout=32, H=6, W=31, kh=1, kw=5, padding=(0, 2), bias=True,
+         seed=18, Ho=4, Wo=29),
+    Case("f32_tiny_cin3", "f32", N=2, Cin=3, Cout=5, H=8, W=8, bias=True, seed=19, offset_dist=("normal", 1.0)),
+    Case("f16_k7_dil3", "f16", N=1, Cin=16, Cout=16, H=20, W=20, kh=7, kw=7, padding=(9, 9), dilation=(3, 3),
+         bias=False, seed=20, offset_dist=("normal", 2.0)),
+]
+
+
+@pytest.mark.parametrize("case", SWEEP, ids=[c.name for c in SWEEP])
+def test_sweep_full_compare(oracle_mod, case):
+    inp = make_inputs(case)
+    gpu = np64(gpu_out(case, inp))
+    ref = oracle_out(oracle_mod, case, inp)
+    compare(gpu, ref, case.dtype, case.name)
+
+
+@pytest.mark.parametrize("case", [SWEEP[0], SWEEP[1], SWEEP[2], SWEEP[3]], ids=lambda c: c.name)
+def test_im2col_gemm_ablation(oracle_mod, case):
+    inp = make_inputs(case)
+    gpu = np64(gpu_out(case, inp, algo="im2col_gemm"))
+    ref = oracle_out(oracle_mod, case, inp)
+    compare(gpu, ref, case.dtype, "im2col_" + case.name)
+
+
+def test_im2col_gemm_neck_f16(oracle_mod):
+    case = CONFIGS["neck_f16"]
+    inp = make_inputs(case)
+    gpu = np64(gpu_out(case, inp, algo="im2col_gemm"))
+    for r in (0, 40, 79):
+        ref = oracle_out(oracle_mod, case, inp, ho_range=(r, r + 1))
+        compare(gpu[:, :, r], ref[:, :, r], case.dtype, f"im2col neck row {r}")
+
+
+def test_zero_mask_gives_bias():
+    case = dataclasses.replace(SWEEP[2], name="f32_mask0", seed=30)
+    inp = make_inputs(case)
+    inp["mask"] = torch.zeros_like(inp["mask"])
+    gpu = gpu_out(case, inp).cpu()
+    expect = inp["bias"][None, :, None, None].expand_as(gpu)
+    assert torch.equal(gpu, expect)
+
+
+def test_huge_offsets_read_nothing():
+    """Offsets far outside the image (and NaN-free huge values) give bias only."""
+    case = dataclasses.replace(SWEEP[0], name="f16_far", seed=31)
+    inp = make_inputs(case)
+    inp["offset"] = torch.full_like(inp["offset"], 3.0e4)
+    gpu = gpu_out(case, inp).cpu()
+    expect = inp["bias"][None, :, None, None].expand_as(gpu)
+    assert torch.equal(gpu, expect)
+
+
+def test_deterministic_bitwise():
+    case = CONFIGS["multidg_bf16"]
+    inp = make_inputs(case)
+    a = gpu_out(case, inp)
+    b = gpu_out(case, inp)
+    assert torch.equal(a, b)
+
+
+def test_wait_timeout_selftest_then_gpu_still_works():
+    """The bounded wait gives up on a barrier nothing signals, reports a
+    timeout, and the context stays usable."""
+    buf = torch.zeros(4, dtype=torch.int32, device="cuda")
+    assert mdcn.mdcn_selftest_wait_timeout(buf, 2000) == mdcn.MDCN_ERR_TIMEOUT
+    bits = int(buf[0].item())
+    assert bits & 1 and bits & (1 << 14) and not bits & (1 << 31)
+    case = SWEEP[9]
+    inp = make_inputs(case)
+    out = gpu_out(case, inp)
+    assert torch.isfinite(out).all()
