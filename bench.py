@@ -248,6 +248,7 @@ def run_ours(args, case, world, rank, local, dist):
     def step(ev=None):
         mdcn.mdcn_prepare_input(h, x, off, m, w, b, ws, stream)
         mdcn.mdcn_pack_weight(h, x, off, m, w, b, ws, stream)
+        mdcn.mdcn_prepare_samples(h, x, off, m, w, b, ws, stream)
         if ev is not None:
             ev[0].record(stream)
         mdcn.mdcn_forward_prepared(h, x, off, m, w, b, out, ws, stream)

@@ -93,6 +93,23 @@ typedef struct mdcn_handle_* mdcn_handle;
  * On error *out is left unchanged. Host only; touches no GPU. */
 mdcn_status mdcn_create(const mdcn_attrs* attrs, mdcn_handle* out);
 
+/* Optional overrides of the fused kernel's automatic execution plan, for
+ * benchmarking and tuning; results are identical for every setting. A zero
+ * (or -1 for tile_mode) keeps the automatic choice. */
+typedef struct mdcn_tuning {
+    int32_t stages;    /* shared-memory pipeline stages: 2, 4, 6 or 8 (0: automatic) */
+    int32_t tile_mode; /* pixel tile: 0 = 128 consecutive pixels of N*Ho*Wo, 1 = 8x16 block of one image,
+                          -1 = automatic */
+    int32_t max_ctas;  /* cap on persistent CTAs (0: one per SM) */
+    int32_t reserved;  /* must be 0 */
+} mdcn_tuning;
+
+/* mdcn_create with plan overrides (tuning may be NULL = automatic). Errors as
+ * mdcn_create, plus MDCN_ERR_ATTR for an override out of range. A plan that
+ * the overrides make impossible (e.g. too many stages for shared memory) is
+ * reported by the later calls as MDCN_ERR_UNSUPPORTED. */
+mdcn_status mdcn_create_tuned(const mdcn_attrs* attrs, const mdcn_tuning* tuning, mdcn_handle* out);
+
 /* Frees the handle (NULL is accepted). Nothing else is freed. */
 mdcn_status mdcn_destroy(mdcn_handle handle);
 
@@ -107,7 +124,8 @@ mdcn_status mdcn_destroy(mdcn_handle handle);
 mdcn_status mdcn_output_dims(mdcn_handle handle, const mdcn_dims* dims, int64_t out_dims[4]);
 
 /* Bytes of device workspace mdcn_forward needs for these dims and dtype
- * (channels-last copy of x, the repacked weight and a status word). Host only. */
+ * (a status word, the channels-last copy of x, the repacked weight and the
+ * sampling descriptors). Host only. */
 mdcn_status mdcn_workspace_size(mdcn_handle handle, const mdcn_dims* dims, mdcn_dtype dtype,
                                 size_t* bytes);
 
@@ -115,8 +133,8 @@ mdcn_status mdcn_workspace_size(mdcn_handle handle, const mdcn_dims* dims, mdcn_
  * producer warps sample and modulate the columns straight into shared
  * memory, tcgen05 tensor-core MMAs accumulate in tensor memory, the epilogue
  * adds the bias and writes NCHW. The im2col column matrix never reaches
- * device memory. Two small layout kernels run first (x to channels-last,
- * weight repack), into workspace.
+ * device memory. Three small kernels run first, into workspace: x to
+ * channels-last, the weight repack, and the sampling descriptors.
  *   x [N,Cin,H,W], offset [N,2*dg*kh*kw,Ho,Wo], mask [N,dg*kh*kw,Ho,Wo],
  *   weight [Cout,Cin/group,kh,kw], bias_or_null [Cout] or NULL,
  *   out [N,Cout,Ho,Wo] (written), workspace of workspace_bytes (scratch,
@@ -129,21 +147,27 @@ mdcn_status mdcn_forward(mdcn_handle handle, const void* x, const void* offset, 
                          void* workspace, size_t workspace_bytes,
                          const mdcn_dims* dims, mdcn_dtype dtype, void* stream);
 
-/* The three steps of mdcn_forward as separate calls, for callers that
- * pack a constant weight once or time the steps on their own. Same
- * arguments, rules and workspace as mdcn_forward; run on one stream in this
- * order with one workspace:
- *   mdcn_prepare_input:   x -> channels-last copy in workspace; clears the
- *                         workspace status word;
- *   mdcn_pack_weight:     weight -> packed K-major copy in workspace;
- *   mdcn_forward_prepared: the fused kernel, reading both copies. */
+/* The four steps of mdcn_forward as separate calls, for callers that pack a
+ * constant weight once or time the steps on their own. Same argument rules
+ * and workspace as mdcn_forward; x, weight, offset and mask are read only by
+ * the step that names them. Run on one stream, with one workspace, and
+ * mdcn_forward_prepared after the other three:
+ *   mdcn_prepare_input:    x -> channels-last copy in workspace; clears the
+ *                          workspace status word;
+ *   mdcn_pack_weight:      weight -> packed K-major copy in workspace;
+ *   mdcn_prepare_samples:  offset, mask -> per (pixel, deformable group, tap)
+ *                          sampling descriptors in workspace (section 5
+ *                          step 1: point, corner validity, bilinear weights
+ *                          times the mask);
+ *   mdcn_forward_prepared: the fused gather + contraction + bias kernel. */
 mdcn_status mdcn_prepare_input(mdcn_handle handle, const void* x, void* workspace, size_t workspace_bytes,
                                const mdcn_dims* dims, mdcn_dtype dtype, void* stream);
 mdcn_status mdcn_pack_weight(mdcn_handle handle, const void* weight, void* workspace, size_t workspace_bytes,
                              const mdcn_dims* dims, mdcn_dtype dtype, void* stream);
-mdcn_status mdcn_forward_prepared(mdcn_handle handle, const void* offset, const void* mask,
-                                  const void* bias_or_null, void* out, void* workspace, size_t workspace_bytes,
-                                  const mdcn_dims* dims, mdcn_dtype dtype, void* stream);
+mdcn_status mdcn_prepare_samples(mdcn_handle handle, const void* offset, const void* mask, void* workspace,
+                                 size_t workspace_bytes, const mdcn_dims* dims, mdcn_dtype dtype, void* stream);
+mdcn_status mdcn_forward_prepared(mdcn_handle handle, const void* bias_or_null, void* out, void* workspace,
+                                  size_t workspace_bytes, const mdcn_dims* dims, mdcn_dtype dtype, void* stream);
 
 /* Workspace bytes for mdcn_forward_im2col_gemm (the column matrix of the
  * whole batch plus a float32 GEMM output). Host only. */

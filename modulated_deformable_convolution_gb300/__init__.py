@@ -22,7 +22,7 @@ from ._abi import (MDCN_BF16, MDCN_ERR_ALIGN, MDCN_ERR_ARCH, MDCN_ERR_ATTR, MDCN
 
 __all__ = ["Handle", "MdcnError", "forward", "mdcn_create", "mdcn_destroy", "mdcn_output_dims",
            "mdcn_workspace_size", "mdcn_forward", "mdcn_prepare_input", "mdcn_pack_weight",
-           "mdcn_forward_prepared", "mdcn_im2col_gemm_workspace_size", "mdcn_forward_im2col_gemm",
+           "mdcn_prepare_samples", "mdcn_forward_prepared", "mdcn_im2col_gemm_workspace_size", "mdcn_forward_im2col_gemm",
            "mdcn_query_status", "mdcn_selftest_wait_timeout", "mdcn_status_string", "library_path"]
 
 _DTYPES = {torch.float32: MDCN_F32, torch.float16: MDCN_F16, torch.bfloat16: MDCN_BF16}
@@ -63,8 +63,10 @@ def _pair(v):
     return v
 
 
-def mdcn_create(stride=1, padding=0, dilation=1, group=1, deformable_group=1):
-    """mdcn_create: returns the opaque handle (an int) or raises MdcnError."""
+def mdcn_create(stride=1, padding=0, dilation=1, group=1, deformable_group=1, tuning=None):
+    """mdcn_create (or mdcn_create_tuned when ``tuning`` is a dict with keys
+    stages, tile_mode, max_ctas): returns the opaque handle (an int) or raises
+    MdcnError."""
     a = _abi.mdcn_attrs()
     a.stride[:] = _pair(stride)
     a.padding[:] = _pair(padding)
@@ -72,7 +74,12 @@ def mdcn_create(stride=1, padding=0, dilation=1, group=1, deformable_group=1):
     a.group = int(group)
     a.deformable_group = int(deformable_group)
     h = ctypes.c_void_p()
-    _check(_lib().mdcn_create(ctypes.byref(a), ctypes.byref(h)), "mdcn_create")
+    if tuning is None:
+        _check(_lib().mdcn_create(ctypes.byref(a), ctypes.byref(h)), "mdcn_create")
+    else:
+        t = _abi.mdcn_tuning(int(tuning.get("stages", 0)), int(tuning.get("tile_mode", -1)),
+                             int(tuning.get("max_ctas", 0)), 0)
+        _check(_lib().mdcn_create_tuned(ctypes.byref(a), ctypes.byref(t), ctypes.byref(h)), "mdcn_create_tuned")
     return h.value
 
 
@@ -83,10 +90,10 @@ def mdcn_destroy(handle) -> None:
 class Handle:
     """Owns one library handle (the five section-3 attributes)."""
 
-    def __init__(self, stride=1, padding=0, dilation=1, group=1, deformable_group=1):
+    def __init__(self, stride=1, padding=0, dilation=1, group=1, deformable_group=1, tuning=None):
         self.attrs = dict(stride=_pair(stride), padding=_pair(padding), dilation=_pair(dilation), group=int(group),
                           deformable_group=int(deformable_group))
-        self.value = mdcn_create(**self.attrs)
+        self.value = mdcn_create(**self.attrs, tuning=tuning)
 
     def close(self):
         if getattr(self, "value", None):
@@ -202,16 +209,24 @@ def mdcn_pack_weight(handle, x, offset, mask, weight, bias, workspace, stream=No
                                        _stream(x.device, stream)), "mdcn_pack_weight")
 
 
+def mdcn_prepare_samples(handle, x, offset, mask, weight, bias, workspace, stream=None) -> None:
+    """Step 3 of mdcn_forward: offset, mask -> sampling descriptors in workspace."""
+    d = _dims(x, offset, mask, weight, bias)
+    with torch.cuda.device(x.device):
+        _check(_lib().mdcn_prepare_samples(_hval(handle), _ptr(offset), _ptr(mask), _ptr(workspace),
+                                           workspace.numel() * workspace.element_size(), ctypes.byref(d), _dtype(x),
+                                           _stream(x.device, stream)), "mdcn_prepare_samples")
+
+
 def mdcn_forward_prepared(handle, x, offset, mask, weight, bias, out, workspace, stream=None) -> None:
-    """Step 3 of mdcn_forward: the fused kernel on the prepared workspace
-    (x and weight only supply dims and dtype here)."""
+    """Step 4 of mdcn_forward: the fused kernel on the prepared workspace
+    (x, offset, mask and weight only supply dims and dtype here)."""
     _check_tensors(x, offset, mask, weight, bias, out)
     d = _dims(x, offset, mask, weight, bias)
     with torch.cuda.device(x.device):
-        _check(_lib().mdcn_forward_prepared(_hval(handle), _ptr(offset), _ptr(mask), _ptr(bias), _ptr(out),
-                                            _ptr(workspace), workspace.numel() * workspace.element_size(),
-                                            ctypes.byref(d), _dtype(x), _stream(x.device, stream)),
-               "mdcn_forward_prepared")
+        _check(_lib().mdcn_forward_prepared(_hval(handle), _ptr(bias), _ptr(out), _ptr(workspace),
+                                            workspace.numel() * workspace.element_size(), ctypes.byref(d), _dtype(x),
+                                            _stream(x.device, stream)), "mdcn_forward_prepared")
 
 
 def mdcn_forward_im2col_gemm(handle, x, offset, mask, weight, bias, out, workspace, stream=None) -> None:

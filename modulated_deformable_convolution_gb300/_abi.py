@@ -35,6 +35,11 @@ class mdcn_attrs(ctypes.Structure):
                 ("deformable_group", i64)]
 
 
+class mdcn_tuning(ctypes.Structure):
+    _fields_ = [("stages", ctypes.c_int32), ("tile_mode", ctypes.c_int32), ("max_ctas", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
 class mdcn_dims(ctypes.Structure):
     _fields_ = [("x", i64 * 4), ("offset", i64 * 4), ("mask", i64 * 4), ("weight", i64 * 4), ("bias", i64)]
 
@@ -63,6 +68,8 @@ def load(path: str = LIB_PATH):
         st = ctypes.c_int
         lib.mdcn_create.argtypes = [ctypes.POINTER(mdcn_attrs), ctypes.POINTER(vp)]
         lib.mdcn_create.restype = st
+        lib.mdcn_create_tuned.argtypes = [ctypes.POINTER(mdcn_attrs), ctypes.POINTER(mdcn_tuning), ctypes.POINTER(vp)]
+        lib.mdcn_create_tuned.restype = st
         lib.mdcn_destroy.argtypes = [vp]
         lib.mdcn_destroy.restype = st
         lib.mdcn_output_dims.argtypes = [vp, ctypes.POINTER(mdcn_dims), ctypes.POINTER(i64)]
@@ -76,8 +83,11 @@ def load(path: str = LIB_PATH):
         lib.mdcn_prepare_input.restype = st
         lib.mdcn_pack_weight.argtypes = [vp, vp, vp, ctypes.c_size_t, ctypes.POINTER(mdcn_dims), ctypes.c_int, vp]
         lib.mdcn_pack_weight.restype = st
-        lib.mdcn_forward_prepared.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_size_t, ctypes.POINTER(mdcn_dims),
-                                              ctypes.c_int, vp]
+        lib.mdcn_prepare_samples.argtypes = [vp, vp, vp, vp, ctypes.c_size_t, ctypes.POINTER(mdcn_dims), ctypes.c_int,
+                                             vp]
+        lib.mdcn_prepare_samples.restype = st
+        lib.mdcn_forward_prepared.argtypes = [vp, vp, vp, vp, ctypes.c_size_t, ctypes.POINTER(mdcn_dims), ctypes.c_int,
+                                              vp]
         lib.mdcn_forward_prepared.restype = st
         lib.mdcn_im2col_gemm_workspace_size.argtypes = [vp, ctypes.POINTER(mdcn_dims), ctypes.c_int,
                                                         ctypes.POINTER(ctypes.c_size_t)]

@@ -18,6 +18,7 @@
 
 struct mdcn_handle_ {
     mdcn_attrs attrs;
+    mdcn_tuning tuning;
 };
 
 namespace {
@@ -96,7 +97,8 @@ mdcn_status check_dims(const mdcn_attrs& a, const mdcn_dims& d, int64_t out[4]) 
     return MDCN_OK;
 }
 
-mdcn_status make_plan(const mdcn_attrs& a, const mdcn_dims* d, mdcn_dtype dtype, Plan* pl) {
+mdcn_status make_plan(const mdcn_attrs& a, const mdcn_tuning& tuning, const mdcn_dims* d, mdcn_dtype dtype,
+                      Plan* pl) {
     if (!d || !pl) return MDCN_ERR_NULL;
     if (dtype != MDCN_F32 && dtype != MDCN_F16 && dtype != MDCN_BF16) return MDCN_ERR_DTYPE;
     int64_t od[4];
@@ -154,7 +156,7 @@ mdcn_status make_plan(const mdcn_attrs& a, const mdcn_dims* d, mdcn_dtype dtype,
     p.Cp = (p.Cin / U) * UP;
     if (ceil_div(p.Cp, 32) > 65535) return MDCN_ERR_UNSUPPORTED;
 
-    // N tiling: up to 256 output channels per MMA, two MMAs (512 TMEM columns) per CTA
+    // N tiling: up to 256 output channels per MMA, two MMAs (512 TMEM columns) per tile
     if (Og <= 256) {
         p.nsub = 1;
         p.ntiles_n = 1;
@@ -165,22 +167,46 @@ mdcn_status make_plan(const mdcn_attrs& a, const mdcn_dims* d, mdcn_dtype dtype,
         const int64_t per = ceil_div(Og, p.ntiles_n);
         p.BNs = static_cast<int32_t>(round_up(ceil_div(per, 2), 16));
     }
-    if (p.ntiles_n > 65535 || p.group > 65535) return MDCN_ERR_UNSUPPORTED;
+    p.acc_cols = p.nsub * p.BNs;
+    p.nacc = 2 * p.acc_cols <= 512 ? 2 : 1;
     int32_t cols = 32;
-    while (cols < p.nsub * p.BNs) cols <<= 1;
+    while (cols < p.nacc * p.acc_cols) cols <<= 1;
     p.tmem_cols = cols;
-    p.mtiles = ceil_div(p.NP, mdcn::kTileM);
-    if (p.mtiles > kI31) return MDCN_ERR_UNSUPPORTED;
+
+    // pixel tiles: 8 x 16 blocks of one image when they waste (almost) no rows,
+    // else 128 consecutive pixels of N*Ho*Wo
+    p.TH = 8;
+    p.TW = 16;
+    p.tiles_x = ceil_div(p.Wo, p.TW);
+    p.tiles_y = ceil_div(p.Ho, p.TH);
+    const double waste = 1.0 - static_cast<double>(p.P) / static_cast<double>(p.tiles_x * p.TW * p.tiles_y * p.TH);
+    int32_t mode = tuning.tile_mode >= 0 ? tuning.tile_mode : (waste <= 0.06 ? 1 : 0);
+    p.tile_mode = mode;
+    p.mtiles = mode == 1 ? p.N * p.tiles_x * p.tiles_y : ceil_div(p.NP, mdcn::kTileM);
+    int64_t tt = p.mtiles;
+    if (!mul_ok(tt, p.ntiles_n) || !mul_ok(tt, p.group)) return MDCN_ERR_UNSUPPORTED;
+    p.tiles_total = tt;
+
     const int64_t halves = dtype == MDCN_F32 ? 2 : 1;
     p.a_bytes = static_cast<int32_t>(mdcn::kTileM * 128 * halves);
     p.b_bytes = static_cast<int32_t>(p.nsub * p.BNs * 128 * halves);
-    p.desc_bytes = mdcn::kGatherWarps * mdcn::kRowsPerWarp * mdcn::kTapBlock * mdcn::kDescBytes;
-    const int32_t fixed = 1024 + p.desc_bytes + 512;
-    int32_t stages = (mdcn::kSmemLimit - fixed) / (p.a_bytes + p.b_bytes);
-    if (stages > 6) stages = 6;
-    if (stages < 2) return MDCN_ERR_UNSUPPORTED;
+    p.desc_size = dtype == MDCN_F32 ? 32 : 16;
+    p.desc_slot_bytes = mdcn::kTileM * mdcn::kTapBlock * p.desc_size;
+    // TMA-store epilogue: 2-D tiles whose 16-channel boxes stay inside a group
+    // and whose output rows are 16-byte multiples
+    p.epi_tma = (mode == 1 && (p.Wo * elem) % 16 == 0 && Og % 16 == 0) ? 1 : 0;
+    p.epi_bytes = p.epi_tma ? mdcn::kEpiWarps * 2 * 16 * 32 * static_cast<int32_t>(elem) : 0;
+    const int32_t fixed = 1024 + 2 * p.desc_slot_bytes + p.epi_bytes + 256;
+    const int32_t per_stage = p.a_bytes + p.b_bytes;
+    // stages: 2, 4, 6 or 8; the gather produces kgroups k-tiles at once (4 when
+    // the stages allow it, else 2), and kgroups must divide the stage count
+    const int32_t max_stages = (mdcn::kSmemLimit - fixed) / per_stage;
+    int32_t stages = tuning.stages > 0 ? tuning.stages : (max_stages >= 4 ? 4 : 2);
+    if (stages < 2 || stages > 8 || (stages & 1) || stages > max_stages) return MDCN_ERR_UNSUPPORTED;
     p.stages = stages;
-    p.smem_bytes = fixed + stages * (p.a_bytes + p.b_bytes);
+    p.kgroups = (stages % 4 == 0) ? 4 : 2;
+    p.smem_bytes = fixed + stages * per_stage;
+    p.grid = 0;  // set at launch from the SM count
 
     // workspace: [status 256 B][x channels-last][packed weight]
     const int64_t wtiles = ceil_div(p.W, 32);
@@ -192,18 +218,26 @@ mdcn_status make_plan(const mdcn_attrs& a, const mdcn_dims* d, mdcn_dtype dtype,
     p.wp_rows = rows;
     int64_t wpb = rows;
     if (!mul_ok(wpb, p.KP) || !mul_ok(wpb, elem) || rows > kI31) return MDCN_ERR_UNSUPPORTED;
+    // sample descriptors: mtiles x dg x K x 128 rows x desc_size
+    int64_t dbytes = p.mtiles;
+    if (!mul_ok(dbytes, p.dg) || !mul_ok(dbytes, p.K) || !mul_ok(dbytes, mdcn::kTileM) ||
+        !mul_ok(dbytes, p.desc_size))
+        return MDCN_ERR_UNSUPPORTED;
+    if (p.mtiles > 2147483647 || p.dg > 65535) return MDCN_ERR_UNSUPPORTED;  // sampling grid
     p.off_xt = mdcn::kStatusBytes;
     p.off_wp = align256(p.off_xt + static_cast<size_t>(xt));
-    p.ws_bytes = align256(p.off_wp + static_cast<size_t>(wpb));
+    p.off_desc = align256(p.off_wp + static_cast<size_t>(wpb));
+    p.ws_bytes = align256(p.off_desc + static_cast<size_t>(dbytes));
     *pl = p;
     return MDCN_OK;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// compute capability 10.3 check, cached per device
-mdcn_status check_device() {
+// compute capability 10.3 check, cached per device; *sms = SM count
+mdcn_status check_device(int* sms = nullptr) {
     static std::atomic<int> cached[64];
+    static std::atomic<int> sm_count[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -215,6 +249,10 @@ mdcn_status check_device() {
         if (e != cudaSuccess) return cuda_fail(e);
         e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
         if (e != cudaSuccess) return cuda_fail(e);
+        int nsm = 0;
+        e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e);
+        sm_count[dev].store(nsm, std::memory_order_relaxed);
         v = (major == 10 && minor == 3) ? 1 : 2;
         if (v == 1) {
             for (int dt = 0; dt < 3; ++dt) {
@@ -224,6 +262,7 @@ mdcn_status check_device() {
         }
         cached[dev].store(v, std::memory_order_release);
     }
+    if (sms) *sms = sm_count[dev].load(std::memory_order_relaxed);
     return v == 1 ? MDCN_OK : MDCN_ERR_ARCH;
 }
 
@@ -239,25 +278,42 @@ mdcn_status check_forward_args(mdcn_handle h, const void* x, const void* offset,
 
 // Plan + workspace-size + device checks shared by the fused-path entry points.
 mdcn_status plan_for_call(mdcn_handle h, const mdcn_dims* dims, mdcn_dtype dtype, size_t ws_bytes, Plan* p) {
-    mdcn_status s = make_plan(h->attrs, dims, dtype, p);
+    mdcn_status s = make_plan(h->attrs, h->tuning, dims, dtype, p);
     if (s != MDCN_OK) return s;
     if (ws_bytes < p->ws_bytes) return MDCN_ERR_WORKSPACE;
-    return check_device();
+    int sms = 0;
+    s = check_device(&sms);
+    if (s != MDCN_OK) return s;
+    int64_t grid = sms > 0 ? sms : 1;
+    if (h->tuning.max_ctas > 0 && h->tuning.max_ctas < grid) grid = h->tuning.max_ctas;
+    if (grid > p->tiles_total) grid = p->tiles_total;
+    p->grid = static_cast<int32_t>(grid);
+    return MDCN_OK;
 }
 
 }  // namespace
 
 extern "C" {
 
-mdcn_status mdcn_create(const mdcn_attrs* attrs, mdcn_handle* out) {
+mdcn_status mdcn_create_tuned(const mdcn_attrs* attrs, const mdcn_tuning* tuning, mdcn_handle* out) {
     if (!attrs || !out) return MDCN_ERR_NULL;
     if (!attrs_valid(*attrs)) return MDCN_ERR_ATTR;
+    mdcn_tuning tu{0, -1, 0, 0};
+    if (tuning) {
+        tu = *tuning;
+        if (tu.stages < 0 || tu.stages == 1 || tu.stages > 8 || tu.tile_mode < -1 || tu.tile_mode > 1 ||
+            tu.max_ctas < 0 || tu.reserved != 0)
+            return MDCN_ERR_ATTR;
+    }
     mdcn_handle h = new (std::nothrow) mdcn_handle_;
     if (!h) return MDCN_ERR_UNSUPPORTED;
     h->attrs = *attrs;
+    h->tuning = tu;
     *out = h;
     return MDCN_OK;
 }
+
+mdcn_status mdcn_create(const mdcn_attrs* attrs, mdcn_handle* out) { return mdcn_create_tuned(attrs, nullptr, out); }
 
 mdcn_status mdcn_destroy(mdcn_handle handle) {
     delete handle;
@@ -276,7 +332,7 @@ mdcn_status mdcn_output_dims(mdcn_handle handle, const mdcn_dims* dims, int64_t 
 mdcn_status mdcn_workspace_size(mdcn_handle handle, const mdcn_dims* dims, mdcn_dtype dtype, size_t* bytes) {
     if (!handle || !dims || !bytes) return MDCN_ERR_NULL;
     Plan p;
-    mdcn_status s = make_plan(handle->attrs, dims, dtype, &p);
+    mdcn_status s = make_plan(handle->attrs, handle->tuning, dims, dtype, &p);
     if (s != MDCN_OK) return s;
     *bytes = p.ws_bytes;
     return MDCN_OK;
@@ -293,7 +349,8 @@ mdcn_status mdcn_forward(mdcn_handle handle, const void* x, const void* offset, 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = mdcn::launch_prep_input(p, x, workspace, st);
     if (e == cudaSuccess) e = mdcn::launch_pack_weight(p, weight, workspace, st);
-    if (e == cudaSuccess) e = mdcn::launch_fused(p, offset, mask, bias_or_null, out, workspace, st);
+    if (e == cudaSuccess) e = mdcn::launch_sample(p, offset, mask, workspace, st);
+    if (e == cudaSuccess) e = mdcn::launch_fused(p, bias_or_null, out, workspace, st);
     if (e != cudaSuccess) return cuda_fail(e);
     return MDCN_OK;
 }
@@ -322,18 +379,27 @@ mdcn_status mdcn_pack_weight(mdcn_handle handle, const void* weight, void* works
     return MDCN_OK;
 }
 
-mdcn_status mdcn_forward_prepared(mdcn_handle handle, const void* offset, const void* mask, const void* bias_or_null,
-                                  void* out, void* workspace, size_t workspace_bytes, const mdcn_dims* dims,
-                                  mdcn_dtype dtype, void* stream) {
-    if (!handle || !offset || !mask || !out || !workspace || !dims) return MDCN_ERR_NULL;
-    if ((bias_or_null == nullptr) != (dims->bias == 0)) return bias_or_null ? MDCN_ERR_SHAPE : MDCN_ERR_NULL;
-    if (!aligned16(offset) || !aligned16(mask) || !aligned16(out) || !aligned16(workspace) ||
-        (bias_or_null && !aligned16(bias_or_null)))
-        return MDCN_ERR_ALIGN;
+mdcn_status mdcn_prepare_samples(mdcn_handle handle, const void* offset, const void* mask, void* workspace,
+                                 size_t workspace_bytes, const mdcn_dims* dims, mdcn_dtype dtype, void* stream) {
+    if (!handle || !offset || !mask || !workspace || !dims) return MDCN_ERR_NULL;
+    if (!aligned16(offset) || !aligned16(mask) || !aligned16(workspace)) return MDCN_ERR_ALIGN;
     Plan p;
     mdcn_status s = plan_for_call(handle, dims, dtype, workspace_bytes, &p);
     if (s != MDCN_OK) return s;
-    cudaError_t e = mdcn::launch_fused(p, offset, mask, bias_or_null, out, workspace, static_cast<cudaStream_t>(stream));
+    cudaError_t e = mdcn::launch_sample(p, offset, mask, workspace, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    return MDCN_OK;
+}
+
+mdcn_status mdcn_forward_prepared(mdcn_handle handle, const void* bias_or_null, void* out, void* workspace,
+                                  size_t workspace_bytes, const mdcn_dims* dims, mdcn_dtype dtype, void* stream) {
+    if (!handle || !out || !workspace || !dims) return MDCN_ERR_NULL;
+    if ((bias_or_null == nullptr) != (dims->bias == 0)) return bias_or_null ? MDCN_ERR_SHAPE : MDCN_ERR_NULL;
+    if (!aligned16(out) || !aligned16(workspace) || (bias_or_null && !aligned16(bias_or_null))) return MDCN_ERR_ALIGN;
+    Plan p;
+    mdcn_status s = plan_for_call(handle, dims, dtype, workspace_bytes, &p);
+    if (s != MDCN_OK) return s;
+    cudaError_t e = mdcn::launch_fused(p, bias_or_null, out, workspace, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
     return MDCN_OK;
 }
@@ -342,7 +408,7 @@ mdcn_status mdcn_im2col_gemm_workspace_size(mdcn_handle handle, const mdcn_dims*
                                             size_t* bytes) {
     if (!handle || !dims || !bytes) return MDCN_ERR_NULL;
     Plan p;
-    mdcn_status s = make_plan(handle->attrs, dims, dtype, &p);
+    mdcn_status s = make_plan(handle->attrs, handle->tuning, dims, dtype, &p);
     if (s != MDCN_OK) return s;
     if (p.P > kI31 || static_cast<int64_t>(p.Cg) * p.K > kI31 || p.N > kI31) return MDCN_ERR_UNSUPPORTED;
     *bytes = mdcn::im2col_workspace_bytes(p);
@@ -359,7 +425,7 @@ mdcn_status mdcn_forward_im2col_gemm(mdcn_handle handle, const void* x, const vo
     if (s != MDCN_OK) return s;
     if (workspace_bytes < need) return MDCN_ERR_WORKSPACE;
     Plan p;
-    s = make_plan(handle->attrs, dims, dtype, &p);
+    s = make_plan(handle->attrs, handle->tuning, dims, dtype, &p);
     if (s != MDCN_OK) return s;
     s = check_device();
     if (s != MDCN_OK) return s;
@@ -389,7 +455,8 @@ mdcn_status mdcn_selftest_wait_timeout(void* status_word, uint32_t limit_us, voi
     mdcn_status s = check_device();
     if (s != MDCN_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e = mdcn::launch_wait_selftest(static_cast<uint32_t*>(status_word), uint64_t(limit_us) * 1000u, st);
+    // limit in SM cycles at the 2.07 GHz maximum clock (longer in time at lower clocks)
+    cudaError_t e = mdcn::launch_wait_selftest(static_cast<uint32_t*>(status_word), uint64_t(limit_us) * 2070u, st);
     if (e != cudaSuccess) return cuda_fail(e);
     uint32_t bits = 0;
     e = cudaMemcpyAsync(&bits, status_word, sizeof(bits), cudaMemcpyDeviceToHost, st);

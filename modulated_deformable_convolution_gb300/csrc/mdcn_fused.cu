@@ -1,24 +1,34 @@
-// Fused implicit-GEMM kernel of the modulated deformable convolution forward
-// ("TensorRT plugin walkthrough: modulatedDeformConvPlugin", section 5,
-// steps 1-3, done in one kernel without the column buffer).
+// Sampling kernel and fused implicit-GEMM kernel of the modulated deformable
+// convolution forward ("TensorRT plugin walkthrough: modulatedDeformConvPlugin",
+// section 5, steps 1-3, without the column buffer).
 //
-// One CTA computes a tile of 128 output pixels x (nsub*BNs) output channels
-// of one convolution group:
-//   warp 0     TMA: weight k-tiles (128-byte swizzled, K-major) -> smem ring
-//   warp 1     allocates tensor memory; lane 0 issues tcgen05.mma
-//              (A = modulated columns, B = weights, D = fp32 in TMEM)
-//   warps 2-9  producers: per (pixel, tap) sample descriptor (4 corner
-//              validity bits, 4 bilinear weights x mask), then per k-tile the
-//              4-corner gather of 128-byte channel runs of channels-last x,
-//              weighted sum, written 128-byte-swizzled into the A stage;
-//              afterwards the epilogue: TMEM -> registers -> +bias -> NCHW.
-// Stage hand-off uses mbarriers: full (producers), tma (transaction bytes),
-// empty (tcgen05.commit). Every wait is bounded (mdcn_ptx.cuh).
+// sample_kernel: one 16-byte (fp32: 32-byte) descriptor per (pixel tile,
+// deformable group, tap, tile row): the sampling point
+// (ho*sh - ph + i*dh + dh_off, wo*sw - pw + j*dw + dw_off), its 4 corner
+// validity bits and the 4 bilinear weights times the mask, laid out in the
+// fused kernel's tile order in workspace (it stays in L2).
+//
+// fused_kernel: persistent CTAs (one per SM) loop over output tiles of 128
+// pixels x (nsub*BNs) output channels of one convolution group. Warp roles:
+//   warp 0      TMA: weight k-tiles (K-major, 128-byte swizzle) -> B stages,
+//               and bulk copies of descriptor groups -> two-slot ring
+//   warp 1      allocates tensor memory; lane 0 issues tcgen05.mma
+//               (A = modulated columns, B = weights, D = fp32 in TMEM,
+//               two accumulators so the epilogue overlaps the next tile)
+//   warps 4-11  gather, as G warp groups each producing every G-th k-tile
+//               (one tap, 128 bytes of channels): per row, 4 lanes x 32 bytes of
+//               the 4 corners of the channels-last copy of x, weighted sum,
+//               128-byte-swizzled store into the A stage
+//   warps 12-15 epilogue: TMEM -> registers -> +bias -> NCHW output
+//   warps 2-3   idle
+// Hand-offs use mbarriers; every wait is bounded (mdcn_ptx.cuh), and a wait
+// that gives up raises a CTA-wide abort that every role observes.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "mdcn_launch.h"
@@ -52,8 +62,7 @@ struct Elem<kBF16> {
 
 struct FusedParams {
     const void* xt;
-    const void* offset;
-    const void* mask;
+    const void* desc;
     const void* bias;
     void* out;
     uint32_t* status;
@@ -68,15 +77,12 @@ __device__ __forceinline__ void from_f(float v, float* d) { *d = v; }
 __device__ __forceinline__ void from_f(float v, __half* d) { *d = __float2half_rn(v); }
 __device__ __forceinline__ void from_f(float v, __nv_bfloat16* d) { *d = __float2bfloat16_rn(v); }
 
-// Bilinear weight of one corner as stored in a descriptor: fp32 bits for
-// float32, the 16-bit value broadcast to both halves of a pair otherwise.
-__device__ __forceinline__ uint32_t wbits(float w, float*) { return __float_as_uint(w); }
-__device__ __forceinline__ uint32_t wbits(float w, __half*) {
-    __half2 h = __float2half2_rn(w);
+__device__ __forceinline__ uint32_t pack2(float a, float b, __half*) {
+    __half2 h = __floats2half2_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&h);
 }
-__device__ __forceinline__ uint32_t wbits(float w, __nv_bfloat16*) {
-    __nv_bfloat162 h = __float2bfloat162_rn(w);
+__device__ __forceinline__ uint32_t pack2(float a, float b, __nv_bfloat16*) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
@@ -93,91 +99,319 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     return v;
 }
 
-// Sample descriptor of output pixel p (linear over N*Ho*Wo), tap `tap`,
-// deformable group gd (section 5 step 1): the sampling point
-// (ho*sh - ph + i*dh + dh_off, wo*sw - pw + j*dw + dw_off); outside the open
-// range (-1, H) x (-1, W) every weight is 0; otherwise the four corners with
-// bilinear weights times the mask, a corner outside the image disabled.
-// Layout (32 bytes): int64 element offset of corner (y0, x0) in the
-// channels-last x, uint32 corner-valid bits, pad, 4 x weight bits.
+// Output pixel of tile row r: returns false for rows past the edge.
+struct Pixel {
+    int64_t n, ho, wo;
+    bool valid;
+};
+
+__device__ __forceinline__ Pixel tile_pixel(const Plan& pl, int64_t mt, int r) {
+    Pixel px;
+    if (pl.tile_mode == 0) {
+        const int64_t p = mt * kTileM + r;
+        px.valid = p < pl.NP;
+        const int64_t pp = px.valid ? p : 0;
+        px.n = pp / pl.P;
+        const int64_t hw = pp - px.n * pl.P;
+        px.ho = hw / pl.Wo;
+        px.wo = hw - px.ho * pl.Wo;
+    } else {
+        const int64_t per_img = pl.tiles_x * pl.tiles_y;
+        px.n = mt / per_img;
+        const int64_t rem = mt - px.n * per_img;
+        const int64_t ty = rem / pl.tiles_x;
+        const int64_t tx = rem - ty * pl.tiles_x;
+        px.ho = ty * pl.TH + r / pl.TW;
+        px.wo = tx * pl.TW + r % pl.TW;
+        px.valid = px.ho < pl.Ho && px.wo < pl.Wo;
+    }
+    return px;
+}
+
+struct TileId {
+    int32_t g, nt;
+    int64_t mt;
+};
+
+__device__ __forceinline__ TileId decode_tile(const Plan& pl, int64_t t) {
+    TileId id;
+    id.mt = t % pl.mtiles;
+    const int64_t r = t / pl.mtiles;
+    id.nt = static_cast<int32_t>(r % pl.ntiles_n);
+    id.g = static_cast<int32_t>(r / pl.ntiles_n);
+    return id;
+}
+
+// 16-bit: out = w00*v0 + w01*v1 + w10*v2 + w11*v3 on one pair of channels;
+// wa = (w00, w01), wb = (w10, w11).
+__device__ __forceinline__ uint32_t blend(uint32_t wa, uint32_t wb, uint32_t v0, uint32_t v1, uint32_t v2,
+                                          uint32_t v3, __half*) {
+    const __half2 a = *reinterpret_cast<const __half2*>(&wa), b = *reinterpret_cast<const __half2*>(&wb);
+    __half2 acc = __hmul2(__low2half2(a), *reinterpret_cast<const __half2*>(&v0));
+    acc = __hfma2(__high2half2(a), *reinterpret_cast<const __half2*>(&v1), acc);
+    acc = __hfma2(__low2half2(b), *reinterpret_cast<const __half2*>(&v2), acc);
+    acc = __hfma2(__high2half2(b), *reinterpret_cast<const __half2*>(&v3), acc);
+    return *reinterpret_cast<uint32_t*>(&acc);
+}
+
+__device__ __forceinline__ uint32_t blend(uint32_t wa, uint32_t wb, uint32_t v0, uint32_t v1, uint32_t v2,
+                                          uint32_t v3, __nv_bfloat16*) {
+    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&wa);
+    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&wb);
+    __nv_bfloat162 acc = __hmul2(__low2bfloat162(a), *reinterpret_cast<const __nv_bfloat162*>(&v0));
+    acc = __hfma2(__high2bfloat162(a), *reinterpret_cast<const __nv_bfloat162*>(&v1), acc);
+    acc = __hfma2(__low2bfloat162(b), *reinterpret_cast<const __nv_bfloat162*>(&v2), acc);
+    acc = __hfma2(__high2bfloat162(b), *reinterpret_cast<const __nv_bfloat162*>(&v3), acc);
+    return *reinterpret_cast<uint32_t*>(&acc);
+}
+
+// ---------------------------------------------------------------- sampling kernel
+// Grid (mtiles, dg), 128 threads = tile rows; each thread writes the
+// descriptors of its pixel for every tap: desc[((mt*dg + gd)*K + tap)*128 + row].
+// Descriptor: int64 element offset of corner (y0, x0) in the channels-last x
+// with the 4 corner-valid bits in its low bits (offsets are multiples of 32
+// elements), then the 4 weights (16-bit pairs for 16-bit types, fp32 words
+// in a second 16 bytes for fp32).
 template <typename T>
-__device__ __forceinline__ void make_desc(const Plan& pl, const T* __restrict__ offset, const T* __restrict__ mask,
-                                          int64_t p, int32_t tap, int32_t gd, uint32_t dst) {
-    int64_t base = 0;
-    uint32_t flags = 0;
-    float w00 = 0.f, w01 = 0.f, w10 = 0.f, w11 = 0.f;
-    if (p < pl.NP) {
-        const int64_t n = p / pl.P;
-        const int64_t hw = p - n * pl.P;
-        const int64_t ho = hw / pl.Wo;
-        const int64_t wo = hw - ho * pl.Wo;
-        const int32_t i = tap / static_cast<int32_t>(pl.kw);
-        const int32_t j = tap - i * static_cast<int32_t>(pl.kw);
-        const int64_t K = pl.K;
-        const int64_t och = static_cast<int64_t>(gd) * 2 * K + 2 * tap;
-        const int64_t ostride = pl.P;
-        const int64_t obase = (n * 2 * pl.dg * K + och) * ostride + hw;
-        const float dhv = to_f(offset[obase]);
-        const float dwv = to_f(offset[obase + ostride]);
-        const float m = to_f(mask[(n * pl.dg * K + static_cast<int64_t>(gd) * K + tap) * ostride + hw]);
-        const float hf = static_cast<float>(ho * pl.sh - pl.ph + static_cast<int64_t>(i) * pl.dh) + dhv;
-        const float wf = static_cast<float>(wo * pl.sw - pl.pw + static_cast<int64_t>(j) * pl.dw) + dwv;
-        if (hf > -1.0f && hf < static_cast<float>(pl.H) && wf > -1.0f && wf < static_cast<float>(pl.W)) {
-            const float h0f = floorf(hf), w0f = floorf(wf);
-            const float lh = hf - h0f, lw = wf - w0f;
-            const float hh = 1.0f - lh, hw_ = 1.0f - lw;
-            const int64_t y0 = static_cast<int64_t>(h0f);
-            const int64_t x0 = static_cast<int64_t>(w0f);
-            w00 = hh * hw_ * m;
-            w01 = hh * lw * m;
-            w10 = lh * hw_ * m;
-            w11 = lh * lw * m;
-            const bool top = y0 >= 0, bottom = y0 + 1 < pl.H, left = x0 >= 0, right = x0 + 1 < pl.W;
-            flags = (top && left ? 1u : 0u) | (top && right ? 2u : 0u) | (bottom && left ? 4u : 0u) |
-                    (bottom && right ? 8u : 0u);
-            base = ((n * pl.H + y0) * pl.W + x0) * pl.Cp;
+__global__ void __launch_bounds__(kTileM) sample_kernel(const T* __restrict__ offset, const T* __restrict__ mask,
+                                                        uint8_t* __restrict__ desc, Plan pl) {
+    const int64_t mt = blockIdx.x;
+    const int64_t gd = blockIdx.y;
+    const int row = threadIdx.x;
+    const Pixel q = tile_pixel(pl, mt, row);
+    const int64_t K = pl.K;
+    const int64_t P = pl.P;
+    const int64_t n = q.valid ? q.n : 0;
+    const int64_t hw = q.valid ? q.ho * pl.Wo + q.wo : 0;
+    const T* po = offset + (n * 2 * pl.dg * K + gd * 2 * K) * P + hw;
+    const T* pm = mask + (n * pl.dg * K + gd * K) * P + hw;
+    const float hbase = static_cast<float>(q.ho * pl.sh - pl.ph);
+    const float wbase = static_cast<float>(q.wo * pl.sw - pl.pw);
+    const int64_t nbase = q.n * pl.H;
+    const uint32_t dsz = static_cast<uint32_t>(pl.desc_size);
+    uint8_t* dst = desc + ((mt * pl.dg + gd) * K * kTileM + row) * dsz;
+    int32_t i = 0, j = 0;
+    for (int32_t tb = 0; tb < pl.K; tb += kTapBlock) {
+        const int32_t ntb = min(kTapBlock, pl.K - tb);
+        float dhv[kTapBlock], dwv[kTapBlock], mv[kTapBlock];
+#pragma unroll
+        for (int kb = 0; kb < kTapBlock; ++kb) {
+            const int64_t tap = tb + (kb < ntb ? kb : 0);
+            dhv[kb] = to_f(po[2 * tap * P]);
+            dwv[kb] = to_f(po[(2 * tap + 1) * P]);
+            mv[kb] = to_f(pm[tap * P]);
+        }
+#pragma unroll
+        for (int kb = 0; kb < kTapBlock; ++kb) {
+            if (kb < ntb) {
+                int64_t off = 0;
+                uint32_t flags = 0;
+                float w00 = 0.f, w01 = 0.f, w10 = 0.f, w11 = 0.f;
+                const float hf = hbase + static_cast<float>(i * pl.dh) + dhv[kb];
+                const float wf = wbase + static_cast<float>(j * pl.dw) + dwv[kb];
+                if (q.valid && hf > -1.0f && hf < static_cast<float>(pl.H) && wf > -1.0f &&
+                    wf < static_cast<float>(pl.W)) {
+                    const float h0f = floorf(hf), w0f = floorf(wf);
+                    const float lh = hf - h0f, lw = wf - w0f;
+                    const float hh = 1.0f - lh, hw_ = 1.0f - lw;
+                    const float m = mv[kb];
+                    const int32_t y0 = static_cast<int32_t>(h0f);
+                    const int32_t x0 = static_cast<int32_t>(w0f);
+                    w00 = hh * hw_ * m;
+                    w01 = hh * lw * m;
+                    w10 = lh * hw_ * m;
+                    w11 = lh * lw * m;
+                    const bool top = y0 >= 0, bottom = y0 + 1 < pl.H;
+                    const bool left = x0 >= 0, right = x0 + 1 < pl.W;
+                    flags = (top && left ? 1u : 0u) | (top && right ? 2u : 0u) | (bottom && left ? 4u : 0u) |
+                            (bottom && right ? 8u : 0u);
+                    off = ((nbase + y0) * pl.W + x0) * pl.Cp;
+                }
+                const uint64_t packed = static_cast<uint64_t>(off) | flags;
+                uint4 d0;
+                d0.x = static_cast<uint32_t>(packed);
+                d0.y = static_cast<uint32_t>(packed >> 32);
+                uint8_t* dp = dst + static_cast<int64_t>(tb + kb) * kTileM * dsz;
+                if constexpr (sizeof(T) == 4) {
+                    d0.z = 0u;
+                    d0.w = 0u;
+                    reinterpret_cast<uint4*>(dp)[0] = d0;
+                    reinterpret_cast<uint4*>(dp)[1] =
+                        make_uint4(__float_as_uint(w00), __float_as_uint(w01), __float_as_uint(w10), __float_as_uint(w11));
+                } else {
+                    T* tag = nullptr;
+                    d0.z = pack2(w00, w01, tag);
+                    d0.w = pack2(w10, w11, tag);
+                    reinterpret_cast<uint4*>(dp)[0] = d0;
+                }
+            }
+            if (++j == static_cast<int32_t>(pl.kw)) {
+                j = 0;
+                ++i;
+            }
         }
     }
-    T* tag = nullptr;
-    sts128(dst, static_cast<uint32_t>(static_cast<uint64_t>(base)), static_cast<uint32_t>(static_cast<uint64_t>(base) >> 32),
-           flags, 0u);
-    sts128(dst + 16, wbits(w00, tag), wbits(w01, tag), wbits(w10, tag), wbits(w11, tag));
 }
 
-// 16-bit element pairs: acc = sum_c w_c * v_c on packed halves.
-__device__ __forceinline__ uint32_t combine2(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3, uint32_t v0,
-                                             uint32_t v1, uint32_t v2, uint32_t v3, __half*) {
-    const __half2 a0 = *reinterpret_cast<const __half2*>(&w0), a1 = *reinterpret_cast<const __half2*>(&w1);
-    const __half2 a2 = *reinterpret_cast<const __half2*>(&w2), a3 = *reinterpret_cast<const __half2*>(&w3);
-    const __half2 b0 = *reinterpret_cast<const __half2*>(&v0), b1 = *reinterpret_cast<const __half2*>(&v1);
-    const __half2 b2 = *reinterpret_cast<const __half2*>(&v2), b3 = *reinterpret_cast<const __half2*>(&v3);
-    __half2 acc = __hmul2(a0, b0);
-    acc = __hfma2(a1, b1, acc);
-    acc = __hfma2(a2, b2, acc);
-    acc = __hfma2(a3, b3, acc);
-    return *reinterpret_cast<uint32_t*>(&acc);
+// ---------------------------------------------------------------- gather helpers
+// Position in a CTA's k-tile sequence. A tile's k-tiles form descriptor
+// groups (unit ul, tap block b); each group holds its chunks x taps k-tiles.
+// The rg/rk fields rotate the group order and the k-tile order inside a
+// group; they are kept at zero (the order of the packed weight), which makes
+// every plan choice accumulate each output in the same order.
+struct Cursor {
+    int64_t t, mt;
+    int32_t g, nt;
+    int32_t gi, j;        // processing position: group, k-tile within the group
+    int32_t rg, rk;       // rotations of the groups and of the k-tiles in this group
+    int32_t ul, b, ntbg, nktg, ch, kb, kt;  // the k-tile at that position
+    uint32_t gr;          // descriptor groups entered so far (across tiles)
+    bool live;
+};
+
+__device__ __forceinline__ void cursor_group(const Plan& pl, Cursor& c) {
+    const int32_t ngroups = pl.Ug * pl.ntb;
+    int32_t ag = c.gi + c.rg;
+    if (ag >= ngroups) ag -= ngroups;
+    c.ul = ag / pl.ntb;
+    c.b = ag - c.ul * pl.ntb;
+    c.ntbg = min(kTapBlock, pl.K - c.b * kTapBlock);
+    c.nktg = c.ntbg * pl.nch;
+    c.rk = 0;
 }
 
-__device__ __forceinline__ uint32_t combine2(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3, uint32_t v0,
-                                             uint32_t v1, uint32_t v2, uint32_t v3, __nv_bfloat16*) {
-    const __nv_bfloat162 a0 = *reinterpret_cast<const __nv_bfloat162*>(&w0);
-    const __nv_bfloat162 a1 = *reinterpret_cast<const __nv_bfloat162*>(&w1);
-    const __nv_bfloat162 a2 = *reinterpret_cast<const __nv_bfloat162*>(&w2);
-    const __nv_bfloat162 a3 = *reinterpret_cast<const __nv_bfloat162*>(&w3);
-    const __nv_bfloat162 b0 = *reinterpret_cast<const __nv_bfloat162*>(&v0);
-    const __nv_bfloat162 b1 = *reinterpret_cast<const __nv_bfloat162*>(&v1);
-    const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&v2);
-    const __nv_bfloat162 b3 = *reinterpret_cast<const __nv_bfloat162*>(&v3);
-    __nv_bfloat162 acc = __hmul2(a0, b0);
-    acc = __hfma2(a1, b1, acc);
-    acc = __hfma2(a2, b2, acc);
-    acc = __hfma2(a3, b3, acc);
-    return *reinterpret_cast<uint32_t*>(&acc);
+__device__ __forceinline__ void cursor_ktile(const Plan& pl, Cursor& c) {
+    int32_t a = c.j + c.rk;
+    if (a >= c.nktg) a -= c.nktg;
+    c.ch = a / c.ntbg;
+    c.kb = a - c.ch * c.ntbg;
+    c.kt = (c.ul * pl.K + c.b * kTapBlock) * pl.nch + a;  // global k-tile index (B coordinate)
+}
+
+__device__ __forceinline__ void cursor_tile(const Plan& pl, Cursor& c, int64_t t) {
+    c.t = t;
+    c.live = t < pl.tiles_total;
+    if (!c.live) return;
+    const TileId id = decode_tile(pl, t);
+    c.g = id.g;
+    c.nt = id.nt;
+    c.mt = id.mt;
+    c.rg = 0;
+    c.gi = 0;
+    c.j = 0;
+    cursor_group(pl, c);
+    cursor_ktile(pl, c);
+}
+
+__device__ __forceinline__ void cursor_init(const Plan& pl, Cursor& c, int64_t first_tile) {
+    c.gr = 0;
+    cursor_tile(pl, c, first_tile);
+}
+
+__device__ __forceinline__ void cursor_advance(const Plan& pl, Cursor& c, int64_t tile_step) {
+    if (++c.j < c.nktg) {
+        cursor_ktile(pl, c);
+        return;
+    }
+    c.j = 0;
+    ++c.gr;
+    if (++c.gi < pl.Ug * pl.ntb) {
+        cursor_group(pl, c);
+        cursor_ktile(pl, c);
+        return;
+    }
+    cursor_tile(pl, c, c.t + tile_step);
+}
+
+// Moves the cursor to the first k-tile of its next group.
+__device__ __forceinline__ void cursor_next_group(const Plan& pl, Cursor& c, int64_t tile_step) {
+    c.j = c.nktg - 1;
+    cursor_advance(pl, c, tile_step);
+}
+
+template <typename T>
+struct GatherCtx {
+    const T* xt;
+    int64_t c1, c2, c3;  // element offsets of corners (y0, x0+1), (y0+1, x0), (y0+1, x0+1)
+    int lane, q4, rsub, row0;
+    uint32_t dsz;
+};
+
+struct RowBuf {  // one row-iteration of one lane: 4 corners x 32 bytes, and the row's descriptor
+    uint4 v[4][2];
+    uint4 w;     // 16-bit types: .z = (w00, w01), .w = (w10, w11); fp32: the 4 weights
+};
+
+__device__ __forceinline__ uint32_t swz128(int row, int chunk) {
+    return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+__device__ __forceinline__ float blend_f32(float w00, float w01, float w10, float w11, uint32_t v0, uint32_t v1,
+                                           uint32_t v2, uint32_t v3) {
+    float a = w00 * __uint_as_float(v0);
+    a = fmaf(w01, __uint_as_float(v1), a);
+    a = fmaf(w10, __uint_as_float(v2), a);
+    return fmaf(w11, __uint_as_float(v3), a);
+}
+
+// Row-iteration it of a k-tile: reads the row's descriptor (tap kb) and
+// issues the loads of its 4 corners (32 bytes per lane, chunks 2*q4, 2*q4+1).
+template <typename T, bool kF32Path>
+__device__ __forceinline__ void row_issue(const GatherCtx<T>& cx, uint32_t dbase, int kb, int64_t cb, int it,
+                                          RowBuf& rb) {
+    const int row = cx.row0 + 8 * it + cx.rsub;
+    const uint32_t da = dbase + static_cast<uint32_t>(kb * kTileM + row) * cx.dsz;
+    const uint4 e = lds128(da);
+    if constexpr (kF32Path) {
+        rb.w = lds128(da + 16);
+    } else {
+        rb.w = e;
+    }
+    const uint64_t packed = (static_cast<uint64_t>(e.y) << 32) | e.x;
+    const uint32_t fl = e.x & 15u;
+    const T* p = cx.xt + static_cast<int64_t>(packed & ~static_cast<uint64_t>(31)) + cb;
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+        const int64_t co = cc == 0 ? 0 : (cc == 1 ? cx.c1 : (cc == 2 ? cx.c2 : cx.c3));
+        rb.v[cc][0] = make_uint4(0u, 0u, 0u, 0u);
+        rb.v[cc][1] = make_uint4(0u, 0u, 0u, 0u);
+        if (fl & (1u << cc)) ldg256(p + co, rb.v[cc][0], rb.v[cc][1]);
+    }
+}
+
+// Weighted sum of the 4 corners of row-iteration it into the A stage a_s.
+template <typename T, bool kF32Path>
+__device__ __forceinline__ void row_combine(const GatherCtx<T>& cx, uint32_t a_s, int it, const RowBuf& rb) {
+    const int row = cx.row0 + 8 * it + cx.rsub;
+    const uint32_t o0 = swz128(row, 2 * cx.q4), o1 = swz128(row, 2 * cx.q4 + 1);
+    const uint4 w = rb.w;
+#pragma unroll
+    for (int hv = 0; hv < 2; ++hv) {
+        const uint4 a = rb.v[0][hv], b = rb.v[1][hv], c = rb.v[2][hv], d = rb.v[3][hv];
+        const uint32_t o = hv ? o1 : o0;
+        if constexpr (kF32Path) {
+            const float w00 = __uint_as_float(w.x), w01 = __uint_as_float(w.y);
+            const float w10 = __uint_as_float(w.z), w11 = __uint_as_float(w.w);
+            const float s0 = blend_f32(w00, w01, w10, w11, a.x, b.x, c.x, d.x);
+            const float s1 = blend_f32(w00, w01, w10, w11, a.y, b.y, c.y, d.y);
+            const float s2 = blend_f32(w00, w01, w10, w11, a.z, b.z, c.z, d.z);
+            const float s3 = blend_f32(w00, w01, w10, w11, a.w, b.w, c.w, d.w);
+            const float h0 = to_tf32(s0), h1 = to_tf32(s1), h2 = to_tf32(s2), h3 = to_tf32(s3);
+            sts128(a_s + o, __float_as_uint(h0), __float_as_uint(h1), __float_as_uint(h2), __float_as_uint(h3));
+            sts128(a_s + kTileM * 128 + o, __float_as_uint(s0 - h0), __float_as_uint(s1 - h1),
+                   __float_as_uint(s2 - h2), __float_as_uint(s3 - h3));
+        } else {
+            T* tag = nullptr;
+            sts128(a_s + o, blend(w.z, w.w, a.x, b.x, c.x, d.x, tag), blend(w.z, w.w, a.y, b.y, c.y, d.y, tag),
+                   blend(w.z, w.w, a.z, b.z, c.z, d.z, tag), blend(w.z, w.w, a.w, b.w, c.w, d.w, tag));
+        }
+    }
 }
 
 template <int DT>
 __global__ void __launch_bounds__(kFusedThreads, 1)
-    fused_kernel(const __grid_constant__ CUtensorMap tmap, const FusedParams prm) {
+    fused_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap omap,
+                 const FusedParams prm) {
     using T = typename Elem<DT>::T;
     constexpr bool kF32Path = (DT == kF32);
     const Plan& pl = prm.pl;
@@ -191,37 +425,48 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     const uint32_t a_bytes = static_cast<uint32_t>(pl.a_bytes);
     const uint32_t b_bytes = static_cast<uint32_t>(pl.b_bytes);
     const uint32_t a0 = sbase;
-    const uint32_t b0 = sbase + S * a_bytes;
-    const uint32_t d0 = b0 + S * b_bytes;
-    const uint32_t bar0 = d0 + static_cast<uint32_t>(pl.desc_bytes);
+    const uint32_t b0 = a0 + S * a_bytes;
+    const uint32_t d0 = b0 + S * b_bytes;  // descriptor ring, 2 slots
+    const uint32_t dslot = static_cast<uint32_t>(pl.desc_slot_bytes);
+    const uint32_t e0s = d0 + 2 * dslot;  // epilogue staging (TMA-store path)
+    const uint32_t bar0 = e0s + static_cast<uint32_t>(pl.epi_bytes);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto tma_bar = [&](int s) { return bar0 + 8u * (S + s); };
     auto empty_bar = [&](int s) { return bar0 + 8u * (2 * S + s); };
-    const uint32_t acc_bar = bar0 + 8u * (3 * S);
-    const uint32_t slot_off = (bar0 - sbase) + 8u * (3 * S + 1);
+    const uint32_t xb = bar0 + 8u * (3 * S);
+    auto accf_bar = [&](int b) { return xb + 8u * b; };
+    auto acce_bar = [&](int b) { return xb + 16u + 8u * b; };
+    auto dfull_bar = [&](int b) { return xb + 32u + 8u * b; };
+    auto dempty_bar = [&](int b) { return xb + 48u + 8u * b; };
+    const uint32_t drain_bar = xb + 64u;
+    const uint32_t slot_off = (xb - sbase) + 72u;
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + slot_off);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + slot_off + 4);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int64_t m0 = static_cast<int64_t>(blockIdx.x) * kTileM;
-    const int32_t nt = blockIdx.y;
-    const int32_t g = blockIdx.z;
-    const int32_t ncol0 = nt * pl.nsub * pl.BNs;  // first output channel (within the group) of this tile
     const int32_t KT = pl.KT;
+    const int64_t first_tile = blockIdx.x;
+    const int64_t tile_step = gridDim.x;
 
-    if (warp == 0 && lane == 0) {
+    if (warp == kWarpTma && lane == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(full_bar(s), kGatherWarps);
+            mbar_init(full_bar(s), kGatherWarps / pl.kgroups);
             mbar_init(tma_bar(s), 1);
             mbar_init(empty_bar(s), 1);
         }
-        mbar_init(acc_bar, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf_bar(b), 1);
+            mbar_init(acce_bar(b), kEpiWarps);
+            mbar_init(dfull_bar(b), 1);
+            mbar_init(dempty_bar(b), kGatherWarps);
+        }
+        mbar_init(drain_bar, 1);
         *abort_flag = 0;
         fence_mbarrier_init();
         tma_prefetch_desc(&tmap);
     }
-    if (warp == 1) {
+    if (warp == kWarpMma) {
         tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), static_cast<uint32_t>(pl.tmem_cols));
         tmem_relinquish();
     }
@@ -230,213 +475,305 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    if (warp == 0) {
+    // Register split per warpgroup (launch: 128 per thread x 512 threads; the
+    // host refuses to launch a build whose register count is not exactly 128):
+    // TMA/MMA 80, gather 2 x 176, epilogue 80 -> 512 x 128 in total. Each
+    // warpgroup's branch starts with its own setmaxnreg, so the compiler
+    // allocates each role's code within that role's budget.
+    const int wg = warp >> 2;
+    if (wg == 0) {
+    setmaxnreg_dec<kRegsCtrl>();
+    if (warp == kWarpTma) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            const int32_t row0 = g * pl.Og + ncol0;
             const uint32_t sub_bytes = static_cast<uint32_t>(pl.BNs) * 128u;
             const uint32_t half_bytes = sub_bytes * pl.nsub;
-            int32_t issued = 0;
-            for (int32_t kt = 0; kt < KT; ++kt) {
-                const int s = kt % S;
-                const uint32_t ph = (kt / S) & 1;
-                if (!mbar_wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, prm.status, kSiteTmaEmpty)) break;
-                mbar_arrive_expect_tx(tma_bar(s), b_bytes);
-                const uint32_t dst = b0 + s * b_bytes;
+            const uint8_t* dglob = static_cast<const uint8_t*>(prm.desc);
+            const uint32_t dsz = static_cast<uint32_t>(pl.desc_size);
+            // descriptor groups are copied up to one group ahead of the k-tiles
+            Cursor dc;  // first k-tile of the next group to copy
+            cursor_init(pl, dc, first_tile);
+            Cursor kc;  // next weight k-tile to load
+            cursor_init(pl, kc, first_tile);
+            bool ok = true;
+            uint32_t s = 0;
+            while (kc.live && ok) {
+                while (dc.live && dc.gr <= kc.gr + 1) {
+                    const int slot = dc.gr & 1;
+                    if (!mbar_wait_bounded(dempty_bar(slot), ((dc.gr >> 1) & 1) ^ 1u, abort_flag, prm.status,
+                                           kSiteTmaEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    const int64_t unit = static_cast<int64_t>(dc.g) * pl.Ug + dc.ul;
+                    const int64_t gd = (unit * pl.U) / pl.Cd;
+                    const uint32_t bytes = static_cast<uint32_t>(dc.ntbg) * kTileM * dsz;
+                    const uint8_t* src =
+                        dglob + ((dc.mt * pl.dg + gd) * pl.K + static_cast<int64_t>(dc.b) * kTapBlock) * kTileM * dsz;
+                    mbar_arrive_expect_tx(dfull_bar(slot), bytes);
+                    bulk_load(d0 + slot * dslot, src, bytes, dfull_bar(slot));
+                    cursor_next_group(pl, dc, tile_step);
+                }
+                if (!ok) break;
+                const int st = s % S;
+                if (!mbar_wait_bounded(empty_bar(st), ((s / S) & 1) ^ 1u, abort_flag, prm.status, kSiteTmaEmpty)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(tma_bar(st), b_bytes);
+                const uint32_t dst = b0 + st * b_bytes;
+                const int32_t row0 = kc.g * pl.Og + kc.nt * pl.acc_cols;
 #pragma unroll 1
                 for (int h = 0; h < (kF32Path ? 2 : 1); ++h)
 #pragma unroll 1
                     for (int j = 0; j < pl.nsub; ++j)
-                        tma_load_2d(dst + h * half_bytes + j * sub_bytes, &tmap, kt * pl.BKc,
-                                    row0 + h * static_cast<int32_t>(pl.Cout) + j * pl.BNs, tma_bar(s));
-                issued = kt + 1;
+                        tma_load_2d(dst + h * half_bytes + j * sub_bytes, &tmap, kc.kt * pl.BKc,
+                                    row0 + h * static_cast<int32_t>(pl.Cout) + j * pl.BNs, tma_bar(st));
+                ++s;
+                cursor_advance(pl, kc, tile_step);
             }
-            if (*abort_flag) {
-                // Let the copies already issued land before the CTA exits.
-                const int32_t first = issued > S ? issued - S : 0;
-                for (int32_t kt = first; kt < issued; ++kt) {
-                    volatile int never = 0;
-                    mbar_wait_bounded(tma_bar(kt % S), (kt / S) & 1, &never, prm.status, kSiteDrain, 100000000ull);
-                }
+            if (!ok) {
+                // let the copies already issued land before the CTA exits
+                const uint32_t first = s > static_cast<uint32_t>(S) ? s - S : 0;
+                volatile int never = 0;
+                for (uint32_t q = first; q < s; ++q)
+                    mbar_wait_bounded(tma_bar(q % S), (q / S) & 1, &never, prm.status, kSiteDrain, 200000000ull);
+                const uint32_t gfirst = dc.gr > 2u ? dc.gr - 2u : 0u;
+                for (uint32_t q = gfirst; q < dc.gr; ++q)
+                    mbar_wait_bounded(dfull_bar(q & 1), (q >> 1) & 1, &never, prm.status, kSiteDrain, 200000000ull);
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == kWarpMma) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t idesc = make_idesc(Elem<DT>::fmt, kTileM, static_cast<uint32_t>(pl.BNs));
             const uint32_t sub_bytes = static_cast<uint32_t>(pl.BNs) * 128u;
             const uint32_t half_bytes = sub_bytes * pl.nsub;
-            for (int32_t kt = 0; kt < KT; ++kt) {
-                const int s = kt % S;
-                const uint32_t ph = (kt / S) & 1;
-                if (!mbar_wait_bounded(full_bar(s), ph, abort_flag, prm.status, kSiteMmaFull)) break;
-                if (!mbar_wait_bounded(tma_bar(s), ph, abort_flag, prm.status, kSiteMmaTma)) break;
+            uint32_t s = 0, i = 0;
+            bool ok = true;
+            for (int64_t t = first_tile; t < pl.tiles_total && ok; t += tile_step, ++i) {
+                const int ab = static_cast<int>(i % pl.nacc);
+                const uint32_t use = i / pl.nacc;
+                if (!mbar_wait_bounded(acce_bar(ab), (use & 1) ^ 1u, abort_flag, prm.status, kSiteMmaFull)) break;
                 tc_fence_after();
-                const uint32_t a_s = a0 + s * a_bytes;
-                const uint32_t b_s = b0 + s * b_bytes;
+                const uint32_t dacc = tmem_base + static_cast<uint32_t>(ab * pl.acc_cols);
+                for (int32_t kt = 0; kt < KT; ++kt, ++s) {
+                    const int st = s % S;
+                    const uint32_t ph = (s / S) & 1;
+                    if (!mbar_wait_bounded(full_bar(st), ph, abort_flag, prm.status, kSiteMmaFull) ||
+                        !mbar_wait_bounded(tma_bar(st), ph, abort_flag, prm.status, kSiteMmaTma)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_s = a0 + st * a_bytes;
+                    const uint32_t b_s = b0 + st * b_bytes;
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {  // 4 MMA K-steps of 32 bytes per 128-byte k-tile
-                    const uint64_t adesc = smem_desc_sw128(a_s + kk * 32);
+                    for (int kk = 0; kk < 4; ++kk) {  // 4 MMA K-steps of 32 bytes per 128-byte k-tile
+                        const uint64_t adesc = smem_desc_sw128(a_s + kk * 32);
 #pragma unroll 1
-                    for (int j = 0; j < pl.nsub; ++j) {
-                        const uint32_t d = tmem_base + static_cast<uint32_t>(j * pl.BNs);
-                        const uint64_t bdesc = smem_desc_sw128(b_s + j * sub_bytes + kk * 32);
-                        const uint32_t accum = (kt > 0 || kk > 0) ? 1u : 0u;
-                        if constexpr (kF32Path) {
-                            const uint64_t adesc_lo = smem_desc_sw128(a_s + kTileM * 128 + kk * 32);
-                            const uint64_t bdesc_lo = smem_desc_sw128(b_s + half_bytes + j * sub_bytes + kk * 32);
-                            mma_tf32(d, adesc, bdesc, idesc, accum);
-                            mma_tf32(d, adesc, bdesc_lo, idesc, 1u);
-                            mma_tf32(d, adesc_lo, bdesc, idesc, 1u);
-                        } else {
-                            mma_f16(d, adesc, bdesc, idesc, accum);
+                        for (int j = 0; j < pl.nsub; ++j) {
+                            const uint32_t d = dacc + static_cast<uint32_t>(j * pl.BNs);
+                            const uint64_t bdesc = smem_desc_sw128(b_s + j * sub_bytes + kk * 32);
+                            const uint32_t accum = (kt > 0 || kk > 0) ? 1u : 0u;
+                            if constexpr (kF32Path) {
+                                const uint64_t adesc_lo = smem_desc_sw128(a_s + kTileM * 128 + kk * 32);
+                                const uint64_t bdesc_lo = smem_desc_sw128(b_s + half_bytes + j * sub_bytes + kk * 32);
+                                mma_tf32(d, adesc, bdesc, idesc, accum);
+                                mma_tf32(d, adesc, bdesc_lo, idesc, 1u);
+                                mma_tf32(d, adesc_lo, bdesc, idesc, 1u);
+                            } else {
+                                mma_f16(d, adesc, bdesc, idesc, accum);
+                            }
                         }
                     }
+                    mma_commit(empty_bar(st));
                 }
-                mma_commit(empty_bar(s));
+                mma_commit(accf_bar(ab));
             }
-            mma_commit(acc_bar);  // always: the epilogue waits on it
+            // every MMA issued by this thread completes before TMEM is released
+            mma_commit(drain_bar);
+            volatile int never = 0;
+            mbar_wait_bounded(drain_bar, 0, &never, prm.status, kSiteDrain, 200000000ull);
+        }
+    }
+    } else if (wg == 1 || wg == 2) {
+        setmaxnreg_inc<kRegsGather>();
+        // ------------------------------------------------------------ gather producers
+        // Two k-tiles in flight per warp: the corner loads of k-tile n+1 are issued
+        // before k-tile n is combined and stored, so one L2 round trip overlaps the
+        // previous k-tile's work instead of stalling every k-tile.
+        // k-tile-parallel gather: the 8 warps form G = pl.kgroups groups; group p
+        // produces every G-th k-tile of a tile, so G k-tiles are in production at
+        // once and a stage (stages are a multiple of G) always belongs to one
+        // group. Each of a group's 8/G warps handles 16*G rows as 2*G
+        // row-iterations of 8 rows, the corner loads running 2 row-iterations
+        // ahead of the weighted sums.
+        const int gw = warp - kWarpGather;
+        const int G = pl.kgroups;
+        const int wpg = kGatherWarps / G;  // warps per k-tile
+        const int pair = gw / wpg;
+        const int nits = 2 * G;            // row-iterations per warp and k-tile
+        GatherCtx<T> cx;
+        cx.lane = lane;
+        cx.q4 = lane & 3;     // lane's 32 bytes of the 128-byte row
+        cx.rsub = lane >> 2;  // row within a group of 8
+        cx.row0 = (gw % wpg) * 8 * nits;
+        cx.xt = static_cast<const T*>(prm.xt);
+        cx.c1 = pl.Cp;
+        cx.c2 = pl.W * pl.Cp;
+        cx.c3 = (pl.W + 1) * pl.Cp;
+        cx.dsz = static_cast<uint32_t>(pl.desc_size);
+        constexpr int kVec = 16 / sizeof(T);
+        const int32_t ngroups = pl.Ug * pl.ntb;
+        uint32_t gr = 0, tile_i = 0;
+        bool ok = true;
+        for (int64_t t = first_tile; t < pl.tiles_total && ok; t += tile_step, ++tile_i) {
+            const TileId id = decode_tile(pl, t);
+            int32_t q = 0;  // first k-tile (processing order) of the current group
+            for (int32_t gi = 0; gi < ngroups && ok; ++gi, ++gr) {
+                const int32_t ul = gi / pl.ntb;
+                const int32_t b = gi - ul * pl.ntb;
+                const int32_t ntbg = min(kTapBlock, pl.K - b * kTapBlock);
+                const int32_t nktg = ntbg * pl.nch;
+                const int slot = gr & 1;
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(dfull_bar(slot), (gr >> 1) & 1, abort_flag, prm.status,
+                                                               kSiteGatherEmpty))) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t dbase = d0 + slot * dslot;
+                const int64_t unit = static_cast<int64_t>(id.g) * pl.Ug + ul;
+                for (int32_t j = (pair - (q % G) + G) % G; j < nktg; j += G) {
+                    const int32_t ch = j / ntbg;
+                    const int32_t kb = j - ch * ntbg;
+                    const int64_t cb = unit * pl.UP + static_cast<int64_t>(ch) * pl.BKc + cx.q4 * 2 * kVec;
+                    const uint32_t step = tile_i * static_cast<uint32_t>(KT) + static_cast<uint32_t>(q + j);
+                    const int st = step % S;
+                    RowBuf rb[3];
+                    row_issue<T, kF32Path>(cx, dbase, kb, cb, 0, rb[0]);
+                    row_issue<T, kF32Path>(cx, dbase, kb, cb, 1, rb[1]);
+                    // the stage is free once the MMAs that read it completed (tcgen05.commit);
+                    // lane 0 polls, the warp follows it
+                    int got = 0;
+                    if (lane == 0)
+                        got = mbar_wait_bounded(empty_bar(st), ((step / S) & 1) ^ 1u, abort_flag, prm.status,
+                                                kSiteGatherEmpty);
+                    if (!__shfl_sync(0xffffffffu, got, 0)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t a_s = a0 + st * a_bytes;
+#pragma unroll
+                    for (int it = 0; it < 2 * 4; ++it) {
+                        if (it < nits) {
+                            if (it + 2 < nits) row_issue<T, kF32Path>(cx, dbase, kb, cb, it + 2, rb[(it + 2) % 3]);
+                            row_combine<T, kF32Path>(cx, a_s, it, rb[it % 3]);
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(full_bar(st));
+                }
+                q += nktg;
+                // every gather warp releases every descriptor group, used or not
+                __syncwarp();
+                if (lane == 0) mbar_arrive(dempty_bar(slot));
+            }
         }
     } else {
-        // ------------------------------------------------------------ producers
-        const int pw = warp - 2;
-        const uint32_t dc = d0 + static_cast<uint32_t>(pw) * (kRowsPerWarp * kTapBlock * kDescBytes);
-        const T* __restrict__ xt = static_cast<const T*>(prm.xt);
-        const T* __restrict__ offset = static_cast<const T*>(prm.offset);
-        const T* __restrict__ mask = static_cast<const T*>(prm.mask);
-        const int q = lane & 7;       // 16-byte column chunk of the 128-byte k-tile row
-        const int rsub = lane >> 3;   // row within a group of 4
-        const int64_t Cp = pl.Cp;
-        const int64_t coff[4] = {0, Cp, pl.W * Cp, (pl.W + 1) * Cp};
-        constexpr int kVec = 16 / sizeof(T);  // elements per 16-byte vector
-        bool ok = true;
-        for (int32_t kt = 0; kt < KT && ok; ++kt) {
-            const KTile t = decode_ktile(kt, pl.K, pl.nch);
-            const int32_t unit = g * pl.Ug + t.ul;  // global unit index
-            if (t.ch == 0 && t.kb == 0) {
-                // sample descriptors of this warp's 16 rows for the taps of block t.b
-                const int32_t gd = static_cast<int32_t>((static_cast<int64_t>(unit) * pl.U) / pl.Cd);
-                __syncwarp();
-                for (int e = lane; e < kRowsPerWarp * t.ntb; e += 32) {
-                    const int r = e % kRowsPerWarp;
-                    const int kb2 = e / kRowsPerWarp;
-                    make_desc<T>(pl, offset, mask, m0 + pw * kRowsPerWarp + r, t.b * kTapBlock + kb2, gd,
-                                 dc + static_cast<uint32_t>(kb2 * kRowsPerWarp + r) * kDescBytes);
-                }
-                __syncwarp();
-            }
-            const int s = kt % S;
-            const uint32_t ph = (kt / S) & 1;
-            // warp-uniform decision: every lane leaves together on a timeout
-            const bool got = mbar_wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, prm.status, kSiteGatherEmpty);
-            if (!__all_sync(0xffffffffu, got)) {
-                ok = false;
-                break;
-            }
-            const int64_t cbase = static_cast<int64_t>(unit) * pl.UP + static_cast<int64_t>(t.ch) * pl.BKc + q * kVec;
-            const uint32_t a_s = a0 + s * a_bytes;
-            uint4 v[4][4];
-            uint4 wv[4];
-#pragma unroll
-            for (int it = 0; it < 4; ++it) {
-                const int r = it * 4 + rsub;
-                const uint32_t da = dc + static_cast<uint32_t>(t.kb * kRowsPerWarp + r) * kDescBytes;
-                const uint4 dd = lds128(da);
-                wv[it] = lds128(da + 16);
-                const int64_t base = static_cast<int64_t>((static_cast<uint64_t>(dd.y) << 32) | dd.x);
-                const uint32_t fl = dd.z;
-                const uint4* src = reinterpret_cast<const uint4*>(xt + base + cbase);
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    v[it][c] = make_uint4(0u, 0u, 0u, 0u);
-                    if (fl & (1u << c)) v[it][c] = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(src) + coff[c]));
-                }
-            }
-#pragma unroll
-            for (int it = 0; it < 4; ++it) {
-                const int row = pw * kRowsPerWarp + it * 4 + rsub;
-                const uint32_t dst = a_s + static_cast<uint32_t>(row) * 128u + (static_cast<uint32_t>(q ^ (row & 7)) << 4);
-                if constexpr (kF32Path) {
-                    const float w0 = __uint_as_float(wv[it].x), w1 = __uint_as_float(wv[it].y);
-                    const float w2 = __uint_as_float(wv[it].z), w3 = __uint_as_float(wv[it].w);
-                    float acc[4];
-                    const uint32_t* p0 = reinterpret_cast<const uint32_t*>(&v[it][0]);
-                    const uint32_t* p1 = reinterpret_cast<const uint32_t*>(&v[it][1]);
-                    const uint32_t* p2 = reinterpret_cast<const uint32_t*>(&v[it][2]);
-                    const uint32_t* p3 = reinterpret_cast<const uint32_t*>(&v[it][3]);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        float a = w0 * __uint_as_float(p0[e]);
-                        a = fmaf(w1, __uint_as_float(p1[e]), a);
-                        a = fmaf(w2, __uint_as_float(p2[e]), a);
-                        a = fmaf(w3, __uint_as_float(p3[e]), a);
-                        acc[e] = a;
-                    }
-                    float hi[4], lo[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        hi[e] = to_tf32(acc[e]);
-                        lo[e] = acc[e] - hi[e];
-                    }
-                    sts128(dst, __float_as_uint(hi[0]), __float_as_uint(hi[1]), __float_as_uint(hi[2]),
-                           __float_as_uint(hi[3]));
-                    sts128(dst + kTileM * 128, __float_as_uint(lo[0]), __float_as_uint(lo[1]), __float_as_uint(lo[2]),
-                           __float_as_uint(lo[3]));
-                } else {
-                    T* tag = nullptr;
-                    const uint32_t* p0 = reinterpret_cast<const uint32_t*>(&v[it][0]);
-                    const uint32_t* p1 = reinterpret_cast<const uint32_t*>(&v[it][1]);
-                    const uint32_t* p2 = reinterpret_cast<const uint32_t*>(&v[it][2]);
-                    const uint32_t* p3 = reinterpret_cast<const uint32_t*>(&v[it][3]);
-                    uint32_t o[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        o[e] = combine2(wv[it].x, wv[it].y, wv[it].z, wv[it].w, p0[e], p1[e], p2[e], p3[e], tag);
-                    sts128(dst, o[0], o[1], o[2], o[3]);
-                }
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(full_bar(s));
-        }
-
+        setmaxnreg_dec<kRegsEpi>();
         // ------------------------------------------------------------ epilogue
-        const bool acc_ok =
-            __all_sync(0xffffffffu, mbar_wait_bounded(acc_bar, 0, abort_flag, prm.status, kSiteEpilogue));
-        tc_fence_after();
-        if (acc_ok) {
-            const int quarter = warp & 3;
-            const int set = pw >> 2;  // two warps per TMEM lane quarter split the columns
-            const int row = quarter * 32 + lane;
-            const int64_t p = m0 + row;
-            const bool valid = p < pl.NP;
-            const int64_t n = valid ? p / pl.P : 0;
-            const int64_t hw = valid ? p - n * pl.P : 0;
-            T* __restrict__ out = static_cast<T*>(prm.out);
-            const T* __restrict__ bias = static_cast<const T*>(prm.bias);
-            const int32_t ncols = pl.nsub * pl.BNs;
-            for (int c16 = set; c16 * 16 < ncols; c16 += 2) {
-                float vals[16];
-                tmem_ld16(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(c16 * 16), vals);
-                if (valid) {
+        const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+        const int row = quarter * 32 + lane;
+        T* __restrict__ out = static_cast<T*>(prm.out);
+        const T* __restrict__ bias = static_cast<const T*>(prm.bias);
+        uint32_t i = 0;
+        for (int64_t t = first_tile; t < pl.tiles_total; t += tile_step, ++i) {
+            const TileId id = decode_tile(pl, t);
+            const int ab = static_cast<int>(i % pl.nacc);
+            const uint32_t use = i / pl.nacc;
+            if (!__all_sync(0xffffffffu,
+                            mbar_wait_bounded(accf_bar(ab), use & 1, abort_flag, prm.status, kSiteEpilogue)))
+                break;
+            tc_fence_after();
+            const Pixel px = tile_pixel(pl, id.mt, row);
+            const int64_t hw = px.ho * pl.Wo + px.wo;
+            const int32_t ncol0 = id.nt * pl.acc_cols;
+            const int64_t obase = (px.n * pl.Cout + static_cast<int64_t>(id.g) * pl.Og) * pl.P + hw;
+            const uint32_t tl = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                static_cast<uint32_t>(ab * pl.acc_cols);
+            if (pl.epi_tma) {
+                // 16-channel chunks: TMEM -> +bias -> staging [16 ch][2 rows][16 px] -> one TMA box
+                // store per chunk (rows/cols past the image are clipped by the tensor map)
+                const uint32_t stage0 = e0s + static_cast<uint32_t>(quarter) * (2u * 16u * 32u * sizeof(T));
+                const int64_t per_img = pl.tiles_x * pl.tiles_y;
+                const int64_t rem = id.mt - px.n * per_img;
+                const int64_t ty = rem / pl.tiles_x;
+                const int32_t gy = static_cast<int32_t>(ty * pl.TH + 2 * quarter);
+                const int32_t gx = static_cast<int32_t>((rem - ty * pl.tiles_x) * pl.TW);
+                int chunk = 0;
+                for (int c16 = 0; c16 < pl.acc_cols; c16 += 16) {
+                    float vals[16];
+                    tmem_ld16(tl + static_cast<uint32_t>(c16), vals);
+                    {
+                        const int32_t ol0 = ncol0 + c16;
+                        if (ol0 < pl.Og) {
+                            const uint32_t buf = stage0 + static_cast<uint32_t>(chunk & 1) * (16u * 32u * sizeof(T));
+                            if (lane == 0) bulk_wait_read<1>();  // the store issued two chunks ago has read buf
+                            __syncwarp();
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int32_t ol = ncol0 + c16 * 16 + e;
-                        if (ol < pl.Og) {
-                            const int64_t o = static_cast<int64_t>(g) * pl.Og + ol;
-                            float r = vals[e];
-                            if (bias) r += to_f(bias[o]);
-                            from_f(r, out + (n * pl.Cout + o) * pl.P + hw);
+                            for (int c = 0; c < 16; ++c) {
+                                float r = vals[c];
+                                if (bias) r += to_f(bias[static_cast<int64_t>(id.g) * pl.Og + ol0 + c]);
+                                T hv;
+                                from_f(r, &hv);
+                                const uint32_t a = buf + static_cast<uint32_t>((c * 32 + lane) * sizeof(T));
+                                if constexpr (sizeof(T) == 4) {
+                                    asm volatile("st.shared.b32 [%0], %1;" ::"r"(a), "r"(__float_as_uint(r)) : "memory");
+                                } else {
+                                    asm volatile("st.shared.b16 [%0], %1;" ::"r"(a), "h"(*reinterpret_cast<uint16_t*>(&hv))
+                                                 : "memory");
+                                }
+                            }
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                tma_store_4d(&omap, buf, gx, gy, static_cast<int32_t>(id.g * pl.Og + ol0),
+                                             static_cast<int32_t>(px.n));
+                                bulk_commit();
+                            }
+                            ++chunk;
+                        }
+                    }
+                }
+            } else {
+                for (int c16 = 0; c16 < pl.acc_cols; c16 += 16) {
+                    float vals[16];
+                    tmem_ld16(tl + static_cast<uint32_t>(c16), vals);
+                    if (px.valid) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int32_t ol = ncol0 + c16 + e;
+                            if (ol < pl.Og) {
+                                float r = vals[e];
+                                if (bias) r += to_f(bias[static_cast<int64_t>(id.g) * pl.Og + ol]);
+                                from_f(r, out + obase + static_cast<int64_t>(ol) * pl.P);
+                            }
                         }
                     }
                 }
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acce_bar(ab));
         }
     }
 
+    if (warp >= kWarpEpi && lane == 0 && pl.epi_tma) bulk_wait_read<0>();
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kWarpMma) {
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem_base, static_cast<uint32_t>(pl.tmem_cols));
@@ -444,7 +781,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
 }
 
 // Tiny kernel for the bounded-wait self-test: waits on a barrier nothing signals.
-__global__ void wait_selftest_kernel(uint32_t* status, uint64_t limit_ns) {
+__global__ void wait_selftest_kernel(uint32_t* status, uint64_t limit_cycles) {
     __shared__ __align__(8) uint64_t bar;
     __shared__ int abort_flag;
     if (threadIdx.x == 0) {
@@ -455,10 +792,9 @@ __global__ void wait_selftest_kernel(uint32_t* status, uint64_t limit_ns) {
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-        const bool ok = mbar_wait_bounded(smem_u32(&bar), 0, &abort_flag, status, kSiteSelftest, limit_ns);
+        const bool ok = mbar_wait_bounded(smem_u32(&bar), 0, &abort_flag, status, kSiteSelftest, limit_cycles);
         if (ok) atomicOr(status, 1u << 31);  // the wait completed although nothing arrived
-        // complete the phase so that no barrier is left pending at exit
-        mbar_arrive(smem_u32(&bar));
+        mbar_arrive(smem_u32(&bar));        // complete the phase before exit
     }
     __syncthreads();
 }
@@ -478,16 +814,14 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
 }
 
 template <int DT>
-cudaError_t launch_fused_t(const Plan& pl, const void* offset, const void* mask, const void* bias, void* out, void* ws,
-                           cudaStream_t st) {
+cudaError_t launch_fused_t(const Plan& pl, const void* bias, void* out, void* ws, cudaStream_t st) {
     using T = typename Elem<DT>::T;
     uint8_t* base = static_cast<uint8_t*>(ws);
     const T* wp = reinterpret_cast<const T*>(base + pl.off_wp);
     auto encode = get_encode_fn();
     if (!encode) return cudaErrorNotSupported;
     CUtensorMap tmap;
-    const cuuint64_t rows = static_cast<cuuint64_t>(pl.wp_rows);
-    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(pl.KP), rows};
+    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(pl.KP), static_cast<cuuint64_t>(pl.wp_rows)};
     const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(pl.KP) * sizeof(T)};
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(pl.BKc), static_cast<cuuint32_t>(pl.BNs)};
     const cuuint32_t estride[2] = {1, 1};
@@ -495,43 +829,84 @@ cudaError_t launch_fused_t(const Plan& pl, const void* offset, const void* mask,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    CUtensorMap omap;
+    std::memset(&omap, 0, sizeof(omap));
+    if (pl.epi_tma) {
+        const cuuint64_t odim[4] = {static_cast<cuuint64_t>(pl.Wo), static_cast<cuuint64_t>(pl.Ho),
+                                    static_cast<cuuint64_t>(pl.Cout), static_cast<cuuint64_t>(pl.N)};
+        const cuuint64_t ostr[3] = {static_cast<cuuint64_t>(pl.Wo) * sizeof(T),
+                                    static_cast<cuuint64_t>(pl.P) * sizeof(T),
+                                    static_cast<cuuint64_t>(pl.P) * static_cast<cuuint64_t>(pl.Cout) * sizeof(T)};
+        const cuuint32_t obox[4] = {16, 2, 16, 1};
+        const cuuint32_t oes[4] = {1, 1, 1, 1};
+        r = encode(&omap, Elem<DT>::tma, 4, out, odim, ostr, obox, oes, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
     FusedParams prm;
     prm.xt = base + pl.off_xt;
-    prm.offset = offset;
-    prm.mask = mask;
+    prm.desc = base + pl.off_desc;
     prm.bias = bias;
     prm.out = out;
     prm.status = reinterpret_cast<uint32_t*>(base);
     prm.pl = pl;
-    dim3 grid(static_cast<unsigned>(pl.mtiles), static_cast<unsigned>(pl.ntiles_n), static_cast<unsigned>(pl.group));
-    fused_kernel<DT><<<grid, kFusedThreads, pl.smem_bytes, st>>>(tmap, prm);
+    fused_kernel<DT><<<static_cast<unsigned>(pl.grid), kFusedThreads, pl.smem_bytes, st>>>(tmap, omap, prm);
     return cudaGetLastError();
 }
 
 }  // namespace
 
+// Sets the dynamic shared memory limit and checks that the build launches
+// with exactly kRegsLaunch registers per thread: the warpgroup register
+// split (setmaxnreg) is sized for that pool, so any other count is refused.
+template <int DT>
+static cudaError_t prepare_one(int smem_bytes) {
+    cudaError_t e = cudaFuncSetAttribute(fused_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    if (e != cudaSuccess) return e;
+    cudaFuncAttributes attr;
+    e = cudaFuncGetAttributes(&attr, fused_kernel<DT>);
+    if (e != cudaSuccess) return e;
+    return attr.numRegs == kRegsLaunch ? cudaSuccess : cudaErrorInvalidDeviceFunction;
+}
+
 cudaError_t prepare_fused_attributes(int dtype, int smem_bytes) {
     switch (dtype) {
-        case kF32:
-            return cudaFuncSetAttribute(fused_kernel<kF32>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
-        case kF16:
-            return cudaFuncSetAttribute(fused_kernel<kF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
-        default:
-            return cudaFuncSetAttribute(fused_kernel<kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+        case kF32: return prepare_one<kF32>(smem_bytes);
+        case kF16: return prepare_one<kF16>(smem_bytes);
+        default: return prepare_one<kBF16>(smem_bytes);
     }
 }
 
-cudaError_t launch_fused(const Plan& pl, const void* offset, const void* mask, const void* bias, void* out, void* ws,
-                         cudaStream_t st) {
+cudaError_t launch_fused(const Plan& pl, const void* bias, void* out, void* ws, cudaStream_t st) {
     switch (pl.dtype) {
-        case kF32: return launch_fused_t<kF32>(pl, offset, mask, bias, out, ws, st);
-        case kF16: return launch_fused_t<kF16>(pl, offset, mask, bias, out, ws, st);
-        default: return launch_fused_t<kBF16>(pl, offset, mask, bias, out, ws, st);
+        case kF32: return launch_fused_t<kF32>(pl, bias, out, ws, st);
+        case kF16: return launch_fused_t<kF16>(pl, bias, out, ws, st);
+        default: return launch_fused_t<kBF16>(pl, bias, out, ws, st);
     }
 }
 
-cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t st) {
-    wait_selftest_kernel<<<1, 32, 0, st>>>(status, limit_ns);
+cudaError_t launch_sample(const Plan& pl, const void* offset, const void* mask, void* ws, cudaStream_t st) {
+    uint8_t* desc = static_cast<uint8_t*>(ws) + pl.off_desc;
+    const dim3 grid(static_cast<unsigned>(pl.mtiles), static_cast<unsigned>(pl.dg));
+    switch (pl.dtype) {
+        case kF32:
+            sample_kernel<float><<<grid, kTileM, 0, st>>>(static_cast<const float*>(offset),
+                                                          static_cast<const float*>(mask), desc, pl);
+            break;
+        case kF16:
+            sample_kernel<__half><<<grid, kTileM, 0, st>>>(static_cast<const __half*>(offset),
+                                                           static_cast<const __half*>(mask), desc, pl);
+            break;
+        default:
+            sample_kernel<__nv_bfloat16><<<grid, kTileM, 0, st>>>(static_cast<const __nv_bfloat16*>(offset),
+                                                                  static_cast<const __nv_bfloat16*>(mask), desc, pl);
+            break;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_cycles, cudaStream_t st) {
+    wait_selftest_kernel<<<1, 32, 0, st>>>(status, limit_cycles);
     return cudaGetLastError();
 }
 

@@ -7,12 +7,23 @@
 
 namespace mdcn {
 
-constexpr int kTileM = 128;       // output pixels per CTA tile (MMA M)
-constexpr int kTapBlock = 9;      // taps whose sample descriptors are cached at once
-constexpr int kGatherWarps = 8;   // producer warps (16 tile rows each); also the epilogue warps
-constexpr int kRowsPerWarp = kTileM / kGatherWarps;
-constexpr int kFusedThreads = 64 + 32 * kGatherWarps;  // warp 0 TMA, warp 1 MMA, 8 gather/epilogue warps
-constexpr int kDescBytes = 32;    // one cached sample descriptor
+constexpr int kTileM = 128;       // output pixels per tile (MMA M)
+constexpr int kTapBlock = 9;      // taps whose sample descriptors form one descriptor group
+// Warp roles of the fused kernel (16 warps):
+constexpr int kWarpTma = 0;       // TMA loads of weight k-tiles
+constexpr int kWarpMma = 1;       // TMEM allocation; lane 0 issues tcgen05.mma
+constexpr int kWarpGather = 4;    // 8 warps: gather + modulate into A stages
+constexpr int kGatherWarps = 8;
+constexpr int kWarpEpi = 12;      // 4 warps: TMEM -> +bias -> NCHW
+constexpr int kEpiWarps = 4;
+constexpr int kFusedThreads = 32 * 16;
+// Registers per thread: at launch, and per warpgroup after setmaxnreg
+// (warpgroup 0 = TMA/MMA, 1-2 = gather, 3 = epilogue).
+constexpr int kRegsLaunch = 128;
+constexpr int kRegsCtrl = 80;
+constexpr int kRegsGather = 176;
+constexpr int kRegsEpi = 80;
+static_assert(kRegsCtrl + 2 * kRegsGather + kRegsEpi == 4 * kRegsLaunch, "warpgroup register split must fit");
 constexpr int kSmemLimit = 227 * 1024;
 constexpr size_t kStatusBytes = 256;  // workspace header holding the device status word
 
@@ -43,19 +54,30 @@ struct Plan {
     int64_t wp_rows;         // packed weight rows: Cout (x2 for f32 hi/lo), at least BNs, zero-padded
 
     // ---- tiling of the fused kernel
+    int32_t tile_mode;       // 0: 128 consecutive pixels of N*Ho*Wo; 1: TH x TW block of one image
+    int32_t TH, TW;          // 2-D tile shape (TH*TW = 128)
+    int64_t tiles_x, tiles_y;
+    int64_t mtiles;          // pixel tiles
+    int64_t tiles_total;     // mtiles * ntiles_n * group
     int32_t BNs;             // output channels per MMA (multiple of 16, <= 256)
     int32_t nsub;            // MMAs per k-step along N (1 or 2)
     int32_t ntiles_n;        // N tiles per group
-    int64_t mtiles;          // ceil(NP / kTileM)
-    int32_t stages;
+    int32_t acc_cols;        // TMEM columns of one accumulator = nsub * BNs
+    int32_t nacc;            // accumulators in TMEM (2: epilogue overlaps the next tile)
     int32_t tmem_cols;
+    int32_t stages;          // 2, 4, 6 or 8
+    int32_t kgroups;         // k-tiles produced concurrently by the gather warps (2 or 4; divides stages)
     int32_t a_bytes;         // one A stage (both tf32 halves for f32)
     int32_t b_bytes;         // one B stage
-    int32_t desc_bytes;      // sample-descriptor cache
+    int32_t desc_size;       // bytes per sample descriptor (16, or 32 for f32)
+    int32_t desc_slot_bytes; // one descriptor group: kTileM rows x kTapBlock taps
+    int32_t epi_tma;         // 1: epilogue writes 16-channel boxes with TMA stores (2-D tiles)
+    int32_t epi_bytes;       // shared-memory staging of the TMA-store epilogue
     int32_t smem_bytes;      // dynamic shared memory of the fused kernel
+    int32_t grid;            // persistent CTAs
 
     // ---- workspace layout (byte offsets)
-    size_t off_xt, off_wp, ws_bytes;
+    size_t off_xt, off_wp, off_desc, ws_bytes;
 };
 
 }  // namespace mdcn

@@ -25,41 +25,41 @@ template <>
 __device__ __forceinline__ __nv_bfloat16 zero_of<__nv_bfloat16>() { return __float2bfloat16_rn(0.0f); }
 
 // One block transposes a 32 (w) x 32 (padded channel) tile of one (n, h) row;
-// block (0, 0) also clears the device status word.
+// the 32 channels lie inside one unit (UP is a multiple of 32), so the source
+// channel needs no per-element division. Block (0, 0) also clears the device
+// status word. Grid: x = (n*H + h) * wtiles + w tile, y = padded-channel tile.
 template <typename T>
 __global__ void __launch_bounds__(256) nhwc_pad_kernel(const T* __restrict__ x, T* __restrict__ xt,
-                                                       uint32_t* __restrict__ status, int64_t Cin, int64_t H,
-                                                       int64_t W, int64_t Cp, int32_t U, int32_t UP, int64_t wtiles) {
+                                                       uint32_t* __restrict__ status, int64_t Cin, int64_t HW,
+                                                       int32_t W, int64_t Cp, int32_t U, int32_t UP,
+                                                       int32_t wtiles) {
     __shared__ T tile[32][33];
     if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0 && threadIdx.y == 0) *status = 0u;
-    const int64_t bx = blockIdx.x;
-    const int64_t nh = bx / wtiles;          // n*H + h
-    const int64_t w0 = (bx - nh * wtiles) * 32;
-    const int64_t n = nh / H;
-    const int64_t h = nh - n * H;
+    const uint32_t bx = blockIdx.x;
+    const uint32_t nh = bx / static_cast<uint32_t>(wtiles);  // n*H + h
+    const int32_t w0 = static_cast<int32_t>(bx - nh * static_cast<uint32_t>(wtiles)) * 32;
     const int64_t pc0 = static_cast<int64_t>(blockIdx.y) * 32;
+    const int64_t unit = pc0 / UP;
+    const int32_t within0 = static_cast<int32_t>(pc0 - unit * UP);
     const int tx = threadIdx.x, ty = threadIdx.y;
+    // x[n][c][h][w] = x + (n*Cin + c)*H*W + h*W + w; with nh = n*H + h:
+    const int64_t n = nh / static_cast<uint64_t>(HW / W);
+    const int64_t h = nh - n * (HW / W);
+    const T* src = x + n * Cin * HW + h * W + w0 + tx;
+    const bool wok = w0 + tx < W;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const int64_t pc = pc0 + ty + 8 * i;
-        const int64_t w = w0 + tx;
+        const int32_t within = within0 + ty + 8 * i;
         T v = zero_of<T>();
-        if (pc < Cp && w < W) {
-            const int64_t unit = pc / UP;
-            const int64_t within = pc - unit * UP;
-            if (within < U) {
-                const int64_t c = unit * U + within;
-                v = x[((n * Cin + c) * H + h) * W + w];
-            }
-        }
+        if (wok && within < U) v = src[(unit * U + within) * HW];
         tile[ty + 8 * i][tx] = v;
     }
     __syncthreads();
+    T* dst = xt + static_cast<int64_t>(nh) * W * Cp + pc0 + tx;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const int64_t w = w0 + ty + 8 * i;
-        const int64_t pc = pc0 + tx;
-        if (w < W && pc < Cp) xt[(nh * W + w) * Cp + pc] = tile[tx][ty + 8 * i];
+        const int32_t w = w0 + ty + 8 * i;
+        if (w < W && pc0 + tx < Cp) dst[static_cast<int64_t>(w) * Cp] = tile[tx][ty + 8 * i];
     }
 }
 
@@ -73,23 +73,23 @@ template <>
 __device__ __forceinline__ float load_f<__nv_bfloat16>(const __nv_bfloat16* p) { return __bfloat162float(*p); }
 
 // Packs the weight into the fused kernel's K order (zero pad included).
+// Grid: x over k-tiles of one row (blockDim.x = BKc lanes per k-tile, several
+// k-tiles per block), y over rows (looping when rows exceed the grid).
 template <typename T>
 __global__ void __launch_bounds__(256) pack_weight_kernel(const T* __restrict__ weight, T* __restrict__ wp, Plan pl) {
     const int64_t rows = pl.Cout * (pl.dtype == kF32 ? 2 : 1);
-    const int64_t total = pl.wp_rows * pl.KP;
-    for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
-         e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t r = e / pl.KP;
-        const int64_t kk = e - r * pl.KP;
-        const int64_t o = r % pl.Cout;
-        const bool lo_half = r >= pl.Cout;
-        const int32_t kt = static_cast<int32_t>(kk / pl.BKc);
-        const int32_t ci = static_cast<int32_t>(kk - static_cast<int64_t>(kt) * pl.BKc);
-        const KTile t = decode_ktile(kt, pl.K, pl.nch);
-        const int32_t within = t.ch * pl.BKc + ci;  // channel within the unit
+    const int32_t ktiles_per_block = 256 / pl.BKc;
+    const int32_t kt = blockIdx.x * ktiles_per_block + static_cast<int32_t>(threadIdx.x) / pl.BKc;
+    const int32_t ci = static_cast<int32_t>(threadIdx.x) % pl.BKc;
+    if (kt >= pl.KT) return;
+    const KTile t = decode_ktile(kt, pl.K, pl.nch);
+    const int32_t within = t.ch * pl.BKc + ci;  // channel within the unit
+    const int64_t cl = static_cast<int64_t>(t.ul) * pl.U + within;  // channel within the group
+    for (int64_t r = blockIdx.y; r < pl.wp_rows; r += gridDim.y) {
         T v = zero_of<T>();
         if (within < pl.U && r < rows) {
-            const int64_t cl = static_cast<int64_t>(t.ul) * pl.U + within;  // channel within the group
+            const bool lo_half = r >= pl.Cout;
+            const int64_t o = lo_half ? r - pl.Cout : r;
             const T* src = weight + (o * pl.Cg + cl) * pl.K + t.tap;
             if constexpr (sizeof(T) == 4) {
                 const float f = load_f<T>(src);
@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(256) pack_weight_kernel(const T* __restrict__ 
                 v = *src;
             }
         }
-        wp[e] = v;
+        wp[r * pl.KP + static_cast<int64_t>(kt) * pl.BKc + ci] = v;
     }
 }
 
@@ -112,8 +112,9 @@ static cudaError_t prep_input_t(const Plan& pl, const void* x, void* ws, cudaStr
     T* xt = reinterpret_cast<T*>(base + pl.off_xt);
     const int64_t wtiles = (pl.W + 31) / 32;
     dim3 grid(static_cast<unsigned>(pl.N * pl.H * wtiles), static_cast<unsigned>((pl.Cp + 31) / 32));
-    nhwc_pad_kernel<T><<<grid, dim3(32, 8), 0, st>>>(static_cast<const T*>(x), xt, status, pl.Cin, pl.H, pl.W, pl.Cp,
-                                                     pl.U, pl.UP, wtiles);
+    nhwc_pad_kernel<T><<<grid, dim3(32, 8), 0, st>>>(static_cast<const T*>(x), xt, status, pl.Cin, pl.H * pl.W,
+                                                     static_cast<int32_t>(pl.W), pl.Cp, pl.U, pl.UP,
+                                                     static_cast<int32_t>(wtiles));
     return cudaGetLastError();
 }
 
@@ -121,10 +122,10 @@ template <typename T>
 static cudaError_t pack_weight_t(const Plan& pl, const void* weight, void* ws, cudaStream_t st) {
     uint8_t* base = static_cast<uint8_t*>(ws);
     T* wp = reinterpret_cast<T*>(base + pl.off_wp);
-    const int64_t total = pl.wp_rows * pl.KP;
-    int64_t blocks = (total + 255) / 256;
-    if (blocks > 4096) blocks = 4096;
-    pack_weight_kernel<T><<<static_cast<unsigned>(blocks), 256, 0, st>>>(static_cast<const T*>(weight), wp, pl);
+    const int32_t ktiles_per_block = 256 / pl.BKc;
+    const unsigned gx = static_cast<unsigned>((pl.KT + ktiles_per_block - 1) / ktiles_per_block);
+    const unsigned gy = static_cast<unsigned>(pl.wp_rows < 65535 ? pl.wp_rows : 65535);
+    pack_weight_kernel<T><<<dim3(gx, gy), 256, 0, st>>>(static_cast<const T*>(weight), wp, pl);
     return cudaGetLastError();
 }
 

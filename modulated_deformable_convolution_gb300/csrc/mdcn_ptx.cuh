@@ -18,9 +18,12 @@ constexpr uint32_t kSiteEpilogue = 1u << 12;
 constexpr uint32_t kSiteDrain = 1u << 13;
 constexpr uint32_t kSiteSelftest = 1u << 14;
 
-// Wall-clock limit of every pipeline wait in the fused kernel. A correct
-// launch never waits more than microseconds; the limit only bounds a bug.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+// Limit of every pipeline wait in the fused kernel, in SM clock cycles
+// (4e9 cycles: about 2 s at the 2.07 GHz maximum clock, longer at lower
+// clocks). A correct launch never waits more than microseconds; the limit
+// only bounds a bug. The cycle counter is read every 64 polls, so a wait
+// that completes is noticed after one mbarrier test, not after a timer read.
+constexpr uint64_t kWaitLimitCycles = 4000000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -63,22 +66,36 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for the phase of the given parity to complete, for at most
-// kWaitLimitNs (or until another role of the CTA raised *abort). On giving
-// up it records the site in the status word, raises *abort and returns false.
+// limit_cycles SM cycles (or until another role of the CTA raised *abort).
+// On giving up it records the site in the status word, raises *abort and
+// returns false.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort,
                                                   uint32_t* status, uint32_t site,
-                                                  uint64_t limit_ns = kWaitLimitNs) {
+                                                  uint64_t limit_cycles = kWaitLimitCycles) {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (true) {
+    const uint64_t t0 = clock64();
+    for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (*abort) return false;
-        if (globaltimer_ns() - t0 > limit_ns) {
-            *abort = 1;
-            if (status) atomicOr(status, kStatusTimeout | site);
-            return false;
+        if ((it & 63u) == 0) {
+            if (*abort) return false;
+            if (static_cast<uint64_t>(clock64()) - t0 > limit_cycles) {
+                *abort = 1;
+                if (status) atomicOr(status, kStatusTimeout | site);
+                return false;
+            }
         }
     }
+}
+
+// ---------------------------------------------------------------- registers
+// Per-warpgroup register count (all warps of the warpgroup execute it).
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // ---------------------------------------------------------------- fences
@@ -110,6 +127,36 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int3
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
         ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(bar)
         : "memory");
+}
+
+// Untiled bulk copy global -> shared (both 16-byte aligned, size a multiple
+// of 16); completion is signalled as transaction bytes on the mbarrier.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// 4-D tiled store of one box from shared memory (bulk-group completion);
+// elements outside the tensor are not written.
+__device__ __forceinline__ void tma_store_4d(const void* tmap, uint32_t src, int32_t c0, int32_t c1, int32_t c2,
+                                             int32_t c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4}], [%5];"
+        ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(src)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Waits until at most N committed bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 // ---------------------------------------------------------------- tcgen05
@@ -193,6 +240,43 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Up to 4 x (32 lanes x 16 columns) TMEM loads issued back to back, one wait:
+// v[16*k + c] = column (taddr.col + 16*k + c) of this thread's lane, k < n.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, int n, float (&v)[64]) {
+    uint32_t r[64];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        if (k < n) {
+            asm volatile(
+                "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+                "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+                : "=r"(r[16 * k + 0]), "=r"(r[16 * k + 1]), "=r"(r[16 * k + 2]), "=r"(r[16 * k + 3]),
+                  "=r"(r[16 * k + 4]), "=r"(r[16 * k + 5]), "=r"(r[16 * k + 6]), "=r"(r[16 * k + 7]),
+                  "=r"(r[16 * k + 8]), "=r"(r[16 * k + 9]), "=r"(r[16 * k + 10]), "=r"(r[16 * k + 11]),
+                  "=r"(r[16 * k + 12]), "=r"(r[16 * k + 13]), "=r"(r[16 * k + 14]), "=r"(r[16 * k + 15])
+                : "r"(taddr + 16u * k)
+                : "memory");
+        } else {
+#pragma unroll
+            for (int c = 0; c < 16; ++c) r[16 * k + c] = 0u;
+        }
+    }
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 256-bit read-only global load (32-byte aligned address).
+__device__ __forceinline__ void ldg256(const void* p, uint4& a, uint4& b) {
+    asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+                 : "l"(p));
+}
+
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
 }
 
 // Round-to-nearest (ties away) fp32 -> tf32, returned as an fp32 bit pattern

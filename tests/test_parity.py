@@ -30,10 +30,10 @@ def oracle_out(oracle_mod, case, inp, ho_range=None):
                               np64(inp["bias"]), ho_range=ho_range, **case.attrs())
 
 
-def gpu_out(case, inp, algo="fused", check_status=True):
+def gpu_out(case, inp, algo="fused", check_status=True, tuning=None):
     dev = torch.device("cuda", 0)
     d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
-    h = mdcn.Handle(**case.attrs())
+    h = mdcn.Handle(**case.attrs(), tuning=tuning)
     if algo == "fused":
         need = mdcn.mdcn_workspace_size(h, d["x"], d["offset"], d["mask"], d["weight"], d["bias"])
         ws = torch.empty(need, dtype=torch.uint8, device=dev)
@@ -111,6 +111,43 @@ def test_sweep_full_compare(oracle_mod, case):
     gpu = np64(gpu_out(case, inp))
     ref = oracle_out(oracle_mod, case, inp)
     compare(gpu, ref, case.dtype, case.name)
+
+
+TUNED = [
+    # 2-D tiles with ragged right edge, TMA-store epilogue (Wo*2 bytes % 16 == 0, Og % 16 == 0)
+    (Case("f16_2d_ragged_tma", "f16", N=2, Cin=64, Cout=32, H=40, W=40, bias=True, seed=40,
+          offset_dist=("normal", 2.0)), dict(tile_mode=1, stages=4)),
+    # grouped, 2-D tiles, TMA-store epilogue with a group channel offset, bf16
+    (Case("bf16_2d_g2_tma", "bf16", N=1, Cin=64, Cout=96, H=24, W=32, group=2, deformable_group=2, bias=True,
+          seed=41), dict(tile_mode=1, stages=2)),
+    # ragged bottom edge (Ho = 20 not a multiple of 8), fp32, 2-D tiles, TMA-store epilogue
+    (Case("f32_2d_bottom_tma", "f32", N=1, Cin=32, Cout=16, H=20, W=16, bias=False, seed=42), dict(tile_mode=1)),
+    # 2-D tiles without the TMA epilogue (Og = 40 not a multiple of 16)
+    (Case("f16_2d_scalar_epi", "f16", N=1, Cin=32, Cout=40, H=16, W=32, bias=True, seed=43), dict(tile_mode=1)),
+    # linear tiles forced on a shape the planner would tile in 2-D, several CTAs per SM count capped
+    (Case("f16_linear_forced", "f16", N=2, Cin=64, Cout=64, H=16, W=16, bias=False, seed=44),
+     dict(tile_mode=0, stages=6, max_ctas=3)),
+    # Cout = 512 in one tile (two MMAs, one TMEM accumulator), 2-D tiles
+    (Case("f16_cout512_2d", "f16", N=1, Cin=64, Cout=512, H=16, W=16, deformable_group=2, bias=False, seed=45),
+     dict(tile_mode=1)),
+]
+
+
+@pytest.mark.parametrize("case,tuning", TUNED, ids=[c.name for c, _ in TUNED])
+def test_tuned_plans(oracle_mod, case, tuning):
+    inp = make_inputs(case)
+    gpu = np64(gpu_out(case, inp, tuning=tuning))
+    ref = oracle_out(oracle_mod, case, inp)
+    compare(gpu, ref, case.dtype, case.name)
+
+
+def test_tunings_agree_bitwise():
+    """Every plan choice computes the same sums in the same order."""
+    case = CONFIGS["neck_f16"]
+    inp = make_inputs(case)
+    ref = gpu_out(case, inp)
+    for tuning in (dict(tile_mode=0), dict(tile_mode=1, stages=2), dict(stages=4, max_ctas=40)):
+        assert torch.equal(gpu_out(case, inp, tuning=tuning), ref), tuning
 
 
 @pytest.mark.parametrize("case", [SWEEP[0], SWEEP[1], SWEEP[2], SWEEP[3]], ids=lambda c: c.name)
