@@ -209,8 +209,9 @@ mdcn_status make_plan(const mdcn_attrs& a, const mdcn_tuning& tuning, const mdcn
     p.grid = 0;  // set at launch from the SM count
 
     // workspace: [status 256 B][x channels-last][packed weight]
-    const int64_t wtiles = ceil_div(p.W, 32);
-    if (p.N * p.H * wtiles > kI31) return MDCN_ERR_UNSUPPORTED;
+    // channels-last conversion stages whole pixels in 40 KB of shared memory
+    if ((p.Cp + 16 / elem) * elem > 40 * 1024) return MDCN_ERR_UNSUPPORTED;
+    if (p.N * p.H * p.W > kI31) return MDCN_ERR_UNSUPPORTED;
     int64_t xt = p.N * p.H;
     if (!mul_ok(xt, p.W) || !mul_ok(xt, p.Cp) || !mul_ok(xt, elem)) return MDCN_ERR_UNSUPPORTED;
     int64_t rows = p.Cout * halves;
@@ -223,7 +224,7 @@ mdcn_status make_plan(const mdcn_attrs& a, const mdcn_tuning& tuning, const mdcn
     if (!mul_ok(dbytes, p.dg) || !mul_ok(dbytes, p.K) || !mul_ok(dbytes, mdcn::kTileM) ||
         !mul_ok(dbytes, p.desc_size))
         return MDCN_ERR_UNSUPPORTED;
-    if (p.mtiles > 2147483647 || p.dg > 65535) return MDCN_ERR_UNSUPPORTED;  // sampling grid
+    if (p.mtiles > 2147483647 || p.dg > 65535 || ceil_div(K, 3) > 65535) return MDCN_ERR_UNSUPPORTED;  // sampling grid
     p.off_xt = mdcn::kStatusBytes;
     p.off_wp = align256(p.off_xt + static_cast<size_t>(xt));
     p.off_desc = align256(p.off_wp + static_cast<size_t>(wpb));

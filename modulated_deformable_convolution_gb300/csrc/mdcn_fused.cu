@@ -166,17 +166,21 @@ __device__ __forceinline__ uint32_t blend(uint32_t wa, uint32_t wb, uint32_t v0,
 }
 
 // ---------------------------------------------------------------- sampling kernel
-// Grid (mtiles, dg), 128 threads = tile rows; each thread writes the
-// descriptors of its pixel for every tap: desc[((mt*dg + gd)*K + tap)*128 + row].
-// Descriptor: int64 element offset of corner (y0, x0) in the channels-last x
-// with the 4 corner-valid bits in its low bits (offsets are multiples of 32
-// elements), then the 4 weights (16-bit pairs for 16-bit types, fp32 words
-// in a second 16 bytes for fp32).
+// Grid (mtiles, dg, ceil(K/3)), 128 threads = tile rows; each thread writes
+// the descriptors of its pixel for 3 taps:
+// desc[((mt*dg + gd)*K + tap)*128 + row]. Descriptor: int64 element offset of
+// corner (y0, x0) in the channels-last x with the 4 corner-valid bits in its
+// low bits (offsets are multiples of 32 elements), then the 4 weights
+// (16-bit pairs for 16-bit types; fp32 words in a second 16 bytes for fp32).
+constexpr int kSampleTaps = 3;
+
 template <typename T>
 __global__ void __launch_bounds__(kTileM) sample_kernel(const T* __restrict__ offset, const T* __restrict__ mask,
                                                         uint8_t* __restrict__ desc, Plan pl) {
     const int64_t mt = blockIdx.x;
     const int64_t gd = blockIdx.y;
+    const int32_t tap0 = blockIdx.z * kSampleTaps;
+    const int32_t ntap = min(kSampleTaps, pl.K - tap0);
     const int row = threadIdx.x;
     const Pixel q = tile_pixel(pl, mt, row);
     const int64_t K = pl.K;
@@ -190,65 +194,62 @@ __global__ void __launch_bounds__(kTileM) sample_kernel(const T* __restrict__ of
     const int64_t nbase = q.n * pl.H;
     const uint32_t dsz = static_cast<uint32_t>(pl.desc_size);
     uint8_t* dst = desc + ((mt * pl.dg + gd) * K * kTileM + row) * dsz;
-    int32_t i = 0, j = 0;
-    for (int32_t tb = 0; tb < pl.K; tb += kTapBlock) {
-        const int32_t ntb = min(kTapBlock, pl.K - tb);
-        float dhv[kTapBlock], dwv[kTapBlock], mv[kTapBlock];
+    float dhv[kSampleTaps], dwv[kSampleTaps], mv[kSampleTaps];
 #pragma unroll
-        for (int kb = 0; kb < kTapBlock; ++kb) {
-            const int64_t tap = tb + (kb < ntb ? kb : 0);
-            dhv[kb] = to_f(po[2 * tap * P]);
-            dwv[kb] = to_f(po[(2 * tap + 1) * P]);
-            mv[kb] = to_f(pm[tap * P]);
+    for (int kb = 0; kb < kSampleTaps; ++kb) {
+        const int64_t tap = tap0 + (kb < ntap ? kb : 0);
+        dhv[kb] = to_f(po[2 * tap * P]);
+        dwv[kb] = to_f(po[(2 * tap + 1) * P]);
+        mv[kb] = to_f(pm[tap * P]);
+    }
+    int32_t i = tap0 / static_cast<int32_t>(pl.kw);
+    int32_t j = tap0 - i * static_cast<int32_t>(pl.kw);
+#pragma unroll
+    for (int kb = 0; kb < kSampleTaps; ++kb) {
+        if (kb < ntap) {
+            int64_t off = 0;
+            uint32_t flags = 0;
+            float w00 = 0.f, w01 = 0.f, w10 = 0.f, w11 = 0.f;
+            const float hf = hbase + static_cast<float>(i * pl.dh) + dhv[kb];
+            const float wf = wbase + static_cast<float>(j * pl.dw) + dwv[kb];
+            if (q.valid && hf > -1.0f && hf < static_cast<float>(pl.H) && wf > -1.0f && wf < static_cast<float>(pl.W)) {
+                const float h0f = floorf(hf), w0f = floorf(wf);
+                const float lh = hf - h0f, lw = wf - w0f;
+                const float hh = 1.0f - lh, hw_ = 1.0f - lw;
+                const float m = mv[kb];
+                const int32_t y0 = static_cast<int32_t>(h0f);
+                const int32_t x0 = static_cast<int32_t>(w0f);
+                w00 = hh * hw_ * m;
+                w01 = hh * lw * m;
+                w10 = lh * hw_ * m;
+                w11 = lh * lw * m;
+                const bool top = y0 >= 0, bottom = y0 + 1 < pl.H;
+                const bool left = x0 >= 0, right = x0 + 1 < pl.W;
+                flags = (top && left ? 1u : 0u) | (top && right ? 2u : 0u) | (bottom && left ? 4u : 0u) |
+                        (bottom && right ? 8u : 0u);
+                off = ((nbase + y0) * pl.W + x0) * pl.Cp;
+            }
+            const uint64_t packed = static_cast<uint64_t>(off) | flags;
+            uint4 d0;
+            d0.x = static_cast<uint32_t>(packed);
+            d0.y = static_cast<uint32_t>(packed >> 32);
+            uint8_t* dp = dst + static_cast<int64_t>(tap0 + kb) * kTileM * dsz;
+            if constexpr (sizeof(T) == 4) {
+                d0.z = 0u;
+                d0.w = 0u;
+                reinterpret_cast<uint4*>(dp)[0] = d0;
+                reinterpret_cast<uint4*>(dp)[1] =
+                    make_uint4(__float_as_uint(w00), __float_as_uint(w01), __float_as_uint(w10), __float_as_uint(w11));
+            } else {
+                T* tag = nullptr;
+                d0.z = pack2(w00, w01, tag);
+                d0.w = pack2(w10, w11, tag);
+                reinterpret_cast<uint4*>(dp)[0] = d0;
+            }
         }
-#pragma unroll
-        for (int kb = 0; kb < kTapBlock; ++kb) {
-            if (kb < ntb) {
-                int64_t off = 0;
-                uint32_t flags = 0;
-                float w00 = 0.f, w01 = 0.f, w10 = 0.f, w11 = 0.f;
-                const float hf = hbase + static_cast<float>(i * pl.dh) + dhv[kb];
-                const float wf = wbase + static_cast<float>(j * pl.dw) + dwv[kb];
-                if (q.valid && hf > -1.0f && hf < static_cast<float>(pl.H) && wf > -1.0f &&
-                    wf < static_cast<float>(pl.W)) {
-                    const float h0f = floorf(hf), w0f = floorf(wf);
-                    const float lh = hf - h0f, lw = wf - w0f;
-                    const float hh = 1.0f - lh, hw_ = 1.0f - lw;
-                    const float m = mv[kb];
-                    const int32_t y0 = static_cast<int32_t>(h0f);
-                    const int32_t x0 = static_cast<int32_t>(w0f);
-                    w00 = hh * hw_ * m;
-                    w01 = hh * lw * m;
-                    w10 = lh * hw_ * m;
-                    w11 = lh * lw * m;
-                    const bool top = y0 >= 0, bottom = y0 + 1 < pl.H;
-                    const bool left = x0 >= 0, right = x0 + 1 < pl.W;
-                    flags = (top && left ? 1u : 0u) | (top && right ? 2u : 0u) | (bottom && left ? 4u : 0u) |
-                            (bottom && right ? 8u : 0u);
-                    off = ((nbase + y0) * pl.W + x0) * pl.Cp;
-                }
-                const uint64_t packed = static_cast<uint64_t>(off) | flags;
-                uint4 d0;
-                d0.x = static_cast<uint32_t>(packed);
-                d0.y = static_cast<uint32_t>(packed >> 32);
-                uint8_t* dp = dst + static_cast<int64_t>(tb + kb) * kTileM * dsz;
-                if constexpr (sizeof(T) == 4) {
-                    d0.z = 0u;
-                    d0.w = 0u;
-                    reinterpret_cast<uint4*>(dp)[0] = d0;
-                    reinterpret_cast<uint4*>(dp)[1] =
-                        make_uint4(__float_as_uint(w00), __float_as_uint(w01), __float_as_uint(w10), __float_as_uint(w11));
-                } else {
-                    T* tag = nullptr;
-                    d0.z = pack2(w00, w01, tag);
-                    d0.w = pack2(w10, w11, tag);
-                    reinterpret_cast<uint4*>(dp)[0] = d0;
-                }
-            }
-            if (++j == static_cast<int32_t>(pl.kw)) {
-                j = 0;
-                ++i;
-            }
+        if (++j == static_cast<int32_t>(pl.kw)) {
+            j = 0;
+            ++i;
         }
     }
 }
@@ -887,7 +888,8 @@ cudaError_t launch_fused(const Plan& pl, const void* bias, void* out, void* ws, 
 
 cudaError_t launch_sample(const Plan& pl, const void* offset, const void* mask, void* ws, cudaStream_t st) {
     uint8_t* desc = static_cast<uint8_t*>(ws) + pl.off_desc;
-    const dim3 grid(static_cast<unsigned>(pl.mtiles), static_cast<unsigned>(pl.dg));
+    const dim3 grid(static_cast<unsigned>(pl.mtiles), static_cast<unsigned>(pl.dg),
+                    static_cast<unsigned>((pl.K + kSampleTaps - 1) / kSampleTaps));
     switch (pl.dtype) {
         case kF32:
             sample_kernel<float><<<grid, kTileM, 0, st>>>(static_cast<const float*>(offset),

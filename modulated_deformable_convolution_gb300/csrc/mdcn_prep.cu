@@ -24,42 +24,61 @@ __device__ __forceinline__ __half zero_of<__half>() { return __float2half_rn(0.0
 template <>
 __device__ __forceinline__ __nv_bfloat16 zero_of<__nv_bfloat16>() { return __float2bfloat16_rn(0.0f); }
 
-// One block transposes a 32 (w) x 32 (padded channel) tile of one (n, h) row;
-// the 32 channels lie inside one unit (UP is a multiple of 32), so the source
-// channel needs no per-element division. Block (0, 0) also clears the device
-// status word. Grid: x = (n*H + h) * wtiles + w tile, y = padded-channel tile.
+// One block converts a run of up to 32 pixels of one (n, h) row: it loads
+// x[n, :, h, w0:w0+wc] (a warp reads 32 consecutive w of one channel) into
+// shared memory as [pixel][padded channel] (pad channels zero), then writes
+// the wc*Cp contiguous elements of the channels-last row with 16-byte stores.
+// Block (0, 0) also clears the device status word. Block (32, 8); grid
+// x = (n*H + h) * wchunks + chunk.
 template <typename T>
 __global__ void __launch_bounds__(256) nhwc_pad_kernel(const T* __restrict__ x, T* __restrict__ xt,
-                                                       uint32_t* __restrict__ status, int64_t Cin, int64_t HW,
-                                                       int32_t W, int64_t Cp, int32_t U, int32_t UP,
-                                                       int32_t wtiles) {
-    __shared__ T tile[32][33];
-    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0 && threadIdx.y == 0) *status = 0u;
-    const uint32_t bx = blockIdx.x;
-    const uint32_t nh = bx / static_cast<uint32_t>(wtiles);  // n*H + h
-    const int32_t w0 = static_cast<int32_t>(bx - nh * static_cast<uint32_t>(wtiles)) * 32;
-    const int64_t pc0 = static_cast<int64_t>(blockIdx.y) * 32;
-    const int64_t unit = pc0 / UP;
-    const int32_t within0 = static_cast<int32_t>(pc0 - unit * UP);
-    const int tx = threadIdx.x, ty = threadIdx.y;
-    // x[n][c][h][w] = x + (n*Cin + c)*H*W + h*W + w; with nh = n*H + h:
-    const int64_t n = nh / static_cast<uint64_t>(HW / W);
-    const int64_t h = nh - n * (HW / W);
-    const T* src = x + n * Cin * HW + h * W + w0 + tx;
-    const bool wok = w0 + tx < W;
+                                                       uint32_t* __restrict__ status, int32_t Cin, int64_t H,
+                                                       int64_t W, int64_t Cp, int32_t U, int32_t UP, int32_t WC,
+                                                       int64_t wchunks) {
+    extern __shared__ uint4 prep_smem[];
+    T* sm = reinterpret_cast<T*>(prep_smem);
+    constexpr int kVec = 16 / sizeof(T);
+    const int32_t pitch = static_cast<int32_t>(Cp) + kVec;  // elements per staged pixel (16-byte multiple)
+    const int tid = threadIdx.y * 32 + threadIdx.x;
+    if (blockIdx.x == 0 && tid == 0) *status = 0u;
+    const int64_t bx = blockIdx.x;
+    const int64_t nh = bx / wchunks;
+    const int64_t w0 = (bx - nh * wchunks) * WC;
+    const int64_t n = nh / H;
+    const int64_t h = nh - n * H;
+    const int32_t wc = static_cast<int32_t>(W - w0 < WC ? W - w0 : WC);
+    const int32_t nvec = wc * pitch / kVec;
+    for (int32_t v = tid; v < nvec; v += 256) prep_smem[v] = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+    const T* src = x + (n * Cin * H + h) * W + w0 + threadIdx.x;
+    if (static_cast<int32_t>(threadIdx.x) < wc) {
+        // 8 channel loads in flight per thread, then their shared-memory stores
+        const int64_t cstride = H * W;
+        for (int32_t c0 = threadIdx.y; c0 < Cin; c0 += 64) {
+            T v[8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int32_t within = within0 + ty + 8 * i;
-        T v = zero_of<T>();
-        if (wok && within < U) v = src[(unit * U + within) * HW];
-        tile[ty + 8 * i][tx] = v;
+            for (int k = 0; k < 8; ++k) {
+                const int32_t c = c0 + 8 * k;
+                if (c < Cin) v[k] = src[static_cast<int64_t>(c) * cstride];
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int32_t c = c0 + 8 * k;
+                if (c < Cin) {
+                    const int32_t unit = c / U;
+                    sm[threadIdx.x * pitch + unit * UP + (c - unit * U)] = v[k];
+                }
+            }
+        }
     }
     __syncthreads();
-    T* dst = xt + static_cast<int64_t>(nh) * W * Cp + pc0 + tx;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int32_t w = w0 + ty + 8 * i;
-        if (w < W && pc0 + tx < Cp) dst[static_cast<int64_t>(w) * Cp] = tile[tx][ty + 8 * i];
+    uint4* dst = reinterpret_cast<uint4*>(xt + (nh * W + w0) * Cp);
+    const int32_t cvec = static_cast<int32_t>(Cp) / kVec;
+    const int32_t nout = wc * cvec;
+    for (int32_t v = tid; v < nout; v += 256) {
+        const int32_t w = v / cvec;
+        const int32_t cv = v - w * cvec;
+        dst[v] = *reinterpret_cast<const uint4*>(sm + w * pitch + cv * kVec);
     }
 }
 
@@ -85,36 +104,53 @@ __global__ void __launch_bounds__(256) pack_weight_kernel(const T* __restrict__ 
     const KTile t = decode_ktile(kt, pl.K, pl.nch);
     const int32_t within = t.ch * pl.BKc + ci;  // channel within the unit
     const int64_t cl = static_cast<int64_t>(t.ul) * pl.U + within;  // channel within the group
-    for (int64_t r = blockIdx.y; r < pl.wp_rows; r += gridDim.y) {
-        T v = zero_of<T>();
-        if (within < pl.U && r < rows) {
-            const bool lo_half = r >= pl.Cout;
-            const int64_t o = lo_half ? r - pl.Cout : r;
-            const T* src = weight + (o * pl.Cg + cl) * pl.K + t.tap;
-            if constexpr (sizeof(T) == 4) {
-                const float f = load_f<T>(src);
-                const float hi = to_tf32(f);
-                v = lo_half ? (f - hi) : hi;
-            } else {
-                v = *src;
+    // 4 rows per iteration: their loads are in flight together
+    for (int64_t r0 = blockIdx.y; r0 < pl.wp_rows; r0 += 4 * static_cast<int64_t>(gridDim.y)) {
+        T v[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int64_t r = r0 + k * static_cast<int64_t>(gridDim.y);
+            v[k] = zero_of<T>();
+            if (within < pl.U && r < rows) {
+                const bool lo_half = r >= pl.Cout;
+                const int64_t o = lo_half ? r - pl.Cout : r;
+                const T* src = weight + (o * pl.Cg + cl) * pl.K + t.tap;
+                if constexpr (sizeof(T) == 4) {
+                    const float f = load_f<T>(src);
+                    const float hi = to_tf32(f);
+                    v[k] = lo_half ? (f - hi) : hi;
+                } else {
+                    v[k] = *src;
+                }
             }
         }
-        wp[r * pl.KP + static_cast<int64_t>(kt) * pl.BKc + ci] = v;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int64_t r = r0 + k * static_cast<int64_t>(gridDim.y);
+            if (r < pl.wp_rows) wp[r * pl.KP + static_cast<int64_t>(kt) * pl.BKc + ci] = v[k];
+        }
     }
 }
 
 }  // namespace
+
+constexpr int64_t kPrepSmemBytes = 40 * 1024;
 
 template <typename T>
 static cudaError_t prep_input_t(const Plan& pl, const void* x, void* ws, cudaStream_t st) {
     uint8_t* base = static_cast<uint8_t*>(ws);
     uint32_t* status = reinterpret_cast<uint32_t*>(base);
     T* xt = reinterpret_cast<T*>(base + pl.off_xt);
-    const int64_t wtiles = (pl.W + 31) / 32;
-    dim3 grid(static_cast<unsigned>(pl.N * pl.H * wtiles), static_cast<unsigned>((pl.Cp + 31) / 32));
-    nhwc_pad_kernel<T><<<grid, dim3(32, 8), 0, st>>>(static_cast<const T*>(x), xt, status, pl.Cin, pl.H * pl.W,
-                                                     static_cast<int32_t>(pl.W), pl.Cp, pl.U, pl.UP,
-                                                     static_cast<int32_t>(wtiles));
+    const int64_t pitch_bytes = (pl.Cp + 16 / static_cast<int64_t>(sizeof(T))) * static_cast<int64_t>(sizeof(T));
+    int64_t wc = kPrepSmemBytes / pitch_bytes;
+    if (wc > 32) wc = 32;
+    if (wc > pl.W) wc = pl.W;
+    if (wc < 1) return cudaErrorInvalidConfiguration;  // a pixel's channels exceed the staging buffer
+    const int64_t wchunks = (pl.W + wc - 1) / wc;
+    const size_t smem = static_cast<size_t>(wc * pitch_bytes);
+    nhwc_pad_kernel<T><<<static_cast<unsigned>(pl.N * pl.H * wchunks), dim3(32, 8), smem, st>>>(
+        static_cast<const T*>(x), xt, status, static_cast<int32_t>(pl.Cin), pl.H, pl.W, pl.Cp, pl.U, pl.UP,
+        static_cast<int32_t>(wc), wchunks);
     return cudaGetLastError();
 }
 
@@ -124,7 +160,8 @@ static cudaError_t pack_weight_t(const Plan& pl, const void* weight, void* ws, c
     T* wp = reinterpret_cast<T*>(base + pl.off_wp);
     const int32_t ktiles_per_block = 256 / pl.BKc;
     const unsigned gx = static_cast<unsigned>((pl.KT + ktiles_per_block - 1) / ktiles_per_block);
-    const unsigned gy = static_cast<unsigned>(pl.wp_rows < 65535 ? pl.wp_rows : 65535);
+    const int64_t gy4 = (pl.wp_rows + 3) / 4;
+    const unsigned gy = static_cast<unsigned>(gy4 < 65535 ? gy4 : 65535);
     pack_weight_kernel<T><<<dim3(gx, gy), 256, 0, st>>>(static_cast<const T*>(weight), wp, pl);
     return cudaGetLastError();
 }
