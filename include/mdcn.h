@@ -185,6 +185,29 @@ mdcn_status mdcn_forward_im2col_gemm(mdcn_handle handle, const void* x, const vo
                                      void* out, void* workspace, size_t workspace_bytes,
                                      const mdcn_dims* dims, mdcn_dtype dtype, void* stream);
 
+/* mdcn_forward without a caller-supplied workspace, for callers that cannot
+ * allocate device memory on their execution path (a serving loop that reserves
+ * all memory at start-up, a runtime whose execute step must not call
+ * cudaMalloc, or plain C code without a device allocator). The source pages
+ * have no counterpart of this entry point.
+ *   - Scratch: a fixed 16 MiB device array inside libmdcn.so, present on every
+ *     GPU that loads the library until the process exits. Calls whose
+ *     mdcn_workspace_size exceeds 16 MiB are rejected with MDCN_ERR_WORKSPACE
+ *     before anything is launched.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *   - The first call on a device looks up the array's device address (one
+ *     cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array, which keeps the last call's
+ *     contents; each call overwrites what it reads, and clears the status word.
+ *     Calls that overlap on the GPU (other streams, other threads) race on the
+ *     array and must be serialised by the caller.
+ *   - Otherwise identical to mdcn_forward: same arguments (minus workspace),
+ *     validation, kernels and results; mdcn_query_status does not apply. */
+mdcn_status mdcn_forward_noalloc(mdcn_handle handle, const void* x, const void* offset, const void* mask,
+                                 const void* weight, const void* bias_or_null, void* out,
+                                 const mdcn_dims* dims, mdcn_dtype dtype, void* stream);
+
 /* Reads the device status word that the last mdcn_forward on this workspace
  * left (synchronising the stream), stores its raw bits in *device_bits (may
  * be NULL) and clears it. Returns MDCN_ERR_TIMEOUT when a pipeline wait in
