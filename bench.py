@@ -245,6 +245,7 @@ def run_ours(args, case, world, rank, local, dist):
     out = torch.empty(mdcn.mdcn_output_dims(h, x, off, m, w, b), dtype=x.dtype, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    plan = mdcn.mdcn_query_plan(h, x, off, m, w, b)
 
     def step(ev=None):
         mdcn.mdcn_prepare_input(h, x, off, m, w, b, ws, stream)
@@ -352,7 +353,8 @@ def run_ours(args, case, world, rank, local, dist):
         peak = peaks["bf16_tflops"]
         peak_note = f"{peak_src} bf16 burst (fp16 has the same dense rate)"
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-            "traffic": profiled_traffic(case.name), "kernel": "fused_kernel", "peak_source": peak_note,
+            "traffic": profiled_traffic(case.name),
+            "kernel": "fused_kernel" + (" + splitk_fixup_kernel" if plan["split"] else ""), "peak_source": peak_note,
             "kernel_us": fused_mean_s * 1e6}
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
@@ -368,7 +370,9 @@ def run_ours(args, case, world, rank, local, dist):
         "config": {"workload": describe(case), "global_batch": case.N * world,
                    "l2": "flushed before every timed step (256 MiB write outside the events)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "step": "channels-last x + weight pack + sampling descriptors + fused kernel (4 launches)"},
+                   "step": "channels-last x + weight pack + sampling descriptors + fused kernel"
+                           + (" + split-tile fix-up" if plan["split"] else "") + f" ({plan['launches']} launches)",
+                   "plan": plan},
         "step_ms": {"mean": ms, "p10": sorted(step_ms)[len(step_ms) // 10],
                     "p90": sorted(step_ms)[(len(step_ms) * 9) // 10]},
         "roofline": roof,
@@ -377,7 +381,7 @@ def run_ours(args, case, world, rank, local, dist):
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "ablation_im2col_gemm": None if abl_ms is None else {"ms_per_call": abl_ms,
                                                              "tflops": flops / (abl_ms * 1e-3) / 1e12},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": plan["launches"] * args.steps,
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)

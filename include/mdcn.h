@@ -94,14 +94,17 @@ typedef struct mdcn_handle_* mdcn_handle;
 mdcn_status mdcn_create(const mdcn_attrs* attrs, mdcn_handle* out);
 
 /* Optional overrides of the fused kernel's automatic execution plan, for
- * benchmarking and tuning; results are identical for every setting. A zero
+ * benchmarking and tuning. Results are bitwise identical for every stages and
+ * kgroups setting; tile_mode and max_ctas move the points where output tiles
+ * are split between CTAs, which changes the order of some fp32 additions. A zero
  * (or -1 for tile_mode) keeps the automatic choice. */
 typedef struct mdcn_tuning {
     int32_t stages;    /* shared-memory pipeline stages: 2, 4, 6 or 8 (0: automatic) */
     int32_t tile_mode; /* pixel tile: 0 = 128 consecutive pixels of N*Ho*Wo, 1 = 8x16 block of one image,
                           -1 = automatic */
     int32_t max_ctas;  /* cap on persistent CTAs (0: one per SM) */
-    int32_t reserved;  /* must be 0 */
+    int32_t kgroups;   /* k-tiles the gather warps produce at once: 1, 2 or 4, dividing the stage count
+                          (0: automatic) */
 } mdcn_tuning;
 
 /* mdcn_create with plan overrides (tuning may be NULL = automatic). Errors as
@@ -124,17 +127,38 @@ mdcn_status mdcn_destroy(mdcn_handle handle);
 mdcn_status mdcn_output_dims(mdcn_handle handle, const mdcn_dims* dims, int64_t out_dims[4]);
 
 /* Bytes of device workspace mdcn_forward needs for these dims and dtype
- * (a status word, the channels-last copy of x, the repacked weight and the
- * sampling descriptors). Host only. */
+ * (a status word, the channels-last copy of x, the repacked weight, the
+ * sampling descriptors, and the fp32 partial sums of output tiles split
+ * between CTAs). Host only. */
 mdcn_status mdcn_workspace_size(mdcn_handle handle, const mdcn_dims* dims, mdcn_dtype dtype,
                                 size_t* bytes);
+
+/* The execution plan mdcn_forward would use for these dims and dtype on the
+ * current device (needs a compute capability 10.3 device for its SM count). */
+typedef struct mdcn_plan_info {
+    int64_t tiles;          /* output tiles: 128 pixels x up to 256 output channels of one group */
+    int64_t ktiles_per_tile; /* k-tiles (128 bytes of channels of one tap) of one tile */
+    int64_t ktiles_per_cta; /* consecutive k-tiles each persistent CTA takes */
+    int32_t ctas;           /* persistent CTAs of the fused kernel */
+    int32_t split;          /* 1 when some tile is split between CTAs (the fix-up kernel runs) */
+    int32_t stages, kgroups, tile_mode;
+    int32_t launches;       /* kernels one mdcn_forward launches: 4, or 5 with the fix-up */
+} mdcn_plan_info;
+
+/* Errors as mdcn_workspace_size, plus MDCN_ERR_ARCH / MDCN_ERR_CUDA from the
+ * device check. The source pages have no counterpart: this is a diagnostic. */
+mdcn_status mdcn_query_plan(mdcn_handle handle, const mdcn_dims* dims, mdcn_dtype dtype, mdcn_plan_info* info);
 
 /* The forward pass (section 5, steps 1-3) as one fused implicit-GEMM kernel:
  * producer warps sample and modulate the columns straight into shared
  * memory, tcgen05 tensor-core MMAs accumulate in tensor memory, the epilogue
  * adds the bias and writes NCHW. The im2col column matrix never reaches
- * device memory. Three small kernels run first, into workspace: x to
- * channels-last, the weight repack, and the sampling descriptors.
+ * device memory. Persistent CTAs (one per SM) take equal consecutive ranges
+ * of the k-tiles of all output tiles; a tile split between CTAs is summed
+ * from their fp32 partials, in k order, by a small fix-up kernel launched
+ * right after (programmatic dependent launch).
+ * Three small kernels run first, into workspace: x to channels-last, the
+ * weight repack, and the sampling descriptors.
  *   x [N,Cin,H,W], offset [N,2*dg*kh*kw,Ho,Wo], mask [N,dg*kh*kw,Ho,Wo],
  *   weight [Cout,Cin/group,kh,kw], bias_or_null [Cout] or NULL,
  *   out [N,Cout,Ho,Wo] (written), workspace of workspace_bytes (scratch,
@@ -159,7 +183,8 @@ mdcn_status mdcn_forward(mdcn_handle handle, const void* x, const void* offset, 
  *                          sampling descriptors in workspace (section 5
  *                          step 1: point, corner validity, bilinear weights
  *                          times the mask);
- *   mdcn_forward_prepared: the fused gather + contraction + bias kernel. */
+ *   mdcn_forward_prepared: the fused gather + contraction + bias kernel, and
+ *                          the split-tile fix-up when tiles are split. */
 mdcn_status mdcn_prepare_input(mdcn_handle handle, const void* x, void* workspace, size_t workspace_bytes,
                                const mdcn_dims* dims, mdcn_dtype dtype, void* stream);
 mdcn_status mdcn_pack_weight(mdcn_handle handle, const void* weight, void* workspace, size_t workspace_bytes,
@@ -190,9 +215,9 @@ mdcn_status mdcn_forward_im2col_gemm(mdcn_handle handle, const void* x, const vo
  * all memory at start-up, a runtime whose execute step must not call
  * cudaMalloc, or plain C code without a device allocator). The source pages
  * have no counterpart of this entry point.
- *   - Scratch: a fixed 16 MiB device array inside libmdcn.so, present on every
+ *   - Scratch: a fixed 64 MiB device array inside libmdcn.so, present on every
  *     GPU that loads the library until the process exits. Calls whose
- *     mdcn_workspace_size exceeds 16 MiB are rejected with MDCN_ERR_WORKSPACE
+ *     mdcn_workspace_size exceeds 64 MiB are rejected with MDCN_ERR_WORKSPACE
  *     before anything is launched.
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  *   - The first call on a device looks up the array's device address (one

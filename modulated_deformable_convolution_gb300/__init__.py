@@ -23,7 +23,8 @@ from ._abi import (MDCN_BF16, MDCN_ERR_ALIGN, MDCN_ERR_ARCH, MDCN_ERR_ATTR, MDCN
 __all__ = ["Handle", "MdcnError", "forward", "mdcn_create", "mdcn_destroy", "mdcn_output_dims",
            "mdcn_workspace_size", "mdcn_forward", "mdcn_prepare_input", "mdcn_pack_weight",
            "mdcn_prepare_samples", "mdcn_forward_prepared", "mdcn_im2col_gemm_workspace_size", "mdcn_forward_im2col_gemm",
-           "mdcn_query_status", "mdcn_selftest_wait_timeout", "mdcn_status_string", "library_path"]
+           "mdcn_query_plan", "mdcn_query_status", "mdcn_selftest_wait_timeout", "mdcn_status_string",
+           "library_path"]
 
 _DTYPES = {torch.float32: MDCN_F32, torch.float16: MDCN_F16, torch.bfloat16: MDCN_BF16}
 
@@ -78,7 +79,7 @@ def mdcn_create(stride=1, padding=0, dilation=1, group=1, deformable_group=1, tu
         _check(_lib().mdcn_create(ctypes.byref(a), ctypes.byref(h)), "mdcn_create")
     else:
         t = _abi.mdcn_tuning(int(tuning.get("stages", 0)), int(tuning.get("tile_mode", -1)),
-                             int(tuning.get("max_ctas", 0)), 0)
+                             int(tuning.get("max_ctas", 0)), int(tuning.get("kgroups", 0)))
         _check(_lib().mdcn_create_tuned(ctypes.byref(a), ctypes.byref(t), ctypes.byref(h)), "mdcn_create_tuned")
     return h.value
 
@@ -149,6 +150,16 @@ def mdcn_workspace_size(handle, x, offset, mask, weight, bias=None, dtype=None) 
     _check(_lib().mdcn_workspace_size(_hval(handle), ctypes.byref(_dims(x, offset, mask, weight, bias)), dt,
                                       ctypes.byref(n)), "mdcn_workspace_size")
     return int(n.value)
+
+
+def mdcn_query_plan(handle, x, offset, mask, weight, bias=None, dtype=None) -> dict:
+    """The fused path's execution plan on the current device, as a dict."""
+    info = _abi.mdcn_plan_info()
+    dt = _dtype(x) if dtype is None else dtype
+    with torch.cuda.device(x.device):
+        _check(_lib().mdcn_query_plan(_hval(handle), ctypes.byref(_dims(x, offset, mask, weight, bias)), dt,
+                                      ctypes.byref(info)), "mdcn_query_plan")
+    return {name: int(getattr(info, name)) for name, _ in info._fields_}
 
 
 def mdcn_im2col_gemm_workspace_size(handle, x, offset, mask, weight, bias=None, dtype=None) -> int:

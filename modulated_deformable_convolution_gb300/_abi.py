@@ -37,7 +37,13 @@ class mdcn_attrs(ctypes.Structure):
 
 class mdcn_tuning(ctypes.Structure):
     _fields_ = [("stages", ctypes.c_int32), ("tile_mode", ctypes.c_int32), ("max_ctas", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("kgroups", ctypes.c_int32)]
+
+
+class mdcn_plan_info(ctypes.Structure):
+    _fields_ = [("tiles", i64), ("ktiles_per_tile", i64), ("ktiles_per_cta", i64), ("ctas", ctypes.c_int32),
+                ("split", ctypes.c_int32), ("stages", ctypes.c_int32), ("kgroups", ctypes.c_int32),
+                ("tile_mode", ctypes.c_int32), ("launches", ctypes.c_int32)]
 
 
 class mdcn_dims(ctypes.Structure):
@@ -94,6 +100,8 @@ def load(path: str = LIB_PATH):
         lib.mdcn_im2col_gemm_workspace_size.restype = st
         lib.mdcn_forward_im2col_gemm.argtypes = fwd
         lib.mdcn_forward_im2col_gemm.restype = st
+        lib.mdcn_query_plan.argtypes = [vp, ctypes.POINTER(mdcn_dims), ctypes.c_int, ctypes.POINTER(mdcn_plan_info)]
+        lib.mdcn_query_plan.restype = st
         lib.mdcn_query_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
         lib.mdcn_query_status.restype = st
         lib.mdcn_selftest_wait_timeout.argtypes = [vp, ctypes.c_uint32, vp]

@@ -196,15 +196,17 @@ mdcn_status make_plan(const mdcn_attrs& a, const mdcn_tuning& tuning, const mdcn
     // and whose output rows are 16-byte multiples
     p.epi_tma = (mode == 1 && (p.Wo * elem) % 16 == 0 && Og % 16 == 0) ? 1 : 0;
     p.epi_bytes = p.epi_tma ? mdcn::kEpiWarps * 2 * 16 * 32 * static_cast<int32_t>(elem) : 0;
-    const int32_t fixed = 1024 + 2 * p.desc_slot_bytes + p.epi_bytes + 256;
+    const int32_t fixed = 1024 + 2 * p.desc_slot_bytes + p.epi_bytes + 512;
     const int32_t per_stage = p.a_bytes + p.b_bytes;
-    // stages: 2, 4, 6 or 8; the gather produces kgroups k-tiles at once (4 when
-    // the stages allow it, else 2), and kgroups must divide the stage count
+    // stages: 2, 4, 6 or 8; the gather produces kgroups k-tiles at once (1, 2
+    // or 4, dividing the stage count; automatic: 2, measured fastest on the
+    // named workloads)
     const int32_t max_stages = (mdcn::kSmemLimit - fixed) / per_stage;
     int32_t stages = tuning.stages > 0 ? tuning.stages : (max_stages >= 4 ? 4 : 2);
     if (stages < 2 || stages > 8 || (stages & 1) || stages > max_stages) return MDCN_ERR_UNSUPPORTED;
     p.stages = stages;
-    p.kgroups = (stages % 4 == 0) ? 4 : 2;
+    p.kgroups = tuning.kgroups > 0 ? tuning.kgroups : 2;
+    if (stages % p.kgroups != 0) return MDCN_ERR_UNSUPPORTED;
     p.smem_bytes = fixed + stages * per_stage;
     p.grid = 0;  // set at launch from the SM count
 
@@ -225,10 +227,15 @@ mdcn_status make_plan(const mdcn_attrs& a, const mdcn_tuning& tuning, const mdcn
         !mul_ok(dbytes, p.desc_size))
         return MDCN_ERR_UNSUPPORTED;
     if (p.mtiles > 2147483647 || p.dg > 65535 || ceil_div(K, 3) > 65535) return MDCN_ERR_UNSUPPORTED;  // sampling grid
+    // stream-K: fp32 partial accumulators of split tiles, 2 slots per CTA
+    p.total_kt = p.tiles_total;
+    if (!mul_ok(p.total_kt, p.KT) || p.total_kt > kI31) return MDCN_ERR_UNSUPPORTED;  // 32-bit tile arithmetic
+    const int64_t part_bytes = static_cast<int64_t>(2) * mdcn::kMaxCtas * p.acc_cols * mdcn::kTileM * 4;
     p.off_xt = mdcn::kStatusBytes;
     p.off_wp = align256(p.off_xt + static_cast<size_t>(xt));
     p.off_desc = align256(p.off_wp + static_cast<size_t>(wpb));
-    p.ws_bytes = align256(p.off_desc + static_cast<size_t>(dbytes));
+    p.off_part = align256(p.off_desc + static_cast<size_t>(dbytes));
+    p.ws_bytes = align256(p.off_part + static_cast<size_t>(part_bytes));
     *pl = p;
     return MDCN_OK;
 }
@@ -286,9 +293,17 @@ mdcn_status plan_for_call(mdcn_handle h, const mdcn_dims* dims, mdcn_dtype dtype
     s = check_device(&sms);
     if (s != MDCN_OK) return s;
     int64_t grid = sms > 0 ? sms : 1;
+    if (grid > mdcn::kMaxCtas) grid = mdcn::kMaxCtas;
     if (h->tuning.max_ctas > 0 && h->tuning.max_ctas < grid) grid = h->tuning.max_ctas;
-    if (grid > p->tiles_total) grid = p->tiles_total;
-    p->grid = static_cast<int32_t>(grid);
+    if (grid > p->total_kt) grid = p->total_kt;
+    // stream-K split: equal consecutive k-tile ranges, none empty. Splitting a
+    // tile costs its CTAs an fp32 partial write each and the fix-up kernel a
+    // read of them, so ranges stay whole tiles unless the busiest CTA's share
+    // drops clearly (measured break-even: about 15% plus 4 k-tiles).
+    const int64_t split = (p->total_kt + grid - 1) / grid;
+    const int64_t whole = (p->tiles_total + grid - 1) / grid * p->KT;
+    p->kt_per_cta = split * 115 / 100 + 4 < whole ? split : whole;
+    p->grid = static_cast<int32_t>((p->total_kt + p->kt_per_cta - 1) / p->kt_per_cta);
     return MDCN_OK;
 }
 
@@ -303,7 +318,7 @@ mdcn_status mdcn_create_tuned(const mdcn_attrs* attrs, const mdcn_tuning* tuning
     if (tuning) {
         tu = *tuning;
         if (tu.stages < 0 || tu.stages == 1 || tu.stages > 8 || tu.tile_mode < -1 || tu.tile_mode > 1 ||
-            tu.max_ctas < 0 || tu.reserved != 0)
+            tu.max_ctas < 0 || !(tu.kgroups == 0 || tu.kgroups == 1 || tu.kgroups == 2 || tu.kgroups == 4))
             return MDCN_ERR_ATTR;
     }
     mdcn_handle h = new (std::nothrow) mdcn_handle_;
@@ -336,6 +351,25 @@ mdcn_status mdcn_workspace_size(mdcn_handle handle, const mdcn_dims* dims, mdcn_
     mdcn_status s = make_plan(handle->attrs, handle->tuning, dims, dtype, &p);
     if (s != MDCN_OK) return s;
     *bytes = p.ws_bytes;
+    return MDCN_OK;
+}
+
+mdcn_status mdcn_query_plan(mdcn_handle handle, const mdcn_dims* dims, mdcn_dtype dtype, mdcn_plan_info* info) {
+    if (!handle || !dims || !info) return MDCN_ERR_NULL;
+    Plan p;
+    mdcn_status s = make_plan(handle->attrs, handle->tuning, dims, dtype, &p);
+    if (s != MDCN_OK) return s;
+    s = plan_for_call(handle, dims, dtype, p.ws_bytes, &p);
+    if (s != MDCN_OK) return s;
+    info->tiles = p.tiles_total;
+    info->ktiles_per_tile = p.KT;
+    info->ktiles_per_cta = p.kt_per_cta;
+    info->ctas = p.grid;
+    info->split = mdcn::splitk_needed(p) ? 1 : 0;
+    info->stages = p.stages;
+    info->kgroups = p.kgroups;
+    info->tile_mode = p.tile_mode;
+    info->launches = 4 + info->split;
     return MDCN_OK;
 }
 

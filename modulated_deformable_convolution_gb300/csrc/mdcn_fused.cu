@@ -66,6 +66,7 @@ struct FusedParams {
     const void* bias;
     void* out;
     uint32_t* status;
+    float* part;      // fp32 partial accumulators of split tiles: 2 slots per CTA
     Plan pl;
 };
 
@@ -254,80 +255,106 @@ __global__ void __launch_bounds__(kTileM) sample_kernel(const T* __restrict__ of
     }
 }
 
+// ---------------------------------------------------------------- work split
+// Stream-K: the k-tiles of all tiles form one sequence (tile t's k-tile k at
+// position t*KT + k) and persistent CTA c takes the contiguous range
+// [c*R, min((c+1)*R, total)), R = pl.kt_per_cta. A CTA's range covers
+// "units": pieces of consecutive tiles, a whole tile or a k-range of one. A
+// tile whose k-tiles fall to several CTAs is summed from their fp32 partial
+// accumulators by the last of them to finish (see the epilogue).
+struct Unit {
+    int64_t t;        // tile
+    int32_t k0, k1;   // k-tile range [k0, k1) of the tile
+};
+
+__device__ __forceinline__ Unit unit_at(const Plan& pl, int64_t pos, int64_t hi) {
+    Unit u;
+    u.t = pos / pl.KT;
+    u.k0 = static_cast<int32_t>(pos - u.t * pl.KT);
+    const int64_t end = hi - u.t * pl.KT;
+    u.k1 = static_cast<int32_t>(end < pl.KT ? end : pl.KT);
+    return u;
+}
+
 // ---------------------------------------------------------------- gather helpers
 // Position in a CTA's k-tile sequence. A tile's k-tiles form descriptor
-// groups (unit ul, tap block b); each group holds its chunks x taps k-tiles.
-// The rg/rk fields rotate the group order and the k-tile order inside a
-// group; they are kept at zero (the order of the packed weight), which makes
-// every plan choice accumulate each output in the same order.
+// groups (unit ul, tap block b), in the order of the packed weight; each group
+// holds its chunks x taps k-tiles.
 struct Cursor {
+    int64_t pos, hi;      // position in the k-tile sequence, end of the CTA's range
     int64_t t, mt;
     int32_t g, nt;
-    int32_t gi, j;        // processing position: group, k-tile within the group
-    int32_t rg, rk;       // rotations of the groups and of the k-tiles in this group
+    int32_t gi, j;        // group, k-tile within the group
     int32_t ul, b, ntbg, nktg, ch, kb, kt;  // the k-tile at that position
-    uint32_t gr;          // descriptor groups entered so far (across tiles)
+    uint32_t gr;          // descriptor groups entered so far
     bool live;
 };
 
 __device__ __forceinline__ void cursor_group(const Plan& pl, Cursor& c) {
-    const int32_t ngroups = pl.Ug * pl.ntb;
-    int32_t ag = c.gi + c.rg;
-    if (ag >= ngroups) ag -= ngroups;
-    c.ul = ag / pl.ntb;
-    c.b = ag - c.ul * pl.ntb;
+    c.ul = c.gi / pl.ntb;
+    c.b = c.gi - c.ul * pl.ntb;
     c.ntbg = min(kTapBlock, pl.K - c.b * kTapBlock);
     c.nktg = c.ntbg * pl.nch;
-    c.rk = 0;
 }
 
 __device__ __forceinline__ void cursor_ktile(const Plan& pl, Cursor& c) {
-    int32_t a = c.j + c.rk;
-    if (a >= c.nktg) a -= c.nktg;
-    c.ch = a / c.ntbg;
-    c.kb = a - c.ch * c.ntbg;
-    c.kt = (c.ul * pl.K + c.b * kTapBlock) * pl.nch + a;  // global k-tile index (B coordinate)
+    c.ch = c.j / c.ntbg;
+    c.kb = c.j - c.ch * c.ntbg;
+    c.kt = (c.ul * pl.K + c.b * kTapBlock) * pl.nch + c.j;  // global k-tile index (B coordinate)
 }
 
 __device__ __forceinline__ void cursor_tile(const Plan& pl, Cursor& c, int64_t t) {
     c.t = t;
-    c.live = t < pl.tiles_total;
-    if (!c.live) return;
     const TileId id = decode_tile(pl, t);
     c.g = id.g;
     c.nt = id.nt;
     c.mt = id.mt;
-    c.rg = 0;
+}
+
+__device__ __forceinline__ void cursor_init(const Plan& pl, Cursor& c, int64_t lo, int64_t hi) {
+    c.gr = 0;
+    c.pos = lo;
+    c.hi = hi;
+    c.live = lo < hi;
+    if (!c.live) return;
+    const int64_t t = lo / pl.KT;
+    int32_t k = static_cast<int32_t>(lo - t * pl.KT);
+    cursor_tile(pl, c, t);
     c.gi = 0;
-    c.j = 0;
     cursor_group(pl, c);
+    while (k >= c.nktg) {
+        k -= c.nktg;
+        ++c.gi;
+        cursor_group(pl, c);
+    }
+    c.j = k;
     cursor_ktile(pl, c);
 }
 
-__device__ __forceinline__ void cursor_init(const Plan& pl, Cursor& c, int64_t first_tile) {
-    c.gr = 0;
-    cursor_tile(pl, c, first_tile);
-}
-
-__device__ __forceinline__ void cursor_advance(const Plan& pl, Cursor& c, int64_t tile_step) {
+__device__ __forceinline__ void cursor_advance(const Plan& pl, Cursor& c) {
+    if (++c.pos >= c.hi) {
+        c.live = false;
+        return;
+    }
     if (++c.j < c.nktg) {
         cursor_ktile(pl, c);
         return;
     }
     c.j = 0;
     ++c.gr;
-    if (++c.gi < pl.Ug * pl.ntb) {
-        cursor_group(pl, c);
-        cursor_ktile(pl, c);
-        return;
+    if (++c.gi == pl.Ug * pl.ntb) {
+        c.gi = 0;
+        cursor_tile(pl, c, c.t + 1);
     }
-    cursor_tile(pl, c, c.t + tile_step);
+    cursor_group(pl, c);
+    cursor_ktile(pl, c);
 }
 
 // Moves the cursor to the first k-tile of its next group.
-__device__ __forceinline__ void cursor_next_group(const Plan& pl, Cursor& c, int64_t tile_step) {
+__device__ __forceinline__ void cursor_next_group(const Plan& pl, Cursor& c) {
+    c.pos += c.nktg - 1 - c.j;
     c.j = c.nktg - 1;
-    cursor_advance(pl, c, tile_step);
+    cursor_advance(pl, c);
 }
 
 template <typename T>
@@ -447,8 +474,12 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int32_t KT = pl.KT;
-    const int64_t first_tile = blockIdx.x;
-    const int64_t tile_step = gridDim.x;
+    // the split-tile fix-up may be scheduled onto SMs as they free up; it
+    // waits for this whole grid to finish before it reads anything
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // this CTA's range of the k-tile sequence
+    const int64_t lo = static_cast<int64_t>(blockIdx.x) * pl.kt_per_cta;
+    const int64_t hi = min(lo + pl.kt_per_cta, pl.total_kt);
 
     if (warp == kWarpTma && lane == 0) {
         for (int s = 0; s < S; ++s) {
@@ -493,9 +524,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
             const uint32_t dsz = static_cast<uint32_t>(pl.desc_size);
             // descriptor groups are copied up to one group ahead of the k-tiles
             Cursor dc;  // first k-tile of the next group to copy
-            cursor_init(pl, dc, first_tile);
+            cursor_init(pl, dc, lo, hi);
             Cursor kc;  // next weight k-tile to load
-            cursor_init(pl, kc, first_tile);
+            cursor_init(pl, kc, lo, hi);
             bool ok = true;
             uint32_t s = 0;
             while (kc.live && ok) {
@@ -513,7 +544,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                         dglob + ((dc.mt * pl.dg + gd) * pl.K + static_cast<int64_t>(dc.b) * kTapBlock) * kTileM * dsz;
                     mbar_arrive_expect_tx(dfull_bar(slot), bytes);
                     bulk_load(d0 + slot * dslot, src, bytes, dfull_bar(slot));
-                    cursor_next_group(pl, dc, tile_step);
+                    cursor_next_group(pl, dc);
                 }
                 if (!ok) break;
                 const int st = s % S;
@@ -531,7 +562,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                         tma_load_2d(dst + h * half_bytes + j * sub_bytes, &tmap, kc.kt * pl.BKc,
                                     row0 + h * static_cast<int32_t>(pl.Cout) + j * pl.BNs, tma_bar(st));
                 ++s;
-                cursor_advance(pl, kc, tile_step);
+                cursor_advance(pl, kc);
             }
             if (!ok) {
                 // let the copies already issued land before the CTA exits
@@ -552,13 +583,15 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
             const uint32_t half_bytes = sub_bytes * pl.nsub;
             uint32_t s = 0, i = 0;
             bool ok = true;
-            for (int64_t t = first_tile; t < pl.tiles_total && ok; t += tile_step, ++i) {
+            for (int64_t pos = lo; pos < hi && ok; ++i) {
+                const Unit un = unit_at(pl, pos, hi);
+                pos = un.t * KT + un.k1;
                 const int ab = static_cast<int>(i % pl.nacc);
                 const uint32_t use = i / pl.nacc;
                 if (!mbar_wait_bounded(acce_bar(ab), (use & 1) ^ 1u, abort_flag, prm.status, kSiteMmaFull)) break;
                 tc_fence_after();
                 const uint32_t dacc = tmem_base + static_cast<uint32_t>(ab * pl.acc_cols);
-                for (int32_t kt = 0; kt < KT; ++kt, ++s) {
+                for (int32_t kt = un.k0; kt < un.k1; ++kt, ++s) {
                     const int st = s % S;
                     const uint32_t ph = (s / S) & 1;
                     if (!mbar_wait_bounded(full_bar(st), ph, abort_flag, prm.status, kSiteMmaFull) ||
@@ -576,7 +609,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                         for (int j = 0; j < pl.nsub; ++j) {
                             const uint32_t d = dacc + static_cast<uint32_t>(j * pl.BNs);
                             const uint64_t bdesc = smem_desc_sw128(b_s + j * sub_bytes + kk * 32);
-                            const uint32_t accum = (kt > 0 || kk > 0) ? 1u : 0u;
+                            const uint32_t accum = (kt > un.k0 || kk > 0) ? 1u : 0u;
                             if constexpr (kF32Path) {
                                 const uint64_t adesc_lo = smem_desc_sw128(a_s + kTileM * 128 + kk * 32);
                                 const uint64_t bdesc_lo = smem_desc_sw128(b_s + half_bytes + j * sub_bytes + kk * 32);
@@ -605,9 +638,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         // before k-tile n is combined and stored, so one L2 round trip overlaps the
         // previous k-tile's work instead of stalling every k-tile.
         // k-tile-parallel gather: the 8 warps form G = pl.kgroups groups; group p
-        // produces every G-th k-tile of a tile, so G k-tiles are in production at
-        // once and a stage (stages are a multiple of G) always belongs to one
-        // group. Each of a group's 8/G warps handles 16*G rows as 2*G
+        // produces every G-th k-tile of the CTA's sequence (steps p, p + G, ...),
+        // so G k-tiles are in production at once and a stage (stages are a
+        // multiple of G) always belongs to one group. Each of a group's 8/G warps handles 16*G rows as 2*G
         // row-iterations of 8 rows, the corner loads running 2 row-iterations
         // ahead of the weighted sums.
         const int gw = warp - kWarpGather;
@@ -627,16 +660,23 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         cx.dsz = static_cast<uint32_t>(pl.desc_size);
         constexpr int kVec = 16 / sizeof(T);
         const int32_t ngroups = pl.Ug * pl.ntb;
-        uint32_t gr = 0, tile_i = 0;
+        uint32_t gr = 0;     // descriptor groups entered
+        uint32_t sbase = 0;  // CTA step of the current unit's first k-tile
         bool ok = true;
-        for (int64_t t = first_tile; t < pl.tiles_total && ok; t += tile_step, ++tile_i) {
-            const TileId id = decode_tile(pl, t);
+        for (int64_t pos = lo; pos < hi && ok;) {
+            const Unit un = unit_at(pl, pos, hi);
+            pos = un.t * KT + un.k1;
+            const TileId id = decode_tile(pl, un.t);
             int32_t q = 0;  // first k-tile (processing order) of the current group
-            for (int32_t gi = 0; gi < ngroups && ok; ++gi, ++gr) {
+            for (int32_t gi = 0; gi < ngroups && ok && q < un.k1; ++gi) {
                 const int32_t ul = gi / pl.ntb;
                 const int32_t b = gi - ul * pl.ntb;
                 const int32_t ntbg = min(kTapBlock, pl.K - b * kTapBlock);
                 const int32_t nktg = ntbg * pl.nch;
+                if (q + nktg <= un.k0) {  // group before the unit's range: not copied
+                    q += nktg;
+                    continue;
+                }
                 const int slot = gr & 1;
                 if (!__all_sync(0xffffffffu, mbar_wait_bounded(dfull_bar(slot), (gr >> 1) & 1, abort_flag, prm.status,
                                                                kSiteGatherEmpty))) {
@@ -645,11 +685,15 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                 }
                 const uint32_t dbase = d0 + slot * dslot;
                 const int64_t unit = static_cast<int64_t>(id.g) * pl.Ug + ul;
-                for (int32_t j = (pair - (q % G) + G) % G; j < nktg; j += G) {
+                // k-tile j of the group is CTA step sbase + q + j - k0; this warp
+                // group takes the steps equal to pair modulo G
+                const int32_t jlo = max(un.k0 - q, 0), jhi = min(un.k1 - q, nktg);
+                const uint32_t s_lo = sbase + static_cast<uint32_t>(q + jlo - un.k0);
+                for (int32_t j = jlo + (pair - static_cast<int32_t>(s_lo % G) + G) % G; j < jhi; j += G) {
                     const int32_t ch = j / ntbg;
                     const int32_t kb = j - ch * ntbg;
                     const int64_t cb = unit * pl.UP + static_cast<int64_t>(ch) * pl.BKc + cx.q4 * 2 * kVec;
-                    const uint32_t step = tile_i * static_cast<uint32_t>(KT) + static_cast<uint32_t>(q + j);
+                    const uint32_t step = sbase + static_cast<uint32_t>(q + j - un.k0);
                     const int st = step % S;
                     RowBuf rb[3];
                     row_issue<T, kF32Path>(cx, dbase, kb, cb, 0, rb[0]);
@@ -680,7 +724,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                 // every gather warp releases every descriptor group, used or not
                 __syncwarp();
                 if (lane == 0) mbar_arrive(dempty_bar(slot));
+                ++gr;
             }
+            sbase += static_cast<uint32_t>(un.k1 - un.k0);
         }
     } else {
         setmaxnreg_dec<kRegsEpi>();
@@ -690,8 +736,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         T* __restrict__ out = static_cast<T*>(prm.out);
         const T* __restrict__ bias = static_cast<const T*>(prm.bias);
         uint32_t i = 0;
-        for (int64_t t = first_tile; t < pl.tiles_total; t += tile_step, ++i) {
-            const TileId id = decode_tile(pl, t);
+        for (int64_t pos = lo; pos < hi; ++i) {
+            const Unit un = unit_at(pl, pos, hi);
+            pos = un.t * KT + un.k1;
+            const TileId id = decode_tile(pl, un.t);
             const int ab = static_cast<int>(i % pl.nacc);
             const uint32_t use = i / pl.nacc;
             if (!__all_sync(0xffffffffu,
@@ -704,6 +752,24 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
             const int64_t obase = (px.n * pl.Cout + static_cast<int64_t>(id.g) * pl.Og) * pl.P + hw;
             const uint32_t tl = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                 static_cast<uint32_t>(ab * pl.acc_cols);
+            if (un.k0 != 0 || un.k1 != KT) {
+                // split tile: this CTA's partial sum goes to its slot (slot 0 for
+                // its first unit, 1 for its last); the fix-up kernel adds the
+                // slots of each split tile in k order once every CTA is done
+                float* mine = prm.part + static_cast<size_t>(2 * blockIdx.x + (i == 0 ? 0 : 1)) *
+                                             static_cast<size_t>(pl.acc_cols) * kTileM;
+                for (int c32 = 0; c32 < pl.acc_cols; c32 += 32) {
+                    float vals[32];
+                    tmem_ld32(tl + static_cast<uint32_t>(c32), pl.acc_cols - c32 >= 32 ? 2 : 1, vals);
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        if (c < pl.acc_cols - c32) mine[static_cast<size_t>(c32 + c) * kTileM + row] = vals[c];
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acce_bar(ab));
+                continue;
+            }
             if (pl.epi_tma) {
                 // 16-channel chunks: TMEM -> +bias -> staging [16 ch][2 rows][16 px] -> one TMA box
                 // store per chunk (rows/cols past the image are clipped by the tensor map)
@@ -800,6 +866,124 @@ __global__ void wait_selftest_kernel(uint32_t* status, uint64_t limit_cycles) {
     __syncthreads();
 }
 
+// ---------------------------------------------------------------- split-tile fix-up
+// Grid (tiles_total, ceil(acc_cols / 32)), 128 threads = tile rows. For every
+// tile whose k-tiles fell to several CTAs: the CTAs' fp32 partial sums, in k
+// order, plus the bias, converted and stored as NCHW output. Launched
+// programmatically dependent on the fused kernel: it waits for that grid to
+// complete before reading. The planner keeps the k-tile count of all tiles
+// below 2^31, so the tile arithmetic here is 32-bit; warp 0 resolves the tile
+// and its contributors' slots once for the block.
+constexpr int kFixupSlots = 32;  // contributors resolved by warp 0; any further ones per thread
+
+template <typename T>
+__global__ void __launch_bounds__(kTileM) splitk_fixup_kernel(const float* __restrict__ part,
+                                                              const T* __restrict__ bias, T* __restrict__ out,
+                                                              Plan pl) {
+    __shared__ int64_t slot_off[kFixupSlots];
+    __shared__ int64_t tile_out0;
+    __shared__ int32_t tile_info[6];  // c_first, c_last (0 when not split), g, ncol0, rows, width
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const uint32_t t = blockIdx.x;
+    const uint32_t R = static_cast<uint32_t>(pl.kt_per_cta);
+    const uint32_t KT = static_cast<uint32_t>(pl.KT);
+    const int64_t slot_floats = static_cast<int64_t>(pl.acc_cols) * kTileM;
+    if (threadIdx.x < 32) {
+        const uint32_t c_first = (t * KT) / R, c_last = (t * KT + KT - 1) / R;
+        const uint32_t k = threadIdx.x;
+        if (c_first + k <= c_last && k < kFixupSlots) {
+            const uint32_t c = c_first + k;
+            slot_off[k] = static_cast<int64_t>(2 * c + ((c * R) / KT == t ? 0 : 1)) * slot_floats;
+        }
+        if (threadIdx.x == 0) {
+            tile_info[0] = static_cast<int32_t>(c_first);
+            tile_info[1] = c_first == c_last ? -1 : static_cast<int32_t>(c_last);
+            const uint32_t mtiles = static_cast<uint32_t>(pl.mtiles);
+            const uint32_t mt = t % mtiles;
+            const uint32_t rq = t / mtiles;
+            const uint32_t nt = rq % static_cast<uint32_t>(pl.ntiles_n);
+            const uint32_t g = rq / static_cast<uint32_t>(pl.ntiles_n);
+            tile_info[2] = static_cast<int32_t>(g);
+            tile_info[3] = static_cast<int32_t>(nt) * pl.acc_cols;
+            if (pl.tile_mode == 0) {
+                const int64_t p0 = static_cast<int64_t>(mt) * kTileM;  // first pixel of N*Ho*Wo
+                tile_info[4] = static_cast<int32_t>(min(static_cast<int64_t>(kTileM), pl.NP - p0));
+                tile_info[5] = 0;
+                tile_out0 = p0;
+            } else {
+                const uint32_t tx_n = static_cast<uint32_t>(pl.tiles_x);
+                const uint32_t per_img = tx_n * static_cast<uint32_t>(pl.tiles_y);
+                const uint32_t n = mt / per_img;
+                const uint32_t rem = mt - n * per_img;
+                const uint32_t ty = rem / tx_n;
+                const uint32_t tx = rem - ty * tx_n;
+                const int64_t ho0 = static_cast<int64_t>(ty) * pl.TH, wo0 = static_cast<int64_t>(tx) * pl.TW;
+                tile_info[4] = static_cast<int32_t>(min(static_cast<int64_t>(pl.TH), pl.Ho - ho0));
+                tile_info[5] = static_cast<int32_t>(min(static_cast<int64_t>(pl.TW), pl.Wo - wo0));
+                tile_out0 = (static_cast<int64_t>(n) * pl.Cout + static_cast<int64_t>(g) * pl.Og) * pl.P +
+                            ho0 * pl.Wo + wo0;
+            }
+        }
+    }
+    __syncthreads();
+    const int32_t c_first = tile_info[0], c_last = tile_info[1];
+    if (c_last < 0) return;  // one CTA summed the whole tile
+    const int32_t g = tile_info[2];
+    const int row = threadIdx.x;
+    int64_t obase;
+    if (pl.tile_mode == 0) {
+        if (row >= tile_info[4]) return;
+        const int64_t p = tile_out0 + row;
+        const int64_t n = p / pl.P;
+        obase = (n * pl.Cout + static_cast<int64_t>(g) * pl.Og) * pl.P + (p - n * pl.P);
+    } else {
+        const int r = row / pl.TW, c = row - r * pl.TW;
+        if (r >= tile_info[4] || c >= tile_info[5]) return;
+        obase = tile_out0 + static_cast<int64_t>(r) * pl.Wo + c;
+    }
+    const int32_t col0 = static_cast<int32_t>(blockIdx.y) * 32;
+    const int32_t ncol0 = tile_info[3] + col0;
+    const int32_t ncols = min(32, min(pl.acc_cols - col0, pl.Og - ncol0));
+    if (ncols <= 0) return;
+    const int64_t off = static_cast<int64_t>(col0) * kTileM + row;
+    auto slot_src = [&](int32_t c) -> const float* {
+        const int32_t k = c - c_first;
+        const int64_t so = k < kFixupSlots ? slot_off[k]
+                                           : static_cast<int64_t>(2 * static_cast<uint32_t>(c) +
+                                                                  ((static_cast<uint32_t>(c) * R) / KT == t ? 0 : 1)) *
+                                                 slot_floats;
+        return part + so + off;
+    };
+    // the first two contributors' loads all in flight together, then any others
+    float r[32], v[32];
+    const float* s0 = slot_src(c_first);
+    const float* s1 = slot_src(c_first + 1);
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+        r[e] = e < ncols ? s0[static_cast<int64_t>(e) * kTileM] : 0.f;
+        v[e] = e < ncols ? s1[static_cast<int64_t>(e) * kTileM] : 0.f;
+    }
+#pragma unroll
+    for (int e = 0; e < 32; ++e) r[e] += v[e];
+    for (int32_t c = c_first + 2; c <= c_last; ++c) {
+        const float* sc = slot_src(c);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] = e < ncols ? sc[static_cast<int64_t>(e) * kTileM] : 0.f;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) r[e] += v[e];
+    }
+    T* o = out + obase + static_cast<int64_t>(ncol0) * pl.P;
+    const T* bb = bias ? bias + static_cast<int64_t>(g) * pl.Og + ncol0 : nullptr;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+        if (e < ncols) {
+            float val = r[e];
+            if (bb) val += to_f(bb[e]);
+            from_f(val, o + static_cast<int64_t>(e) * pl.P);
+        }
+    }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -850,9 +1034,23 @@ cudaError_t launch_fused_t(const Plan& pl, const void* bias, void* out, void* ws
     prm.bias = bias;
     prm.out = out;
     prm.status = reinterpret_cast<uint32_t*>(base);
+    prm.part = reinterpret_cast<float*>(base + pl.off_part);
     prm.pl = pl;
     fused_kernel<DT><<<static_cast<unsigned>(pl.grid), kFusedThreads, pl.smem_bytes, st>>>(tmap, omap, prm);
-    return cudaGetLastError();
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || !splitk_needed(pl)) return e;
+    // split tiles: the fix-up, launched while the fused grid drains
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(pl.tiles_total), static_cast<unsigned>((pl.acc_cols + 31) / 32));
+    cfg.blockDim = dim3(kTileM);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, splitk_fixup_kernel<T>, static_cast<const float*>(prm.part),
+                              static_cast<const T*>(bias), static_cast<T*>(out), pl);
 }
 
 }  // namespace

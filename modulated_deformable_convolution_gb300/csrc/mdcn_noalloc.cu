@@ -17,7 +17,7 @@ namespace {
 
 // Largest workspace this entry point can serve (mdcn_workspace_size of the
 // call must not exceed it).
-constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
+constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;  // 64 MiB
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 

@@ -25,6 +25,7 @@ constexpr int kRegsGather = 176;
 constexpr int kRegsEpi = 80;
 static_assert(kRegsCtrl + 2 * kRegsGather + kRegsEpi == 4 * kRegsLaunch, "warpgroup register split must fit");
 constexpr int kSmemLimit = 227 * 1024;
+constexpr int kMaxCtas = 160;         // persistent CTAs at most (one per SM; the workspace holds 2 partial slots each)
 constexpr size_t kStatusBytes = 256;  // workspace header holding the device status word
 
 enum DType : int32_t { kF32 = 0, kF16 = 1, kBF16 = 2 };
@@ -66,7 +67,7 @@ struct Plan {
     int32_t nacc;            // accumulators in TMEM (2: epilogue overlaps the next tile)
     int32_t tmem_cols;
     int32_t stages;          // 2, 4, 6 or 8
-    int32_t kgroups;         // k-tiles produced concurrently by the gather warps (2 or 4; divides stages)
+    int32_t kgroups;         // k-tiles produced concurrently by the gather warps (1, 2 or 4; divides stages)
     int32_t a_bytes;         // one A stage (both tf32 halves for f32)
     int32_t b_bytes;         // one B stage
     int32_t desc_size;       // bytes per sample descriptor (16, or 32 for f32)
@@ -75,9 +76,15 @@ struct Plan {
     int32_t epi_bytes;       // shared-memory staging of the TMA-store epilogue
     int32_t smem_bytes;      // dynamic shared memory of the fused kernel
     int32_t grid;            // persistent CTAs
+    int64_t total_kt;        // k-tiles of all tiles: tiles_total * KT
+    int64_t kt_per_cta;      // stream-K: consecutive k-tiles per CTA (set with grid)
 
     // ---- workspace layout (byte offsets)
-    size_t off_xt, off_wp, off_desc, ws_bytes;
+    size_t off_xt, off_wp, off_desc, off_part, ws_bytes;
 };
+
+// True when some tile's k-tiles fall to more than one CTA (the CTA ranges do
+// not all end on tile boundaries), so the fix-up kernel has work.
+inline bool splitk_needed(const Plan& p) { return p.grid > 1 && p.kt_per_cta % p.KT != 0; }
 
 }  // namespace mdcn

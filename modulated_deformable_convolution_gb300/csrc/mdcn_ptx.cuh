@@ -242,6 +242,31 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 1 or 2 x (32 lanes x 16 columns) TMEM loads issued back to back, one wait.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, int n, float (&v)[32]) {
+    uint32_t r[32];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        if (k < n) {
+            asm volatile(
+                "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+                "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+                : "=r"(r[16 * k + 0]), "=r"(r[16 * k + 1]), "=r"(r[16 * k + 2]), "=r"(r[16 * k + 3]),
+                  "=r"(r[16 * k + 4]), "=r"(r[16 * k + 5]), "=r"(r[16 * k + 6]), "=r"(r[16 * k + 7]),
+                  "=r"(r[16 * k + 8]), "=r"(r[16 * k + 9]), "=r"(r[16 * k + 10]), "=r"(r[16 * k + 11]),
+                  "=r"(r[16 * k + 12]), "=r"(r[16 * k + 13]), "=r"(r[16 * k + 14]), "=r"(r[16 * k + 15])
+                : "r"(taddr + 16u * k)
+                : "memory");
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) r[16 * k + i] = 0u;
+        }
+    }
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 // Up to 4 x (32 lanes x 16 columns) TMEM loads issued back to back, one wait:
 // v[16*k + c] = column (taddr.col + 16*k + c) of this thread's lane, k < n.
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, int n, float (&v)[64]) {

@@ -68,6 +68,20 @@ def test_create_rejects_out_of_range_attrs(lib, bad):
     assert h.value == 1234  # untouched on error
 
 
+@pytest.mark.parametrize("tuning,ok", [
+    ((0, -1, 0, 0), True), ((4, 1, 8, 4), True), ((2, 0, 0, 1), True), ((6, -1, 0, 2), True),
+    ((0, -1, 0, 3), False), ((0, -1, 0, 8), False), ((1, -1, 0, 0), False), ((10, -1, 0, 0), False),
+    ((0, 2, 0, 0), False), ((0, -1, -1, 0), False),
+])
+def test_create_tuned_validates(lib, tuning, ok):
+    h = ctypes.c_void_p()
+    t = _abi.mdcn_tuning(*tuning)
+    s = lib.mdcn_create_tuned(ctypes.byref(attrs()), ctypes.byref(t), ctypes.byref(h))
+    assert s == (0 if ok else _abi.MDCN_ERR_ATTR)
+    if ok:
+        assert lib.mdcn_destroy(h) == 0
+
+
 def test_create_null(lib):
     h = ctypes.c_void_p()
     assert lib.mdcn_create(None, ctypes.byref(h)) == _abi.MDCN_ERR_NULL
@@ -194,6 +208,10 @@ def test_forward_without_device_reports_cuda_error(lib):
     d = dims(bias=True)
     p = [FAKE + 256 * i for i in range(7)]
     assert fwd(lib, h, p, d) in (_abi.MDCN_ERR_CUDA, _abi.MDCN_ERR_ARCH)
+    info = _abi.mdcn_plan_info()
+    assert lib.mdcn_query_plan(h, ctypes.byref(d), _abi.MDCN_F16, ctypes.byref(info)) in (
+        _abi.MDCN_ERR_CUDA, _abi.MDCN_ERR_ARCH)
+    assert lib.mdcn_query_plan(h, ctypes.byref(d), _abi.MDCN_F16, None) == _abi.MDCN_ERR_NULL
     lib.mdcn_destroy(h)
 
 

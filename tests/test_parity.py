@@ -130,6 +130,15 @@ TUNED = [
     # Cout = 512 in one tile (two MMAs, one TMEM accumulator), 2-D tiles
     (Case("f16_cout512_2d", "f16", N=1, Cin=64, Cout=512, H=16, W=16, deformable_group=2, bias=False, seed=45),
      dict(tile_mode=1)),
+    # one k-tile at a time across all 8 gather warps; two tap blocks (K = 15) of two channel chunks
+    (Case("bf16_k5x3_kg1", "bf16", N=2, Cin=128, Cout=64, H=12, W=12, kh=5, kw=3, padding=(2, 1), bias=True,
+          seed=46, offset_dist=("normal", 2.0)), dict(kgroups=1, stages=2)),
+    # four k-tiles at once; 1x1 kernel with 3 deformable groups: groups of one k-tile, most warps skip most groups
+    (Case("f16_1x1_dg3_kg4", "f16", N=2, Cin=96, Cout=32, H=9, W=11, kh=1, kw=1, padding=(0, 0),
+          deformable_group=3, bias=True, seed=47, offset_dist=("uniform", -3.0, 3.0)), dict(kgroups=4, stages=4)),
+    # fp32, 10 tiles of 9 k-tiles over 4 CTAs: 23 k-tiles each, tiles split at three points
+    (Case("f32_split4", "f32", N=1, Cin=64, Cout=48, H=24, W=24, group=2, deformable_group=2, bias=True, seed=48,
+          offset_dist=("normal", 2.0)), dict(max_ctas=4)),
 ]
 
 
@@ -142,12 +151,27 @@ def test_tuned_plans(oracle_mod, case, tuning):
 
 
 def test_tunings_agree_bitwise():
-    """Every plan choice computes the same sums in the same order."""
+    """The stage count and the number of k-tiles produced at once do not change
+    which sums are formed nor their order: outputs are bitwise equal."""
     case = CONFIGS["neck_f16"]
     inp = make_inputs(case)
     ref = gpu_out(case, inp)
-    for tuning in (dict(tile_mode=0), dict(tile_mode=1, stages=2), dict(stages=4, max_ctas=40)):
+    for tuning in (dict(stages=2), dict(stages=4, kgroups=4), dict(stages=4, kgroups=1), dict(stages=2, kgroups=1)):
         assert torch.equal(gpu_out(case, inp, tuning=tuning), ref), tuning
+
+
+@pytest.mark.parametrize("tuning", [dict(max_ctas=40), dict(max_ctas=7), dict(max_ctas=151), dict(tile_mode=0)],
+                         ids=["ctas40_whole_tiles", "ctas7", "ctas151", "linear_tiles"])
+def test_split_points_move(oracle_mod, tuning):
+    """Other CTA counts and tile shapes split other tiles between CTAs (and
+    max_ctas=40 splits none on this shape): every result stays within the
+    tolerance, on rows that cross tile and split boundaries."""
+    case = CONFIGS["neck_f16"]
+    inp = make_inputs(case)
+    gpu = np64(gpu_out(case, inp, tuning=tuning))
+    for r in (0, 7, 8, 40, 79):
+        ref = oracle_out(oracle_mod, case, inp, ho_range=(r, r + 1))
+        compare(gpu[:, :, r], ref[:, :, r], case.dtype, f"neck {tuning} row {r}")
 
 
 @pytest.mark.parametrize("case", [SWEEP[0], SWEEP[1], SWEEP[2], SWEEP[3]], ids=lambda c: c.name)
@@ -165,6 +189,24 @@ def test_im2col_gemm_neck_f16(oracle_mod):
     for r in (0, 40, 79):
         ref = oracle_out(oracle_mod, case, inp, ho_range=(r, r + 1))
         compare(gpu[:, :, r], ref[:, :, r], case.dtype, f"im2col neck row {r}")
+
+
+def test_query_plan_split_choice():
+    """The planner splits tiles between CTAs where that evens out the work
+    (neck: 200 tiles over one CTA per SM) and keeps whole tiles where the
+    split would not pay (largec: 2 tiles of 72 k-tiles per CTA)."""
+    dev = torch.device("cuda", 0)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    for name, split in (("neck_f16", 1), ("largec_f16", 0)):
+        case = CONFIGS[name]
+        d = {k: (None if v is None else v.to(dev)) for k, v in make_inputs(case).items()}
+        h = mdcn.Handle(**case.attrs())
+        plan = mdcn.mdcn_query_plan(h, d["x"], d["offset"], d["mask"], d["weight"], d["bias"])
+        assert plan["split"] == split, (name, plan)
+        assert plan["launches"] == 4 + split
+        assert plan["ctas"] <= sms and plan["ctas"] * plan["ktiles_per_cta"] >= plan["tiles"] * plan["ktiles_per_tile"]
+        if not split:
+            assert plan["ktiles_per_cta"] % plan["ktiles_per_tile"] == 0
 
 
 def test_zero_mask_gives_bias():
