@@ -1,5 +1,8 @@
 // Layout-prep kernels of the fused path:
-//   x      [N, Cin, H, W]      -> xt [N, H, W, Cp]   (channels-last, units padded)
+//   x      [N, Cin, H, W]      -> xt [N, H, W, Cp]   (channels-last, units padded;
+//                                 a register-blocked kernel where H*W and the
+//                                 unit are multiples of 16 bytes of elements,
+//                                 a shared-memory staged one otherwise)
 //   weight [Cout, Cg, kh, kw]  -> wp [R, KP]         (K-major in the fused K order)
 // For float32 the packed weight holds two row blocks: rows [0, Cout) the
 // tf32-rounded weight (hi) and rows [Cout, 2*Cout) the remainder (lo), the
@@ -82,6 +85,72 @@ __global__ void __launch_bounds__(256) nhwc_pad_kernel(const T* __restrict__ x, 
     }
 }
 
+// Register-blocked conversion, for images whose pixel count H*W and channel
+// unit U are multiples of kVec = 16 / sizeof(T) (8 for 16-bit types, 4 for
+// fp32). Each lane moves one kVec-channel x kVec-pixel block: kVec 16-byte
+// loads (kVec pixels of one channel each), a transpose in registers, and kVec
+// 16-byte stores (kVec channels of one pixel each). A warp covers 8 channel
+// groups x 4 pixel groups; output channels in a unit's padding are written as
+// zeros. Grid (ceil(pixel blocks / 8), channel blocks, N), 8 warps per block,
+// one pixel block (4 * kVec pixels) per warp. Block (0, 0, 0) also clears the
+// device status word.
+template <typename T>
+__global__ void __launch_bounds__(256) nhwc_block_kernel(const T* __restrict__ x, T* __restrict__ xt,
+                                                         uint32_t* __restrict__ status, int32_t Cin, int64_t P,
+                                                         int64_t Cp, int32_t U, int32_t UP) {
+    constexpr int kVec = 16 / sizeof(T);
+    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0) *status = 0u;
+    const int lane = threadIdx.x & 31;
+    const int cg = lane & 7, pg = lane >> 3;
+    const int64_t n = blockIdx.z;
+    const int64_t oc0 = (static_cast<int64_t>(blockIdx.y) * 8 + cg) * kVec;  // output channel (padded)
+    const int64_t p0 = ((static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5)) * 4 + pg) * kVec;
+    if (oc0 >= Cp || p0 >= P) return;
+    const int32_t unit = static_cast<int32_t>(oc0 / UP);
+    const int32_t within = static_cast<int32_t>(oc0) - unit * UP;
+    uint4 in[kVec];
+    if (within < U) {
+        const T* src = x + (n * Cin + static_cast<int64_t>(unit) * U + within) * P + p0;
+#pragma unroll
+        for (int i = 0; i < kVec; ++i) in[i] = __ldg(reinterpret_cast<const uint4*>(src + i * P));
+    } else {
+#pragma unroll
+        for (int i = 0; i < kVec; ++i) in[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    uint4 out[kVec];
+    if constexpr (kVec == 8) {
+        // 8x8 halves: pair channels (c, c+1) per pixel, then pick words
+        uint32_t w[8][4], t[8][4];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            w[c][0] = in[c].x;
+            w[c][1] = in[c].y;
+            w[c][2] = in[c].z;
+            w[c][3] = in[c].w;
+        }
+#pragma unroll
+        for (int c = 0; c < 8; c += 2)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                t[c][k] = __byte_perm(w[c][k], w[c + 1][k], 0x5410);      // (c, c+1) at pixel 2k
+                t[c + 1][k] = __byte_perm(w[c][k], w[c + 1][k], 0x7632);  // (c, c+1) at pixel 2k+1
+            }
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            out[q] = make_uint4(t[0 + (q & 1)][q >> 1], t[2 + (q & 1)][q >> 1], t[4 + (q & 1)][q >> 1],
+                                t[6 + (q & 1)][q >> 1]);
+    } else {
+        // 4x4 words
+        out[0] = make_uint4(in[0].x, in[1].x, in[2].x, in[3].x);
+        out[1] = make_uint4(in[0].y, in[1].y, in[2].y, in[3].y);
+        out[2] = make_uint4(in[0].z, in[1].z, in[2].z, in[3].z);
+        out[3] = make_uint4(in[0].w, in[1].w, in[2].w, in[3].w);
+    }
+    T* dst = xt + (n * P + p0) * Cp + oc0;
+#pragma unroll
+    for (int q = 0; q < kVec; ++q) *reinterpret_cast<uint4*>(dst + q * Cp) = out[q];
+}
+
 template <typename T>
 __device__ __forceinline__ float load_f(const T* p);
 template <>
@@ -141,6 +210,17 @@ static cudaError_t prep_input_t(const Plan& pl, const void* x, void* ws, cudaStr
     uint8_t* base = static_cast<uint8_t*>(ws);
     uint32_t* status = reinterpret_cast<uint32_t*>(base);
     T* xt = reinterpret_cast<T*>(base + pl.off_xt);
+    constexpr int64_t kVec = 16 / static_cast<int64_t>(sizeof(T));
+    const int64_t P = pl.H * pl.W;
+    const int64_t pblocks = (P / kVec + 3) / 4;        // 4 * kVec pixels per warp
+    const int64_t cblocks = (pl.Cp / kVec + 7) / 8;    // 8 * kVec output channels per warp
+    if (P % kVec == 0 && pl.U % kVec == 0 && pl.N <= 65535 && cblocks <= 65535 && (pblocks + 7) / 8 <= 2147483647) {
+        const dim3 grid(static_cast<unsigned>((pblocks + 7) / 8), static_cast<unsigned>(cblocks),
+                        static_cast<unsigned>(pl.N));
+        nhwc_block_kernel<T><<<grid, 256, 0, st>>>(static_cast<const T*>(x), xt, status,
+                                                   static_cast<int32_t>(pl.Cin), P, pl.Cp, pl.U, pl.UP);
+        return cudaGetLastError();
+    }
     const int64_t pitch_bytes = (pl.Cp + 16 / static_cast<int64_t>(sizeof(T))) * static_cast<int64_t>(sizeof(T));
     int64_t wc = kPrepSmemBytes / pitch_bytes;
     if (wc > 32) wc = 32;
