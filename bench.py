@@ -250,7 +250,6 @@ def run_ours(args, case, world, rank, local, dist):
     def step(ev=None):
         mdcn.mdcn_prepare_input(h, x, off, m, w, b, ws, stream)
         mdcn.mdcn_pack_weight(h, x, off, m, w, b, ws, stream)
-        mdcn.mdcn_prepare_samples(h, x, off, m, w, b, ws, stream)
         if ev is not None:
             ev[0].record(stream)
         mdcn.mdcn_forward_prepared(h, x, off, m, w, b, out, ws, stream)
@@ -370,7 +369,7 @@ def run_ours(args, case, world, rank, local, dist):
         "config": {"workload": describe(case), "global_batch": case.N * world,
                    "l2": "flushed before every timed step (256 MiB write outside the events)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "step": "channels-last x + weight pack + sampling descriptors + fused kernel"
+                   "step": "channels-last x + weight pack + fused kernel (sampling in-kernel)"
                            + (" + split-tile fix-up" if plan["split"] else "") + f" ({plan['launches']} launches)",
                    "plan": plan},
         "step_ms": {"mean": ms, "p10": sorted(step_ms)[len(step_ms) // 10],
@@ -404,7 +403,6 @@ def run_fused_only(args, case):
     st = torch.cuda.current_stream(dev)
     mdcn.mdcn_prepare_input(h, x, off, m, w, b, ws, st)
     mdcn.mdcn_pack_weight(h, x, off, m, w, b, ws, st)
-    mdcn.mdcn_prepare_samples(h, x, off, m, w, b, ws, st)
     mdcn.mdcn_forward_prepared(h, x, off, m, w, b, out, ws, st)
     torch.cuda.synchronize()
     torch.cuda._sleep(int(2e5) * args.fused_only)

@@ -127,9 +127,8 @@ mdcn_status mdcn_destroy(mdcn_handle handle);
 mdcn_status mdcn_output_dims(mdcn_handle handle, const mdcn_dims* dims, int64_t out_dims[4]);
 
 /* Bytes of device workspace mdcn_forward needs for these dims and dtype
- * (a status word, the channels-last copy of x, the repacked weight, the
- * sampling descriptors, and the fp32 partial sums of output tiles split
- * between CTAs). Host only. */
+ * (a status word, the channels-last copy of x, the repacked weight, and the
+ * fp32 partial sums of output tiles split between CTAs). Host only. */
 mdcn_status mdcn_workspace_size(mdcn_handle handle, const mdcn_dims* dims, mdcn_dtype dtype,
                                 size_t* bytes);
 
@@ -142,7 +141,7 @@ typedef struct mdcn_plan_info {
     int32_t ctas;           /* persistent CTAs of the fused kernel */
     int32_t split;          /* 1 when some tile is split between CTAs (the fix-up kernel runs) */
     int32_t stages, kgroups, tile_mode;
-    int32_t launches;       /* kernels one mdcn_forward launches: 4, or 5 with the fix-up */
+    int32_t launches;       /* kernels one mdcn_forward launches: 3, or 4 with the fix-up */
 } mdcn_plan_info;
 
 /* Errors as mdcn_workspace_size, plus MDCN_ERR_ARCH / MDCN_ERR_CUDA from the
@@ -150,15 +149,15 @@ typedef struct mdcn_plan_info {
 mdcn_status mdcn_query_plan(mdcn_handle handle, const mdcn_dims* dims, mdcn_dtype dtype, mdcn_plan_info* info);
 
 /* The forward pass (section 5, steps 1-3) as one fused implicit-GEMM kernel:
- * producer warps sample and modulate the columns straight into shared
- * memory, tcgen05 tensor-core MMAs accumulate in tensor memory, the epilogue
- * adds the bias and writes NCHW. The im2col column matrix never reaches
- * device memory. Persistent CTAs (one per SM) take equal consecutive ranges
- * of the k-tiles of all output tiles; a tile split between CTAs is summed
- * from their fp32 partials, in k order, by a small fix-up kernel launched
- * right after (programmatic dependent launch).
- * Three small kernels run first, into workspace: x to channels-last, the
- * weight repack, and the sampling descriptors.
+ * producer warps compute each sampling point from offset and mask, gather
+ * and modulate the columns straight into shared memory, tcgen05 tensor-core
+ * MMAs accumulate in tensor memory, the epilogue adds the bias and writes
+ * NCHW. The im2col column matrix never reaches device memory. Persistent CTAs
+ * (one per SM) take equal consecutive ranges of the k-tiles of all output
+ * tiles; a tile split between CTAs is summed from their fp32 partials, in k
+ * order, by a small fix-up kernel launched right after (programmatic
+ * dependent launch). Two small kernels run first, into workspace: x to
+ * channels-last and the weight repack.
  *   x [N,Cin,H,W], offset [N,2*dg*kh*kw,Ho,Wo], mask [N,dg*kh*kw,Ho,Wo],
  *   weight [Cout,Cin/group,kh,kw], bias_or_null [Cout] or NULL,
  *   out [N,Cout,Ho,Wo] (written), workspace of workspace_bytes (scratch,
@@ -171,28 +170,24 @@ mdcn_status mdcn_forward(mdcn_handle handle, const void* x, const void* offset, 
                          void* workspace, size_t workspace_bytes,
                          const mdcn_dims* dims, mdcn_dtype dtype, void* stream);
 
-/* The four steps of mdcn_forward as separate calls, for callers that pack a
+/* The three steps of mdcn_forward as separate calls, for callers that pack a
  * constant weight once or time the steps on their own. Same argument rules
- * and workspace as mdcn_forward; x, weight, offset and mask are read only by
- * the step that names them. Run on one stream, with one workspace, and
- * mdcn_forward_prepared after the other three:
+ * and workspace as mdcn_forward; x and weight are read only by the step that
+ * names them. Run on one stream, with one workspace, and
+ * mdcn_forward_prepared after the other two:
  *   mdcn_prepare_input:    x -> channels-last copy in workspace; clears the
  *                          workspace status word;
  *   mdcn_pack_weight:      weight -> packed K-major copy in workspace;
- *   mdcn_prepare_samples:  offset, mask -> per (pixel, deformable group, tap)
- *                          sampling descriptors in workspace (section 5
- *                          step 1: point, corner validity, bilinear weights
- *                          times the mask);
- *   mdcn_forward_prepared: the fused gather + contraction + bias kernel, and
+ *   mdcn_forward_prepared: the fused kernel (sampling from offset and mask,
+ *                          section 5 step 1; gather; contraction; bias), and
  *                          the split-tile fix-up when tiles are split. */
 mdcn_status mdcn_prepare_input(mdcn_handle handle, const void* x, void* workspace, size_t workspace_bytes,
                                const mdcn_dims* dims, mdcn_dtype dtype, void* stream);
 mdcn_status mdcn_pack_weight(mdcn_handle handle, const void* weight, void* workspace, size_t workspace_bytes,
                              const mdcn_dims* dims, mdcn_dtype dtype, void* stream);
-mdcn_status mdcn_prepare_samples(mdcn_handle handle, const void* offset, const void* mask, void* workspace,
-                                 size_t workspace_bytes, const mdcn_dims* dims, mdcn_dtype dtype, void* stream);
-mdcn_status mdcn_forward_prepared(mdcn_handle handle, const void* bias_or_null, void* out, void* workspace,
-                                  size_t workspace_bytes, const mdcn_dims* dims, mdcn_dtype dtype, void* stream);
+mdcn_status mdcn_forward_prepared(mdcn_handle handle, const void* offset, const void* mask, const void* bias_or_null,
+                                  void* out, void* workspace, size_t workspace_bytes, const mdcn_dims* dims,
+                                  mdcn_dtype dtype, void* stream);
 
 /* Workspace bytes for mdcn_forward_im2col_gemm (the column matrix of the
  * whole batch plus a float32 GEMM output). Host only. */

@@ -22,7 +22,7 @@ from ._abi import (MDCN_BF16, MDCN_ERR_ALIGN, MDCN_ERR_ARCH, MDCN_ERR_ATTR, MDCN
 
 __all__ = ["Handle", "MdcnError", "forward", "mdcn_create", "mdcn_destroy", "mdcn_output_dims",
            "mdcn_workspace_size", "mdcn_forward", "mdcn_prepare_input", "mdcn_pack_weight",
-           "mdcn_prepare_samples", "mdcn_forward_prepared", "mdcn_im2col_gemm_workspace_size", "mdcn_forward_im2col_gemm",
+           "mdcn_forward_prepared", "mdcn_im2col_gemm_workspace_size", "mdcn_forward_im2col_gemm",
            "mdcn_query_plan", "mdcn_query_status", "mdcn_selftest_wait_timeout", "mdcn_status_string",
            "library_path"]
 
@@ -220,22 +220,14 @@ def mdcn_pack_weight(handle, x, offset, mask, weight, bias, workspace, stream=No
                                        _stream(x.device, stream)), "mdcn_pack_weight")
 
 
-def mdcn_prepare_samples(handle, x, offset, mask, weight, bias, workspace, stream=None) -> None:
-    """Step 3 of mdcn_forward: offset, mask -> sampling descriptors in workspace."""
-    d = _dims(x, offset, mask, weight, bias)
-    with torch.cuda.device(x.device):
-        _check(_lib().mdcn_prepare_samples(_hval(handle), _ptr(offset), _ptr(mask), _ptr(workspace),
-                                           workspace.numel() * workspace.element_size(), ctypes.byref(d), _dtype(x),
-                                           _stream(x.device, stream)), "mdcn_prepare_samples")
-
-
 def mdcn_forward_prepared(handle, x, offset, mask, weight, bias, out, workspace, stream=None) -> None:
-    """Step 4 of mdcn_forward: the fused kernel on the prepared workspace
-    (x, offset, mask and weight only supply dims and dtype here)."""
+    """Step 3 of mdcn_forward: the fused kernel on the prepared workspace,
+    sampling from offset and mask (x and weight only supply dims and dtype)."""
     _check_tensors(x, offset, mask, weight, bias, out)
     d = _dims(x, offset, mask, weight, bias)
     with torch.cuda.device(x.device):
-        _check(_lib().mdcn_forward_prepared(_hval(handle), _ptr(bias), _ptr(out), _ptr(workspace),
+        _check(_lib().mdcn_forward_prepared(_hval(handle), _ptr(offset), _ptr(mask), _ptr(bias), _ptr(out),
+                                            _ptr(workspace),
                                             workspace.numel() * workspace.element_size(), ctypes.byref(d), _dtype(x),
                                             _stream(x.device, stream)), "mdcn_forward_prepared")
 

@@ -89,11 +89,8 @@ def load(path: str = LIB_PATH):
         lib.mdcn_prepare_input.restype = st
         lib.mdcn_pack_weight.argtypes = [vp, vp, vp, ctypes.c_size_t, ctypes.POINTER(mdcn_dims), ctypes.c_int, vp]
         lib.mdcn_pack_weight.restype = st
-        lib.mdcn_prepare_samples.argtypes = [vp, vp, vp, vp, ctypes.c_size_t, ctypes.POINTER(mdcn_dims), ctypes.c_int,
-                                             vp]
-        lib.mdcn_prepare_samples.restype = st
-        lib.mdcn_forward_prepared.argtypes = [vp, vp, vp, vp, ctypes.c_size_t, ctypes.POINTER(mdcn_dims), ctypes.c_int,
-                                              vp]
+        lib.mdcn_forward_prepared.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_size_t, ctypes.POINTER(mdcn_dims),
+                                              ctypes.c_int, vp]
         lib.mdcn_forward_prepared.restype = st
         lib.mdcn_im2col_gemm_workspace_size.argtypes = [vp, ctypes.POINTER(mdcn_dims), ctypes.c_int,
                                                         ctypes.POINTER(ctypes.c_size_t)]

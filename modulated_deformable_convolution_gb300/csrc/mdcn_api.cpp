@@ -139,6 +139,7 @@ mdcn_status make_plan(const mdcn_attrs& a, const mdcn_tuning& tuning, const mdcn
     p.Cd = static_cast<int32_t>(Cd);
     p.P = p.Ho * p.Wo;
     p.NP = p.N * p.P;
+    if (p.NP > kI31) return MDCN_ERR_UNSUPPORTED;  // 32-bit pixel arithmetic in the kernels
 
     const int64_t elem = dtype == MDCN_F32 ? 4 : 2;
     p.BKc = static_cast<int32_t>(128 / elem);
@@ -175,8 +176,8 @@ mdcn_status make_plan(const mdcn_attrs& a, const mdcn_tuning& tuning, const mdcn
 
     // pixel tiles: 8 x 16 blocks of one image when they waste (almost) no rows,
     // else 128 consecutive pixels of N*Ho*Wo
-    p.TH = 8;
-    p.TW = 16;
+    p.TH = mdcn::kTileH;
+    p.TW = mdcn::kTileW;
     p.tiles_x = ceil_div(p.Wo, p.TW);
     p.tiles_y = ceil_div(p.Ho, p.TH);
     const double waste = 1.0 - static_cast<double>(p.P) / static_cast<double>(p.tiles_x * p.TW * p.tiles_y * p.TH);
@@ -221,20 +222,13 @@ mdcn_status make_plan(const mdcn_attrs& a, const mdcn_tuning& tuning, const mdcn
     p.wp_rows = rows;
     int64_t wpb = rows;
     if (!mul_ok(wpb, p.KP) || !mul_ok(wpb, elem) || rows > kI31) return MDCN_ERR_UNSUPPORTED;
-    // sample descriptors: mtiles x dg x K x 128 rows x desc_size
-    int64_t dbytes = p.mtiles;
-    if (!mul_ok(dbytes, p.dg) || !mul_ok(dbytes, p.K) || !mul_ok(dbytes, mdcn::kTileM) ||
-        !mul_ok(dbytes, p.desc_size))
-        return MDCN_ERR_UNSUPPORTED;
-    if (p.mtiles > 2147483647 || p.dg > 65535 || ceil_div(K, 3) > 65535) return MDCN_ERR_UNSUPPORTED;  // sampling grid
     // stream-K: fp32 partial accumulators of split tiles, 2 slots per CTA
     p.total_kt = p.tiles_total;
     if (!mul_ok(p.total_kt, p.KT) || p.total_kt > kI31) return MDCN_ERR_UNSUPPORTED;  // 32-bit tile arithmetic
     const int64_t part_bytes = static_cast<int64_t>(2) * mdcn::kMaxCtas * p.acc_cols * mdcn::kTileM * 4;
     p.off_xt = mdcn::kStatusBytes;
     p.off_wp = align256(p.off_xt + static_cast<size_t>(xt));
-    p.off_desc = align256(p.off_wp + static_cast<size_t>(wpb));
-    p.off_part = align256(p.off_desc + static_cast<size_t>(dbytes));
+    p.off_part = align256(p.off_wp + static_cast<size_t>(wpb));
     p.ws_bytes = align256(p.off_part + static_cast<size_t>(part_bytes));
     *pl = p;
     return MDCN_OK;
@@ -369,7 +363,7 @@ mdcn_status mdcn_query_plan(mdcn_handle handle, const mdcn_dims* dims, mdcn_dtyp
     info->stages = p.stages;
     info->kgroups = p.kgroups;
     info->tile_mode = p.tile_mode;
-    info->launches = 4 + info->split;
+    info->launches = 3 + info->split;
     return MDCN_OK;
 }
 
@@ -384,8 +378,7 @@ mdcn_status mdcn_forward(mdcn_handle handle, const void* x, const void* offset, 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = mdcn::launch_prep_input(p, x, workspace, st);
     if (e == cudaSuccess) e = mdcn::launch_pack_weight(p, weight, workspace, st);
-    if (e == cudaSuccess) e = mdcn::launch_sample(p, offset, mask, workspace, st);
-    if (e == cudaSuccess) e = mdcn::launch_fused(p, bias_or_null, out, workspace, st);
+    if (e == cudaSuccess) e = mdcn::launch_fused(p, offset, mask, bias_or_null, out, workspace, st);
     if (e != cudaSuccess) return cuda_fail(e);
     return MDCN_OK;
 }
@@ -414,27 +407,18 @@ mdcn_status mdcn_pack_weight(mdcn_handle handle, const void* weight, void* works
     return MDCN_OK;
 }
 
-mdcn_status mdcn_prepare_samples(mdcn_handle handle, const void* offset, const void* mask, void* workspace,
-                                 size_t workspace_bytes, const mdcn_dims* dims, mdcn_dtype dtype, void* stream) {
-    if (!handle || !offset || !mask || !workspace || !dims) return MDCN_ERR_NULL;
-    if (!aligned16(offset) || !aligned16(mask) || !aligned16(workspace)) return MDCN_ERR_ALIGN;
-    Plan p;
-    mdcn_status s = plan_for_call(handle, dims, dtype, workspace_bytes, &p);
-    if (s != MDCN_OK) return s;
-    cudaError_t e = mdcn::launch_sample(p, offset, mask, workspace, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(e);
-    return MDCN_OK;
-}
-
-mdcn_status mdcn_forward_prepared(mdcn_handle handle, const void* bias_or_null, void* out, void* workspace,
-                                  size_t workspace_bytes, const mdcn_dims* dims, mdcn_dtype dtype, void* stream) {
-    if (!handle || !out || !workspace || !dims) return MDCN_ERR_NULL;
+mdcn_status mdcn_forward_prepared(mdcn_handle handle, const void* offset, const void* mask, const void* bias_or_null,
+                                  void* out, void* workspace, size_t workspace_bytes, const mdcn_dims* dims,
+                                  mdcn_dtype dtype, void* stream) {
+    if (!handle || !offset || !mask || !out || !workspace || !dims) return MDCN_ERR_NULL;
     if ((bias_or_null == nullptr) != (dims->bias == 0)) return bias_or_null ? MDCN_ERR_SHAPE : MDCN_ERR_NULL;
-    if (!aligned16(out) || !aligned16(workspace) || (bias_or_null && !aligned16(bias_or_null))) return MDCN_ERR_ALIGN;
+    if (!aligned16(offset) || !aligned16(mask) || !aligned16(out) || !aligned16(workspace) ||
+        (bias_or_null && !aligned16(bias_or_null)))
+        return MDCN_ERR_ALIGN;
     Plan p;
     mdcn_status s = plan_for_call(handle, dims, dtype, workspace_bytes, &p);
     if (s != MDCN_OK) return s;
-    cudaError_t e = mdcn::launch_fused(p, bias_or_null, out, workspace, static_cast<cudaStream_t>(stream));
+    cudaError_t e = mdcn::launch_fused(p, offset, mask, bias_or_null, out, workspace, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
     return MDCN_OK;
 }

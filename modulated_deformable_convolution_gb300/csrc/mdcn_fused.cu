@@ -1,26 +1,24 @@
-// Sampling kernel and fused implicit-GEMM kernel of the modulated deformable
-// convolution forward ("TensorRT plugin walkthrough: modulatedDeformConvPlugin",
-// section 5, steps 1-3, without the column buffer).
+// Fused implicit-GEMM kernel of the modulated deformable convolution forward
+// ("TensorRT plugin walkthrough: modulatedDeformConvPlugin", section 5, steps
+// 1-3, without the column buffer), and the fix-up of tiles split between CTAs.
 //
-// sample_kernel: one 16-byte (fp32: 32-byte) descriptor per (pixel tile,
-// deformable group, tap, tile row): the sampling point
-// (ho*sh - ph + i*dh + dh_off, wo*sw - pw + j*dw + dw_off), its 4 corner
-// validity bits and the 4 bilinear weights times the mask, laid out in the
-// fused kernel's tile order in workspace (it stays in L2).
-//
-// fused_kernel: persistent CTAs (one per SM) loop over output tiles of 128
-// pixels x (nsub*BNs) output channels of one convolution group. Warp roles:
-//   warp 0      TMA: weight k-tiles (K-major, 128-byte swizzle) -> B stages,
-//               and bulk copies of descriptor groups -> two-slot ring
+// fused_kernel: persistent CTAs (one per SM) take equal consecutive ranges of
+// the k-tiles of all output tiles (128 pixels x (nsub*BNs) output channels of
+// one convolution group). Warp roles:
+//   warp 0      TMA: weight k-tiles (K-major, 128-byte swizzle) -> B stages
 //   warp 1      allocates tensor memory; lane 0 issues tcgen05.mma
 //               (A = modulated columns, B = weights, D = fp32 in TMEM,
 //               two accumulators so the epilogue overlaps the next tile)
+//   warps 2-3   sampling: from offset and mask, each tile row's sampling
+//               point, corner validity and bilinear weights times the mask
+//               (one descriptor per row and tap) for a tap block of one
+//               deformable group at a time -> two-slot ring in shared memory
 //   warps 4-11  gather, as G warp groups each producing every G-th k-tile
 //               (one tap, 128 bytes of channels): per row, 4 lanes x 32 bytes of
 //               the 4 corners of the channels-last copy of x, weighted sum,
 //               128-byte-swizzled store into the A stage
-//   warps 12-15 epilogue: TMEM -> registers -> +bias -> NCHW output
-//   warps 2-3   idle
+//   warps 12-15 epilogue: TMEM -> registers -> +bias -> NCHW output (or the
+//               fp32 partial sum of a split tile -> workspace)
 // Hand-offs use mbarriers; every wait is bounded (mdcn_ptx.cuh), and a wait
 // that gives up raises a CTA-wide abort that every role observes.
 #include <cuda.h>
@@ -62,7 +60,8 @@ struct Elem<kBF16> {
 
 struct FusedParams {
     const void* xt;
-    const void* desc;
+    const void* offset;
+    const void* mask;
     const void* bias;
     void* out;
     uint32_t* status;
@@ -106,24 +105,31 @@ struct Pixel {
     bool valid;
 };
 
-__device__ __forceinline__ Pixel tile_pixel(const Plan& pl, int64_t mt, int r) {
+// Pixel indices fit in 32 bits (the planner keeps N*Ho*Wo below 2^31).
+__device__ __forceinline__ Pixel tile_pixel(const Plan& pl, int64_t mt64, int r) {
     Pixel px;
+    const uint32_t mt = static_cast<uint32_t>(mt64);
     if (pl.tile_mode == 0) {
-        const int64_t p = mt * kTileM + r;
-        px.valid = p < pl.NP;
-        const int64_t pp = px.valid ? p : 0;
-        px.n = pp / pl.P;
-        const int64_t hw = pp - px.n * pl.P;
-        px.ho = hw / pl.Wo;
-        px.wo = hw - px.ho * pl.Wo;
+        const uint32_t p = mt * kTileM + static_cast<uint32_t>(r);
+        px.valid = p < static_cast<uint32_t>(pl.NP);
+        const uint32_t pp = px.valid ? p : 0u;
+        const uint32_t P = static_cast<uint32_t>(pl.P), Wo = static_cast<uint32_t>(pl.Wo);
+        const uint32_t n = pp / P;
+        const uint32_t hw = pp - n * P;
+        const uint32_t ho = hw / Wo;
+        px.n = n;
+        px.ho = ho;
+        px.wo = hw - ho * Wo;
     } else {
-        const int64_t per_img = pl.tiles_x * pl.tiles_y;
-        px.n = mt / per_img;
-        const int64_t rem = mt - px.n * per_img;
-        const int64_t ty = rem / pl.tiles_x;
-        const int64_t tx = rem - ty * pl.tiles_x;
-        px.ho = ty * pl.TH + r / pl.TW;
-        px.wo = tx * pl.TW + r % pl.TW;
+        const uint32_t tiles_x = static_cast<uint32_t>(pl.tiles_x);
+        const uint32_t per_img = tiles_x * static_cast<uint32_t>(pl.tiles_y);
+        const uint32_t n = mt / per_img;
+        const uint32_t rem = mt - n * per_img;
+        const uint32_t ty = rem / tiles_x;
+        const uint32_t tx = rem - ty * tiles_x;
+        px.n = n;
+        px.ho = static_cast<int64_t>(ty * kTileH + static_cast<uint32_t>(r) / kTileW);
+        px.wo = static_cast<int64_t>(tx * kTileW + static_cast<uint32_t>(r) % kTileW);
         px.valid = px.ho < pl.Ho && px.wo < pl.Wo;
     }
     return px;
@@ -166,91 +172,156 @@ __device__ __forceinline__ uint32_t blend(uint32_t wa, uint32_t wb, uint32_t v0,
     return *reinterpret_cast<uint32_t*>(&acc);
 }
 
-// ---------------------------------------------------------------- sampling kernel
-// Grid (mtiles, dg, ceil(K/3)), 128 threads = tile rows; each thread writes
-// the descriptors of its pixel for 3 taps:
-// desc[((mt*dg + gd)*K + tap)*128 + row]. Descriptor: int64 element offset of
+// ---------------------------------------------------------------- sample descriptors
+// Descriptor of (tile row, deformable group, tap): the int64 element offset of
 // corner (y0, x0) in the channels-last x with the 4 corner-valid bits in its
-// low bits (offsets are multiples of 32 elements), then the 4 weights
-// (16-bit pairs for 16-bit types; fp32 words in a second 16 bytes for fp32).
-constexpr int kSampleTaps = 3;
+// low bits (offsets are multiples of 32 elements), then the 4 bilinear
+// weights times the mask (16-bit pairs for 16-bit types; fp32 words in a
+// second 16 bytes for fp32). Sampling point (section 5 step 1):
+// (ho*sh - ph + i*dh + dh_off, wo*sw - pw + j*dw + dw_off); a point outside
+// (-1, H) x (-1, W) and the corners outside the image contribute nothing.
+//
+// Where a tile row's sampling inputs are: its pixel, and its offset and mask
+// elements of tap tap0 (taps follow at a stride of P elements).
+template <typename T>
+struct SampleRow {
+    const T* po;   // offset channel 2*tap0 (h) of the row's pixel; w follows at +P
+    const T* pm;   // mask channel tap0
+    float hbase, wbase;
+    int64_t nbase;
+    bool valid;
+};
 
 template <typename T>
-__global__ void __launch_bounds__(kTileM) sample_kernel(const T* __restrict__ offset, const T* __restrict__ mask,
-                                                        uint8_t* __restrict__ desc, Plan pl) {
-    const int64_t mt = blockIdx.x;
-    const int64_t gd = blockIdx.y;
-    const int32_t tap0 = blockIdx.z * kSampleTaps;
-    const int32_t ntap = min(kSampleTaps, pl.K - tap0);
-    const int row = threadIdx.x;
+__device__ __forceinline__ SampleRow<T> sample_row_at(const Plan& pl, const T* offset, const T* mask, int64_t mt,
+                                                      int64_t gd, int row, int32_t tap0) {
     const Pixel q = tile_pixel(pl, mt, row);
     const int64_t K = pl.K;
     const int64_t P = pl.P;
     const int64_t n = q.valid ? q.n : 0;
     const int64_t hw = q.valid ? q.ho * pl.Wo + q.wo : 0;
-    const T* po = offset + (n * 2 * pl.dg * K + gd * 2 * K) * P + hw;
-    const T* pm = mask + (n * pl.dg * K + gd * K) * P + hw;
-    const float hbase = static_cast<float>(q.ho * pl.sh - pl.ph);
-    const float wbase = static_cast<float>(q.wo * pl.sw - pl.pw);
-    const int64_t nbase = q.n * pl.H;
-    const uint32_t dsz = static_cast<uint32_t>(pl.desc_size);
-    uint8_t* dst = desc + ((mt * pl.dg + gd) * K * kTileM + row) * dsz;
-    float dhv[kSampleTaps], dwv[kSampleTaps], mv[kSampleTaps];
-#pragma unroll
-    for (int kb = 0; kb < kSampleTaps; ++kb) {
-        const int64_t tap = tap0 + (kb < ntap ? kb : 0);
-        dhv[kb] = to_f(po[2 * tap * P]);
-        dwv[kb] = to_f(po[(2 * tap + 1) * P]);
-        mv[kb] = to_f(pm[tap * P]);
+    SampleRow<T> r;
+    r.po = offset + (n * 2 * pl.dg * K + gd * 2 * K + 2 * static_cast<int64_t>(tap0)) * P + hw;
+    r.pm = mask + (n * pl.dg * K + gd * K + tap0) * P + hw;
+    r.hbase = static_cast<float>(q.ho * pl.sh - pl.ph);
+    r.wbase = static_cast<float>(q.wo * pl.sw - pl.pw);
+    r.nbase = q.n * pl.H;
+    r.valid = q.valid;
+    return r;
+}
+
+// Descriptor of one (row, tap) from its offset pair and mask value.
+template <typename T>
+__device__ __forceinline__ void write_desc(const Plan& pl, const SampleRow<T>& r, int32_t i, int32_t j, float dhv,
+                                           float dwv, float mv, uint8_t* dp) {
+    int64_t off = 0;
+    uint32_t flags = 0;
+    float w00 = 0.f, w01 = 0.f, w10 = 0.f, w11 = 0.f;
+    const float hf = r.hbase + static_cast<float>(i * pl.dh) + dhv;
+    const float wf = r.wbase + static_cast<float>(j * pl.dw) + dwv;
+    if (r.valid && hf > -1.0f && hf < static_cast<float>(pl.H) && wf > -1.0f && wf < static_cast<float>(pl.W)) {
+        const float h0f = floorf(hf), w0f = floorf(wf);
+        const float lh = hf - h0f, lw = wf - w0f;
+        const float hh = 1.0f - lh, hw_ = 1.0f - lw;
+        const int32_t y0 = static_cast<int32_t>(h0f);
+        const int32_t x0 = static_cast<int32_t>(w0f);
+        w00 = hh * hw_ * mv;
+        w01 = hh * lw * mv;
+        w10 = lh * hw_ * mv;
+        w11 = lh * lw * mv;
+        const bool top = y0 >= 0, bottom = y0 + 1 < pl.H;
+        const bool left = x0 >= 0, right = x0 + 1 < pl.W;
+        flags = (top && left ? 1u : 0u) | (top && right ? 2u : 0u) | (bottom && left ? 4u : 0u) |
+                (bottom && right ? 8u : 0u);
+        off = ((r.nbase + y0) * pl.W + x0) * pl.Cp;
     }
+    const uint64_t packed = static_cast<uint64_t>(off) | flags;
+    uint4 d0;
+    d0.x = static_cast<uint32_t>(packed);
+    d0.y = static_cast<uint32_t>(packed >> 32);
+    if constexpr (sizeof(T) == 4) {
+        d0.z = 0u;
+        d0.w = 0u;
+        reinterpret_cast<uint4*>(dp)[0] = d0;
+        reinterpret_cast<uint4*>(dp)[1] =
+            make_uint4(__float_as_uint(w00), __float_as_uint(w01), __float_as_uint(w10), __float_as_uint(w11));
+    } else {
+        T* tag = nullptr;
+        d0.z = pack2(w00, w01, tag);
+        d0.w = pack2(w10, w11, tag);
+        reinterpret_cast<uint4*>(dp)[0] = d0;
+    }
+}
+
+// One thread writes the descriptors of tile rows row and row + 64 for taps
+// [tap0, tap0 + ntap) to dst + (kb * kTileM + row) * dsz, kb = tap - tap0;
+// the offset and mask loads of kSampleTaps taps of both rows are issued
+// together.
+constexpr int kSampleTaps = 3;
+
+template <typename T>
+__device__ __forceinline__ void sample_rows(const Plan& pl, const T* __restrict__ offset, const T* __restrict__ mask,
+                                            int64_t mt, int64_t gd, int row, int32_t tap0, int32_t ntap,
+                                            uint8_t* dst, uint32_t dsz) {
+    const int64_t P = pl.P;
+    const SampleRow<T> ra = sample_row_at(pl, offset, mask, mt, gd, row, tap0);
+    const SampleRow<T> rb = sample_row_at(pl, offset, mask, mt, gd, row + 64, tap0);
     int32_t i = tap0 / static_cast<int32_t>(pl.kw);
     int32_t j = tap0 - i * static_cast<int32_t>(pl.kw);
+#pragma unroll 1
+    for (int32_t kb0 = 0; kb0 < ntap; kb0 += kSampleTaps) {
+        float v[2][3][kSampleTaps];  // [row][dh, dw, mask][tap]
 #pragma unroll
-    for (int kb = 0; kb < kSampleTaps; ++kb) {
-        if (kb < ntap) {
-            int64_t off = 0;
-            uint32_t flags = 0;
-            float w00 = 0.f, w01 = 0.f, w10 = 0.f, w11 = 0.f;
-            const float hf = hbase + static_cast<float>(i * pl.dh) + dhv[kb];
-            const float wf = wbase + static_cast<float>(j * pl.dw) + dwv[kb];
-            if (q.valid && hf > -1.0f && hf < static_cast<float>(pl.H) && wf > -1.0f && wf < static_cast<float>(pl.W)) {
-                const float h0f = floorf(hf), w0f = floorf(wf);
-                const float lh = hf - h0f, lw = wf - w0f;
-                const float hh = 1.0f - lh, hw_ = 1.0f - lw;
-                const float m = mv[kb];
-                const int32_t y0 = static_cast<int32_t>(h0f);
-                const int32_t x0 = static_cast<int32_t>(w0f);
-                w00 = hh * hw_ * m;
-                w01 = hh * lw * m;
-                w10 = lh * hw_ * m;
-                w11 = lh * lw * m;
-                const bool top = y0 >= 0, bottom = y0 + 1 < pl.H;
-                const bool left = x0 >= 0, right = x0 + 1 < pl.W;
-                flags = (top && left ? 1u : 0u) | (top && right ? 2u : 0u) | (bottom && left ? 4u : 0u) |
-                        (bottom && right ? 8u : 0u);
-                off = ((nbase + y0) * pl.W + x0) * pl.Cp;
+        for (int u = 0; u < kSampleTaps; ++u) {
+            const int64_t kb = kb0 + u < ntap ? kb0 + u : kb0;
+            v[0][0][u] = to_f(ra.po[(2 * kb) * P]);
+            v[0][1][u] = to_f(ra.po[(2 * kb + 1) * P]);
+            v[0][2][u] = to_f(ra.pm[kb * P]);
+            v[1][0][u] = to_f(rb.po[(2 * kb) * P]);
+            v[1][1][u] = to_f(rb.po[(2 * kb + 1) * P]);
+            v[1][2][u] = to_f(rb.pm[kb * P]);
+        }
+#pragma unroll
+        for (int u = 0; u < kSampleTaps; ++u) {
+            if (kb0 + u < ntap) {
+                uint8_t* dp = dst + (static_cast<uint32_t>(kb0 + u) * kTileM + row) * dsz;
+                write_desc(pl, ra, i, j, v[0][0][u], v[0][1][u], v[0][2][u], dp);
+                write_desc(pl, rb, i, j, v[1][0][u], v[1][1][u], v[1][2][u], dp + 64 * dsz);
             }
-            const uint64_t packed = static_cast<uint64_t>(off) | flags;
-            uint4 d0;
-            d0.x = static_cast<uint32_t>(packed);
-            d0.y = static_cast<uint32_t>(packed >> 32);
-            uint8_t* dp = dst + static_cast<int64_t>(tap0 + kb) * kTileM * dsz;
-            if constexpr (sizeof(T) == 4) {
-                d0.z = 0u;
-                d0.w = 0u;
-                reinterpret_cast<uint4*>(dp)[0] = d0;
-                reinterpret_cast<uint4*>(dp)[1] =
-                    make_uint4(__float_as_uint(w00), __float_as_uint(w01), __float_as_uint(w10), __float_as_uint(w11));
-            } else {
-                T* tag = nullptr;
-                d0.z = pack2(w00, w01, tag);
-                d0.w = pack2(w10, w11, tag);
-                reinterpret_cast<uint4*>(dp)[0] = d0;
+            if (++j == static_cast<int32_t>(pl.kw)) {
+                j = 0;
+                ++i;
             }
         }
-        if (++j == static_cast<int32_t>(pl.kw)) {
-            j = 0;
-            ++i;
+    }
+}
+
+// One tile row, taps tap0 + kb for kb = kb_first, kb_first + kb_step, ... <
+// ntap (at most kSampleTaps of them): every load first, then the descriptors.
+template <typename T>
+__device__ __forceinline__ void sample_row_taps(const Plan& pl, const T* __restrict__ offset,
+                                                const T* __restrict__ mask, int64_t mt, int64_t gd, int row,
+                                                int32_t tap0, int32_t ntap, int32_t kb_first, int32_t kb_step,
+                                                uint8_t* dst, uint32_t dsz) {
+    const int64_t P = pl.P;
+    const SampleRow<T> r = sample_row_at(pl, offset, mask, mt, gd, row, tap0);
+    float v[3][kSampleTaps];
+#pragma unroll
+    for (int u = 0; u < kSampleTaps; ++u) {
+        const int32_t kb0 = kb_first + u * kb_step;
+        const int64_t kb = kb0 < ntap ? kb0 : 0;
+        v[0][u] = to_f(r.po[(2 * kb) * P]);
+        v[1][u] = to_f(r.po[(2 * kb + 1) * P]);
+        v[2][u] = to_f(r.pm[kb * P]);
+    }
+#pragma unroll
+    for (int u = 0; u < kSampleTaps; ++u) {
+        const int32_t kb = kb_first + u * kb_step;
+        if (kb < ntap) {
+            const int32_t tap = tap0 + kb;
+            const int32_t i = tap / static_cast<int32_t>(pl.kw);
+            const int32_t j = tap - i * static_cast<int32_t>(pl.kw);
+            write_desc(pl, r, i, j, v[0][u], v[1][u], v[2][u], dst + (static_cast<uint32_t>(kb) * kTileM + row) * dsz);
         }
     }
 }
@@ -490,7 +561,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         for (int b = 0; b < 2; ++b) {
             mbar_init(accf_bar(b), 1);
             mbar_init(acce_bar(b), kEpiWarps);
-            mbar_init(dfull_bar(b), 1);
+            mbar_init(dfull_bar(b), 2);
             mbar_init(dempty_bar(b), kGatherWarps);
         }
         mbar_init(drain_bar, 1);
@@ -507,9 +578,25 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
+    // The CTA's first descriptor group is sampled by all 512 threads together
+    // (thread t: row t % 128, taps t / 128, t / 128 + 4, t / 128 + 8): the
+    // first k-tiles of every role wait for it. Warps 2-3 then mark it full
+    // and sample the following groups.
+    {
+        Cursor c0;
+        cursor_init(pl, c0, lo, hi);
+        if (c0.live) {
+            const int64_t gd = (static_cast<int64_t>(c0.g) * pl.Ug + c0.ul) * pl.U / pl.Cd;
+            sample_row_taps<T>(pl, static_cast<const T*>(prm.offset), static_cast<const T*>(prm.mask), c0.mt, gd,
+                               threadIdx.x % kTileM, c0.b * kTapBlock, c0.ntbg, threadIdx.x / kTileM, 4,
+                               gbase + (d0 - sbase), static_cast<uint32_t>(pl.desc_size));
+        }
+        __syncthreads();
+    }
+
     // Register split per warpgroup (launch: 128 per thread x 512 threads; the
     // host refuses to launch a build whose register count is not exactly 128):
-    // TMA/MMA 80, gather 2 x 176, epilogue 80 -> 512 x 128 in total. Each
+    // TMA/MMA/sampling 96, gather 2 x 176, epilogue 64 -> 512 x 128 in total. Each
     // warpgroup's branch starts with its own setmaxnreg, so the compiler
     // allocates each role's code within that role's budget.
     const int wg = warp >> 2;
@@ -520,33 +607,11 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         if (lane == 0) {
             const uint32_t sub_bytes = static_cast<uint32_t>(pl.BNs) * 128u;
             const uint32_t half_bytes = sub_bytes * pl.nsub;
-            const uint8_t* dglob = static_cast<const uint8_t*>(prm.desc);
-            const uint32_t dsz = static_cast<uint32_t>(pl.desc_size);
-            // descriptor groups are copied up to one group ahead of the k-tiles
-            Cursor dc;  // first k-tile of the next group to copy
-            cursor_init(pl, dc, lo, hi);
             Cursor kc;  // next weight k-tile to load
             cursor_init(pl, kc, lo, hi);
             bool ok = true;
             uint32_t s = 0;
             while (kc.live && ok) {
-                while (dc.live && dc.gr <= kc.gr + 1) {
-                    const int slot = dc.gr & 1;
-                    if (!mbar_wait_bounded(dempty_bar(slot), ((dc.gr >> 1) & 1) ^ 1u, abort_flag, prm.status,
-                                           kSiteTmaEmpty)) {
-                        ok = false;
-                        break;
-                    }
-                    const int64_t unit = static_cast<int64_t>(dc.g) * pl.Ug + dc.ul;
-                    const int64_t gd = (unit * pl.U) / pl.Cd;
-                    const uint32_t bytes = static_cast<uint32_t>(dc.ntbg) * kTileM * dsz;
-                    const uint8_t* src =
-                        dglob + ((dc.mt * pl.dg + gd) * pl.K + static_cast<int64_t>(dc.b) * kTapBlock) * kTileM * dsz;
-                    mbar_arrive_expect_tx(dfull_bar(slot), bytes);
-                    bulk_load(d0 + slot * dslot, src, bytes, dfull_bar(slot));
-                    cursor_next_group(pl, dc);
-                }
-                if (!ok) break;
                 const int st = s % S;
                 if (!mbar_wait_bounded(empty_bar(st), ((s / S) & 1) ^ 1u, abort_flag, prm.status, kSiteTmaEmpty)) {
                     ok = false;
@@ -570,9 +635,6 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                 volatile int never = 0;
                 for (uint32_t q = first; q < s; ++q)
                     mbar_wait_bounded(tma_bar(q % S), (q / S) & 1, &never, prm.status, kSiteDrain, 200000000ull);
-                const uint32_t gfirst = dc.gr > 2u ? dc.gr - 2u : 0u;
-                for (uint32_t q = gfirst; q < dc.gr; ++q)
-                    mbar_wait_bounded(dfull_bar(q & 1), (q >> 1) & 1, &never, prm.status, kSiteDrain, 200000000ull);
             }
         }
     } else if (warp == kWarpMma) {
@@ -629,6 +691,34 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
             mma_commit(drain_bar);
             volatile int never = 0;
             mbar_wait_bounded(drain_bar, 0, &never, prm.status, kSiteDrain, 200000000ull);
+        }
+    } else {
+        // ------------------------------------------------------------ sampling
+        // Warps 2-3 fill the descriptor ring: for each descriptor group of the
+        // CTA's range, in order, once every gather warp has released its slot:
+        // thread t writes rows t and t + 64 for the group's taps.
+        const T* offset = static_cast<const T*>(prm.offset);
+        const T* mask = static_cast<const T*>(prm.mask);
+        const int sid = (warp - 2) * 32 + lane;
+        const uint32_t dsz = static_cast<uint32_t>(pl.desc_size);
+        Cursor dc;  // first k-tile of the next group to sample
+        cursor_init(pl, dc, lo, hi);
+        if (dc.live) {  // the first group, sampled by every thread above
+            if (lane == 0) mbar_arrive(dfull_bar(0));
+            cursor_next_group(pl, dc);
+        }
+        while (dc.live) {
+            const int slot = dc.gr & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(dempty_bar(slot), ((dc.gr >> 1) & 1) ^ 1u, abort_flag,
+                                                           prm.status, kSiteTmaEmpty)))
+                break;
+            const int64_t unit = static_cast<int64_t>(dc.g) * pl.Ug + dc.ul;
+            const int64_t gd = (unit * pl.U) / pl.Cd;
+            uint8_t* ring = gbase + (d0 - sbase) + slot * dslot;
+            sample_rows<T>(pl, offset, mask, dc.mt, gd, sid, dc.b * kTapBlock, dc.ntbg, ring, dsz);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(dfull_bar(slot));
+            cursor_next_group(pl, dc);
         }
     }
     } else if (wg == 1 || wg == 2) {
@@ -999,7 +1089,8 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
 }
 
 template <int DT>
-cudaError_t launch_fused_t(const Plan& pl, const void* bias, void* out, void* ws, cudaStream_t st) {
+cudaError_t launch_fused_t(const Plan& pl, const void* offset, const void* mask, const void* bias, void* out, void* ws,
+                           cudaStream_t st) {
     using T = typename Elem<DT>::T;
     uint8_t* base = static_cast<uint8_t*>(ws);
     const T* wp = reinterpret_cast<const T*>(base + pl.off_wp);
@@ -1030,7 +1121,8 @@ cudaError_t launch_fused_t(const Plan& pl, const void* bias, void* out, void* ws
     }
     FusedParams prm;
     prm.xt = base + pl.off_xt;
-    prm.desc = base + pl.off_desc;
+    prm.offset = offset;
+    prm.mask = mask;
     prm.bias = bias;
     prm.out = out;
     prm.status = reinterpret_cast<uint32_t*>(base);
@@ -1076,33 +1168,13 @@ cudaError_t prepare_fused_attributes(int dtype, int smem_bytes) {
     }
 }
 
-cudaError_t launch_fused(const Plan& pl, const void* bias, void* out, void* ws, cudaStream_t st) {
+cudaError_t launch_fused(const Plan& pl, const void* offset, const void* mask, const void* bias, void* out, void* ws,
+                         cudaStream_t st) {
     switch (pl.dtype) {
-        case kF32: return launch_fused_t<kF32>(pl, bias, out, ws, st);
-        case kF16: return launch_fused_t<kF16>(pl, bias, out, ws, st);
-        default: return launch_fused_t<kBF16>(pl, bias, out, ws, st);
+        case kF32: return launch_fused_t<kF32>(pl, offset, mask, bias, out, ws, st);
+        case kF16: return launch_fused_t<kF16>(pl, offset, mask, bias, out, ws, st);
+        default: return launch_fused_t<kBF16>(pl, offset, mask, bias, out, ws, st);
     }
-}
-
-cudaError_t launch_sample(const Plan& pl, const void* offset, const void* mask, void* ws, cudaStream_t st) {
-    uint8_t* desc = static_cast<uint8_t*>(ws) + pl.off_desc;
-    const dim3 grid(static_cast<unsigned>(pl.mtiles), static_cast<unsigned>(pl.dg),
-                    static_cast<unsigned>((pl.K + kSampleTaps - 1) / kSampleTaps));
-    switch (pl.dtype) {
-        case kF32:
-            sample_kernel<float><<<grid, kTileM, 0, st>>>(static_cast<const float*>(offset),
-                                                          static_cast<const float*>(mask), desc, pl);
-            break;
-        case kF16:
-            sample_kernel<__half><<<grid, kTileM, 0, st>>>(static_cast<const __half*>(offset),
-                                                           static_cast<const __half*>(mask), desc, pl);
-            break;
-        default:
-            sample_kernel<__nv_bfloat16><<<grid, kTileM, 0, st>>>(static_cast<const __nv_bfloat16*>(offset),
-                                                                  static_cast<const __nv_bfloat16*>(mask), desc, pl);
-            break;
-    }
-    return cudaGetLastError();
 }
 
 cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_cycles, cudaStream_t st) {

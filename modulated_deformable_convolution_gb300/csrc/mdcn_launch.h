@@ -12,13 +12,11 @@ namespace mdcn {
 cudaError_t launch_prep_input(const Plan& pl, const void* x, void* ws, cudaStream_t st);
 cudaError_t launch_pack_weight(const Plan& pl, const void* weight, void* ws, cudaStream_t st);
 
-// Sample descriptors (sampling points, corner validity, bilinear weights x
-// mask) of every tile row, deformable group and tap, into the workspace.
-cudaError_t launch_sample(const Plan& pl, const void* offset, const void* mask, void* ws, cudaStream_t st);
-
-// The fused gather + contraction + bias kernel (reads the three workspace
-// products of launch_prep_input, launch_pack_weight and launch_sample).
-cudaError_t launch_fused(const Plan& pl, const void* bias, void* out, void* ws, cudaStream_t st);
+// The fused sampling + gather + contraction + bias kernel (reads offset, mask
+// and the two workspace products of launch_prep_input and
+// launch_pack_weight), then the split-tile fix-up when tiles are split.
+cudaError_t launch_fused(const Plan& pl, const void* offset, const void* mask, const void* bias, void* out, void* ws,
+                         cudaStream_t st);
 
 // Dynamic shared memory the fused kernel may use on this device (set once).
 cudaError_t prepare_fused_attributes(int dtype, int smem_bytes);

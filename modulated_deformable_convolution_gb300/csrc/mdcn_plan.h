@@ -8,6 +8,9 @@
 namespace mdcn {
 
 constexpr int kTileM = 128;       // output pixels per tile (MMA M)
+constexpr int kTileH = 8;         // 2-D tile: kTileH image rows x kTileW pixels
+constexpr int kTileW = 16;
+static_assert(kTileH * kTileW == kTileM, "2-D tile covers one tile");
 constexpr int kTapBlock = 9;      // taps whose sample descriptors form one descriptor group
 // Warp roles of the fused kernel (16 warps):
 constexpr int kWarpTma = 0;       // TMA loads of weight k-tiles
@@ -18,11 +21,11 @@ constexpr int kWarpEpi = 12;      // 4 warps: TMEM -> +bias -> NCHW
 constexpr int kEpiWarps = 4;
 constexpr int kFusedThreads = 32 * 16;
 // Registers per thread: at launch, and per warpgroup after setmaxnreg
-// (warpgroup 0 = TMA/MMA, 1-2 = gather, 3 = epilogue).
+// (warpgroup 0 = TMA/MMA/sampling, 1-2 = gather, 3 = epilogue).
 constexpr int kRegsLaunch = 128;
-constexpr int kRegsCtrl = 80;
+constexpr int kRegsCtrl = 96;
 constexpr int kRegsGather = 176;
-constexpr int kRegsEpi = 80;
+constexpr int kRegsEpi = 64;
 static_assert(kRegsCtrl + 2 * kRegsGather + kRegsEpi == 4 * kRegsLaunch, "warpgroup register split must fit");
 constexpr int kSmemLimit = 227 * 1024;
 constexpr int kMaxCtas = 160;         // persistent CTAs at most (one per SM; the workspace holds 2 partial slots each)
@@ -80,7 +83,7 @@ struct Plan {
     int64_t kt_per_cta;      // stream-K: consecutive k-tiles per CTA (set with grid)
 
     // ---- workspace layout (byte offsets)
-    size_t off_xt, off_wp, off_desc, off_part, ws_bytes;
+    size_t off_xt, off_wp, off_part, ws_bytes;
 };
 
 // True when some tile's k-tiles fall to more than one CTA (the CTA ranges do
