@@ -141,7 +141,8 @@ typedef struct mdcn_plan_info {
     int32_t ctas;           /* persistent CTAs of the fused kernel */
     int32_t split;          /* 1 when some tile is split between CTAs (the fix-up kernel runs) */
     int32_t stages, kgroups, tile_mode;
-    int32_t launches;       /* kernels one mdcn_forward launches: 3, or 4 with the fix-up */
+    int32_t launches;       /* kernels one mdcn_forward launches: prep (1, or 2 when x needs the staged
+                               transpose), the fused kernel, and the fix-up when split */
 } mdcn_plan_info;
 
 /* Errors as mdcn_workspace_size, plus MDCN_ERR_ARCH / MDCN_ERR_CUDA from the

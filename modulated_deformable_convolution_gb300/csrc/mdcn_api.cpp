@@ -222,6 +222,17 @@ mdcn_status make_plan(const mdcn_attrs& a, const mdcn_tuning& tuning, const mdcn
     p.wp_rows = rows;
     int64_t wpb = rows;
     if (!mul_ok(wpb, p.KP) || !mul_ok(wpb, elem) || rows > kI31) return MDCN_ERR_UNSUPPORTED;
+    {
+        // register-blocked channels-last conversion: H*W and the unit in whole
+        // 16-byte vectors, grid within limits
+        const int64_t vec = 16 / elem;
+        const int64_t pblocks = (p.H * p.W / vec + 3) / 4;
+        const int64_t cblocks = (p.Cp / vec + 7) / 8;
+        p.xt_block = ((p.H * p.W) % vec == 0 && p.U % vec == 0 && p.N <= 65535 && cblocks <= 65535 &&
+                      (pblocks + 7) / 8 <= 65535)
+                         ? 1
+                         : 0;
+    }
     // stream-K: fp32 partial accumulators of split tiles, 2 slots per CTA
     p.total_kt = p.tiles_total;
     if (!mul_ok(p.total_kt, p.KT) || p.total_kt > kI31) return MDCN_ERR_UNSUPPORTED;  // 32-bit tile arithmetic
@@ -363,7 +374,7 @@ mdcn_status mdcn_query_plan(mdcn_handle handle, const mdcn_dims* dims, mdcn_dtyp
     info->stages = p.stages;
     info->kgroups = p.kgroups;
     info->tile_mode = p.tile_mode;
-    info->launches = 3 + info->split;
+    info->launches = (p.xt_block ? 2 : 3) + info->split;
     return MDCN_OK;
 }
 
@@ -376,8 +387,7 @@ mdcn_status mdcn_forward(mdcn_handle handle, const void* x, const void* offset, 
     s = plan_for_call(handle, dims, dtype, workspace_bytes, &p);
     if (s != MDCN_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e = mdcn::launch_prep_input(p, x, workspace, st);
-    if (e == cudaSuccess) e = mdcn::launch_pack_weight(p, weight, workspace, st);
+    cudaError_t e = mdcn::launch_prep_both(p, x, weight, workspace, st);
     if (e == cudaSuccess) e = mdcn::launch_fused(p, offset, mask, bias_or_null, out, workspace, st);
     if (e != cudaSuccess) return cuda_fail(e);
     return MDCN_OK;

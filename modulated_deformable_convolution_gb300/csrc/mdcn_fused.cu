@@ -591,6 +591,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                                threadIdx.x % kTileM, c0.b * kTapBlock, c0.ntbg, threadIdx.x / kTileM, 4,
                                gbase + (d0 - sbase), static_cast<uint32_t>(pl.desc_size));
         }
+        // Everything so far reads only offset and mask; the channels-last x and
+        // the packed weight come from the kernel launched before this one,
+        // which this grid may overlap (programmatic dependent launch).
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         __syncthreads();
     }
 
@@ -1128,8 +1132,20 @@ cudaError_t launch_fused_t(const Plan& pl, const void* offset, const void* mask,
     prm.status = reinterpret_cast<uint32_t*>(base);
     prm.part = reinterpret_cast<float*>(base + pl.off_part);
     prm.pl = pl;
-    fused_kernel<DT><<<static_cast<unsigned>(pl.grid), kFusedThreads, pl.smem_bytes, st>>>(tmap, omap, prm);
-    cudaError_t e = cudaGetLastError();
+    // launched dependent on the prep kernel: the prologue (barriers, tensor
+    // memory, the first descriptor group) overlaps its tail
+    cudaLaunchConfig_t fcfg = {};
+    fcfg.gridDim = dim3(static_cast<unsigned>(pl.grid));
+    fcfg.blockDim = dim3(kFusedThreads);
+    fcfg.dynamicSmemBytes = static_cast<size_t>(pl.smem_bytes);
+    fcfg.stream = st;
+    cudaLaunchAttribute fattr[1];
+    fattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    fattr[0].val.programmaticStreamSerializationAllowed = 1;
+    fcfg.attrs = fattr;
+    fcfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&fcfg, fused_kernel<DT>, tmap, omap, prm);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess || !splitk_needed(pl)) return e;
     // split tiles: the fix-up, launched while the fused grid drains
     cudaLaunchConfig_t cfg = {};

@@ -11,6 +11,8 @@ namespace mdcn {
 // (also clears the workspace status word), weight -> packed K-major.
 cudaError_t launch_prep_input(const Plan& pl, const void* x, void* ws, cudaStream_t st);
 cudaError_t launch_pack_weight(const Plan& pl, const void* weight, void* ws, cudaStream_t st);
+// Both of the above, in one launch where the shape allows.
+cudaError_t launch_prep_both(const Plan& pl, const void* x, const void* weight, void* ws, cudaStream_t st);
 
 // The fused sampling + gather + contraction + bias kernel (reads offset, mask
 // and the two workspace products of launch_prep_input and

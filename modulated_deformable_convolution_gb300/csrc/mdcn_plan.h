@@ -79,6 +79,8 @@ struct Plan {
     int32_t epi_bytes;       // shared-memory staging of the TMA-store epilogue
     int32_t smem_bytes;      // dynamic shared memory of the fused kernel
     int32_t grid;            // persistent CTAs
+    int32_t xt_block;        // 1: x goes channels-last through the register-blocked kernel, which
+                             //    mdcn_forward launches together with the weight pack
     int64_t total_kt;        // k-tiles of all tiles: tiles_total * KT
     int64_t kt_per_cta;      // stream-K: consecutive k-tiles per CTA (set with grid)
 

@@ -95,16 +95,16 @@ __global__ void __launch_bounds__(256) nhwc_pad_kernel(const T* __restrict__ x, 
 // one pixel block (4 * kVec pixels) per warp. Block (0, 0, 0) also clears the
 // device status word.
 template <typename T>
-__global__ void __launch_bounds__(256) nhwc_block_kernel(const T* __restrict__ x, T* __restrict__ xt,
-                                                         uint32_t* __restrict__ status, int32_t Cin, int64_t P,
-                                                         int64_t Cp, int32_t U, int32_t UP) {
+__device__ __forceinline__ void nhwc_block_body(const T* __restrict__ x, T* __restrict__ xt,
+                                                uint32_t* __restrict__ status, int32_t Cin, int64_t P, int64_t Cp,
+                                                int32_t U, int32_t UP, uint32_t bx, uint32_t by, uint32_t bz) {
     constexpr int kVec = 16 / sizeof(T);
-    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0) *status = 0u;
+    if (bx == 0 && by == 0 && bz == 0 && threadIdx.x == 0) *status = 0u;
     const int lane = threadIdx.x & 31;
     const int cg = lane & 7, pg = lane >> 3;
-    const int64_t n = blockIdx.z;
-    const int64_t oc0 = (static_cast<int64_t>(blockIdx.y) * 8 + cg) * kVec;  // output channel (padded)
-    const int64_t p0 = ((static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5)) * 4 + pg) * kVec;
+    const int64_t n = bz;
+    const int64_t oc0 = (static_cast<int64_t>(by) * 8 + cg) * kVec;  // output channel (padded)
+    const int64_t p0 = ((static_cast<int64_t>(bx) * 8 + (threadIdx.x >> 5)) * 4 + pg) * kVec;
     if (oc0 >= Cp || p0 >= P) return;
     const int32_t unit = static_cast<int32_t>(oc0 / UP);
     const int32_t within = static_cast<int32_t>(oc0) - unit * UP;
@@ -152,6 +152,13 @@ __global__ void __launch_bounds__(256) nhwc_block_kernel(const T* __restrict__ x
 }
 
 template <typename T>
+__global__ void __launch_bounds__(256) nhwc_block_kernel(const T* __restrict__ x, T* __restrict__ xt,
+                                                         uint32_t* __restrict__ status, int32_t Cin, int64_t P,
+                                                         int64_t Cp, int32_t U, int32_t UP) {
+    nhwc_block_body<T>(x, xt, status, Cin, P, Cp, U, UP, blockIdx.x, blockIdx.y, blockIdx.z);
+}
+
+template <typename T>
 __device__ __forceinline__ float load_f(const T* p);
 template <>
 __device__ __forceinline__ float load_f<float>(const float* p) { return *p; }
@@ -164,21 +171,22 @@ __device__ __forceinline__ float load_f<__nv_bfloat16>(const __nv_bfloat16* p) {
 // Grid: x over k-tiles of one row (blockDim.x = BKc lanes per k-tile, several
 // k-tiles per block), y over rows (looping when rows exceed the grid).
 template <typename T>
-__global__ void __launch_bounds__(256) pack_weight_kernel(const T* __restrict__ weight, T* __restrict__ wp, Plan pl) {
+__device__ __forceinline__ void pack_weight_body(const T* __restrict__ weight, T* __restrict__ wp, const Plan& pl,
+                                                 uint32_t bx, uint32_t by, uint32_t gy) {
     const int64_t rows = pl.Cout * (pl.dtype == kF32 ? 2 : 1);
     const int32_t ktiles_per_block = 256 / pl.BKc;
-    const int32_t kt = blockIdx.x * ktiles_per_block + static_cast<int32_t>(threadIdx.x) / pl.BKc;
+    const int32_t kt = static_cast<int32_t>(bx) * ktiles_per_block + static_cast<int32_t>(threadIdx.x) / pl.BKc;
     const int32_t ci = static_cast<int32_t>(threadIdx.x) % pl.BKc;
     if (kt >= pl.KT) return;
     const KTile t = decode_ktile(kt, pl.K, pl.nch);
     const int32_t within = t.ch * pl.BKc + ci;  // channel within the unit
     const int64_t cl = static_cast<int64_t>(t.ul) * pl.U + within;  // channel within the group
     // 4 rows per iteration: their loads are in flight together
-    for (int64_t r0 = blockIdx.y; r0 < pl.wp_rows; r0 += 4 * static_cast<int64_t>(gridDim.y)) {
+    for (int64_t r0 = by; r0 < pl.wp_rows; r0 += 4 * static_cast<int64_t>(gy)) {
         T v[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const int64_t r = r0 + k * static_cast<int64_t>(gridDim.y);
+            const int64_t r = r0 + k * static_cast<int64_t>(gy);
             v[k] = zero_of<T>();
             if (within < pl.U && r < rows) {
                 const bool lo_half = r >= pl.Cout;
@@ -195,9 +203,33 @@ __global__ void __launch_bounds__(256) pack_weight_kernel(const T* __restrict__ 
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const int64_t r = r0 + k * static_cast<int64_t>(gridDim.y);
+            const int64_t r = r0 + k * static_cast<int64_t>(gy);
             if (r < pl.wp_rows) wp[r * pl.KP + static_cast<int64_t>(kt) * pl.BKc + ci] = v[k];
         }
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) pack_weight_kernel(const T* __restrict__ weight, T* __restrict__ wp, Plan pl) {
+    pack_weight_body<T>(weight, wp, pl, blockIdx.x, blockIdx.y, gridDim.y);
+}
+
+// Both prep steps in one launch (register-blocked transpose blocks first,
+// then weight-pack blocks); the fused kernel, launched dependent on it,
+// may start its prologue as soon as every block of this grid has begun.
+template <typename T>
+__global__ void __launch_bounds__(256) prep_both_kernel(const T* __restrict__ x, const T* __restrict__ weight,
+                                                        T* __restrict__ xt, T* __restrict__ wp,
+                                                        uint32_t* __restrict__ status, Plan pl, uint32_t tgx,
+                                                        uint32_t tgy, uint32_t nt, uint32_t pgx, uint32_t pgy) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const uint32_t b = blockIdx.x;
+    if (b < nt) {
+        nhwc_block_body<T>(x, xt, status, static_cast<int32_t>(pl.Cin), pl.H * pl.W, pl.Cp, pl.U, pl.UP, b % tgx,
+                           (b / tgx) % tgy, b / (tgx * tgy));
+    } else {
+        const uint32_t q = b - nt;
+        pack_weight_body<T>(weight, wp, pl, q % pgx, q / pgx, pgy);
     }
 }
 
@@ -205,18 +237,35 @@ __global__ void __launch_bounds__(256) pack_weight_kernel(const T* __restrict__ 
 
 constexpr int64_t kPrepSmemBytes = 40 * 1024;
 
+// Grid of the register-blocked transpose, or false when the shape needs the
+// shared-memory staged one.
+template <typename T>
+static bool block_transpose_grid(const Plan& pl, dim3* grid) {
+    constexpr int64_t kVec = 16 / static_cast<int64_t>(sizeof(T));
+    const int64_t P = pl.H * pl.W;
+    const int64_t pblocks = (P / kVec + 3) / 4;        // 4 * kVec pixels per warp
+    const int64_t cblocks = (pl.Cp / kVec + 7) / 8;    // 8 * kVec output channels per warp
+    if (!pl.xt_block) return false;  // the planner's check of the same conditions
+    *grid = dim3(static_cast<unsigned>((pblocks + 7) / 8), static_cast<unsigned>(cblocks), static_cast<unsigned>(pl.N));
+    return true;
+}
+
+template <typename T>
+static void pack_grid(const Plan& pl, unsigned* gx, unsigned* gy) {
+    const int32_t ktiles_per_block = 256 / pl.BKc;
+    *gx = static_cast<unsigned>((pl.KT + ktiles_per_block - 1) / ktiles_per_block);
+    const int64_t gy4 = (pl.wp_rows + 3) / 4;
+    *gy = static_cast<unsigned>(gy4 < 65535 ? gy4 : 65535);
+}
+
 template <typename T>
 static cudaError_t prep_input_t(const Plan& pl, const void* x, void* ws, cudaStream_t st) {
     uint8_t* base = static_cast<uint8_t*>(ws);
     uint32_t* status = reinterpret_cast<uint32_t*>(base);
     T* xt = reinterpret_cast<T*>(base + pl.off_xt);
-    constexpr int64_t kVec = 16 / static_cast<int64_t>(sizeof(T));
     const int64_t P = pl.H * pl.W;
-    const int64_t pblocks = (P / kVec + 3) / 4;        // 4 * kVec pixels per warp
-    const int64_t cblocks = (pl.Cp / kVec + 7) / 8;    // 8 * kVec output channels per warp
-    if (P % kVec == 0 && pl.U % kVec == 0 && pl.N <= 65535 && cblocks <= 65535 && (pblocks + 7) / 8 <= 2147483647) {
-        const dim3 grid(static_cast<unsigned>((pblocks + 7) / 8), static_cast<unsigned>(cblocks),
-                        static_cast<unsigned>(pl.N));
+    dim3 grid;
+    if (block_transpose_grid<T>(pl, &grid)) {
         nhwc_block_kernel<T><<<grid, 256, 0, st>>>(static_cast<const T*>(x), xt, status,
                                                    static_cast<int32_t>(pl.Cin), P, pl.Cp, pl.U, pl.UP);
         return cudaGetLastError();
@@ -238,12 +287,41 @@ template <typename T>
 static cudaError_t pack_weight_t(const Plan& pl, const void* weight, void* ws, cudaStream_t st) {
     uint8_t* base = static_cast<uint8_t*>(ws);
     T* wp = reinterpret_cast<T*>(base + pl.off_wp);
-    const int32_t ktiles_per_block = 256 / pl.BKc;
-    const unsigned gx = static_cast<unsigned>((pl.KT + ktiles_per_block - 1) / ktiles_per_block);
-    const int64_t gy4 = (pl.wp_rows + 3) / 4;
-    const unsigned gy = static_cast<unsigned>(gy4 < 65535 ? gy4 : 65535);
+    unsigned gx, gy;
+    pack_grid<T>(pl, &gx, &gy);
     pack_weight_kernel<T><<<dim3(gx, gy), 256, 0, st>>>(static_cast<const T*>(weight), wp, pl);
     return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t prep_both_t(const Plan& pl, const void* x, const void* weight, void* ws, cudaStream_t st) {
+    dim3 tg;
+    if (!block_transpose_grid<T>(pl, &tg)) {
+        const cudaError_t e = prep_input_t<T>(pl, x, ws, st);
+        return e != cudaSuccess ? e : pack_weight_t<T>(pl, weight, ws, st);
+    }
+    unsigned pgx, pgy;
+    pack_grid<T>(pl, &pgx, &pgy);
+    const uint64_t nt = static_cast<uint64_t>(tg.x) * tg.y * tg.z;
+    const uint64_t np = static_cast<uint64_t>(pgx) * pgy;
+    if (nt + np > 2147483647ull) {
+        const cudaError_t e = prep_input_t<T>(pl, x, ws, st);
+        return e != cudaSuccess ? e : pack_weight_t<T>(pl, weight, ws, st);
+    }
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    prep_both_kernel<T><<<static_cast<unsigned>(nt + np), 256, 0, st>>>(
+        static_cast<const T*>(x), static_cast<const T*>(weight), reinterpret_cast<T*>(base + pl.off_xt),
+        reinterpret_cast<T*>(base + pl.off_wp), reinterpret_cast<uint32_t*>(base), pl, tg.x, tg.y,
+        static_cast<uint32_t>(nt), pgx, pgy);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prep_both(const Plan& pl, const void* x, const void* weight, void* ws, cudaStream_t st) {
+    switch (pl.dtype) {
+        case kF32: return prep_both_t<float>(pl, x, weight, ws, st);
+        case kF16: return prep_both_t<__half>(pl, x, weight, ws, st);
+        default: return prep_both_t<__nv_bfloat16>(pl, x, weight, ws, st);
+    }
 }
 
 cudaError_t launch_prep_input(const Plan& pl, const void* x, void* ws, cudaStream_t st) {
