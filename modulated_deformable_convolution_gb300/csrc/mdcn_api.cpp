@@ -215,8 +215,12 @@ mdcn_status make_plan(const mdcn_attrs& a, const mdcn_tuning& tuning, const mdcn
     // channels-last conversion stages whole pixels in 40 KB of shared memory
     if ((p.Cp + 16 / elem) * elem > 40 * 1024) return MDCN_ERR_UNSUPPORTED;
     if (p.N * p.H * p.W > kI31) return MDCN_ERR_UNSUPPORTED;
+    // channels-last x, plus one all-zero pixel that the gather reads for
+    // corners outside the image
     int64_t xt = p.N * p.H;
-    if (!mul_ok(xt, p.W) || !mul_ok(xt, p.Cp) || !mul_ok(xt, elem)) return MDCN_ERR_UNSUPPORTED;
+    if (!mul_ok(xt, p.W)) return MDCN_ERR_UNSUPPORTED;
+    xt += 1;
+    if (!mul_ok(xt, p.Cp) || !mul_ok(xt, elem)) return MDCN_ERR_UNSUPPORTED;
     int64_t rows = p.Cout * halves;
     if (rows < p.BNs) rows = p.BNs;
     p.wp_rows = rows;

@@ -173,11 +173,10 @@ __device__ __forceinline__ uint32_t blend(uint32_t wa, uint32_t wb, uint32_t v0,
 }
 
 // ---------------------------------------------------------------- sample descriptors
-// Descriptor of (tile row, deformable group, tap): the int64 element offset of
-// corner (y0, x0) in the channels-last x with the 4 corner-valid bits in its
-// low bits (offsets are multiples of 32 elements), then the 4 bilinear
-// weights times the mask (16-bit pairs for 16-bit types; fp32 words in a
-// second 16 bytes for fp32). Sampling point (section 5 step 1):
+// Descriptor of (tile row, deformable group, tap): the pixel index of corner
+// (y0, x0) in the channels-last x (int32), the 4 corner-valid bits, then the
+// 4 bilinear weights times the mask (16-bit pairs in the last 8 bytes for
+// 16-bit types; fp32 words in a second 16 bytes for fp32). Sampling point (section 5 step 1):
 // (ho*sh - ph + i*dh + dh_off, wo*sw - pw + j*dw + dw_off); a point outside
 // (-1, H) x (-1, W) and the corners outside the image contribute nothing.
 //
@@ -214,7 +213,7 @@ __device__ __forceinline__ SampleRow<T> sample_row_at(const Plan& pl, const T* o
 template <typename T>
 __device__ __forceinline__ void write_desc(const Plan& pl, const SampleRow<T>& r, int32_t i, int32_t j, float dhv,
                                            float dwv, float mv, uint8_t* dp) {
-    int64_t off = 0;
+    int32_t base = 0;  // pixel index of corner (y0, x0) in the channels-last x (may be -1 - W .. )
     uint32_t flags = 0;
     float w00 = 0.f, w01 = 0.f, w10 = 0.f, w11 = 0.f;
     const float hf = r.hbase + static_cast<float>(i * pl.dh) + dhv;
@@ -233,12 +232,11 @@ __device__ __forceinline__ void write_desc(const Plan& pl, const SampleRow<T>& r
         const bool left = x0 >= 0, right = x0 + 1 < pl.W;
         flags = (top && left ? 1u : 0u) | (top && right ? 2u : 0u) | (bottom && left ? 4u : 0u) |
                 (bottom && right ? 8u : 0u);
-        off = ((r.nbase + y0) * pl.W + x0) * pl.Cp;
+        base = static_cast<int32_t>((r.nbase + y0) * pl.W + x0);
     }
-    const uint64_t packed = static_cast<uint64_t>(off) | flags;
     uint4 d0;
-    d0.x = static_cast<uint32_t>(packed);
-    d0.y = static_cast<uint32_t>(packed >> 32);
+    d0.x = static_cast<uint32_t>(base);
+    d0.y = flags;
     if constexpr (sizeof(T) == 4) {
         d0.z = 0u;
         d0.w = 0u;
@@ -431,7 +429,11 @@ __device__ __forceinline__ void cursor_next_group(const Plan& pl, Cursor& c) {
 template <typename T>
 struct GatherCtx {
     const T* xt;
-    int64_t c1, c2, c3;  // element offsets of corners (y0, x0+1), (y0+1, x0), (y0+1, x0+1)
+    int32_t d1, dW, dW1;  // pixel deltas of corners (y0, x0+1), (y0+1, x0), (y0+1, x0+1): 1, W, W+1
+    int32_t zpix;         // the all-zero pixel after the image data, read for corners outside the image
+    int32_t pix_bytes;    // bytes per channels-last pixel
+    uint32_t row_desc;    // this lane's descriptor within a tap block, row-iteration 0
+    uint32_t row_sts;     // this lane's A-stage offset (128-byte swizzle), row-iteration 0, chunk 2*q4
     int lane, q4, rsub, row0;
     uint32_t dsz;
 };
@@ -453,36 +455,35 @@ __device__ __forceinline__ float blend_f32(float w00, float w01, float w10, floa
     return fmaf(w11, __uint_as_float(v3), a);
 }
 
-// Row-iteration it of a k-tile: reads the row's descriptor (tap kb) and
-// issues the loads of its 4 corners (32 bytes per lane, chunks 2*q4, 2*q4+1).
+// Row-iteration it of a k-tile: reads the row's descriptor (in the tap block
+// at dtap) and loads its 4 corners (32 bytes per lane, chunks 2*q4, 2*q4+1)
+// from cbp = the lane's channels of pixel 0. Every corner is loaded: one
+// outside the image reads the zero pixel, so no load is conditional.
 template <typename T, bool kF32Path>
-__device__ __forceinline__ void row_issue(const GatherCtx<T>& cx, uint32_t dbase, int kb, int64_t cb, int it,
+__device__ __forceinline__ void row_issue(const GatherCtx<T>& cx, uint32_t dtap, const char* cbp, int it,
                                           RowBuf& rb) {
-    const int row = cx.row0 + 8 * it + cx.rsub;
-    const uint32_t da = dbase + static_cast<uint32_t>(kb * kTileM + row) * cx.dsz;
+    const uint32_t da = dtap + cx.row_desc + static_cast<uint32_t>(it) * 8u * cx.dsz;
     const uint4 e = lds128(da);
     if constexpr (kF32Path) {
         rb.w = lds128(da + 16);
     } else {
         rb.w = e;
     }
-    const uint64_t packed = (static_cast<uint64_t>(e.y) << 32) | e.x;
-    const uint32_t fl = e.x & 15u;
-    const T* p = cx.xt + static_cast<int64_t>(packed & ~static_cast<uint64_t>(31)) + cb;
+    const int32_t base = static_cast<int32_t>(e.x);
+    const uint32_t fl = e.y;
 #pragma unroll
     for (int cc = 0; cc < 4; ++cc) {
-        const int64_t co = cc == 0 ? 0 : (cc == 1 ? cx.c1 : (cc == 2 ? cx.c2 : cx.c3));
-        rb.v[cc][0] = make_uint4(0u, 0u, 0u, 0u);
-        rb.v[cc][1] = make_uint4(0u, 0u, 0u, 0u);
-        if (fl & (1u << cc)) ldg256(p + co, rb.v[cc][0], rb.v[cc][1]);
+        const int32_t delta = cc == 0 ? 0 : (cc == 1 ? cx.d1 : (cc == 2 ? cx.dW : cx.dW1));
+        const int32_t pix = (fl >> cc) & 1u ? base + delta : cx.zpix;
+        ldg256(cbp + static_cast<int64_t>(pix) * cx.pix_bytes, rb.v[cc][0], rb.v[cc][1]);
     }
 }
 
 // Weighted sum of the 4 corners of row-iteration it into the A stage a_s.
 template <typename T, bool kF32Path>
 __device__ __forceinline__ void row_combine(const GatherCtx<T>& cx, uint32_t a_s, int it, const RowBuf& rb) {
-    const int row = cx.row0 + 8 * it + cx.rsub;
-    const uint32_t o0 = swz128(row, 2 * cx.q4), o1 = swz128(row, 2 * cx.q4 + 1);
+    // rows of a row-iteration are 8 apart in 128-byte lines: row & 7 == rsub
+    const uint32_t o0 = cx.row_sts + static_cast<uint32_t>(it) * 1024u, o1 = o0 ^ 16u;
     const uint4 w = rb.w;
 #pragma unroll
     for (int hv = 0; hv < 2; ++hv) {
@@ -748,10 +749,14 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         cx.rsub = lane >> 2;  // row within a group of 8
         cx.row0 = (gw % wpg) * 8 * nits;
         cx.xt = static_cast<const T*>(prm.xt);
-        cx.c1 = pl.Cp;
-        cx.c2 = pl.W * pl.Cp;
-        cx.c3 = (pl.W + 1) * pl.Cp;
+        cx.d1 = 1;
+        cx.dW = static_cast<int32_t>(pl.W);
+        cx.dW1 = static_cast<int32_t>(pl.W + 1);
+        cx.zpix = static_cast<int32_t>(pl.N * pl.H * pl.W);
+        cx.pix_bytes = static_cast<int32_t>(pl.Cp * static_cast<int64_t>(sizeof(T)));
         cx.dsz = static_cast<uint32_t>(pl.desc_size);
+        cx.row_desc = static_cast<uint32_t>(cx.row0 + cx.rsub) * cx.dsz;
+        cx.row_sts = swz128(cx.row0 + cx.rsub, 2 * cx.q4);
         constexpr int kVec = 16 / sizeof(T);
         const int32_t ngroups = pl.Ug * pl.ntb;
         uint32_t gr = 0;     // descriptor groups entered
@@ -787,11 +792,13 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                     const int32_t ch = j / ntbg;
                     const int32_t kb = j - ch * ntbg;
                     const int64_t cb = unit * pl.UP + static_cast<int64_t>(ch) * pl.BKc + cx.q4 * 2 * kVec;
+                    const char* cbp = reinterpret_cast<const char*>(cx.xt + cb);
+                    const uint32_t dtap = dbase + static_cast<uint32_t>(kb * kTileM) * cx.dsz;
                     const uint32_t step = sbase + static_cast<uint32_t>(q + j - un.k0);
                     const int st = step % S;
                     RowBuf rb[3];
-                    row_issue<T, kF32Path>(cx, dbase, kb, cb, 0, rb[0]);
-                    row_issue<T, kF32Path>(cx, dbase, kb, cb, 1, rb[1]);
+                    row_issue<T, kF32Path>(cx, dtap, cbp, 0, rb[0]);
+                    row_issue<T, kF32Path>(cx, dtap, cbp, 1, rb[1]);
                     // the stage is free once the MMAs that read it completed (tcgen05.commit);
                     // lane 0 polls, the warp follows it
                     int got = 0;
@@ -806,7 +813,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
 #pragma unroll
                     for (int it = 0; it < 2 * 4; ++it) {
                         if (it < nits) {
-                            if (it + 2 < nits) row_issue<T, kF32Path>(cx, dbase, kb, cb, it + 2, rb[(it + 2) % 3]);
+                            if (it + 2 < nits) row_issue<T, kF32Path>(cx, dtap, cbp, it + 2, rb[(it + 2) % 3]);
                             row_combine<T, kF32Path>(cx, a_s, it, rb[it % 3]);
                         }
                     }

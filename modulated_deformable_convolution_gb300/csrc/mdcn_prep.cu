@@ -1,5 +1,6 @@
 // Layout-prep kernels of the fused path:
-//   x      [N, Cin, H, W]      -> xt [N, H, W, Cp]   (channels-last, units padded;
+//   x      [N, Cin, H, W]      -> xt [N*H*W + 1, Cp] (channels-last, units padded,
+//                                 then one all-zero pixel;
 //                                 a register-blocked kernel where H*W and the
 //                                 unit are multiples of 16 bytes of elements,
 //                                 a shared-memory staged one otherwise)
@@ -27,23 +28,34 @@ __device__ __forceinline__ __half zero_of<__half>() { return __float2half_rn(0.0
 template <>
 __device__ __forceinline__ __nv_bfloat16 zero_of<__nv_bfloat16>() { return __float2bfloat16_rn(0.0f); }
 
+// The all-zero pixel after the image data (read for corners outside the
+// image), written by one block: Cp elements, 16 bytes per thread and pass.
+template <typename T>
+__device__ __forceinline__ void write_zero_pixel(T* zp, int64_t Cp, int nthreads, int tid) {
+    const int64_t nv = Cp * static_cast<int64_t>(sizeof(T)) / 16;
+    for (int64_t v = tid; v < nv; v += nthreads) reinterpret_cast<uint4*>(zp)[v] = make_uint4(0u, 0u, 0u, 0u);
+}
+
 // One block converts a run of up to 32 pixels of one (n, h) row: it loads
 // x[n, :, h, w0:w0+wc] (a warp reads 32 consecutive w of one channel) into
 // shared memory as [pixel][padded channel] (pad channels zero), then writes
 // the wc*Cp contiguous elements of the channels-last row with 16-byte stores.
-// Block (0, 0) also clears the device status word. Block (32, 8); grid
+// Block 0 also clears the device status word and writes the zero pixel. Block (32, 8); grid
 // x = (n*H + h) * wchunks + chunk.
 template <typename T>
 __global__ void __launch_bounds__(256) nhwc_pad_kernel(const T* __restrict__ x, T* __restrict__ xt,
                                                        uint32_t* __restrict__ status, int32_t Cin, int64_t H,
                                                        int64_t W, int64_t Cp, int32_t U, int32_t UP, int32_t WC,
-                                                       int64_t wchunks) {
+                                                       int64_t wchunks, int64_t zero_off) {
     extern __shared__ uint4 prep_smem[];
     T* sm = reinterpret_cast<T*>(prep_smem);
     constexpr int kVec = 16 / sizeof(T);
     const int32_t pitch = static_cast<int32_t>(Cp) + kVec;  // elements per staged pixel (16-byte multiple)
     const int tid = threadIdx.y * 32 + threadIdx.x;
-    if (blockIdx.x == 0 && tid == 0) *status = 0u;
+    if (blockIdx.x == 0) {
+        if (tid == 0) *status = 0u;
+        write_zero_pixel(xt + zero_off, Cp, 256, tid);
+    }
     const int64_t bx = blockIdx.x;
     const int64_t nh = bx / wchunks;
     const int64_t w0 = (bx - nh * wchunks) * WC;
@@ -93,13 +105,17 @@ __global__ void __launch_bounds__(256) nhwc_pad_kernel(const T* __restrict__ x, 
 // groups x 4 pixel groups; output channels in a unit's padding are written as
 // zeros. Grid (ceil(pixel blocks / 8), channel blocks, N), 8 warps per block,
 // one pixel block (4 * kVec pixels) per warp. Block (0, 0, 0) also clears the
-// device status word.
+// device status word and writes the zero pixel.
 template <typename T>
 __device__ __forceinline__ void nhwc_block_body(const T* __restrict__ x, T* __restrict__ xt,
                                                 uint32_t* __restrict__ status, int32_t Cin, int64_t P, int64_t Cp,
-                                                int32_t U, int32_t UP, uint32_t bx, uint32_t by, uint32_t bz) {
+                                                int32_t U, int32_t UP, int64_t zero_off, uint32_t bx, uint32_t by,
+                                                uint32_t bz) {
     constexpr int kVec = 16 / sizeof(T);
-    if (bx == 0 && by == 0 && bz == 0 && threadIdx.x == 0) *status = 0u;
+    if (bx == 0 && by == 0 && bz == 0) {
+        if (threadIdx.x == 0) *status = 0u;
+        write_zero_pixel(xt + zero_off, Cp, 256, threadIdx.x);
+    }
     const int lane = threadIdx.x & 31;
     const int cg = lane & 7, pg = lane >> 3;
     const int64_t n = bz;
@@ -154,8 +170,8 @@ __device__ __forceinline__ void nhwc_block_body(const T* __restrict__ x, T* __re
 template <typename T>
 __global__ void __launch_bounds__(256) nhwc_block_kernel(const T* __restrict__ x, T* __restrict__ xt,
                                                          uint32_t* __restrict__ status, int32_t Cin, int64_t P,
-                                                         int64_t Cp, int32_t U, int32_t UP) {
-    nhwc_block_body<T>(x, xt, status, Cin, P, Cp, U, UP, blockIdx.x, blockIdx.y, blockIdx.z);
+                                                         int64_t Cp, int32_t U, int32_t UP, int64_t zero_off) {
+    nhwc_block_body<T>(x, xt, status, Cin, P, Cp, U, UP, zero_off, blockIdx.x, blockIdx.y, blockIdx.z);
 }
 
 template <typename T>
@@ -225,8 +241,8 @@ __global__ void __launch_bounds__(256) prep_both_kernel(const T* __restrict__ x,
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const uint32_t b = blockIdx.x;
     if (b < nt) {
-        nhwc_block_body<T>(x, xt, status, static_cast<int32_t>(pl.Cin), pl.H * pl.W, pl.Cp, pl.U, pl.UP, b % tgx,
-                           (b / tgx) % tgy, b / (tgx * tgy));
+        nhwc_block_body<T>(x, xt, status, static_cast<int32_t>(pl.Cin), pl.H * pl.W, pl.Cp, pl.U, pl.UP,
+                           pl.N * pl.H * pl.W * pl.Cp, b % tgx, (b / tgx) % tgy, b / (tgx * tgy));
     } else {
         const uint32_t q = b - nt;
         pack_weight_body<T>(weight, wp, pl, q % pgx, q / pgx, pgy);
@@ -267,7 +283,8 @@ static cudaError_t prep_input_t(const Plan& pl, const void* x, void* ws, cudaStr
     dim3 grid;
     if (block_transpose_grid<T>(pl, &grid)) {
         nhwc_block_kernel<T><<<grid, 256, 0, st>>>(static_cast<const T*>(x), xt, status,
-                                                   static_cast<int32_t>(pl.Cin), P, pl.Cp, pl.U, pl.UP);
+                                                   static_cast<int32_t>(pl.Cin), P, pl.Cp, pl.U, pl.UP,
+                                                   pl.N * P * pl.Cp);
         return cudaGetLastError();
     }
     const int64_t pitch_bytes = (pl.Cp + 16 / static_cast<int64_t>(sizeof(T))) * static_cast<int64_t>(sizeof(T));
@@ -279,7 +296,7 @@ static cudaError_t prep_input_t(const Plan& pl, const void* x, void* ws, cudaStr
     const size_t smem = static_cast<size_t>(wc * pitch_bytes);
     nhwc_pad_kernel<T><<<static_cast<unsigned>(pl.N * pl.H * wchunks), dim3(32, 8), smem, st>>>(
         static_cast<const T*>(x), xt, status, static_cast<int32_t>(pl.Cin), pl.H, pl.W, pl.Cp, pl.U, pl.UP,
-        static_cast<int32_t>(wc), wchunks);
+        static_cast<int32_t>(wc), wchunks, pl.N * pl.H * pl.W * pl.Cp);
     return cudaGetLastError();
 }
 
