@@ -27,6 +27,7 @@
 #include <cuda_fp16.h>
 
 #include <cstring>
+#include <type_traits>
 #include <mutex>
 
 #include "mdcn_launch.h"
@@ -729,106 +730,117 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     } else if (wg == 1 || wg == 2) {
         setmaxnreg_inc<kRegsGather>();
         // ------------------------------------------------------------ gather producers
-        // Two k-tiles in flight per warp: the corner loads of k-tile n+1 are issued
-        // before k-tile n is combined and stored, so one L2 round trip overlaps the
-        // previous k-tile's work instead of stalling every k-tile.
         // k-tile-parallel gather: the 8 warps form G = pl.kgroups groups; group p
         // produces every G-th k-tile of the CTA's sequence (steps p, p + G, ...),
         // so G k-tiles are in production at once and a stage (stages are a
-        // multiple of G) always belongs to one group. Each of a group's 8/G warps handles 16*G rows as 2*G
-        // row-iterations of 8 rows, the corner loads running 2 row-iterations
-        // ahead of the weighted sums.
+        // multiple of G) always belongs to one group. Each of a group's 8/G
+        // warps handles 16*G rows as 2*G row-iterations of 8 rows, the corner
+        // loads running 2 row-iterations ahead of the weighted sums. G is a
+        // compile-time constant of each of the three variants below.
         const int gw = warp - kWarpGather;
-        const int G = pl.kgroups;
-        const int wpg = kGatherWarps / G;  // warps per k-tile
-        const int pair = gw / wpg;
-        const int nits = 2 * G;            // row-iterations per warp and k-tile
-        GatherCtx<T> cx;
-        cx.lane = lane;
-        cx.q4 = lane & 3;     // lane's 32 bytes of the 128-byte row
-        cx.rsub = lane >> 2;  // row within a group of 8
-        cx.row0 = (gw % wpg) * 8 * nits;
-        cx.xt = static_cast<const T*>(prm.xt);
-        cx.d1 = 1;
-        cx.dW = static_cast<int32_t>(pl.W);
-        cx.dW1 = static_cast<int32_t>(pl.W + 1);
-        cx.zpix = static_cast<int32_t>(pl.N * pl.H * pl.W);
-        cx.pix_bytes = static_cast<int32_t>(pl.Cp * static_cast<int64_t>(sizeof(T)));
-        cx.dsz = static_cast<uint32_t>(pl.desc_size);
-        cx.row_desc = static_cast<uint32_t>(cx.row0 + cx.rsub) * cx.dsz;
-        cx.row_sts = swz128(cx.row0 + cx.rsub, 2 * cx.q4);
-        constexpr int kVec = 16 / sizeof(T);
-        const int32_t ngroups = pl.Ug * pl.ntb;
-        uint32_t gr = 0;     // descriptor groups entered
-        uint32_t sbase = 0;  // CTA step of the current unit's first k-tile
-        bool ok = true;
-        for (int64_t pos = lo; pos < hi && ok;) {
-            const Unit un = unit_at(pl, pos, hi);
-            pos = un.t * KT + un.k1;
-            const TileId id = decode_tile(pl, un.t);
-            int32_t q = 0;  // first k-tile (processing order) of the current group
-            for (int32_t gi = 0; gi < ngroups && ok && q < un.k1; ++gi) {
-                const int32_t ul = gi / pl.ntb;
-                const int32_t b = gi - ul * pl.ntb;
-                const int32_t ntbg = min(kTapBlock, pl.K - b * kTapBlock);
-                const int32_t nktg = ntbg * pl.nch;
-                if (q + nktg <= un.k0) {  // group before the unit's range: not copied
-                    q += nktg;
-                    continue;
-                }
-                const int slot = gr & 1;
-                if (!__all_sync(0xffffffffu, mbar_wait_bounded(dfull_bar(slot), (gr >> 1) & 1, abort_flag, prm.status,
-                                                               kSiteGatherEmpty))) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t dbase = d0 + slot * dslot;
-                const int64_t unit = static_cast<int64_t>(id.g) * pl.Ug + ul;
-                // k-tile j of the group is CTA step sbase + q + j - k0; this warp
-                // group takes the steps equal to pair modulo G
-                const int32_t jlo = max(un.k0 - q, 0), jhi = min(un.k1 - q, nktg);
-                const uint32_t s_lo = sbase + static_cast<uint32_t>(q + jlo - un.k0);
-                for (int32_t j = jlo + (pair - static_cast<int32_t>(s_lo % G) + G) % G; j < jhi; j += G) {
-                    const int32_t ch = j / ntbg;
-                    const int32_t kb = j - ch * ntbg;
-                    const int64_t cb = unit * pl.UP + static_cast<int64_t>(ch) * pl.BKc + cx.q4 * 2 * kVec;
-                    const char* cbp = reinterpret_cast<const char*>(cx.xt + cb);
-                    const uint32_t dtap = dbase + static_cast<uint32_t>(kb * kTileM) * cx.dsz;
-                    const uint32_t step = sbase + static_cast<uint32_t>(q + j - un.k0);
-                    const int st = step % S;
-                    RowBuf rb[3];
-                    row_issue<T, kF32Path>(cx, dtap, cbp, 0, rb[0]);
-                    row_issue<T, kF32Path>(cx, dtap, cbp, 1, rb[1]);
-                    // the stage is free once the MMAs that read it completed (tcgen05.commit);
-                    // lane 0 polls, the warp follows it
-                    int got = 0;
-                    if (lane == 0)
-                        got = mbar_wait_bounded(empty_bar(st), ((step / S) & 1) ^ 1u, abort_flag, prm.status,
-                                                kSiteGatherEmpty);
-                    if (!__shfl_sync(0xffffffffu, got, 0)) {
+        auto gather = [&](auto g_const) {
+            constexpr int G = decltype(g_const)::value;
+            constexpr int wpg = kGatherWarps / G;  // warps per k-tile
+            constexpr int nits = 2 * G;            // row-iterations per warp and k-tile
+            const int pair = gw / wpg;
+            GatherCtx<T> cx;
+            cx.lane = lane;
+            cx.q4 = lane & 3;     // lane's 32 bytes of the 128-byte row
+            cx.rsub = lane >> 2;  // row within a group of 8
+            cx.row0 = (gw % wpg) * 8 * nits;
+            cx.xt = static_cast<const T*>(prm.xt);
+            cx.d1 = 1;
+            cx.dW = static_cast<int32_t>(pl.W);
+            cx.dW1 = static_cast<int32_t>(pl.W + 1);
+            cx.zpix = static_cast<int32_t>(pl.N * pl.H * pl.W);
+            cx.pix_bytes = static_cast<int32_t>(pl.Cp * static_cast<int64_t>(sizeof(T)));
+            cx.dsz = static_cast<uint32_t>(pl.desc_size);
+            cx.row_desc = static_cast<uint32_t>(cx.row0 + cx.rsub) * cx.dsz;
+            cx.row_sts = swz128(cx.row0 + cx.rsub, 2 * cx.q4);
+            constexpr int kVec = 16 / sizeof(T);
+            const int32_t ntb = pl.ntb, Kt = pl.K, nch = pl.nch, Ug = pl.Ug, BKc = pl.BKc;
+            const int64_t UP = pl.UP;
+            const int32_t ngroups = Ug * ntb;
+            // this warp group's steps are pair, pair + G, ...: stage and phase advance by G
+            uint32_t st = static_cast<uint32_t>(pair), phase = 0;
+            uint32_t gr = 0;     // descriptor groups entered
+            uint32_t sbase = 0;  // CTA step of the current unit's first k-tile
+            bool ok = true;
+            for (int64_t pos = lo; pos < hi && ok;) {
+                const Unit un = unit_at(pl, pos, hi);
+                pos = un.t * KT + un.k1;
+                const TileId id = decode_tile(pl, un.t);
+                int32_t q = 0;  // first k-tile (processing order) of the current group
+                for (int32_t gi = 0; gi < ngroups && ok && q < un.k1; ++gi) {
+                    const int32_t ul = gi / ntb;
+                    const int32_t b = gi - ul * ntb;
+                    const int32_t ntbg = min(kTapBlock, Kt - b * kTapBlock);
+                    const int32_t nktg = ntbg * nch;
+                    if (q + nktg <= un.k0) {  // group before the unit's range: not sampled
+                        q += nktg;
+                        continue;
+                    }
+                    const int slot = gr & 1;
+                    if (!__all_sync(0xffffffffu, mbar_wait_bounded(dfull_bar(slot), (gr >> 1) & 1, abort_flag,
+                                                                   prm.status, kSiteGatherEmpty))) {
                         ok = false;
                         break;
                     }
-                    const uint32_t a_s = a0 + st * a_bytes;
+                    const uint32_t dbase = d0 + slot * dslot;
+                    const int64_t unit = static_cast<int64_t>(id.g) * Ug + ul;
+                    // k-tile j of the group is CTA step sbase + q + j - k0; this warp
+                    // group takes the steps equal to pair modulo G
+                    const int32_t jlo = max(un.k0 - q, 0), jhi = min(un.k1 - q, nktg);
+                    const uint32_t s_lo = sbase + static_cast<uint32_t>(q + jlo - un.k0);
+                    for (int32_t j = jlo + (pair - static_cast<int32_t>(s_lo % G) + G) % G; j < jhi; j += G) {
+                        const int32_t ch = j / ntbg;
+                        const int32_t kb = j - ch * ntbg;
+                        const int64_t cb = unit * UP + static_cast<int64_t>(ch) * BKc + cx.q4 * 2 * kVec;
+                        const char* cbp = reinterpret_cast<const char*>(cx.xt + cb);
+                        const uint32_t dtap = dbase + static_cast<uint32_t>(kb * kTileM) * cx.dsz;
+                        RowBuf rb[3];
+                        row_issue<T, kF32Path>(cx, dtap, cbp, 0, rb[0]);
+                        row_issue<T, kF32Path>(cx, dtap, cbp, 1, rb[1]);
+                        // the stage is free once the MMAs that read it completed
+                        // (tcgen05.commit); lane 0 polls, the warp follows it
+                        int got = 0;
+                        if (lane == 0)
+                            got = mbar_wait_bounded(empty_bar(st), phase ^ 1u, abort_flag, prm.status,
+                                                    kSiteGatherEmpty);
+                        if (!__shfl_sync(0xffffffffu, got, 0)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t a_s = a0 + st * a_bytes;
 #pragma unroll
-                    for (int it = 0; it < 2 * 4; ++it) {
-                        if (it < nits) {
+                        for (int it = 0; it < nits; ++it) {
                             if (it + 2 < nits) row_issue<T, kF32Path>(cx, dtap, cbp, it + 2, rb[(it + 2) % 3]);
                             row_combine<T, kF32Path>(cx, a_s, it, rb[it % 3]);
                         }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(full_bar(st));
+                        st += G;
+                        if (st >= static_cast<uint32_t>(S)) {
+                            st -= S;
+                            phase ^= 1u;
+                        }
                     }
-                    fence_proxy_async_smem();
+                    q += nktg;
+                    // every gather warp releases every descriptor group, used or not
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(full_bar(st));
+                    if (lane == 0) mbar_arrive(dempty_bar(slot));
+                    ++gr;
                 }
-                q += nktg;
-                // every gather warp releases every descriptor group, used or not
-                __syncwarp();
-                if (lane == 0) mbar_arrive(dempty_bar(slot));
-                ++gr;
+                sbase += static_cast<uint32_t>(un.k1 - un.k0);
             }
-            sbase += static_cast<uint32_t>(un.k1 - un.k0);
-        }
+        };
+        if (pl.kgroups == 1)
+            gather(std::integral_constant<int, 1>{});
+        else if (pl.kgroups == 4)
+            gather(std::integral_constant<int, 4>{});
+        else
+            gather(std::integral_constant<int, 2>{});
     } else {
         setmaxnreg_dec<kRegsEpi>();
         // ------------------------------------------------------------ epilogue
