@@ -649,7 +649,15 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
             const uint32_t idesc = make_idesc(Elem<DT>::fmt, kTileM, static_cast<uint32_t>(pl.BNs));
             const uint32_t sub_bytes = static_cast<uint32_t>(pl.BNs) * 128u;
             const uint32_t half_bytes = sub_bytes * pl.nsub;
-            uint32_t s = 0, i = 0;
+            const int nsub = pl.nsub;
+            // Shared-memory descriptors differ only in their start-address field
+            // (address >> 4, 14 bits): every descriptor of the loop is a base one
+            // plus an offset. Per k-tile the thread waits, issues and commits.
+            const uint64_t adesc0 = smem_desc_sw128(a0);
+            const uint64_t bdesc0 = smem_desc_sw128(b0);
+            const uint32_t a_step = a_bytes >> 4, b_step = b_bytes >> 4;
+            const uint32_t sub_step = sub_bytes >> 4, half_step = half_bytes >> 4, alo_step = (kTileM * 128) >> 4;
+            uint32_t st = 0, ph = 0, i = 0;
             bool ok = true;
             for (int64_t pos = lo; pos < hi && ok; ++i) {
                 const Unit un = unit_at(pl, pos, hi);
@@ -659,37 +667,39 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                 if (!mbar_wait_bounded(acce_bar(ab), (use & 1) ^ 1u, abort_flag, prm.status, kSiteMmaFull)) break;
                 tc_fence_after();
                 const uint32_t dacc = tmem_base + static_cast<uint32_t>(ab * pl.acc_cols);
-                for (int32_t kt = un.k0; kt < un.k1; ++kt, ++s) {
-                    const int st = s % S;
-                    const uint32_t ph = (s / S) & 1;
+                for (int32_t kt = un.k0; kt < un.k1; ++kt) {
                     if (!mbar_wait_bounded(full_bar(st), ph, abort_flag, prm.status, kSiteMmaFull) ||
                         !mbar_wait_bounded(tma_bar(st), ph, abort_flag, prm.status, kSiteMmaTma)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_s = a0 + st * a_bytes;
-                    const uint32_t b_s = b0 + st * b_bytes;
+                    const uint64_t ad = adesc0 + st * a_step;
+                    const uint64_t bd = bdesc0 + st * b_step;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {  // 4 MMA K-steps of 32 bytes per 128-byte k-tile
-                        const uint64_t adesc = smem_desc_sw128(a_s + kk * 32);
-#pragma unroll 1
-                        for (int j = 0; j < pl.nsub; ++j) {
-                            const uint32_t d = dacc + static_cast<uint32_t>(j * pl.BNs);
-                            const uint64_t bdesc = smem_desc_sw128(b_s + j * sub_bytes + kk * 32);
-                            const uint32_t accum = (kt > un.k0 || kk > 0) ? 1u : 0u;
-                            if constexpr (kF32Path) {
-                                const uint64_t adesc_lo = smem_desc_sw128(a_s + kTileM * 128 + kk * 32);
-                                const uint64_t bdesc_lo = smem_desc_sw128(b_s + half_bytes + j * sub_bytes + kk * 32);
-                                mma_tf32(d, adesc, bdesc, idesc, accum);
-                                mma_tf32(d, adesc, bdesc_lo, idesc, 1u);
-                                mma_tf32(d, adesc_lo, bdesc, idesc, 1u);
-                            } else {
-                                mma_f16(d, adesc, bdesc, idesc, accum);
+                        const uint32_t accum = (kt > un.k0 || kk > 0) ? 1u : 0u;
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) {
+                            if (j < nsub) {
+                                const uint32_t d = dacc + static_cast<uint32_t>(j * pl.BNs);
+                                const uint64_t adesc = ad + 2u * kk;
+                                const uint64_t bdesc = bd + j * sub_step + 2u * kk;
+                                if constexpr (kF32Path) {
+                                    mma_tf32(d, adesc, bdesc, idesc, accum);
+                                    mma_tf32(d, adesc, bdesc + half_step, idesc, 1u);
+                                    mma_tf32(d, adesc + alo_step, bdesc, idesc, 1u);
+                                } else {
+                                    mma_f16(d, adesc, bdesc, idesc, accum);
+                                }
                             }
                         }
                     }
                     mma_commit(empty_bar(st));
+                    if (++st == static_cast<uint32_t>(S)) {
+                        st = 0;
+                        ph ^= 1u;
+                    }
                 }
                 mma_commit(accf_bar(ab));
             }
