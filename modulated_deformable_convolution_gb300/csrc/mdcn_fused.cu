@@ -610,32 +610,38 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     setmaxnreg_dec<kRegsCtrl>();
     if (warp == kWarpTma) {
         // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
+        // The whole warp runs the loop; the elected lane issues.
+        {
             const uint32_t sub_bytes = static_cast<uint32_t>(pl.BNs) * 128u;
             const uint32_t half_bytes = sub_bytes * pl.nsub;
+            const int nsub = pl.nsub;
             Cursor kc;  // next weight k-tile to load
             cursor_init(pl, kc, lo, hi);
             bool ok = true;
-            uint32_t s = 0;
+            uint32_t s = 0, st = 0, ph = 0;
             while (kc.live && ok) {
-                const int st = s % S;
-                if (!mbar_wait_bounded(empty_bar(st), ((s / S) & 1) ^ 1u, abort_flag, prm.status, kSiteTmaEmpty)) {
+                if (!warp_wait_bounded(empty_bar(st), ph ^ 1u, abort_flag, prm.status, kSiteTmaEmpty)) {
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(tma_bar(st), b_bytes);
+                mbar_arrive_expect_tx_elect(tma_bar(st), b_bytes);
                 const uint32_t dst = b0 + st * b_bytes;
                 const int32_t row0 = kc.g * pl.Og + kc.nt * pl.acc_cols;
-#pragma unroll 1
+#pragma unroll
                 for (int h = 0; h < (kF32Path ? 2 : 1); ++h)
-#pragma unroll 1
-                    for (int j = 0; j < pl.nsub; ++j)
-                        tma_load_2d(dst + h * half_bytes + j * sub_bytes, &tmap, kc.kt * pl.BKc,
-                                    row0 + h * static_cast<int32_t>(pl.Cout) + j * pl.BNs, tma_bar(st));
+#pragma unroll
+                    for (int j = 0; j < 2; ++j)
+                        if (j < nsub)
+                            tma_load_2d_elect(dst + h * half_bytes + j * sub_bytes, &tmap, kc.kt * pl.BKc,
+                                              row0 + h * static_cast<int32_t>(pl.Cout) + j * pl.BNs, tma_bar(st));
                 ++s;
+                if (++st == static_cast<uint32_t>(S)) {
+                    st = 0;
+                    ph ^= 1u;
+                }
                 cursor_advance(pl, kc);
             }
-            if (!ok) {
+            if (!ok && lane == 0) {
                 // let the copies already issued land before the CTA exits
                 const uint32_t first = s > static_cast<uint32_t>(S) ? s - S : 0;
                 volatile int never = 0;
