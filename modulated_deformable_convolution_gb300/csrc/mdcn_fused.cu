@@ -651,14 +651,17 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // The whole warp runs the loop converged (its waits poll and vote on
+        // every lane), so the descriptors stay in uniform registers; the
+        // elected lane issues each tcgen05 instruction.
+        {
             const uint32_t idesc = make_idesc(Elem<DT>::fmt, kTileM, static_cast<uint32_t>(pl.BNs));
             const uint32_t sub_bytes = static_cast<uint32_t>(pl.BNs) * 128u;
             const uint32_t half_bytes = sub_bytes * pl.nsub;
             const int nsub = pl.nsub;
             // Shared-memory descriptors differ only in their start-address field
             // (address >> 4, 14 bits): every descriptor of the loop is a base one
-            // plus an offset. Per k-tile the thread waits, issues and commits.
+            // plus an offset. Per k-tile the warp waits, issues and commits.
             const uint64_t adesc0 = smem_desc_sw128(a0);
             const uint64_t bdesc0 = smem_desc_sw128(b0);
             const uint32_t a_step = a_bytes >> 4, b_step = b_bytes >> 4;
@@ -670,12 +673,12 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                 pos = un.t * KT + un.k1;
                 const int ab = static_cast<int>(i % pl.nacc);
                 const uint32_t use = i / pl.nacc;
-                if (!mbar_wait_bounded(acce_bar(ab), (use & 1) ^ 1u, abort_flag, prm.status, kSiteMmaFull)) break;
+                if (!warp_wait2(acce_bar(ab), 0u, (use & 1) ^ 1u, abort_flag, prm.status, kSiteMmaFull)) break;
                 tc_fence_after();
                 const uint32_t dacc = tmem_base + static_cast<uint32_t>(ab * pl.acc_cols);
                 for (int32_t kt = un.k0; kt < un.k1; ++kt) {
-                    if (!mbar_wait_bounded(full_bar(st), ph, abort_flag, prm.status, kSiteMmaFull) ||
-                        !mbar_wait_bounded(tma_bar(st), ph, abort_flag, prm.status, kSiteMmaTma)) {
+                    // the A stage gathered and the B stage landed, polled together
+                    if (!warp_wait2(full_bar(st), tma_bar(st), ph, abort_flag, prm.status, kSiteMmaFull)) {
                         ok = false;
                         break;
                     }
@@ -692,27 +695,27 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                                 const uint64_t adesc = ad + 2u * kk;
                                 const uint64_t bdesc = bd + j * sub_step + 2u * kk;
                                 if constexpr (kF32Path) {
-                                    mma_tf32(d, adesc, bdesc, idesc, accum);
-                                    mma_tf32(d, adesc, bdesc + half_step, idesc, 1u);
-                                    mma_tf32(d, adesc + alo_step, bdesc, idesc, 1u);
+                                    mma_tf32_elect(d, adesc, bdesc, idesc, accum);
+                                    mma_tf32_elect(d, adesc, bdesc + half_step, idesc, 1u);
+                                    mma_tf32_elect(d, adesc + alo_step, bdesc, idesc, 1u);
                                 } else {
-                                    mma_f16(d, adesc, bdesc, idesc, accum);
+                                    mma_f16_elect(d, adesc, bdesc, idesc, accum);
                                 }
                             }
                         }
                     }
-                    mma_commit(empty_bar(st));
+                    mma_commit_elect(empty_bar(st));
                     if (++st == static_cast<uint32_t>(S)) {
                         st = 0;
                         ph ^= 1u;
                     }
                 }
-                mma_commit(accf_bar(ab));
+                mma_commit_elect(accf_bar(ab));
             }
-            // every MMA issued by this thread completes before TMEM is released
-            mma_commit(drain_bar);
+            // every MMA issued by the elected lane completes before TMEM is released
+            mma_commit_elect(drain_bar);
             volatile int never = 0;
-            mbar_wait_bounded(drain_bar, 0, &never, prm.status, kSiteDrain, 200000000ull);
+            warp_wait2(drain_bar, 0u, 0, &never, prm.status, kSiteDrain, 200000000ull);
         }
     } else {
         // ------------------------------------------------------------ sampling

@@ -97,6 +97,34 @@ __device__ __forceinline__ bool warp_wait_bounded(uint32_t bar, uint32_t parity,
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
+// Bounded wait for the given phases of two barriers (bar2 = 0: only bar1) by
+// a converged warp: every lane polls both barriers each round, so the two
+// polls' latencies overlap, and the warp votes; no lane diverges.
+__device__ __forceinline__ bool warp_wait2(uint32_t bar1, uint32_t bar2, uint32_t parity, volatile int* abort,
+                                           uint32_t* status, uint32_t site,
+                                           uint64_t limit_cycles = kWaitLimitCycles) {
+    auto ready = [&]() {
+        const bool a = mbar_try_wait(bar1, parity);
+        const bool b = bar2 == 0u || mbar_try_wait(bar2, parity);
+        return __all_sync(0xffffffffu, a && b);
+    };
+    if (ready()) return true;
+    const uint64_t t0 = clock64();
+    for (uint32_t it = 1;; ++it) {
+        if (ready()) return true;
+        if ((it & 63u) == 0) {
+            if (__any_sync(0xffffffffu, *abort != 0)) return false;
+            if (__any_sync(0xffffffffu, static_cast<uint64_t>(clock64()) - t0 > limit_cycles)) {
+                if ((threadIdx.x & 31) == 0) {
+                    *abort = 1;
+                    if (status) atomicOr(status, kStatusTimeout | site);
+                }
+                return false;
+            }
+        }
+    }
+}
+
 // ---------------------------------------------------------------- registers
 // Per-warpgroup register count (all warps of the warpgroup execute it).
 template <uint32_t N>
