@@ -248,7 +248,7 @@ def run_ours(args, case, world, rank, local, dist):
     plan = mdcn.mdcn_query_plan(h, x, off, m, w, b)
 
     def step():
-        # the public call: prep launch(es), the fused kernel, the split-tile fix-up
+        # the public call: prep launch(es), the fused kernel
         mdcn.mdcn_forward(h, x, off, m, w, b, out, ws, stream)
 
     def fused_step(ev):
@@ -361,7 +361,7 @@ def run_ours(args, case, world, rank, local, dist):
         peak_note = f"{peak_src} bf16 burst (fp16 has the same dense rate)"
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
             "traffic": profiled_traffic(case.name),
-            "kernel": "fused_kernel" + (" + splitk_fixup_kernel" if plan["split"] else ""), "peak_source": peak_note,
+            "kernel": "fused_kernel", "peak_source": peak_note,
             "kernel_us": fused_mean_s * 1e6}
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
@@ -378,7 +378,8 @@ def run_ours(args, case, world, rank, local, dist):
                    "l2": "flushed before every timed step (256 MiB write outside the events)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "step": "mdcn_forward: channels-last x + weight pack, fused kernel (sampling in-kernel)"
-                           + (", split-tile fix-up" if plan["split"] else "") + f" ({plan['launches']} launches)",
+                           + (", stream-K split tiles summed in-kernel" if plan["split"] else "")
+                           + f" ({plan['launches']} launches)",
                    "plan": plan},
         "step_ms": {"mean": ms, "p10": sorted(step_ms)[len(step_ms) // 10],
                     "p90": sorted(step_ms)[(len(step_ms) * 9) // 10]},

@@ -139,10 +139,10 @@ typedef struct mdcn_plan_info {
     int64_t ktiles_per_tile; /* k-tiles (128 bytes of channels of one tap) of one tile */
     int64_t ktiles_per_cta; /* consecutive k-tiles each persistent CTA takes */
     int32_t ctas;           /* persistent CTAs of the fused kernel */
-    int32_t split;          /* 1 when some tile is split between CTAs (the fix-up kernel runs) */
+    int32_t split;          /* 1 when some tile is split between CTAs (summed inside the fused kernel) */
     int32_t stages, kgroups, tile_mode;
     int32_t launches;       /* kernels one mdcn_forward launches: prep (1, or 2 when x needs the staged
-                               transpose), the fused kernel, and the fix-up when split */
+                               transpose) and the fused kernel */
 } mdcn_plan_info;
 
 /* Errors as mdcn_workspace_size, plus MDCN_ERR_ARCH / MDCN_ERR_CUDA from the
@@ -155,10 +155,11 @@ mdcn_status mdcn_query_plan(mdcn_handle handle, const mdcn_dims* dims, mdcn_dtyp
  * MMAs accumulate in tensor memory, the epilogue adds the bias and writes
  * NCHW. The im2col column matrix never reaches device memory. Persistent CTAs
  * (one per SM) take equal consecutive ranges of the k-tiles of all output
- * tiles; a tile split between CTAs is summed from their fp32 partials, in k
- * order, by a small fix-up kernel launched right after (programmatic
- * dependent launch). Two small kernels run first, into workspace: x to
- * channels-last and the weight repack.
+ * tiles (stream-K). A tile split between CTAs is finished by the CTA holding
+ * its first k-tiles, which reaches it last: it adds the other CTAs' fp32
+ * partial sums, in k order, before its epilogue. One small kernel runs
+ * first, into workspace: x to channels-last and the weight repack (two
+ * launches for shapes whose transpose needs the staged kernel).
  *   x [N,Cin,H,W], offset [N,2*dg*kh*kw,Ho,Wo], mask [N,dg*kh*kw,Ho,Wo],
  *   weight [Cout,Cin/group,kh,kw], bias_or_null [Cout] or NULL,
  *   out [N,Cout,Ho,Wo] (written), workspace of workspace_bytes (scratch,
@@ -180,8 +181,8 @@ mdcn_status mdcn_forward(mdcn_handle handle, const void* x, const void* offset, 
  *                          workspace status word;
  *   mdcn_pack_weight:      weight -> packed K-major copy in workspace;
  *   mdcn_forward_prepared: the fused kernel (sampling from offset and mask,
- *                          section 5 step 1; gather; contraction; bias), and
- *                          the split-tile fix-up when tiles are split. */
+ *                          section 5 step 1; gather; contraction; bias;
+ *                          the sums of split tiles). */
 mdcn_status mdcn_prepare_input(mdcn_handle handle, const void* x, void* workspace, size_t workspace_bytes,
                                const mdcn_dims* dims, mdcn_dtype dtype, void* stream);
 mdcn_status mdcn_pack_weight(mdcn_handle handle, const void* weight, void* workspace, size_t workspace_bytes,

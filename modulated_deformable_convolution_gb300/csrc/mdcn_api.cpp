@@ -195,9 +195,14 @@ mdcn_status make_plan(const mdcn_attrs& a, const mdcn_tuning& tuning, const mdcn
     p.desc_slot_bytes = mdcn::kTileM * mdcn::kTapBlock * p.desc_size;
     // TMA-store epilogue: 2-D tiles whose 16-channel boxes stay inside a group
     // and whose output rows are 16-byte multiples
-    p.epi_tma = (mode == 1 && (p.Wo * elem) % 16 == 0 && Og % 16 == 0) ? 1 : 0;
-    p.epi_bytes = p.epi_tma ? mdcn::kEpiWarps * 2 * 16 * 32 * static_cast<int32_t>(elem) : 0;
-    const int32_t fixed = 1024 + 2 * p.desc_slot_bytes + p.epi_bytes + 512;
+    {
+        // vector epilogue: every group of 16/elem consecutive output pixels that
+        // it stores is inside one row (2-D tiles) or one image, and 16-byte aligned
+        const int64_t v = 16 / elem;
+        p.epi_vec = (p.P % v == 0 && (mode == 0 || p.Wo % v == 0)) ? 1 : 0;
+    }
+    p.epi_bytes = mdcn::kEpiWarps * 16 * 32 * static_cast<int32_t>(elem);
+    const int32_t fixed = 1024 + 2 * p.desc_slot_bytes + p.epi_bytes + mdcn::kBiasBytes + 512;
     const int32_t per_stage = p.a_bytes + p.b_bytes;
     // stages: 2, 4, 6 or 8; the gather produces kgroups k-tiles at once (1, 2
     // or 4, dividing the stage count; automatic: 2, measured fastest on the
@@ -211,7 +216,7 @@ mdcn_status make_plan(const mdcn_attrs& a, const mdcn_tuning& tuning, const mdcn
     p.smem_bytes = fixed + stages * per_stage;
     p.grid = 0;  // set at launch from the SM count
 
-    // workspace: [status 256 B][x channels-last][packed weight]
+    // workspace: [status word, split-tile counters: 1 KB][x channels-last][packed weight][partials]
     // channels-last conversion stages whole pixels in 40 KB of shared memory
     if ((p.Cp + 16 / elem) * elem > 40 * 1024) return MDCN_ERR_UNSUPPORTED;
     if (p.N * p.H * p.W > kI31) return MDCN_ERR_UNSUPPORTED;
@@ -237,10 +242,10 @@ mdcn_status make_plan(const mdcn_attrs& a, const mdcn_tuning& tuning, const mdcn
                          ? 1
                          : 0;
     }
-    // stream-K: fp32 partial accumulators of split tiles, 2 slots per CTA
+    // stream-K: fp32 partial accumulators of split tiles, one slot per CTA
     p.total_kt = p.tiles_total;
     if (!mul_ok(p.total_kt, p.KT) || p.total_kt > kI31) return MDCN_ERR_UNSUPPORTED;  // 32-bit tile arithmetic
-    const int64_t part_bytes = static_cast<int64_t>(2) * mdcn::kMaxCtas * p.acc_cols * mdcn::kTileM * 4;
+    const int64_t part_bytes = static_cast<int64_t>(mdcn::kMaxCtas) * p.acc_cols * mdcn::kTileM * 4;
     p.off_xt = mdcn::kStatusBytes;
     p.off_wp = align256(p.off_xt + static_cast<size_t>(xt));
     p.off_part = align256(p.off_wp + static_cast<size_t>(wpb));
@@ -378,7 +383,7 @@ mdcn_status mdcn_query_plan(mdcn_handle handle, const mdcn_dims* dims, mdcn_dtyp
     info->stages = p.stages;
     info->kgroups = p.kgroups;
     info->tile_mode = p.tile_mode;
-    info->launches = (p.xt_block ? 2 : 3) + info->split;
+    info->launches = p.xt_block ? 2 : 3;
     return MDCN_OK;
 }
 

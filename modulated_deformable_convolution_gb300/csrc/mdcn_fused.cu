@@ -1,6 +1,6 @@
 // Fused implicit-GEMM kernel of the modulated deformable convolution forward
 // ("TensorRT plugin walkthrough: modulatedDeformConvPlugin", section 5, steps
-// 1-3, without the column buffer), and the fix-up of tiles split between CTAs.
+// 1-3, without the column buffer).
 //
 // fused_kernel: persistent CTAs (one per SM) take equal consecutive ranges of
 // the k-tiles of all output tiles (128 pixels x (nsub*BNs) output channels of
@@ -17,8 +17,11 @@
 //               (one tap, 128 bytes of channels): per row, 4 lanes x 32 bytes of
 //               the 4 corners of the channels-last copy of x, weighted sum,
 //               128-byte-swizzled store into the A stage
-//   warps 12-15 epilogue: TMEM -> registers -> +bias -> NCHW output (or the
-//               fp32 partial sum of a split tile -> workspace)
+//   warps 12-15 epilogue: TMEM -> registers -> +bias -> NCHW output. A tile
+//               split between CTAs (stream-K): each CTA but the one holding
+//               its first k-tiles writes an fp32 partial sum to the workspace
+//               and counts itself in; that first CTA, which reaches the tile
+//               last, adds the partials in k order and stores the output
 // Hand-offs use mbarriers; every wait is bounded (mdcn_ptx.cuh), and a wait
 // that gives up raises a CTA-wide abort that every role observes.
 #include <cuda.h>
@@ -66,7 +69,9 @@ struct FusedParams {
     const void* bias;
     void* out;
     uint32_t* status;
-    float* part;      // fp32 partial accumulators of split tiles: 2 slots per CTA
+    float* part;           // fp32 partial accumulators of split tiles: one slot per CTA
+    uint32_t* split_count;  // per split tile (by its first CTA): contributors' epilogue warps done
+    int32_t epi_vec;        // the plan allows 16-byte output stores and out is 16-byte aligned
     Plan pl;
 };
 
@@ -77,6 +82,33 @@ __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float
 __device__ __forceinline__ void from_f(float v, float* d) { *d = v; }
 __device__ __forceinline__ void from_f(float v, __half* d) { *d = __float2half_rn(v); }
 __device__ __forceinline__ void from_f(float v, __nv_bfloat16* d) { *d = __float2bfloat16_rn(v); }
+
+template <typename T>
+__device__ __forceinline__ T ld_shared_elem(uint32_t addr) {
+    if constexpr (sizeof(T) == 4) {
+        uint32_t v;
+        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+        return __uint_as_float(v);
+    } else {
+        uint16_t v;
+        asm volatile("ld.shared.b16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
+        T h;
+        *reinterpret_cast<uint16_t*>(&h) = v;
+        return h;
+    }
+}
+
+// One value converted to T, stored to shared memory.
+template <typename T>
+__device__ __forceinline__ void st_shared_elem(uint32_t addr, float v) {
+    if constexpr (sizeof(T) == 4) {
+        asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(__float_as_uint(v)) : "memory");
+    } else {
+        T h;
+        from_f(v, &h);
+        asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(*reinterpret_cast<uint16_t*>(&h)) : "memory");
+    }
+}
 
 __device__ __forceinline__ uint32_t pack2(float a, float b, __half*) {
     __half2 h = __floats2half2_rn(a, b);
@@ -511,8 +543,7 @@ __device__ __forceinline__ void row_combine(const GatherCtx<T>& cx, uint32_t a_s
 
 template <int DT>
 __global__ void __launch_bounds__(kFusedThreads, 1)
-    fused_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap omap,
-                 const FusedParams prm) {
+    fused_kernel(const __grid_constant__ CUtensorMap tmap, const FusedParams prm) {
     using T = typename Elem<DT>::T;
     constexpr bool kF32Path = (DT == kF32);
     const Plan& pl = prm.pl;
@@ -529,8 +560,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     const uint32_t b0 = a0 + S * a_bytes;
     const uint32_t d0 = b0 + S * b_bytes;  // descriptor ring, 2 slots
     const uint32_t dslot = static_cast<uint32_t>(pl.desc_slot_bytes);
-    const uint32_t e0s = d0 + 2 * dslot;  // epilogue staging (TMA-store path)
-    const uint32_t bar0 = e0s + static_cast<uint32_t>(pl.epi_bytes);
+    const uint32_t e0s = d0 + 2 * dslot;  // epilogue staging: [16 channels][32 pixels] per warp
+    const uint32_t bias_s = e0s + static_cast<uint32_t>(pl.epi_bytes);  // fp32 bias of the tile's columns
+    const uint32_t bar0 = bias_s + static_cast<uint32_t>(kBiasBytes);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto tma_bar = [&](int s) { return bar0 + 8u * (S + s); };
     auto empty_bar = [&](int s) { return bar0 + 8u * (2 * S + s); };
@@ -541,15 +573,13 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     auto dempty_bar = [&](int b) { return xb + 48u + 8u * b; };
     const uint32_t drain_bar = xb + 64u;
     const uint32_t slot_off = (xb - sbase) + 72u;
+    auto fix_bar = [&](int b) { return xb + 80u + 8u * b; };  // kFixBufs partial-sum buffers
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + slot_off);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + slot_off + 4);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int32_t KT = pl.KT;
-    // the split-tile fix-up may be scheduled onto SMs as they free up; it
-    // waits for this whole grid to finish before it reads anything
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // this CTA's range of the k-tile sequence
     const int64_t lo = static_cast<int64_t>(blockIdx.x) * pl.kt_per_cta;
     const int64_t hi = min(lo + pl.kt_per_cta, pl.total_kt);
@@ -567,6 +597,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
             mbar_init(dempty_bar(b), kGatherWarps);
         }
         mbar_init(drain_bar, 1);
+        for (int b = 0; b < kFixBufs; ++b) mbar_init(fix_bar(b), 1);
         *abort_flag = 0;
         fence_mbarrier_init();
         tma_prefetch_desc(&tmap);
@@ -602,7 +633,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
 
     // Register split per warpgroup (launch: 128 per thread x 512 threads; the
     // host refuses to launch a build whose register count is not exactly 128):
-    // TMA/MMA/sampling 96, gather 2 x 176, epilogue 64 -> 512 x 128 in total. Each
+    // TMA/MMA/sampling 96, gather 2 x 168, epilogue 80 -> 512 x 128 in total. Each
     // warpgroup's branch starts with its own setmaxnreg, so the compiler
     // allocates each role's code within that role's budget.
     const int wg = warp >> 2;
@@ -867,6 +898,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         const int row = quarter * 32 + lane;
         T* __restrict__ out = static_cast<T*>(prm.out);
         const T* __restrict__ bias = static_cast<const T*>(prm.bias);
+        const uint32_t stg = e0s + static_cast<uint32_t>(quarter * 16 * 32 * sizeof(T));
         uint32_t i = 0;
         for (int64_t pos = lo; pos < hi; ++i) {
             const Unit un = unit_at(pl, pos, hi);
@@ -874,22 +906,22 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
             const TileId id = decode_tile(pl, un.t);
             const int ab = static_cast<int>(i % pl.nacc);
             const uint32_t use = i / pl.nacc;
-            if (!__all_sync(0xffffffffu,
-                            mbar_wait_bounded(accf_bar(ab), use & 1, abort_flag, prm.status, kSiteEpilogue)))
+            // the four warps agree on going on (the named barriers below need all of them)
+            if (!bar_red_and(1, kEpiWarps * 32,
+                             __all_sync(0xffffffffu, mbar_wait_bounded(accf_bar(ab), use & 1, abort_flag, prm.status,
+                                                                       kSiteEpilogue))))
                 break;
             tc_fence_after();
-            const Pixel px = tile_pixel(pl, id.mt, row);
-            const int64_t hw = px.ho * pl.Wo + px.wo;
             const int32_t ncol0 = id.nt * pl.acc_cols;
-            const int64_t obase = (px.n * pl.Cout + static_cast<int64_t>(id.g) * pl.Og) * pl.P + hw;
             const uint32_t tl = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                 static_cast<uint32_t>(ab * pl.acc_cols);
-            if (un.k0 != 0 || un.k1 != KT) {
-                // split tile: this CTA's partial sum goes to its slot (slot 0 for
-                // its first unit, 1 for its last); the fix-up kernel adds the
-                // slots of each split tile in k order once every CTA is done
-                float* mine = prm.part + static_cast<size_t>(2 * blockIdx.x + (i == 0 ? 0 : 1)) *
-                                             static_cast<size_t>(pl.acc_cols) * kTileM;
+            const bool split = un.k0 != 0 || un.k1 != KT;
+            const int64_t c_first = split ? (un.t * KT) / pl.kt_per_cta : 0;
+            if (split && c_first != static_cast<int64_t>(blockIdx.x)) {
+                // a split tile whose first k-tiles are another CTA's (this is this
+                // CTA's first unit): the partial sum goes to this CTA's slot, then
+                // each warp counts itself in on the tile's counter
+                float* mine = prm.part + static_cast<size_t>(blockIdx.x) * static_cast<size_t>(pl.acc_cols) * kTileM;
                 for (int c32 = 0; c32 < pl.acc_cols; c32 += 32) {
                     float vals[32];
                     tmem_ld32(tl + static_cast<uint32_t>(c32), pl.acc_cols - c32 >= 32 ? 2 : 1, vals);
@@ -900,76 +932,127 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(acce_bar(ab));
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) atomicAdd(prm.split_count + c_first, 1u);
                 continue;
             }
-            if (pl.epi_tma) {
-                // 16-channel chunks: TMEM -> +bias -> staging [16 ch][2 rows][16 px] -> one TMA box
-                // store per chunk (rows/cols past the image are clipped by the tensor map)
-                const uint32_t stage0 = e0s + static_cast<uint32_t>(quarter) * (2u * 16u * 32u * sizeof(T));
-                const int64_t per_img = pl.tiles_x * pl.tiles_y;
-                const int64_t rem = id.mt - px.n * per_img;
-                const int64_t ty = rem / pl.tiles_x;
-                const int32_t gy = static_cast<int32_t>(ty * pl.TH + 2 * quarter);
-                const int32_t gx = static_cast<int32_t>((rem - ty * pl.tiles_x) * pl.TW);
-                int chunk = 0;
-                for (int c16 = 0; c16 < pl.acc_cols; c16 += 16) {
-                    float vals[16];
-                    tmem_ld16(tl + static_cast<uint32_t>(c16), vals);
-                    {
-                        const int32_t ol0 = ncol0 + c16;
-                        if (ol0 < pl.Og) {
-                            const uint32_t buf = stage0 + static_cast<uint32_t>(chunk & 1) * (16u * 32u * sizeof(T));
-                            if (lane == 0) bulk_wait_read<1>();  // the store issued two chunks ago has read buf
-                            __syncwarp();
-#pragma unroll
-                            for (int c = 0; c < 16; ++c) {
-                                float r = vals[c];
-                                if (bias) r += to_f(bias[static_cast<int64_t>(id.g) * pl.Og + ol0 + c]);
-                                T hv;
-                                from_f(r, &hv);
-                                const uint32_t a = buf + static_cast<uint32_t>((c * 32 + lane) * sizeof(T));
-                                if constexpr (sizeof(T) == 4) {
-                                    asm volatile("st.shared.b32 [%0], %1;" ::"r"(a), "r"(__float_as_uint(r)) : "memory");
-                                } else {
-                                    asm volatile("st.shared.b16 [%0], %1;" ::"r"(a), "h"(*reinterpret_cast<uint16_t*>(&hv))
-                                                 : "memory");
-                                }
-                            }
-                            fence_proxy_async_smem();
-                            __syncwarp();
-                            if (lane == 0) {
-                                tma_store_4d(&omap, buf, gx, gy, static_cast<int32_t>(id.g * pl.Og + ol0),
-                                             static_cast<int32_t>(px.n));
-                                bulk_commit();
-                            }
-                            ++chunk;
-                        }
-                    }
-                }
-            } else {
-                for (int c16 = 0; c16 < pl.acc_cols; c16 += 16) {
-                    float vals[16];
-                    tmem_ld16(tl + static_cast<uint32_t>(c16), vals);
-                    if (px.valid) {
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const int32_t ol = ncol0 + c16 + e;
-                            if (ol < pl.Og) {
-                                float r = vals[e];
-                                if (bias) r += to_f(bias[static_cast<int64_t>(id.g) * pl.Og + ol]);
-                                from_f(r, out + obase + static_cast<int64_t>(ol) * pl.P);
-                            }
-                        }
-                    }
-                }
+            // A whole tile, or a split tile this CTA owns: the owner holds the
+            // tile's first k-tiles as its last unit (all stages are idle once its
+            // accumulator is full) and adds the other m contributors' partials in
+            // k order. They arrive by bulk copies into the stage area: item j =
+            // (16-column chunk j / m, contributor j % m), 8 KB each, in a ring of
+            // nbuf buffers that the four epilogue warps step through together.
+            const int32_t m = split ? static_cast<int32_t>((un.t * KT + KT - 1) / pl.kt_per_cta - c_first) : 0;
+            const int32_t nbuf = min(kFixBufs, static_cast<int32_t>((S * (a_bytes + b_bytes)) / kFixBufBytes));
+            const int32_t nitems = m * (pl.acc_cols / 16);
+            auto fix_issue = [&](int32_t j) {
+                const int32_t b = j % nbuf;
+                const int32_t ch = j / m;
+                const int64_t c = c_first + 1 + (j - ch * m);
+                const float* src = prm.part + (c * pl.acc_cols + ch * 16) * kTileM;
+                mbar_arrive_expect_tx(fix_bar(b), kFixBufBytes);
+                bulk_load(a0 + static_cast<uint32_t>(b) * kFixBufBytes, src, kFixBufBytes, fix_bar(b));
+            };
+            if (m > 0 && warp == kWarpEpi && lane == 0 &&
+                wait_count_bounded(prm.split_count + c_first, static_cast<uint32_t>(kEpiWarps * m), abort_flag,
+                                   prm.status, kSiteSplitWait)) {
+                prm.split_count[c_first] = 0u;  // every contributor is in: zero again for the next call
+                fence_proxy_async_global();
+                for (int32_t j = 0; j < min(nbuf, nitems); ++j) fix_issue(j);
             }
+            bool fix_ok = true;
+            auto fix_add = [&](int c16, float(&vals)[16]) {
+                for (int32_t k = 0; k < m; ++k) {
+                    const int32_t j = (c16 >> 4) * m + k;
+                    const int32_t b = j % nbuf;
+                    const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(fix_bar(b), (j / nbuf) & 1, abort_flag,
+                                                                               prm.status, kSiteSplitWait));
+                    if (got) {
+                        // 8 loads in flight before their adds
+                        const uint32_t src = a0 + static_cast<uint32_t>(b) * kFixBufBytes + static_cast<uint32_t>(row) * 4u;
+#pragma unroll
+                        for (int h = 0; h < 16; h += 8) {
+                            float pv[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) pv[e] = lds_f32(src + static_cast<uint32_t>(h + e) * (kTileM * 4u));
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) vals[h + e] += pv[e];
+                        }
+                    }
+                    // the buffer is free once all four warps have read it
+                    if (!bar_red_and(1, kEpiWarps * 32, got)) {
+                        fix_ok = false;
+                        return;
+                    }
+                    if (warp == kWarpEpi && lane == 0 && j + nbuf < nitems) {
+                        fence_proxy_async_smem();
+                        fix_issue(j + nbuf);
+                    }
+                }
+            };
+            // the tile's bias columns -> shared memory (fp32); every warp is past
+            // the previous tile (barrier above), and all have written before any reads
+            if (bias) {
+                for (int c = row; c < pl.acc_cols; c += kTileM) {
+                    const int32_t ol = ncol0 + c;
+                    st_shared_f32(bias_s + 4u * c, ol < pl.Og ? to_f(bias[static_cast<int64_t>(id.g) * pl.Og + ol]) : 0.f);
+                }
+                named_bar_sync(1, kEpiWarps * 32);
+            }
+            // vector path: this lane's group of kVecPx consecutive pixels (group
+            // lane % kGroups of the warp's 32 rows) and its first output element
+            constexpr int kVecPx = 16 / sizeof(T);
+            constexpr int kGroups = 32 / kVecPx;
+            const Pixel gp = tile_pixel(pl, id.mt, quarter * 32 + (lane % kGroups) * kVecPx);
+            const int64_t gbase = (gp.n * pl.Cout + static_cast<int64_t>(id.g) * pl.Og + ncol0) * pl.P +
+                                  gp.ho * pl.Wo + gp.wo;
+            for (int c16 = 0; c16 < pl.acc_cols; c16 += 16) {
+                float vals[16];
+                tmem_ld16(tl + static_cast<uint32_t>(c16), vals);
+                if (m > 0) {
+                    fix_add(c16, vals);
+                    if (!fix_ok) break;
+                }
+                if (ncol0 + c16 >= pl.Og) continue;
+                if (bias) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) vals[e] += ld_shared_f32(bias_s + 4u * (c16 + e));
+                }
+                // [16 channels][32 pixels] in this warp's staging, then stored
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    st_shared_elem<T>(stg + static_cast<uint32_t>((e * 32 + lane) * sizeof(T)), vals[e]);
+                __syncwarp();
+                if (prm.epi_vec) {
+                    // 16-byte stores of kVecPx consecutive pixels of one channel
+#pragma unroll
+                    for (int k = 0; k < 16 * kGroups / 32; ++k) {
+                        const int e = lane / kGroups + k * (32 / kGroups);  // channel of the chunk
+                        const uint32_t src = stg + static_cast<uint32_t>((e * 32 + (lane % kGroups) * kVecPx) * sizeof(T));
+                        if (gp.valid && ncol0 + c16 + e < pl.Og)
+                            st_global_v4(out + gbase + static_cast<int64_t>(c16 + e) * pl.P, ld_shared_v4(src));
+                    }
+                } else {
+                    // one element at a time: lane = pixel
+                    const Pixel px = tile_pixel(pl, id.mt, row);
+                    if (px.valid) {
+                        T* o = out + (px.n * pl.Cout + static_cast<int64_t>(id.g) * pl.Og + ncol0 + c16) * pl.P +
+                               px.ho * pl.Wo + px.wo;
+                        for (int e = 0; e < 16 && ncol0 + c16 + e < pl.Og; ++e)
+                            o[static_cast<int64_t>(e) * pl.P] =
+                                ld_shared_elem<T>(stg + static_cast<uint32_t>((e * 32 + lane) * sizeof(T)));
+                    }
+                }
+                __syncwarp();
+            }
+            if (!fix_ok) break;
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acce_bar(ab));
         }
     }
 
-    if (warp >= kWarpEpi && lane == 0 && pl.epi_tma) bulk_wait_read<0>();
     tc_fence_before();
     __syncthreads();
     if (warp == kWarpMma) {
@@ -996,124 +1079,6 @@ __global__ void wait_selftest_kernel(uint32_t* status, uint64_t limit_cycles) {
         mbar_arrive(smem_u32(&bar));        // complete the phase before exit
     }
     __syncthreads();
-}
-
-// ---------------------------------------------------------------- split-tile fix-up
-// Grid (tiles_total, ceil(acc_cols / 32)), 128 threads = tile rows. For every
-// tile whose k-tiles fell to several CTAs: the CTAs' fp32 partial sums, in k
-// order, plus the bias, converted and stored as NCHW output. Launched
-// programmatically dependent on the fused kernel: it waits for that grid to
-// complete before reading. The planner keeps the k-tile count of all tiles
-// below 2^31, so the tile arithmetic here is 32-bit; warp 0 resolves the tile
-// and its contributors' slots once for the block.
-constexpr int kFixupSlots = 32;  // contributors resolved by warp 0; any further ones per thread
-
-template <typename T>
-__global__ void __launch_bounds__(kTileM) splitk_fixup_kernel(const float* __restrict__ part,
-                                                              const T* __restrict__ bias, T* __restrict__ out,
-                                                              Plan pl) {
-    __shared__ int64_t slot_off[kFixupSlots];
-    __shared__ int64_t tile_out0;
-    __shared__ int32_t tile_info[6];  // c_first, c_last (0 when not split), g, ncol0, rows, width
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    const uint32_t t = blockIdx.x;
-    const uint32_t R = static_cast<uint32_t>(pl.kt_per_cta);
-    const uint32_t KT = static_cast<uint32_t>(pl.KT);
-    const int64_t slot_floats = static_cast<int64_t>(pl.acc_cols) * kTileM;
-    if (threadIdx.x < 32) {
-        const uint32_t c_first = (t * KT) / R, c_last = (t * KT + KT - 1) / R;
-        const uint32_t k = threadIdx.x;
-        if (c_first + k <= c_last && k < kFixupSlots) {
-            const uint32_t c = c_first + k;
-            slot_off[k] = static_cast<int64_t>(2 * c + ((c * R) / KT == t ? 0 : 1)) * slot_floats;
-        }
-        if (threadIdx.x == 0) {
-            tile_info[0] = static_cast<int32_t>(c_first);
-            tile_info[1] = c_first == c_last ? -1 : static_cast<int32_t>(c_last);
-            const uint32_t mtiles = static_cast<uint32_t>(pl.mtiles);
-            const uint32_t mt = t % mtiles;
-            const uint32_t rq = t / mtiles;
-            const uint32_t nt = rq % static_cast<uint32_t>(pl.ntiles_n);
-            const uint32_t g = rq / static_cast<uint32_t>(pl.ntiles_n);
-            tile_info[2] = static_cast<int32_t>(g);
-            tile_info[3] = static_cast<int32_t>(nt) * pl.acc_cols;
-            if (pl.tile_mode == 0) {
-                const int64_t p0 = static_cast<int64_t>(mt) * kTileM;  // first pixel of N*Ho*Wo
-                tile_info[4] = static_cast<int32_t>(min(static_cast<int64_t>(kTileM), pl.NP - p0));
-                tile_info[5] = 0;
-                tile_out0 = p0;
-            } else {
-                const uint32_t tx_n = static_cast<uint32_t>(pl.tiles_x);
-                const uint32_t per_img = tx_n * static_cast<uint32_t>(pl.tiles_y);
-                const uint32_t n = mt / per_img;
-                const uint32_t rem = mt - n * per_img;
-                const uint32_t ty = rem / tx_n;
-                const uint32_t tx = rem - ty * tx_n;
-                const int64_t ho0 = static_cast<int64_t>(ty) * pl.TH, wo0 = static_cast<int64_t>(tx) * pl.TW;
-                tile_info[4] = static_cast<int32_t>(min(static_cast<int64_t>(pl.TH), pl.Ho - ho0));
-                tile_info[5] = static_cast<int32_t>(min(static_cast<int64_t>(pl.TW), pl.Wo - wo0));
-                tile_out0 = (static_cast<int64_t>(n) * pl.Cout + static_cast<int64_t>(g) * pl.Og) * pl.P +
-                            ho0 * pl.Wo + wo0;
-            }
-        }
-    }
-    __syncthreads();
-    const int32_t c_first = tile_info[0], c_last = tile_info[1];
-    if (c_last < 0) return;  // one CTA summed the whole tile
-    const int32_t g = tile_info[2];
-    const int row = threadIdx.x;
-    int64_t obase;
-    if (pl.tile_mode == 0) {
-        if (row >= tile_info[4]) return;
-        const int64_t p = tile_out0 + row;
-        const int64_t n = p / pl.P;
-        obase = (n * pl.Cout + static_cast<int64_t>(g) * pl.Og) * pl.P + (p - n * pl.P);
-    } else {
-        const int r = row / pl.TW, c = row - r * pl.TW;
-        if (r >= tile_info[4] || c >= tile_info[5]) return;
-        obase = tile_out0 + static_cast<int64_t>(r) * pl.Wo + c;
-    }
-    const int32_t col0 = static_cast<int32_t>(blockIdx.y) * 32;
-    const int32_t ncol0 = tile_info[3] + col0;
-    const int32_t ncols = min(32, min(pl.acc_cols - col0, pl.Og - ncol0));
-    if (ncols <= 0) return;
-    const int64_t off = static_cast<int64_t>(col0) * kTileM + row;
-    auto slot_src = [&](int32_t c) -> const float* {
-        const int32_t k = c - c_first;
-        const int64_t so = k < kFixupSlots ? slot_off[k]
-                                           : static_cast<int64_t>(2 * static_cast<uint32_t>(c) +
-                                                                  ((static_cast<uint32_t>(c) * R) / KT == t ? 0 : 1)) *
-                                                 slot_floats;
-        return part + so + off;
-    };
-    // the first two contributors' loads all in flight together, then any others
-    float r[32], v[32];
-    const float* s0 = slot_src(c_first);
-    const float* s1 = slot_src(c_first + 1);
-#pragma unroll
-    for (int e = 0; e < 32; ++e) {
-        r[e] = e < ncols ? s0[static_cast<int64_t>(e) * kTileM] : 0.f;
-        v[e] = e < ncols ? s1[static_cast<int64_t>(e) * kTileM] : 0.f;
-    }
-#pragma unroll
-    for (int e = 0; e < 32; ++e) r[e] += v[e];
-    for (int32_t c = c_first + 2; c <= c_last; ++c) {
-        const float* sc = slot_src(c);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) v[e] = e < ncols ? sc[static_cast<int64_t>(e) * kTileM] : 0.f;
-#pragma unroll
-        for (int e = 0; e < 32; ++e) r[e] += v[e];
-    }
-    T* o = out + obase + static_cast<int64_t>(ncol0) * pl.P;
-    const T* bb = bias ? bias + static_cast<int64_t>(g) * pl.Og + ncol0 : nullptr;
-#pragma unroll
-    for (int e = 0; e < 32; ++e) {
-        if (e < ncols) {
-            float val = r[e];
-            if (bb) val += to_f(bb[e]);
-            from_f(val, o + static_cast<int64_t>(e) * pl.P);
-        }
-    }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
@@ -1147,20 +1112,6 @@ cudaError_t launch_fused_t(const Plan& pl, const void* offset, const void* mask,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    CUtensorMap omap;
-    std::memset(&omap, 0, sizeof(omap));
-    if (pl.epi_tma) {
-        const cuuint64_t odim[4] = {static_cast<cuuint64_t>(pl.Wo), static_cast<cuuint64_t>(pl.Ho),
-                                    static_cast<cuuint64_t>(pl.Cout), static_cast<cuuint64_t>(pl.N)};
-        const cuuint64_t ostr[3] = {static_cast<cuuint64_t>(pl.Wo) * sizeof(T),
-                                    static_cast<cuuint64_t>(pl.P) * sizeof(T),
-                                    static_cast<cuuint64_t>(pl.P) * static_cast<cuuint64_t>(pl.Cout) * sizeof(T)};
-        const cuuint32_t obox[4] = {16, 2, 16, 1};
-        const cuuint32_t oes[4] = {1, 1, 1, 1};
-        r = encode(&omap, Elem<DT>::tma, 4, out, odim, ostr, obox, oes, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    }
     FusedParams prm;
     prm.xt = base + pl.off_xt;
     prm.offset = offset;
@@ -1169,6 +1120,8 @@ cudaError_t launch_fused_t(const Plan& pl, const void* offset, const void* mask,
     prm.out = out;
     prm.status = reinterpret_cast<uint32_t*>(base);
     prm.part = reinterpret_cast<float*>(base + pl.off_part);
+    prm.split_count = reinterpret_cast<uint32_t*>(base + kSplitCountOffset);
+    prm.epi_vec = pl.epi_vec && (reinterpret_cast<uintptr_t>(out) & 15u) == 0 ? 1 : 0;
     prm.pl = pl;
     // launched dependent on the prep kernel: the prologue (barriers, tensor
     // memory, the first descriptor group) overlaps its tail
@@ -1182,28 +1135,18 @@ cudaError_t launch_fused_t(const Plan& pl, const void* offset, const void* mask,
     fattr[0].val.programmaticStreamSerializationAllowed = 1;
     fcfg.attrs = fattr;
     fcfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&fcfg, fused_kernel<DT>, tmap, omap, prm);
+    cudaError_t e = cudaLaunchKernelEx(&fcfg, fused_kernel<DT>, tmap, prm);
     if (e == cudaSuccess) e = cudaGetLastError();
-    if (e != cudaSuccess || !splitk_needed(pl)) return e;
-    // split tiles: the fix-up, launched while the fused grid drains
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(pl.tiles_total), static_cast<unsigned>((pl.acc_cols + 31) / 32));
-    cfg.blockDim = dim3(kTileM);
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, splitk_fixup_kernel<T>, static_cast<const float*>(prm.part),
-                              static_cast<const T*>(bias), static_cast<T*>(out), pl);
+    return e;
 }
 
 }  // namespace
 
 // Sets the dynamic shared memory limit and checks that the build launches
-// with exactly kRegsLaunch registers per thread: the warpgroup register
-// split (setmaxnreg) is sized for that pool, so any other count is refused.
+// with exactly kRegsLaunch registers per thread (the warpgroup register
+// split, setmaxnreg, is sized for that pool) and holds no static shared
+// memory (the plan may give the whole per-CTA limit to dynamic shared
+// memory); any other build is refused.
 template <int DT>
 static cudaError_t prepare_one(int smem_bytes) {
     cudaError_t e = cudaFuncSetAttribute(fused_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
@@ -1211,7 +1154,7 @@ static cudaError_t prepare_one(int smem_bytes) {
     cudaFuncAttributes attr;
     e = cudaFuncGetAttributes(&attr, fused_kernel<DT>);
     if (e != cudaSuccess) return e;
-    return attr.numRegs == kRegsLaunch ? cudaSuccess : cudaErrorInvalidDeviceFunction;
+    return attr.numRegs == kRegsLaunch && attr.sharedSizeBytes == 0 ? cudaSuccess : cudaErrorInvalidDeviceFunction;
 }
 
 cudaError_t prepare_fused_attributes(int dtype, int smem_bytes) {

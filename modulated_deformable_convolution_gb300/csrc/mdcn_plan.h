@@ -24,12 +24,17 @@ constexpr int kFusedThreads = 32 * 16;
 // (warpgroup 0 = TMA/MMA/sampling, 1-2 = gather, 3 = epilogue).
 constexpr int kRegsLaunch = 128;
 constexpr int kRegsCtrl = 96;
-constexpr int kRegsGather = 176;
-constexpr int kRegsEpi = 64;
+constexpr int kRegsGather = 168;
+constexpr int kRegsEpi = 80;
 static_assert(kRegsCtrl + 2 * kRegsGather + kRegsEpi == 4 * kRegsLaunch, "warpgroup register split must fit");
 constexpr int kSmemLimit = 227 * 1024;
-constexpr int kMaxCtas = 160;         // persistent CTAs at most (one per SM; the workspace holds 2 partial slots each)
-constexpr size_t kStatusBytes = 256;  // workspace header holding the device status word
+constexpr int kMaxCtas = 160;         // persistent CTAs at most (one per SM; the workspace holds a partial slot each)
+constexpr size_t kStatusBytes = 1024;     // workspace header: the device status word, the split-tile counters
+constexpr size_t kSplitCountOffset = 64;  // uint32[kMaxCtas]: per split tile (by its first CTA), epilogue warps done
+static_assert(kSplitCountOffset + 4 * kMaxCtas <= kStatusBytes, "split counters must fit the header");
+constexpr int kBiasBytes = 512 * 4;  // the epilogue's fp32 copy of one tile's bias columns (up to 512)
+constexpr int kFixBufs = 8;                          // partial-sum buffers of a split tile's owner (in its idle stages)
+constexpr uint32_t kFixBufBytes = 16u * 128u * 4u;   // one buffer: 16 accumulator columns x 128 rows, fp32
 
 enum DType : int32_t { kF32 = 0, kF16 = 1, kBF16 = 2 };
 
@@ -75,7 +80,7 @@ struct Plan {
     int32_t b_bytes;         // one B stage
     int32_t desc_size;       // bytes per sample descriptor (16, or 32 for f32)
     int32_t desc_slot_bytes; // one descriptor group: kTileM rows x kTapBlock taps
-    int32_t epi_tma;         // 1: epilogue writes 16-channel boxes with TMA stores (2-D tiles)
+    int32_t epi_vec;         // 1: output groups of 16 bytes of consecutive pixels stay aligned and whole
     int32_t epi_bytes;       // shared-memory staging of the TMA-store epilogue
     int32_t smem_bytes;      // dynamic shared memory of the fused kernel
     int32_t grid;            // persistent CTAs

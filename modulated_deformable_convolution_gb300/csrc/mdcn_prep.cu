@@ -54,6 +54,7 @@ __global__ void __launch_bounds__(256) nhwc_pad_kernel(const T* __restrict__ x, 
     const int tid = threadIdx.y * 32 + threadIdx.x;
     if (blockIdx.x == 0) {
         if (tid == 0) *status = 0u;
+        for (int i = tid; i < kMaxCtas; i += 256) status[kSplitCountOffset / 4 + i] = 0u;
         write_zero_pixel(xt + zero_off, Cp, 256, tid);
     }
     const int64_t bx = blockIdx.x;
@@ -114,6 +115,7 @@ __device__ __forceinline__ void nhwc_block_body(const T* __restrict__ x, T* __re
     constexpr int kVec = 16 / sizeof(T);
     if (bx == 0 && by == 0 && bz == 0) {
         if (threadIdx.x == 0) *status = 0u;
+        for (int i = threadIdx.x; i < kMaxCtas; i += 256) status[kSplitCountOffset / 4 + i] = 0u;
         write_zero_pixel(xt + zero_off, Cp, 256, threadIdx.x);
     }
     const int lane = threadIdx.x & 31;

@@ -17,6 +17,7 @@ constexpr uint32_t kSiteMmaTma = 1u << 11;
 constexpr uint32_t kSiteEpilogue = 1u << 12;
 constexpr uint32_t kSiteDrain = 1u << 13;
 constexpr uint32_t kSiteSelftest = 1u << 14;
+constexpr uint32_t kSiteSplitWait = 1u << 15;
 
 // Limit of every pipeline wait in the fused kernel, in SM clock cycles
 // (4e9 cycles: about 2 s at the 2.07 GHz maximum clock, longer at lower
@@ -139,6 +140,68 @@ __device__ __forceinline__ void setmaxnreg_dec() {
 // ---------------------------------------------------------------- fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Orders this thread's earlier generic-proxy view of global memory (data
+// other CTAs published and this thread acquired) before its later
+// async-proxy (bulk copy) reads of it.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) { return lds_f32(addr); }
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_global_v4(void* p, uint4 v) {
+    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// Named barrier over `count` threads (whole warps) that also ANDs a predicate
+// across them: every participant gets the same answer.
+__device__ __forceinline__ bool bar_red_and(uint32_t id, uint32_t count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.and.pred p, %2, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(pred ? 1u : 0u), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
+// Waits, for at most kWaitLimitCycles, until a global counter that other CTAs
+// raise reaches `target` (acquire: their writes before the raise are then
+// visible). On giving up it records the site, raises *abort, returns false.
+__device__ __forceinline__ bool wait_count_bounded(const uint32_t* p, uint32_t target, volatile int* abort,
+                                                   uint32_t* status, uint32_t site) {
+    const uint64_t t0 = clock64();
+    for (;;) {
+        uint32_t v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+        if (v >= target) return true;
+        if (*abort) return false;
+        if (static_cast<uint64_t>(clock64()) - t0 > kWaitLimitCycles) {
+            *abort = 1;
+            if (status) atomicOr(status, kStatusTimeout | site);
+            return false;
+        }
+        __nanosleep(64);
+    }
 }
 
 __device__ __forceinline__ void tc_fence_before() {

@@ -203,7 +203,7 @@ def test_query_plan_split_choice():
         h = mdcn.Handle(**case.attrs())
         plan = mdcn.mdcn_query_plan(h, d["x"], d["offset"], d["mask"], d["weight"], d["bias"])
         assert plan["split"] == split, (name, plan)
-        assert plan["launches"] == 2 + split  # one prep launch (transpose + pack), the fused kernel, the fix-up
+        assert plan["launches"] == 2  # one prep launch (transpose + pack), the fused kernel
         assert plan["ctas"] <= sms and plan["ctas"] * plan["ktiles_per_cta"] >= plan["tiles"] * plan["ktiles_per_tile"]
         if not split:
             assert plan["ktiles_per_cta"] % plan["ktiles_per_tile"] == 0

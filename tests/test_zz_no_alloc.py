@@ -12,6 +12,7 @@ This file is collected last on purpose, and it does its own set-up, so it runs
 the same alone in a fresh process or after every other test.
 """
 import ctypes
+import dataclasses
 
 import pytest
 import torch
@@ -36,8 +37,8 @@ def _noalloc_fn():
     return f
 
 
-def _inputs(name):
-    case = CONFIGS[name]
+def _inputs(name, **replace):
+    case = dataclasses.replace(CONFIGS[name], **replace) if replace else CONFIGS[name]
     dev = torch.device("cuda", 0)
     d = {k: (None if v is None else v.to(dev)) for k, v in make_inputs(case).items()}
     return case, d
@@ -53,7 +54,7 @@ def _call_noalloc(f, h, d, out):
              ctypes.byref(dims), dt, stream)
 
 
-@pytest.mark.parametrize("name", ["neck_f16", "tiny_f32", "multidg_bf16"])
+@pytest.mark.parametrize("name", ["neck_f16", "tiny_f32", "multidg_bf16", "largec_f16"])
 def test_noalloc_matches_forward_on_two_calls(name):
     f = _noalloc_fn()
     case, d = _inputs(name)
@@ -71,7 +72,7 @@ def test_noalloc_matches_forward_on_two_calls(name):
 
 def test_noalloc_refuses_workloads_beyond_its_scratch():
     f = _noalloc_fn()
-    case, d = _inputs("largec_f16")  # needs about 82 MB of workspace
+    case, d = _inputs("largec_f16", N=32)  # needs about 80 MB of workspace
     h = mdcn.Handle(**case.attrs())
     out = torch.zeros(mdcn.mdcn_output_dims(h, d["x"], d["offset"], d["mask"], d["weight"], d["bias"]),
                       dtype=d["x"].dtype, device=d["x"].device)
