@@ -541,6 +541,102 @@ __device__ __forceinline__ void row_combine(const GatherCtx<T>& cx, uint32_t a_s
     }
 }
 
+// ---------------------------------------------------------------- epilogue helpers
+// 32 accumulator columns from c32 (16 where fewer remain) of this thread's
+// row -> the fp32 partial slot of CTA `cta` ([column][row], so each warp
+// writes 128 contiguous bytes per column).
+template <typename T>
+__device__ __forceinline__ void write_partial32(const Plan& pl, float* part, int64_t cta, uint32_t tl, int c32,
+                                                int row) {
+    float vals[32];
+    tmem_ld32(tl + static_cast<uint32_t>(c32), pl.acc_cols - c32 >= 32 ? 2 : 1, vals);
+    float* mine = part + (cta * pl.acc_cols + c32) * kTileM + row;
+#pragma unroll
+    for (int c = 0; c < 32; ++c)
+        if (c < pl.acc_cols - c32) mine[c * kTileM] = vals[c];
+}
+
+// After this CTA's partial slot is written by the `nthreads` threads that
+// meet at named barrier `bar`: one of them counts the CTA in on the split
+// tile's counter (release: the slot's writes are visible before the count).
+__device__ __forceinline__ void count_in_split(uint32_t* counter, uint32_t bar, uint32_t nthreads, bool leader) {
+    __threadfence();
+    named_bar_sync(bar, nthreads);
+    if (leader) atomicAdd(counter, 1u);
+}
+
+// The tile's bias columns -> shared memory as fp32 (0 past the group's columns).
+template <typename T>
+__device__ __forceinline__ void stage_bias(const Plan& pl, const T* bias, const TileId& id, uint32_t bias_s, int tid,
+                                           int nthreads) {
+    const int32_t ncol0 = id.nt * pl.acc_cols;
+    for (int c = tid; c < pl.acc_cols; c += nthreads) {
+        const int32_t ol = ncol0 + c;
+        st_shared_f32(bias_s + 4u * c, ol < pl.Og ? to_f(bias[static_cast<int64_t>(id.g) * pl.Og + ol]) : 0.f);
+    }
+}
+
+// The group of 16 / sizeof(T) consecutive output pixels whose 16-byte
+// vectors this lane stores: group lane % (32 / that) of the 32 tile rows of
+// lane quarter `quarter`, and the output index of its first pixel in the
+// plane of the tile's first column.
+struct OutGroup {
+    int64_t base;
+    bool valid;
+};
+
+template <typename T>
+__device__ __forceinline__ OutGroup out_group(const Plan& pl, const TileId& id, int quarter, int lane) {
+    constexpr int kVecPx = 16 / sizeof(T);
+    constexpr int kGroups = 32 / kVecPx;
+    const Pixel gp = tile_pixel(pl, id.mt, quarter * 32 + (lane % kGroups) * kVecPx);
+    OutGroup og;
+    og.base = (gp.n * pl.Cout + static_cast<int64_t>(id.g) * pl.Og + id.nt * pl.acc_cols) * pl.P + gp.ho * pl.Wo + gp.wo;
+    og.valid = gp.valid;
+    return og;
+}
+
+// 16 output channels (accumulator columns c16..c16+15) of the warp's 32 rows:
+// + bias, converted, staged as [16 channels][32 pixels] in the warp's
+// staging buffer, then stored as 16-byte vectors of consecutive pixels of
+// one channel (one element per lane and channel where the layout does not
+// allow vectors).
+template <typename T>
+__device__ __forceinline__ void store_chunk16(const Plan& pl, const FusedParams& prm, const TileId& id,
+                                              const OutGroup& og, float* vals, int c16, int row, int lane,
+                                              uint32_t bias_s, uint32_t stg) {
+    const int32_t ncol0 = id.nt * pl.acc_cols;
+    if (ncol0 + c16 >= pl.Og) return;
+    T* __restrict__ out = static_cast<T*>(prm.out);
+    if (prm.bias) {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) vals[e] += ld_shared_f32(bias_s + 4u * (c16 + e));
+    }
+#pragma unroll
+    for (int e = 0; e < 16; ++e) st_shared_elem<T>(stg + static_cast<uint32_t>((e * 32 + lane) * sizeof(T)), vals[e]);
+    __syncwarp();
+    if (prm.epi_vec) {
+        constexpr int kVecPx = 16 / sizeof(T);
+        constexpr int kGroups = 32 / kVecPx;
+#pragma unroll
+        for (int k = 0; k < 16 * kGroups / 32; ++k) {
+            const int e = lane / kGroups + k * (32 / kGroups);  // channel of the chunk
+            const uint32_t src = stg + static_cast<uint32_t>((e * 32 + (lane % kGroups) * kVecPx) * sizeof(T));
+            if (og.valid && ncol0 + c16 + e < pl.Og)
+                st_global_v4(out + og.base + static_cast<int64_t>(c16 + e) * pl.P, ld_shared_v4(src));
+        }
+    } else {
+        const Pixel px = tile_pixel(pl, id.mt, row);
+        if (px.valid) {
+            T* o = out + (px.n * pl.Cout + static_cast<int64_t>(id.g) * pl.Og + ncol0 + c16) * pl.P +
+                   px.ho * pl.Wo + px.wo;
+            for (int e = 0; e < 16 && ncol0 + c16 + e < pl.Og; ++e)
+                o[static_cast<int64_t>(e) * pl.P] = ld_shared_elem<T>(stg + static_cast<uint32_t>((e * 32 + lane) * sizeof(T)));
+        }
+    }
+    __syncwarp();
+}
+
 template <int DT>
 __global__ void __launch_bounds__(kFusedThreads, 1)
     fused_kernel(const __grid_constant__ CUtensorMap tmap, const FusedParams prm) {
@@ -572,8 +668,11 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     auto dfull_bar = [&](int b) { return xb + 32u + 8u * b; };
     auto dempty_bar = [&](int b) { return xb + 48u + 8u * b; };
     const uint32_t drain_bar = xb + 64u;
+    // the gather warps arrive once they hold their registers: the other
+    // warpgroups take their registers back (end of their roles) only after
+    // that, so an early finisher cannot leave the gathers short of registers
+    const uint32_t regs_bar = xb + 80u;
     const uint32_t slot_off = (xb - sbase) + 72u;
-    auto fix_bar = [&](int b) { return xb + 80u + 8u * b; };  // kFixBufs partial-sum buffers
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + slot_off);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + slot_off + 4);
 
@@ -597,7 +696,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
             mbar_init(dempty_bar(b), kGatherWarps);
         }
         mbar_init(drain_bar, 1);
-        for (int b = 0; b < kFixBufs; ++b) mbar_init(fix_bar(b), 1);
+        mbar_init(regs_bar, kGatherWarps);
         *abort_flag = 0;
         fence_mbarrier_init();
         tma_prefetch_desc(&tmap);
@@ -777,8 +876,15 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
             cursor_next_group(pl, dc);
         }
     }
+    {
+        volatile int never = 0;
+        warp_wait_bounded(regs_bar, 0, &never, prm.status, kSiteDrain);
+    }
+    setmaxnreg_inc<kRegsLaunch>();
     } else if (wg == 1 || wg == 2) {
         setmaxnreg_inc<kRegsGather>();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(regs_bar);
         // ------------------------------------------------------------ gather producers
         // k-tile-parallel gather: the 8 warps form G = pl.kgroups groups; group p
         // produces every G-th k-tile of the CTA's sequence (steps p, p + G, ...),
@@ -891,18 +997,20 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
             gather(std::integral_constant<int, 4>{});
         else
             gather(std::integral_constant<int, 2>{});
+        setmaxnreg_dec<kRegsLaunch>();
     } else {
         setmaxnreg_dec<kRegsEpi>();
         // ------------------------------------------------------------ epilogue
+        // Every unit but the CTA's last (the tail below takes that one with all
+        // 16 warps): a whole tile -> output, or the first unit of a tile whose
+        // first k-tiles are another CTA's -> this CTA's partial slot.
         const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
         const int row = quarter * 32 + lane;
-        T* __restrict__ out = static_cast<T*>(prm.out);
-        const T* __restrict__ bias = static_cast<const T*>(prm.bias);
-        const uint32_t stg = e0s + static_cast<uint32_t>(quarter * 16 * 32 * sizeof(T));
         uint32_t i = 0;
         for (int64_t pos = lo; pos < hi; ++i) {
             const Unit un = unit_at(pl, pos, hi);
             pos = un.t * KT + un.k1;
+            if (pos >= hi) break;  // the last unit
             const TileId id = decode_tile(pl, un.t);
             const int ab = static_cast<int>(i % pl.nacc);
             const uint32_t use = i / pl.nacc;
@@ -912,147 +1020,104 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                                                                        kSiteEpilogue))))
                 break;
             tc_fence_after();
-            const int32_t ncol0 = id.nt * pl.acc_cols;
             const uint32_t tl = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                 static_cast<uint32_t>(ab * pl.acc_cols);
-            const bool split = un.k0 != 0 || un.k1 != KT;
-            const int64_t c_first = split ? (un.t * KT) / pl.kt_per_cta : 0;
-            if (split && c_first != static_cast<int64_t>(blockIdx.x)) {
-                // a split tile whose first k-tiles are another CTA's (this is this
-                // CTA's first unit): the partial sum goes to this CTA's slot, then
-                // each warp counts itself in on the tile's counter
-                float* mine = prm.part + static_cast<size_t>(blockIdx.x) * static_cast<size_t>(pl.acc_cols) * kTileM;
-                for (int c32 = 0; c32 < pl.acc_cols; c32 += 32) {
-                    float vals[32];
-                    tmem_ld32(tl + static_cast<uint32_t>(c32), pl.acc_cols - c32 >= 32 ? 2 : 1, vals);
-#pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        if (c < pl.acc_cols - c32) mine[static_cast<size_t>(c32 + c) * kTileM + row] = vals[c];
-                }
+            if (un.k0 != 0 || un.k1 != KT) {
+                // a split tile's tail (its head, and owner, is the CTA before)
+                const int64_t c_first = (un.t * KT) / pl.kt_per_cta;
+                for (int c32 = 0; c32 < pl.acc_cols; c32 += 32)
+                    write_partial32<T>(pl, prm.part, blockIdx.x, tl, c32, row);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(acce_bar(ab));
-                __threadfence();
-                __syncwarp();
-                if (lane == 0) atomicAdd(prm.split_count + c_first, 1u);
+                count_in_split(prm.split_count + c_first, 1, kEpiWarps * 32, warp == kWarpEpi && lane == 0);
                 continue;
             }
-            // A whole tile, or a split tile this CTA owns: the owner holds the
-            // tile's first k-tiles as its last unit (all stages are idle once its
-            // accumulator is full) and adds the other m contributors' partials in
-            // k order. They arrive by bulk copies into the stage area: item j =
-            // (16-column chunk j / m, contributor j % m), 8 KB each, in a ring of
-            // nbuf buffers that the four epilogue warps step through together.
-            const int32_t m = split ? static_cast<int32_t>((un.t * KT + KT - 1) / pl.kt_per_cta - c_first) : 0;
-            const int32_t nbuf = min(kFixBufs, static_cast<int32_t>((S * (a_bytes + b_bytes)) / kFixBufBytes));
-            const int32_t nitems = m * (pl.acc_cols / 16);
-            auto fix_issue = [&](int32_t j) {
-                const int32_t b = j % nbuf;
-                const int32_t ch = j / m;
-                const int64_t c = c_first + 1 + (j - ch * m);
-                const float* src = prm.part + (c * pl.acc_cols + ch * 16) * kTileM;
-                mbar_arrive_expect_tx(fix_bar(b), kFixBufBytes);
-                bulk_load(a0 + static_cast<uint32_t>(b) * kFixBufBytes, src, kFixBufBytes, fix_bar(b));
-            };
-            if (m > 0 && warp == kWarpEpi && lane == 0 &&
-                wait_count_bounded(prm.split_count + c_first, static_cast<uint32_t>(kEpiWarps * m), abort_flag,
-                                   prm.status, kSiteSplitWait)) {
-                prm.split_count[c_first] = 0u;  // every contributor is in: zero again for the next call
-                fence_proxy_async_global();
-                for (int32_t j = 0; j < min(nbuf, nitems); ++j) fix_issue(j);
-            }
-            bool fix_ok = true;
-            auto fix_add = [&](int c16, float(&vals)[16]) {
-                for (int32_t k = 0; k < m; ++k) {
-                    const int32_t j = (c16 >> 4) * m + k;
-                    const int32_t b = j % nbuf;
-                    const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(fix_bar(b), (j / nbuf) & 1, abort_flag,
-                                                                               prm.status, kSiteSplitWait));
-                    if (got) {
-                        // 8 loads in flight before their adds
-                        const uint32_t src = a0 + static_cast<uint32_t>(b) * kFixBufBytes + static_cast<uint32_t>(row) * 4u;
-#pragma unroll
-                        for (int h = 0; h < 16; h += 8) {
-                            float pv[8];
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) pv[e] = lds_f32(src + static_cast<uint32_t>(h + e) * (kTileM * 4u));
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) vals[h + e] += pv[e];
-                        }
-                    }
-                    // the buffer is free once all four warps have read it
-                    if (!bar_red_and(1, kEpiWarps * 32, got)) {
-                        fix_ok = false;
-                        return;
-                    }
-                    if (warp == kWarpEpi && lane == 0 && j + nbuf < nitems) {
-                        fence_proxy_async_smem();
-                        fix_issue(j + nbuf);
-                    }
-                }
-            };
-            // the tile's bias columns -> shared memory (fp32); every warp is past
-            // the previous tile (barrier above), and all have written before any reads
-            if (bias) {
-                for (int c = row; c < pl.acc_cols; c += kTileM) {
-                    const int32_t ol = ncol0 + c;
-                    st_shared_f32(bias_s + 4u * c, ol < pl.Og ? to_f(bias[static_cast<int64_t>(id.g) * pl.Og + ol]) : 0.f);
-                }
+            if (prm.bias) {
+                stage_bias<T>(pl, static_cast<const T*>(prm.bias), id, bias_s, row, kTileM);
                 named_bar_sync(1, kEpiWarps * 32);
             }
-            // vector path: this lane's group of kVecPx consecutive pixels (group
-            // lane % kGroups of the warp's 32 rows) and its first output element
-            constexpr int kVecPx = 16 / sizeof(T);
-            constexpr int kGroups = 32 / kVecPx;
-            const Pixel gp = tile_pixel(pl, id.mt, quarter * 32 + (lane % kGroups) * kVecPx);
-            const int64_t gbase = (gp.n * pl.Cout + static_cast<int64_t>(id.g) * pl.Og + ncol0) * pl.P +
-                                  gp.ho * pl.Wo + gp.wo;
+            const OutGroup og = out_group<T>(pl, id, quarter, lane);
             for (int c16 = 0; c16 < pl.acc_cols; c16 += 16) {
                 float vals[16];
                 tmem_ld16(tl + static_cast<uint32_t>(c16), vals);
-                if (m > 0) {
-                    fix_add(c16, vals);
-                    if (!fix_ok) break;
-                }
-                if (ncol0 + c16 >= pl.Og) continue;
-                if (bias) {
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) vals[e] += ld_shared_f32(bias_s + 4u * (c16 + e));
-                }
-                // [16 channels][32 pixels] in this warp's staging, then stored
-#pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    st_shared_elem<T>(stg + static_cast<uint32_t>((e * 32 + lane) * sizeof(T)), vals[e]);
-                __syncwarp();
-                if (prm.epi_vec) {
-                    // 16-byte stores of kVecPx consecutive pixels of one channel
-#pragma unroll
-                    for (int k = 0; k < 16 * kGroups / 32; ++k) {
-                        const int e = lane / kGroups + k * (32 / kGroups);  // channel of the chunk
-                        const uint32_t src = stg + static_cast<uint32_t>((e * 32 + (lane % kGroups) * kVecPx) * sizeof(T));
-                        if (gp.valid && ncol0 + c16 + e < pl.Og)
-                            st_global_v4(out + gbase + static_cast<int64_t>(c16 + e) * pl.P, ld_shared_v4(src));
-                    }
-                } else {
-                    // one element at a time: lane = pixel
-                    const Pixel px = tile_pixel(pl, id.mt, row);
-                    if (px.valid) {
-                        T* o = out + (px.n * pl.Cout + static_cast<int64_t>(id.g) * pl.Og + ncol0 + c16) * pl.P +
-                               px.ho * pl.Wo + px.wo;
-                        for (int e = 0; e < 16 && ncol0 + c16 + e < pl.Og; ++e)
-                            o[static_cast<int64_t>(e) * pl.P] =
-                                ld_shared_elem<T>(stg + static_cast<uint32_t>((e * 32 + lane) * sizeof(T)));
-                    }
-                }
-                __syncwarp();
+                store_chunk16<T>(pl, prm, id, og, vals, c16, row, lane, bias_s,
+                                 e0s + static_cast<uint32_t>(quarter * 16 * 32 * sizeof(T)));
             }
-            if (!fix_ok) break;
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acce_bar(ab));
         }
+        {
+            volatile int never = 0;
+            warp_wait_bounded(regs_bar, 0, &never, prm.status, kSiteDrain);
+        }
+        setmaxnreg_inc<kRegsLaunch>();
     }
 
+    // ---------------------------------------------------------------- tail
+    // The pipeline has drained (the MMA warp waited for its last commit): the
+    // CTA's last unit is in tensor memory, and all 16 warps write it out,
+    // warp w taking lane quarter w % 4 and every fourth 32-column block from
+    // block w / 4. A split tile's tail (this CTA's only unit) goes to the
+    // partial slot; the head of a split tile (the owner) waits for the other
+    // contributors and adds their partials in k order from L2.
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (lo < hi && *abort_flag == 0) {
+        int64_t pos = lo;
+        uint32_t nu = 0;
+        Unit un;
+        do {
+            un = unit_at(pl, pos, hi);
+            pos = un.t * KT + un.k1;
+            ++nu;
+        } while (pos < hi);
+        const TileId id = decode_tile(pl, un.t);
+        const int ab = static_cast<int>((nu - 1) % pl.nacc);
+        const int quarter = warp & 3, member = warp >> 2;
+        const int row = quarter * 32 + lane;
+        const uint32_t tl = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                            static_cast<uint32_t>(ab * pl.acc_cols);
+        const bool split = un.k0 != 0 || un.k1 != KT;
+        const int64_t c_first = split ? (un.t * KT) / pl.kt_per_cta : static_cast<int64_t>(blockIdx.x);
+        if (c_first != static_cast<int64_t>(blockIdx.x)) {
+            for (int c32 = 32 * member; c32 < pl.acc_cols; c32 += 128)
+                write_partial32<T>(pl, prm.part, blockIdx.x, tl, c32, row);
+            count_in_split(prm.split_count + c_first, 0, kFusedThreads, threadIdx.x == 0);
+        } else {
+            const int32_t m = split ? static_cast<int32_t>((un.t * KT + KT - 1) / pl.kt_per_cta - c_first) : 0;
+            if (prm.bias) stage_bias<T>(pl, static_cast<const T*>(prm.bias), id, bias_s, threadIdx.x, kFusedThreads);
+            int ok = 1;
+            if (m > 0 && threadIdx.x == 0) {
+                ok = wait_count_bounded(prm.split_count + c_first, static_cast<uint32_t>(m), abort_flag, prm.status,
+                                        kSiteSplitWait);
+                if (ok) prm.split_count[c_first] = 0u;  // every contributor is in: zero again for the next call
+            }
+            if (__syncthreads_and(ok)) {
+                const OutGroup og = out_group<T>(pl, id, quarter, lane);
+                // per-warp staging in the (idle) descriptor ring
+                const uint32_t stg = d0 + static_cast<uint32_t>(warp * 16 * 32 * sizeof(T));
+                for (int c32 = 32 * member; c32 < pl.acc_cols; c32 += 128) {
+                    const int nc = min(32, pl.acc_cols - c32);
+                    float vals[32];
+                    tmem_ld32(tl + static_cast<uint32_t>(c32), nc == 32 ? 2 : 1, vals);
+                    for (int32_t k = 1; k <= m; ++k) {
+                        // one contributor's 32 columns, all loads in flight, then added
+                        const float* src = prm.part + ((c_first + k) * pl.acc_cols + c32) * kTileM + row;
+                        float pv[32];
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) pv[e] = e < nc ? __ldcg(src + e * kTileM) : 0.f;
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) vals[e] += pv[e];
+                    }
+                    store_chunk16<T>(pl, prm, id, og, vals, c32, row, lane, bias_s, stg);
+                    if (nc > 16) store_chunk16<T>(pl, prm, id, og, vals + 16, c32 + 16, row, lane, bias_s, stg);
+                }
+            }
+        }
+    }
     tc_fence_before();
     __syncthreads();
     if (warp == kWarpMma) {

@@ -33,8 +33,9 @@ constexpr size_t kStatusBytes = 1024;     // workspace header: the device status
 constexpr size_t kSplitCountOffset = 64;  // uint32[kMaxCtas]: per split tile (by its first CTA), epilogue warps done
 static_assert(kSplitCountOffset + 4 * kMaxCtas <= kStatusBytes, "split counters must fit the header");
 constexpr int kBiasBytes = 512 * 4;  // the epilogue's fp32 copy of one tile's bias columns (up to 512)
-constexpr int kFixBufs = 8;                          // partial-sum buffers of a split tile's owner (in its idle stages)
-constexpr uint32_t kFixBufBytes = 16u * 128u * 4u;   // one buffer: 16 accumulator columns x 128 rows, fp32
+// the tail's per-warp output staging (16 x [16 channels][32 pixels]) lives in
+// the descriptor ring, which is idle by then
+static_assert(kFusedThreads / 32 * 16 * 32 * 4 <= 2 * kTileM * kTapBlock * 16, "tail staging must fit the ring");
 
 enum DType : int32_t { kF32 = 0, kF16 = 1, kBF16 = 2 };
 
