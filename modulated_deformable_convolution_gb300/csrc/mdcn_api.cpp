@@ -205,13 +205,17 @@ mdcn_status make_plan(const mdcn_attrs& a, const mdcn_tuning& tuning, const mdcn
     const int32_t fixed = 1024 + 2 * p.desc_slot_bytes + p.epi_bytes + mdcn::kBiasBytes + 512;
     const int32_t per_stage = p.a_bytes + p.b_bytes;
     // stages: 2, 4, 6 or 8; the gather produces kgroups k-tiles at once (1, 2
-    // or 4, dividing the stage count; automatic: 2, measured fastest on the
-    // named workloads)
+    // or 4, dividing the stage count)
     const int32_t max_stages = (mdcn::kSmemLimit - fixed) / per_stage;
     int32_t stages = tuning.stages > 0 ? tuning.stages : (max_stages >= 4 ? 4 : 2);
     if (stages < 2 || stages > 8 || (stages & 1) || stages > max_stages) return MDCN_ERR_UNSUPPORTED;
     p.stages = stages;
-    p.kgroups = tuning.kgroups > 0 ? tuning.kgroups : 2;
+    // automatic: 2 k-tiles in production at once, which hides the gather's
+    // latency while the contraction of a k-tile is short; 1 (all 8 warps on
+    // one k-tile) when the accumulator is wider than 256 columns and each
+    // k-tile's contraction takes about as long as its gather (measured on
+    // the named workloads)
+    p.kgroups = tuning.kgroups > 0 ? tuning.kgroups : (p.acc_cols > 256 ? 1 : 2);
     if (stages % p.kgroups != 0) return MDCN_ERR_UNSUPPORTED;
     p.smem_bytes = fixed + stages * per_stage;
     p.grid = 0;  // set at launch from the SM count
