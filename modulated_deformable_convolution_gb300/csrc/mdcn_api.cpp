@@ -315,7 +315,7 @@ mdcn_status plan_for_call(mdcn_handle h, const mdcn_dims* dims, mdcn_dtype dtype
     if (h->tuning.max_ctas > 0 && h->tuning.max_ctas < grid) grid = h->tuning.max_ctas;
     if (grid > p->total_kt) grid = p->total_kt;
     // stream-K split: equal consecutive k-tile ranges, none empty. Splitting a
-    // tile costs its CTAs an fp32 partial write each and the fix-up kernel a
+    // tile costs its other CTAs an fp32 partial write each and its owner a
     // read of them, so ranges stay whole tiles unless the busiest CTA's share
     // drops clearly (measured break-even: about 15% plus 4 k-tiles).
     const int64_t split = (p->total_kt + grid - 1) / grid;

@@ -16,7 +16,7 @@ cudaError_t launch_prep_both(const Plan& pl, const void* x, const void* weight, 
 
 // The fused sampling + gather + contraction + bias kernel (reads offset, mask
 // and the two workspace products of launch_prep_input and
-// launch_pack_weight), then the split-tile fix-up when tiles are split.
+// launch_pack_weight); tiles split between CTAs are finished inside it.
 cudaError_t launch_fused(const Plan& pl, const void* offset, const void* mask, const void* bias, void* out, void* ws,
                          cudaStream_t st);
 

@@ -95,7 +95,7 @@ struct Plan {
 };
 
 // True when some tile's k-tiles fall to more than one CTA (the CTA ranges do
-// not all end on tile boundaries), so the fix-up kernel has work.
+// not all end on tile boundaries), so some tile is finished from partials.
 inline bool splitk_needed(const Plan& p) { return p.grid > 1 && p.kt_per_cta % p.KT != 0; }
 
 }  // namespace mdcn
