@@ -191,6 +191,35 @@ mdcn_status mdcn_forward_prepared(mdcn_handle handle, const void* offset, const 
                                   void* out, void* workspace, size_t workspace_bytes, const mdcn_dims* dims,
                                   mdcn_dtype dtype, void* stream);
 
+/* Bytes of the device buffer that mdcn_forward_host needs for these dims
+ * and dtype: room for the device copies of x, offset, mask, weight and bias,
+ * the output, and the mdcn_forward workspace, each 256-byte aligned. Host
+ * only. Errors as mdcn_workspace_size. */
+mdcn_status mdcn_host_buffer_size(mdcn_handle handle, const mdcn_dims* dims, mdcn_dtype dtype, size_t* bytes);
+
+/* The forward from and to HOST memory. The source pages have no counterpart:
+ * this entry point is for callers whose tensors live on the host.
+ *   x_host, offset_host, mask_host, weight_host, bias_host_or_null: host
+ *   pointers to dense NCHW inputs (layouts and rules as mdcn_forward);
+ *   out_host: host pointer receiving the NCHW output;
+ *   device_buffer: caller-owned DEVICE memory of device_buffer_bytes >=
+ *   mdcn_host_buffer_size, 16-byte aligned; it holds the device copies, the
+ *   output and the workspace (contents undefined afterwards).
+ * On the stream, in order: one cudaMemcpyAsync per input into device_buffer,
+ * the kernels of mdcn_forward, one cudaMemcpyAsync of the output to out_host.
+ * Asynchronous like every forward: the host buffers must stay valid and the
+ * inputs unmodified, and out_host must not be read, until the stream has
+ * passed the call. With page-locked host memory (cudaHostAlloc,
+ * cudaHostRegister) the copies run on the copy engines and overlap the work of
+ * other streams, so calls on two streams with two device buffers pipeline the
+ * copies of one call with the kernels of the other; pageable memory works, but
+ * its copies are staged through the driver. Everything is validated before
+ * the first copy: a call that fails validation copies and launches nothing. */
+mdcn_status mdcn_forward_host(mdcn_handle handle, const void* x_host, const void* offset_host, const void* mask_host,
+                              const void* weight_host, const void* bias_host_or_null, void* out_host,
+                              void* device_buffer, size_t device_buffer_bytes, const mdcn_dims* dims,
+                              mdcn_dtype dtype, void* stream);
+
 /* Workspace bytes for mdcn_forward_im2col_gemm (the column matrix of the
  * whole batch plus a float32 GEMM output). Host only. */
 mdcn_status mdcn_im2col_gemm_workspace_size(mdcn_handle handle, const mdcn_dims* dims,

@@ -202,6 +202,36 @@ def mdcn_forward(handle, x, offset, mask, weight, bias, out, workspace, stream=N
                                    ctypes.byref(d), _dtype(x), st), "mdcn_forward")
 
 
+def mdcn_host_buffer_size(handle, x, offset, mask, weight, bias=None, dtype=None) -> int:
+    """Device-buffer bytes of mdcn_forward_host (tensors give only shapes and dtype)."""
+    n = ctypes.c_size_t()
+    dt = _dtype(x) if dtype is None else dtype
+    _check(_lib().mdcn_host_buffer_size(_hval(handle), ctypes.byref(_dims(x, offset, mask, weight, bias)), dt,
+                                        ctypes.byref(n)), "mdcn_host_buffer_size")
+    return int(n.value)
+
+
+def mdcn_forward_host(handle, x, offset, mask, weight, bias, out, device_buffer, stream=None) -> None:
+    """mdcn_forward_host: x, offset, mask, weight, bias and out are HOST (CPU)
+    tensors, page-locked for asynchronous copies; device_buffer is a uint8 CUDA
+    tensor of at least mdcn_host_buffer_size bytes. Asynchronous on the stream."""
+    for t in [x, offset, mask, weight, out] + ([bias] if bias is not None else []):
+        if t.is_cuda:
+            raise ValueError("mdcn_forward_host takes host tensors")
+        if not t.is_contiguous():
+            raise ValueError("every tensor must be contiguous (NCHW)")
+        if t.dtype != x.dtype:
+            raise TypeError("every tensor must have the dtype of x")
+    if not device_buffer.is_cuda:
+        raise ValueError("device_buffer must be a CUDA tensor")
+    d = _dims(x, offset, mask, weight, bias)
+    with torch.cuda.device(device_buffer.device):
+        _check(_lib().mdcn_forward_host(_hval(handle), _ptr(x), _ptr(offset), _ptr(mask), _ptr(weight), _ptr(bias),
+                                        _ptr(out), _ptr(device_buffer),
+                                        device_buffer.numel() * device_buffer.element_size(), ctypes.byref(d),
+                                        _dtype(x), _stream(device_buffer.device, stream)), "mdcn_forward_host")
+
+
 def mdcn_prepare_input(handle, x, offset, mask, weight, bias, workspace, stream=None) -> None:
     """Step 1 of mdcn_forward: x -> channels-last copy in workspace."""
     d = _dims(x, offset, mask, weight, bias)

@@ -99,6 +99,12 @@ def load(path: str = LIB_PATH):
         lib.mdcn_forward_im2col_gemm.restype = st
         lib.mdcn_query_plan.argtypes = [vp, ctypes.POINTER(mdcn_dims), ctypes.c_int, ctypes.POINTER(mdcn_plan_info)]
         lib.mdcn_query_plan.restype = st
+        lib.mdcn_host_buffer_size.argtypes = [vp, ctypes.POINTER(mdcn_dims), ctypes.c_int,
+                                              ctypes.POINTER(ctypes.c_size_t)]
+        lib.mdcn_host_buffer_size.restype = st
+        lib.mdcn_forward_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, ctypes.POINTER(mdcn_dims),
+                                          ctypes.c_int, vp]
+        lib.mdcn_forward_host.restype = st
         lib.mdcn_query_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
         lib.mdcn_query_status.restype = st
         lib.mdcn_selftest_wait_timeout.argtypes = [vp, ctypes.c_uint32, vp]

@@ -406,6 +406,84 @@ mdcn_status mdcn_forward(mdcn_handle handle, const void* x, const void* offset, 
     return MDCN_OK;
 }
 
+// Device-buffer layout of mdcn_forward_host: the device copies of x, offset,
+// mask, weight and bias, the output, and the workspace, each 256-byte
+// aligned (so every part meets the 16-byte rule of the device entry points).
+struct HostLayout {
+    size_t off[7];
+    size_t bytes[7];
+    size_t total;
+};
+
+static mdcn_status host_layout(mdcn_handle h, const mdcn_dims* d, mdcn_dtype dt, HostLayout* L) {
+    Plan p;
+    const mdcn_status s = make_plan(h->attrs, h->tuning, d, dt, &p);
+    if (s != MDCN_OK) return s;
+    const int64_t elem = dt == MDCN_F32 ? 4 : 2;
+    const int64_t* dims4[4] = {d->x, d->offset, d->mask, d->weight};
+    for (int i = 0; i < 4; ++i) {
+        int64_t n = elem;
+        for (int k = 0; k < 4; ++k)
+            if (!mul_ok(n, dims4[i][k])) return MDCN_ERR_UNSUPPORTED;
+        L->bytes[i] = static_cast<size_t>(n);
+    }
+    L->bytes[4] = static_cast<size_t>(d->bias * elem);
+    int64_t nout = elem;
+    if (!mul_ok(nout, p.N) || !mul_ok(nout, p.Cout) || !mul_ok(nout, p.Ho) || !mul_ok(nout, p.Wo))
+        return MDCN_ERR_UNSUPPORTED;
+    L->bytes[5] = static_cast<size_t>(nout);
+    L->bytes[6] = p.ws_bytes;
+    size_t at = 0;
+    for (int i = 0; i < 7; ++i) {
+        L->off[i] = at;
+        at = align256(at + L->bytes[i]);
+    }
+    L->total = at;
+    return MDCN_OK;
+}
+
+mdcn_status mdcn_host_buffer_size(mdcn_handle handle, const mdcn_dims* dims, mdcn_dtype dtype, size_t* bytes) {
+    if (!handle || !dims || !bytes) return MDCN_ERR_NULL;
+    HostLayout L;
+    const mdcn_status s = host_layout(handle, dims, dtype, &L);
+    if (s != MDCN_OK) return s;
+    *bytes = L.total;
+    return MDCN_OK;
+}
+
+mdcn_status mdcn_forward_host(mdcn_handle handle, const void* x_host, const void* offset_host, const void* mask_host,
+                              const void* weight_host, const void* bias_host_or_null, void* out_host,
+                              void* device_buffer, size_t device_buffer_bytes, const mdcn_dims* dims,
+                              mdcn_dtype dtype, void* stream) {
+    if (!handle || !x_host || !offset_host || !mask_host || !weight_host || !out_host || !device_buffer || !dims)
+        return MDCN_ERR_NULL;
+    if ((bias_host_or_null == nullptr) != (dims->bias == 0)) return bias_host_or_null ? MDCN_ERR_SHAPE : MDCN_ERR_NULL;
+    if (!aligned16(device_buffer)) return MDCN_ERR_ALIGN;
+    HostLayout L;
+    mdcn_status s = host_layout(handle, dims, dtype, &L);
+    if (s != MDCN_OK) return s;
+    if (device_buffer_bytes < L.total) return MDCN_ERR_WORKSPACE;
+    Plan p;
+    s = plan_for_call(handle, dims, dtype, L.bytes[6], &p);  // everything checked before the first copy
+    if (s != MDCN_OK) return s;
+    uint8_t* base = static_cast<uint8_t*>(device_buffer);
+    void* dev[7];
+    for (int i = 0; i < 7; ++i) dev[i] = base + L.off[i];
+    const void* src[5] = {x_host, offset_host, mask_host, weight_host, bias_host_or_null};
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    for (int i = 0; i < 5; ++i) {
+        if (L.bytes[i] == 0) continue;
+        const cudaError_t e = cudaMemcpyAsync(dev[i], src[i], L.bytes[i], cudaMemcpyHostToDevice, st);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    s = mdcn_forward(handle, dev[0], dev[1], dev[2], dev[3], bias_host_or_null ? dev[4] : nullptr, dev[5], dev[6],
+                     L.bytes[6], dims, dtype, stream);
+    if (s != MDCN_OK) return s;
+    const cudaError_t e = cudaMemcpyAsync(out_host, dev[5], L.bytes[5], cudaMemcpyDeviceToHost, st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return MDCN_OK;
+}
+
 mdcn_status mdcn_prepare_input(mdcn_handle handle, const void* x, void* workspace, size_t workspace_bytes,
                                const mdcn_dims* dims, mdcn_dtype dtype, void* stream) {
     if (!handle || !x || !workspace || !dims) return MDCN_ERR_NULL;

@@ -226,3 +226,50 @@ def test_python_binding_rejects_cpu_tensors(lib):
         mdcn.mdcn_forward(h, x, off, m, w, None, torch.zeros(1, 8, 4, 4), torch.zeros(16, dtype=torch.uint8))
     with pytest.raises(mdcn.MdcnError):
         mdcn.Handle(stride=0)
+
+
+def test_host_buffer_size_covers_every_part(lib):
+    """mdcn_host_buffer_size: the device copies of the five inputs, the output
+    and the forward's workspace, each rounded up to 256 bytes."""
+    h = handle(lib)
+    d = dims(N=4, Cin=128, H=80, W=80, Cout=128, Ho=80, Wo=80, bias=True)
+    n = ctypes.c_size_t()
+    assert lib.mdcn_host_buffer_size(h, ctypes.byref(d), _abi.MDCN_F16, ctypes.byref(n)) == 0
+    s, ws = ws_size(lib, h, d, _abi.MDCN_F16)
+    parts = [4 * 128 * 80 * 80, 4 * 18 * 80 * 80, 4 * 9 * 80 * 80, 128 * 128 * 9, 128, 4 * 128 * 80 * 80]
+    up = lambda v: (v + 255) // 256 * 256
+    assert n.value == sum(up(2 * p) for p in parts) + up(ws)
+    assert lib.mdcn_host_buffer_size(h, ctypes.byref(d), 9, ctypes.byref(n)) == _abi.MDCN_ERR_DTYPE
+    assert lib.mdcn_host_buffer_size(h, ctypes.byref(d), _abi.MDCN_F16, None) == _abi.MDCN_ERR_NULL
+    lib.mdcn_destroy(h)
+
+
+def test_forward_host_rejects_before_any_copy(lib):
+    """Argument checks of mdcn_forward_host come before its first copy: fake
+    host and device pointers are never touched."""
+    h = handle(lib)
+    d = dims(bias=True)
+    p = [FAKE + 256 * i for i in range(8)]  # x, offset, mask, weight, bias, out (host), device buffer, spare
+
+    def call(q, dd=d, nbytes=1 << 30, dt=_abi.MDCN_F16):
+        return lib.mdcn_forward_host(h, *q[:7], nbytes, ctypes.byref(dd), dt, None)
+
+    for i in (0, 1, 2, 3, 5, 6):
+        q = list(p)
+        q[i] = None
+        assert call(q) == _abi.MDCN_ERR_NULL
+    q = list(p)
+    q[4] = None
+    assert call(q) == _abi.MDCN_ERR_NULL               # dims say bias, none given
+    assert call(p, dd=dims(bias=False)) == _abi.MDCN_ERR_SHAPE
+    q = list(p)
+    q[6] = FAKE + 8
+    assert call(q) == _abi.MDCN_ERR_ALIGN              # device buffer misaligned
+    q = list(p)
+    q[0] = FAKE + 2                                    # host pointers need no alignment
+    assert call(q, nbytes=16) == _abi.MDCN_ERR_WORKSPACE
+    assert call(p, dt=4) == _abi.MDCN_ERR_DTYPE
+    bad = dims(bias=True)
+    bad.offset[1] = 5
+    assert call(p, dd=bad) == _abi.MDCN_ERR_SHAPE
+    lib.mdcn_destroy(h)
