@@ -400,7 +400,10 @@ mdcn_status mdcn_forward(mdcn_handle handle, const void* x, const void* offset, 
     s = plan_for_call(handle, dims, dtype, workspace_bytes, &p);
     if (s != MDCN_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e = mdcn::launch_prep_both(p, x, weight, workspace, st);
+    const size_t elem = dtype == MDCN_F32 ? 4 : 2;
+    const size_t plane = static_cast<size_t>(p.N) * static_cast<size_t>(p.P) * elem;
+    cudaError_t e = mdcn::launch_prep_both(p, x, weight, offset, plane * 2 * p.dg * p.K, mask, plane * p.dg * p.K,
+                                           workspace, st);
     if (e == cudaSuccess) e = mdcn::launch_fused(p, offset, mask, bias_or_null, out, workspace, st);
     if (e != cudaSuccess) return cuda_fail(e);
     return MDCN_OK;

@@ -11,8 +11,10 @@ namespace mdcn {
 // (also clears the workspace status word), weight -> packed K-major.
 cudaError_t launch_prep_input(const Plan& pl, const void* x, void* ws, cudaStream_t st);
 cudaError_t launch_pack_weight(const Plan& pl, const void* weight, void* ws, cudaStream_t st);
-// Both of the above, in one launch where the shape allows.
-cudaError_t launch_prep_both(const Plan& pl, const void* x, const void* weight, void* ws, cudaStream_t st);
+// Both of the above, in one launch where the shape allows; that launch also
+// prefetches offset and mask (bytes each) into L2 for the fused kernel.
+cudaError_t launch_prep_both(const Plan& pl, const void* x, const void* weight, const void* offset,
+                             size_t offset_bytes, const void* mask, size_t mask_bytes, void* ws, cudaStream_t st);
 
 // The fused sampling + gather + contraction + bias kernel (reads offset, mask
 // and the two workspace products of launch_prep_input and

@@ -185,6 +185,11 @@ __device__ __forceinline__ float load_f<__half>(const __half* p) { return __half
 template <>
 __device__ __forceinline__ float load_f<__nv_bfloat16>(const __nv_bfloat16* p) { return __bfloat162float(*p); }
 
+// Weight rows per pack thread and pass: 8 for 16-bit types, 4 for fp32
+// (whose pass also splits each value into tf32 hi and lo; measured best).
+template <typename T>
+__host__ __device__ constexpr int pack_rows() { return sizeof(T) == 4 ? 4 : 8; }
+
 // Packs the weight into the fused kernel's K order (zero pad included).
 // Grid: x over k-tiles of one row (blockDim.x = BKc lanes per k-tile, several
 // k-tiles per block), y over rows (looping when rows exceed the grid).
@@ -199,11 +204,12 @@ __device__ __forceinline__ void pack_weight_body(const T* __restrict__ weight, T
     const KTile t = decode_ktile(kt, pl.K, pl.nch);
     const int32_t within = t.ch * pl.BKc + ci;  // channel within the unit
     const int64_t cl = static_cast<int64_t>(t.ul) * pl.U + within;  // channel within the group
-    // 4 rows per iteration: their loads are in flight together
-    for (int64_t r0 = by; r0 < pl.wp_rows; r0 += 4 * static_cast<int64_t>(gy)) {
-        T v[4];
+    // kRows rows per iteration: their loads are in flight together
+    constexpr int kRows = pack_rows<T>();
+    for (int64_t r0 = by; r0 < pl.wp_rows; r0 += kRows * static_cast<int64_t>(gy)) {
+        T v[kRows];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < kRows; ++k) {
             const int64_t r = r0 + k * static_cast<int64_t>(gy);
             v[k] = zero_of<T>();
             if (within < pl.U && r < rows) {
@@ -220,7 +226,7 @@ __device__ __forceinline__ void pack_weight_body(const T* __restrict__ weight, T
             }
         }
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < kRows; ++k) {
             const int64_t r = r0 + k * static_cast<int64_t>(gy);
             if (r < pl.wp_rows) wp[r * pl.KP + static_cast<int64_t>(kt) * pl.BKc + ci] = v[k];
         }
@@ -239,9 +245,20 @@ template <typename T>
 __global__ void __launch_bounds__(256) prep_both_kernel(const T* __restrict__ x, const T* __restrict__ weight,
                                                         T* __restrict__ xt, T* __restrict__ wp,
                                                         uint32_t* __restrict__ status, Plan pl, uint32_t tgx,
-                                                        uint32_t tgy, uint32_t nt, uint32_t pgx, uint32_t pgy) {
+                                                        uint32_t tgy, uint32_t nt, uint32_t pgx, uint32_t pgy,
+                                                        const char* __restrict__ offset, uint32_t offset_lines,
+                                                        const char* __restrict__ mask, uint32_t mask_lines) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const uint32_t b = blockIdx.x;
+    // offset and mask into L2 (128-byte lines spread over the blocks): the
+    // fused kernel's sampling then reads them from L2, not DRAM
+    {
+        const uint32_t lines = offset_lines + mask_lines;
+        const uint32_t per = (lines + gridDim.x - 1) / gridDim.x;
+        for (uint32_t l = b * per + threadIdx.x; l < min(lines, (b + 1) * per); l += blockDim.x)
+            prefetch_l2(l < offset_lines ? offset + static_cast<size_t>(l) * 128
+                                         : mask + static_cast<size_t>(l - offset_lines) * 128);
+    }
     if (b < nt) {
         nhwc_block_body<T>(x, xt, status, static_cast<int32_t>(pl.Cin), pl.H * pl.W, pl.Cp, pl.U, pl.UP,
                            pl.N * pl.H * pl.W * pl.Cp, b % tgx, (b / tgx) % tgy, b / (tgx * tgy));
@@ -272,8 +289,8 @@ template <typename T>
 static void pack_grid(const Plan& pl, unsigned* gx, unsigned* gy) {
     const int32_t ktiles_per_block = 256 / pl.BKc;
     *gx = static_cast<unsigned>((pl.KT + ktiles_per_block - 1) / ktiles_per_block);
-    const int64_t gy4 = (pl.wp_rows + 3) / 4;
-    *gy = static_cast<unsigned>(gy4 < 65535 ? gy4 : 65535);
+    const int64_t gyr = (pl.wp_rows + pack_rows<T>() - 1) / pack_rows<T>();
+    *gy = static_cast<unsigned>(gyr < 65535 ? gyr : 65535);
 }
 
 template <typename T>
@@ -313,7 +330,8 @@ static cudaError_t pack_weight_t(const Plan& pl, const void* weight, void* ws, c
 }
 
 template <typename T>
-static cudaError_t prep_both_t(const Plan& pl, const void* x, const void* weight, void* ws, cudaStream_t st) {
+static cudaError_t prep_both_t(const Plan& pl, const void* x, const void* weight, const void* offset,
+                               size_t offset_bytes, const void* mask, size_t mask_bytes, void* ws, cudaStream_t st) {
     dim3 tg;
     if (!block_transpose_grid<T>(pl, &tg)) {
         const cudaError_t e = prep_input_t<T>(pl, x, ws, st);
@@ -331,15 +349,19 @@ static cudaError_t prep_both_t(const Plan& pl, const void* x, const void* weight
     prep_both_kernel<T><<<static_cast<unsigned>(nt + np), 256, 0, st>>>(
         static_cast<const T*>(x), static_cast<const T*>(weight), reinterpret_cast<T*>(base + pl.off_xt),
         reinterpret_cast<T*>(base + pl.off_wp), reinterpret_cast<uint32_t*>(base), pl, tg.x, tg.y,
-        static_cast<uint32_t>(nt), pgx, pgy);
+        static_cast<uint32_t>(nt), pgx, pgy, static_cast<const char*>(offset),
+        static_cast<uint32_t>(offset_bytes / 128), static_cast<const char*>(mask), static_cast<uint32_t>(mask_bytes / 128));
     return cudaGetLastError();
 }
 
-cudaError_t launch_prep_both(const Plan& pl, const void* x, const void* weight, void* ws, cudaStream_t st) {
+cudaError_t launch_prep_both(const Plan& pl, const void* x, const void* weight, const void* offset,
+                             size_t offset_bytes, const void* mask, size_t mask_bytes, void* ws, cudaStream_t st) {
+    // line counts fit 32 bits for any offset/mask below 512 GB
+    if (offset_bytes / 128 > 0xffffffffull / 2 || mask_bytes / 128 > 0xffffffffull / 2) offset_bytes = mask_bytes = 0;
     switch (pl.dtype) {
-        case kF32: return prep_both_t<float>(pl, x, weight, ws, st);
-        case kF16: return prep_both_t<__half>(pl, x, weight, ws, st);
-        default: return prep_both_t<__nv_bfloat16>(pl, x, weight, ws, st);
+        case kF32: return prep_both_t<float>(pl, x, weight, offset, offset_bytes, mask, mask_bytes, ws, st);
+        case kF16: return prep_both_t<__half>(pl, x, weight, offset, offset_bytes, mask, mask_bytes, ws, st);
+        default: return prep_both_t<__nv_bfloat16>(pl, x, weight, offset, offset_bytes, mask, mask_bytes, ws, st);
     }
 }
 
