@@ -364,6 +364,44 @@ def run_ours(args, case, world, rank, local, dist):
     except Exception as e:  # the ablation is context only
         log("ablation skipped:", e)
 
+    # the pack form (offset and mask from an ordinary convolution of x in front
+    # of the deformable one), random front-end weights of the layer's shape,
+    # same flush rule; its flops count both convolutions
+    pack = None
+    try:
+        gp = torch.Generator().manual_seed(11)
+        kh, kw = w.shape[2], w.shape[3]
+        K = kh * kw
+        dg = case.attrs()["deformable_group"]
+        Cin = x.shape[1]
+        w_om = (torch.randn(3 * dg * K, Cin, kh, kw, generator=gp) / (Cin * K) ** 0.5).to(x.dtype).to(dev)
+        b_om = (0.5 * torch.randn(3 * dg * K, generator=gp)).to(x.dtype).to(dev)
+        poff, pmsk = torch.empty_like(off), torch.empty_like(m)
+        p_out = torch.empty_like(out)
+        pws = torch.empty(mdcn.mdcn_pack_workspace_size(h, x, poff, pmsk, w, b), dtype=torch.uint8, device=dev)
+        for _ in range(2):
+            mdcn.mdcn_forward_pack(h, x, w_om, b_om, w, b, poff, pmsk, p_out, pws, stream)
+        pt = []
+        for _ in range(min(args.steps, 20)):
+            flush.zero_()
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            mdcn.mdcn_forward_pack(h, x, w_om, b_om, w, b, poff, pmsk, p_out, pws, stream)
+            a1.record(stream)
+            pt.append((a0, a1))
+        torch.cuda.synchronize()
+        if mdcn.mdcn_query_status(pws)[0] != mdcn.MDCN_OK:
+            raise RuntimeError("pack form: device status set")
+        pack_ms = statistics.mean(a.elapsed_time(c) for a, c in pt)
+        fe_flops = 2 * x.shape[0] * 3 * dg * K * off.shape[2] * off.shape[3] * Cin * K
+        pack = {"ms_per_call": pack_ms, "tflops": (case.flops + fe_flops) / (pack_ms * 1e-3) / 1e12,
+                "front_end_flops": fe_flops, "launches": 4,
+                "call": "mdcn_forward_pack: front-end conv (fused kernel, plain) -> offset, sigmoid(mask); "
+                        "then the deformable convolution"}
+        del pws, p_out, poff, pmsk
+    except Exception as e:  # context only
+        log("pack form skipped:", e)
+
     if rank != 0:
         return
     flops = case.flops
@@ -409,6 +447,7 @@ def run_ours(args, case, world, rank, local, dist):
                 "call": "mdcn_forward_host (C ABI, pinned host buffers), steps rotating over 3 streams x 3 device buffers",
                 "single_stream": {"value": world * flops / (e2e_serial_ms * 1e-3) / 1e12,
                                   "ms_per_step": e2e_serial_ms}},
+        "pack_form": pack,
         "ablation_im2col_gemm": None if abl_ms is None else {"ms_per_call": abl_ms,
                                                              "tflops": flops / (abl_ms * 1e-3) / 1e12},
         "gpu_launches": plan["launches"] * args.steps,

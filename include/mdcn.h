@@ -191,6 +191,30 @@ mdcn_status mdcn_forward_prepared(mdcn_handle handle, const void* offset, const 
                                   void* out, void* workspace, size_t workspace_bytes, const mdcn_dims* dims,
                                   mdcn_dtype dtype, void* stream);
 
+/* The "pack" form of the layer: offset and mask computed from x by an
+ * ordinary convolution in front of the deformable one, as mmcv's
+ * ModulatedDeformConv2dPack does (the pages name the modulated deformable
+ * convolution of mmcv but do not spell this front end out; the reading here:
+ *   om     = conv2d(x, weight_om, bias_om) with the handle's stride, padding
+ *            and dilation, group 1; weight_om [3*dg*kh*kw, Cin, kh, kw],
+ *            bias_om [3*dg*kh*kw] (both required);
+ *   offset = om[:, 0 : 2*dg*kh*kw]                 (written to offset_out);
+ *   mask   = sigmoid(om[:, 2*dg*kh*kw : 3*dg*kh*kw]) (written to mask_out);
+ *   out    = mdcn_forward(x, offset, mask, weight, bias_or_null).)
+ * dims describes the deformable layer as for mdcn_forward; its offset and
+ * mask dims (those of offset_out and mask_out) must have the convolution's
+ * spatial size floor((H + 2p - d(k-1) - 1)/s) + 1, else MDCN_ERR_SHAPE. All
+ * pointers are device pointers (16-byte aligned); the workspace is at least
+ * mdcn_pack_workspace_size bytes. Asynchronous on the stream: the front end is
+ * the fused kernel run as a plain convolution with a two-output epilogue,
+ * then the deformable convolution reads offset_out and mask_out (reusing the
+ * workspace's channels-last x when its layout is the same). */
+mdcn_status mdcn_pack_workspace_size(mdcn_handle handle, const mdcn_dims* dims, mdcn_dtype dtype, size_t* bytes);
+mdcn_status mdcn_forward_pack(mdcn_handle handle, const void* x, const void* weight_om, const void* bias_om,
+                              const void* weight, const void* bias_or_null, void* offset_out, void* mask_out,
+                              void* out, void* workspace, size_t workspace_bytes, const mdcn_dims* dims,
+                              mdcn_dtype dtype, void* stream);
+
 /* Bytes of the device buffer that mdcn_forward_host needs for these dims
  * and dtype: room for the device copies of x, offset, mask, weight and bias,
  * the output, and the mdcn_forward workspace, each 256-byte aligned. Host

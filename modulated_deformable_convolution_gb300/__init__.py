@@ -202,6 +202,43 @@ def mdcn_forward(handle, x, offset, mask, weight, bias, out, workspace, stream=N
                                    ctypes.byref(d), _dtype(x), st), "mdcn_forward")
 
 
+def pack_dims(handle, x, weight) -> tuple:
+    """Offset and mask shapes of the pack form for x and weight: the
+    convolution's spatial size with the handle's attributes."""
+    N, Cin, H, W = x.shape
+    _, _, kh, kw = weight.shape
+    a = handle.attrs
+    Ho = (H + 2 * a["padding"][0] - a["dilation"][0] * (kh - 1) - 1) // a["stride"][0] + 1
+    Wo = (W + 2 * a["padding"][1] - a["dilation"][1] * (kw - 1) - 1) // a["stride"][1] + 1
+    K = kh * kw
+    dg = a["deformable_group"]
+    return (N, 2 * dg * K, Ho, Wo), (N, dg * K, Ho, Wo)
+
+
+def mdcn_pack_workspace_size(handle, x, offset, mask, weight, bias=None, dtype=None) -> int:
+    n = ctypes.c_size_t()
+    dt = _dtype(x) if dtype is None else dtype
+    _check(_lib().mdcn_pack_workspace_size(_hval(handle), ctypes.byref(_dims(x, offset, mask, weight, bias)), dt,
+                                           ctypes.byref(n)), "mdcn_pack_workspace_size")
+    return int(n.value)
+
+
+def mdcn_forward_pack(handle, x, weight_om, bias_om, weight, bias, offset_out, mask_out, out, workspace,
+                      stream=None) -> None:
+    """mdcn_forward_pack on torch tensors (device memory): offset_out and
+    mask_out receive the front end's offset and mask, out the layer's output."""
+    _check_tensors(x, offset_out, mask_out, weight, bias, out)
+    for t in (weight_om, bias_om):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != x.dtype:
+            raise ValueError("weight_om and bias_om must be contiguous CUDA tensors of x's dtype")
+    d = _dims(x, offset_out, mask_out, weight, bias)
+    with torch.cuda.device(x.device):
+        _check(_lib().mdcn_forward_pack(_hval(handle), _ptr(x), _ptr(weight_om), _ptr(bias_om), _ptr(weight),
+                                        _ptr(bias), _ptr(offset_out), _ptr(mask_out), _ptr(out), _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(), ctypes.byref(d), _dtype(x),
+                                        _stream(x.device, stream)), "mdcn_forward_pack")
+
+
 def mdcn_host_buffer_size(handle, x, offset, mask, weight, bias=None, dtype=None) -> int:
     """Device-buffer bytes of mdcn_forward_host (tensors give only shapes and dtype)."""
     n = ctypes.c_size_t()

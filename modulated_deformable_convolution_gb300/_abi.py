@@ -99,6 +99,12 @@ def load(path: str = LIB_PATH):
         lib.mdcn_forward_im2col_gemm.restype = st
         lib.mdcn_query_plan.argtypes = [vp, ctypes.POINTER(mdcn_dims), ctypes.c_int, ctypes.POINTER(mdcn_plan_info)]
         lib.mdcn_query_plan.restype = st
+        lib.mdcn_pack_workspace_size.argtypes = [vp, ctypes.POINTER(mdcn_dims), ctypes.c_int,
+                                                 ctypes.POINTER(ctypes.c_size_t)]
+        lib.mdcn_pack_workspace_size.restype = st
+        lib.mdcn_forward_pack.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t,
+                                          ctypes.POINTER(mdcn_dims), ctypes.c_int, vp]
+        lib.mdcn_forward_pack.restype = st
         lib.mdcn_host_buffer_size.argtypes = [vp, ctypes.POINTER(mdcn_dims), ctypes.c_int,
                                               ctypes.POINTER(ctypes.c_size_t)]
         lib.mdcn_host_buffer_size.restype = st

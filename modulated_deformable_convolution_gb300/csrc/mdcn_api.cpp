@@ -183,6 +183,7 @@ mdcn_status make_plan(const mdcn_attrs& a, const mdcn_tuning& tuning, const mdcn
     const double waste = 1.0 - static_cast<double>(p.P) / static_cast<double>(p.tiles_x * p.TW * p.tiles_y * p.TH);
     int32_t mode = tuning.tile_mode >= 0 ? tuning.tile_mode : (waste <= 0.06 ? 1 : 0);
     p.tile_mode = mode;
+    p.plain = 0;
     p.mtiles = mode == 1 ? p.N * p.tiles_x * p.tiles_y : ceil_div(p.NP, mdcn::kTileM);
     int64_t tt = p.mtiles;
     if (!mul_ok(tt, p.ntiles_n) || !mul_ok(tt, p.group)) return MDCN_ERR_UNSUPPORTED;
@@ -303,8 +304,9 @@ mdcn_status check_forward_args(mdcn_handle h, const void* x, const void* offset,
 }
 
 // Plan + workspace-size + device checks shared by the fused-path entry points.
-mdcn_status plan_for_call(mdcn_handle h, const mdcn_dims* dims, mdcn_dtype dtype, size_t ws_bytes, Plan* p) {
-    mdcn_status s = make_plan(h->attrs, h->tuning, dims, dtype, p);
+mdcn_status plan_for(const mdcn_attrs& attrs, const mdcn_tuning& tuning, const mdcn_dims* dims, mdcn_dtype dtype,
+                     size_t ws_bytes, Plan* p) {
+    mdcn_status s = make_plan(attrs, tuning, dims, dtype, p);
     if (s != MDCN_OK) return s;
     if (ws_bytes < p->ws_bytes) return MDCN_ERR_WORKSPACE;
     int sms = 0;
@@ -312,7 +314,7 @@ mdcn_status plan_for_call(mdcn_handle h, const mdcn_dims* dims, mdcn_dtype dtype
     if (s != MDCN_OK) return s;
     int64_t grid = sms > 0 ? sms : 1;
     if (grid > mdcn::kMaxCtas) grid = mdcn::kMaxCtas;
-    if (h->tuning.max_ctas > 0 && h->tuning.max_ctas < grid) grid = h->tuning.max_ctas;
+    if (tuning.max_ctas > 0 && tuning.max_ctas < grid) grid = tuning.max_ctas;
     if (grid > p->total_kt) grid = p->total_kt;
     // stream-K split: equal consecutive k-tile ranges, none empty. Splitting a
     // tile costs its other CTAs an fp32 partial write each and its owner a
@@ -322,6 +324,37 @@ mdcn_status plan_for_call(mdcn_handle h, const mdcn_dims* dims, mdcn_dtype dtype
     const int64_t whole = (p->tiles_total + grid - 1) / grid * p->KT;
     p->kt_per_cta = split * 115 / 100 + 4 < whole ? split : whole;
     p->grid = static_cast<int32_t>((p->total_kt + p->kt_per_cta - 1) / p->kt_per_cta);
+    return MDCN_OK;
+}
+
+mdcn_status plan_for_call(mdcn_handle h, const mdcn_dims* dims, mdcn_dtype dtype, size_t ws_bytes, Plan* p) {
+    return plan_for(h->attrs, h->tuning, dims, dtype, ws_bytes, p);
+}
+
+// The offset/mask front end of the pack form, as an ordinary convolution:
+// the layer's stride, padding and dilation, group 1, no deformation, and
+// 3*dg*kh*kw output channels with a bias. Its spatial size is the
+// convolution's, which the layer's offset and mask dims must match.
+mdcn_status front_end_problem(const mdcn_attrs& a, const mdcn_dims* d, mdcn_attrs* fa, mdcn_dims* fd) {
+    if (!d) return MDCN_ERR_NULL;
+    const int64_t kh = d->weight[2], kw = d->weight[3], K = kh * kw;
+    const int64_t H = d->x[2], W = d->x[3];
+    if (kh < 1 || kw < 1 || H < 1 || W < 1 || K > kI31) return MDCN_ERR_SHAPE;
+    const int64_t Ho = (H + 2 * a.padding[0] - a.dilation[0] * (kh - 1) - 1) / a.stride[0] + 1;
+    const int64_t Wo = (W + 2 * a.padding[1] - a.dilation[1] * (kw - 1) - 1) / a.stride[1] + 1;
+    if (H + 2 * a.padding[0] < a.dilation[0] * (kh - 1) + 1 || W + 2 * a.padding[1] < a.dilation[1] * (kw - 1) + 1)
+        return MDCN_ERR_SHAPE;  // empty convolution output
+    if (d->offset[2] != Ho || d->offset[3] != Wo) return MDCN_ERR_SHAPE;
+    *fa = a;
+    fa->group = 1;
+    fa->deformable_group = 1;
+    *fd = *d;
+    const int64_t com = 3 * a.deformable_group * K;
+    fd->weight[0] = com;
+    fd->weight[1] = d->x[1];
+    fd->offset[1] = 2 * K;
+    fd->mask[1] = K;
+    fd->bias = com;
     return MDCN_OK;
 }
 
@@ -483,6 +516,59 @@ mdcn_status mdcn_forward_host(mdcn_handle handle, const void* x_host, const void
                      L.bytes[6], dims, dtype, stream);
     if (s != MDCN_OK) return s;
     const cudaError_t e = cudaMemcpyAsync(out_host, dev[5], L.bytes[5], cudaMemcpyDeviceToHost, st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return MDCN_OK;
+}
+
+mdcn_status mdcn_pack_workspace_size(mdcn_handle handle, const mdcn_dims* dims, mdcn_dtype dtype, size_t* bytes) {
+    if (!handle || !dims || !bytes) return MDCN_ERR_NULL;
+    mdcn_attrs fa;
+    mdcn_dims fd;
+    mdcn_status s = front_end_problem(handle->attrs, dims, &fa, &fd);
+    if (s != MDCN_OK) return s;
+    Plan pf, pd;
+    s = make_plan(fa, handle->tuning, &fd, dtype, &pf);
+    if (s != MDCN_OK) return s;
+    s = make_plan(handle->attrs, handle->tuning, dims, dtype, &pd);
+    if (s != MDCN_OK) return s;
+    *bytes = pf.ws_bytes > pd.ws_bytes ? pf.ws_bytes : pd.ws_bytes;
+    return MDCN_OK;
+}
+
+mdcn_status mdcn_forward_pack(mdcn_handle handle, const void* x, const void* weight_om, const void* bias_om,
+                              const void* weight, const void* bias_or_null, void* offset_out, void* mask_out,
+                              void* out, void* workspace, size_t workspace_bytes, const mdcn_dims* dims,
+                              mdcn_dtype dtype, void* stream) {
+    if (!weight_om || !bias_om || !offset_out || !mask_out) return MDCN_ERR_NULL;
+    mdcn_status s = check_forward_args(handle, x, offset_out, mask_out, weight, bias_or_null, out, workspace, dims);
+    if (s != MDCN_OK) return s;
+    if (!aligned16(weight_om) || !aligned16(bias_om)) return MDCN_ERR_ALIGN;
+    mdcn_attrs fa;
+    mdcn_dims fd;
+    s = front_end_problem(handle->attrs, dims, &fa, &fd);
+    if (s != MDCN_OK) return s;
+    Plan pf, pd;
+    s = plan_for(fa, handle->tuning, &fd, dtype, workspace_bytes, &pf);
+    if (s != MDCN_OK) return s;
+    s = plan_for_call(handle, dims, dtype, workspace_bytes, &pd);
+    if (s != MDCN_OK) return s;
+    pf.plain = 1;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int32_t split = static_cast<int32_t>(2 * pd.dg * pd.K);
+    // 1: offset and mask from the front end (one workspace, used in turn)
+    cudaError_t e = mdcn::launch_prep_both(pf, x, weight_om, nullptr, 0, nullptr, 0, workspace, st);
+    if (e == cudaSuccess) e = mdcn::launch_fused(pf, nullptr, nullptr, bias_om, offset_out, workspace, st, mask_out, split);
+    // 2: the deformable convolution; when its channels-last x has the front
+    // end's layout, the copy already in the workspace is reused
+    const bool same_xt = pf.Cp == pd.Cp && pf.U == pd.U && pf.UP == pd.UP && pf.off_xt == pd.off_xt &&
+                         pf.off_wp == pd.off_wp;
+    const size_t elem = dtype == MDCN_F32 ? 4 : 2;
+    const size_t plane = static_cast<size_t>(pd.N) * static_cast<size_t>(pd.P) * elem;
+    if (e == cudaSuccess)
+        e = same_xt ? mdcn::launch_pack_weight(pd, weight, workspace, st)
+                    : mdcn::launch_prep_both(pd, x, weight, offset_out, plane * 2 * pd.dg * pd.K, mask_out,
+                                             plane * pd.dg * pd.K, workspace, st);
+    if (e == cudaSuccess) e = mdcn::launch_fused(pd, offset_out, mask_out, bias_or_null, out, workspace, st);
     if (e != cudaSuccess) return cuda_fail(e);
     return MDCN_OK;
 }

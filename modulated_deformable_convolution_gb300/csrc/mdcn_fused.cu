@@ -72,6 +72,11 @@ struct FusedParams {
     float* part;           // fp32 partial accumulators of split tiles: one slot per CTA
     uint32_t* split_count;  // per split tile (by its first CTA): contributors' epilogue warps done
     int32_t epi_vec;        // the plan allows 16-byte output stores and out is 16-byte aligned
+    // two outputs (split_ch > 0): output channels [0, split_ch) go to out as
+    // [N, split_ch, Ho, Wo], the rest through the logistic sigmoid to out2 as
+    // [N, Cout - split_ch, Ho, Wo] (the offset/mask front end)
+    void* out2;
+    int32_t split_ch;
     Plan pl;
 };
 
@@ -233,8 +238,8 @@ __device__ __forceinline__ SampleRow<T> sample_row_at(const Plan& pl, const T* o
     const int64_t n = q.valid ? q.n : 0;
     const int64_t hw = q.valid ? q.ho * pl.Wo + q.wo : 0;
     SampleRow<T> r;
-    r.po = offset + (n * 2 * pl.dg * K + gd * 2 * K + 2 * static_cast<int64_t>(tap0)) * P + hw;
-    r.pm = mask + (n * pl.dg * K + gd * K + tap0) * P + hw;
+    r.po = pl.plain ? nullptr : offset + (n * 2 * pl.dg * K + gd * 2 * K + 2 * static_cast<int64_t>(tap0)) * P + hw;
+    r.pm = pl.plain ? nullptr : mask + (n * pl.dg * K + gd * K + tap0) * P + hw;
     r.hbase = static_cast<float>(q.ho * pl.sh - pl.ph);
     r.wbase = static_cast<float>(q.wo * pl.sw - pl.pw);
     r.nbase = q.n * pl.H;
@@ -261,8 +266,10 @@ __device__ __forceinline__ void write_desc(const Plan& pl, const SampleRow<T>& r
         w01 = hh * lw * mv;
         w10 = lh * hw_ * mv;
         w11 = lh * lw * mv;
-        const bool top = y0 >= 0, bottom = y0 + 1 < pl.H;
-        const bool left = x0 >= 0, right = x0 + 1 < pl.W;
+        // a corner whose bilinear weight is exactly 0 (the point on a pixel row
+        // or column) reads the zero pixel instead: the same sum, fewer loads
+        const bool top = y0 >= 0, bottom = y0 + 1 < pl.H && lh != 0.0f;
+        const bool left = x0 >= 0, right = x0 + 1 < pl.W && lw != 0.0f;
         flags = (top && left ? 1u : 0u) | (top && right ? 2u : 0u) | (bottom && left ? 4u : 0u) |
                 (bottom && right ? 8u : 0u);
         base = static_cast<int32_t>((r.nbase + y0) * pl.W + x0);
@@ -305,12 +312,17 @@ __device__ __forceinline__ void sample_rows(const Plan& pl, const T* __restrict_
 #pragma unroll
         for (int u = 0; u < kSampleTaps; ++u) {
             const int64_t kb = kb0 + u < ntap ? kb0 + u : kb0;
-            v[0][0][u] = to_f(ra.po[(2 * kb) * P]);
-            v[0][1][u] = to_f(ra.po[(2 * kb + 1) * P]);
-            v[0][2][u] = to_f(ra.pm[kb * P]);
-            v[1][0][u] = to_f(rb.po[(2 * kb) * P]);
-            v[1][1][u] = to_f(rb.po[(2 * kb + 1) * P]);
-            v[1][2][u] = to_f(rb.pm[kb * P]);
+            if (pl.plain) {
+                v[0][0][u] = v[0][1][u] = v[1][0][u] = v[1][1][u] = 0.f;
+                v[0][2][u] = v[1][2][u] = 1.f;
+            } else {
+                v[0][0][u] = to_f(ra.po[(2 * kb) * P]);
+                v[0][1][u] = to_f(ra.po[(2 * kb + 1) * P]);
+                v[0][2][u] = to_f(ra.pm[kb * P]);
+                v[1][0][u] = to_f(rb.po[(2 * kb) * P]);
+                v[1][1][u] = to_f(rb.po[(2 * kb + 1) * P]);
+                v[1][2][u] = to_f(rb.pm[kb * P]);
+            }
         }
 #pragma unroll
         for (int u = 0; u < kSampleTaps; ++u) {
@@ -341,9 +353,14 @@ __device__ __forceinline__ void sample_row_taps(const Plan& pl, const T* __restr
     for (int u = 0; u < kSampleTaps; ++u) {
         const int32_t kb0 = kb_first + u * kb_step;
         const int64_t kb = kb0 < ntap ? kb0 : 0;
-        v[0][u] = to_f(r.po[(2 * kb) * P]);
-        v[1][u] = to_f(r.po[(2 * kb + 1) * P]);
-        v[2][u] = to_f(r.pm[kb * P]);
+        if (pl.plain) {
+            v[0][u] = v[1][u] = 0.f;
+            v[2][u] = 1.f;
+        } else {
+            v[0][u] = to_f(r.po[(2 * kb) * P]);
+            v[1][u] = to_f(r.po[(2 * kb + 1) * P]);
+            v[2][u] = to_f(r.pm[kb * P]);
+        }
     }
 #pragma unroll
     for (int u = 0; u < kSampleTaps; ++u) {
@@ -578,10 +595,9 @@ __device__ __forceinline__ void stage_bias(const Plan& pl, const T* bias, const 
 
 // The group of 16 / sizeof(T) consecutive output pixels whose 16-byte
 // vectors this lane stores: group lane % (32 / that) of the 32 tile rows of
-// lane quarter `quarter`, and the output index of its first pixel in the
-// plane of the tile's first column.
+// lane quarter `quarter`: its image and the index of its first pixel.
 struct OutGroup {
-    int64_t base;
+    int64_t n, hw;
     bool valid;
 };
 
@@ -591,9 +607,23 @@ __device__ __forceinline__ OutGroup out_group(const Plan& pl, const TileId& id, 
     constexpr int kGroups = 32 / kVecPx;
     const Pixel gp = tile_pixel(pl, id.mt, quarter * 32 + (lane % kGroups) * kVecPx);
     OutGroup og;
-    og.base = (gp.n * pl.Cout + static_cast<int64_t>(id.g) * pl.Og + id.nt * pl.acc_cols) * pl.P + gp.ho * pl.Wo + gp.wo;
+    og.n = gp.n;
+    og.hw = gp.ho * pl.Wo + gp.wo;
     og.valid = gp.valid;
     return og;
+}
+
+// Where output channel ch (of all Cout) of pixel hw of image n goes: out
+// [N, Cout, Ho, Wo], or with a split, out [N, split, Ho, Wo] below the split
+// and out2 [N, Cout - split, Ho, Wo] from it.
+template <typename T>
+__device__ __forceinline__ T* out_elem(const Plan& pl, const FusedParams& prm, int64_t n, int64_t ch, int64_t hw) {
+    if (prm.split_ch > 0) {
+        const int64_t cs = prm.split_ch;
+        return ch < cs ? static_cast<T*>(prm.out) + (n * cs + ch) * pl.P + hw
+                       : static_cast<T*>(prm.out2) + (n * (pl.Cout - cs) + (ch - cs)) * pl.P + hw;
+    }
+    return static_cast<T*>(prm.out) + (n * pl.Cout + ch) * pl.P + hw;
 }
 
 // 16 output channels (accumulator columns c16..c16+15) of the warp's 32 rows:
@@ -607,10 +637,16 @@ __device__ __forceinline__ void store_chunk16(const Plan& pl, const FusedParams&
                                               uint32_t bias_s, uint32_t stg) {
     const int32_t ncol0 = id.nt * pl.acc_cols;
     if (ncol0 + c16 >= pl.Og) return;
-    T* __restrict__ out = static_cast<T*>(prm.out);
+    const int64_t ch0 = static_cast<int64_t>(id.g) * pl.Og + ncol0 + c16;  // output channel of column c16
     if (prm.bias) {
 #pragma unroll
         for (int e = 0; e < 16; ++e) vals[e] += ld_shared_f32(bias_s + 4u * (c16 + e));
+    }
+    if (prm.split_ch > 0) {
+        // the second output's channels: the logistic sigmoid
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+            if (ch0 + e >= prm.split_ch) vals[e] = 1.0f / (1.0f + expf(-vals[e]));
     }
 #pragma unroll
     for (int e = 0; e < 16; ++e) st_shared_elem<T>(stg + static_cast<uint32_t>((e * 32 + lane) * sizeof(T)), vals[e]);
@@ -623,15 +659,15 @@ __device__ __forceinline__ void store_chunk16(const Plan& pl, const FusedParams&
             const int e = lane / kGroups + k * (32 / kGroups);  // channel of the chunk
             const uint32_t src = stg + static_cast<uint32_t>((e * 32 + (lane % kGroups) * kVecPx) * sizeof(T));
             if (og.valid && ncol0 + c16 + e < pl.Og)
-                st_global_v4(out + og.base + static_cast<int64_t>(c16 + e) * pl.P, ld_shared_v4(src));
+                st_global_v4(out_elem<T>(pl, prm, og.n, ch0 + e, og.hw), ld_shared_v4(src));
         }
     } else {
         const Pixel px = tile_pixel(pl, id.mt, row);
         if (px.valid) {
-            T* o = out + (px.n * pl.Cout + static_cast<int64_t>(id.g) * pl.Og + ncol0 + c16) * pl.P +
-                   px.ho * pl.Wo + px.wo;
+            const int64_t hw = px.ho * pl.Wo + px.wo;
             for (int e = 0; e < 16 && ncol0 + c16 + e < pl.Og; ++e)
-                o[static_cast<int64_t>(e) * pl.P] = ld_shared_elem<T>(stg + static_cast<uint32_t>((e * 32 + lane) * sizeof(T)));
+                *out_elem<T>(pl, prm, px.n, ch0 + e, hw) =
+                    ld_shared_elem<T>(stg + static_cast<uint32_t>((e * 32 + lane) * sizeof(T)));
         }
     }
     __syncwarp();
@@ -1162,7 +1198,7 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
 
 template <int DT>
 cudaError_t launch_fused_t(const Plan& pl, const void* offset, const void* mask, const void* bias, void* out, void* ws,
-                           cudaStream_t st) {
+                           cudaStream_t st, void* out2, int32_t split_ch) {
     using T = typename Elem<DT>::T;
     uint8_t* base = static_cast<uint8_t*>(ws);
     const T* wp = reinterpret_cast<const T*>(base + pl.off_wp);
@@ -1186,7 +1222,12 @@ cudaError_t launch_fused_t(const Plan& pl, const void* offset, const void* mask,
     prm.status = reinterpret_cast<uint32_t*>(base);
     prm.part = reinterpret_cast<float*>(base + pl.off_part);
     prm.split_count = reinterpret_cast<uint32_t*>(base + kSplitCountOffset);
-    prm.epi_vec = pl.epi_vec && (reinterpret_cast<uintptr_t>(out) & 15u) == 0 ? 1 : 0;
+    prm.out2 = out2;
+    prm.split_ch = split_ch;
+    prm.epi_vec = pl.epi_vec && (reinterpret_cast<uintptr_t>(out) & 15u) == 0 &&
+                          (split_ch == 0 || (reinterpret_cast<uintptr_t>(out2) & 15u) == 0)
+                      ? 1
+                      : 0;
     prm.pl = pl;
     // launched dependent on the prep kernel: the prologue (barriers, tensor
     // memory, the first descriptor group) overlaps its tail
@@ -1231,11 +1272,11 @@ cudaError_t prepare_fused_attributes(int dtype, int smem_bytes) {
 }
 
 cudaError_t launch_fused(const Plan& pl, const void* offset, const void* mask, const void* bias, void* out, void* ws,
-                         cudaStream_t st) {
+                         cudaStream_t st, void* out2, int32_t split_ch) {
     switch (pl.dtype) {
-        case kF32: return launch_fused_t<kF32>(pl, offset, mask, bias, out, ws, st);
-        case kF16: return launch_fused_t<kF16>(pl, offset, mask, bias, out, ws, st);
-        default: return launch_fused_t<kBF16>(pl, offset, mask, bias, out, ws, st);
+        case kF32: return launch_fused_t<kF32>(pl, offset, mask, bias, out, ws, st, out2, split_ch);
+        case kF16: return launch_fused_t<kF16>(pl, offset, mask, bias, out, ws, st, out2, split_ch);
+        default: return launch_fused_t<kBF16>(pl, offset, mask, bias, out, ws, st, out2, split_ch);
     }
 }
 

@@ -19,8 +19,11 @@ cudaError_t launch_prep_both(const Plan& pl, const void* x, const void* weight, 
 // The fused sampling + gather + contraction + bias kernel (reads offset, mask
 // and the two workspace products of launch_prep_input and
 // launch_pack_weight); tiles split between CTAs are finished inside it.
+// With split_ch > 0 output channels [0, split_ch) go to out and the rest,
+// through the logistic sigmoid, to out2 (both NCHW with their own channel
+// counts). A plan with pl.plain set reads no offset or mask.
 cudaError_t launch_fused(const Plan& pl, const void* offset, const void* mask, const void* bias, void* out, void* ws,
-                         cudaStream_t st);
+                         cudaStream_t st, void* out2 = nullptr, int32_t split_ch = 0);
 
 // Dynamic shared memory the fused kernel may use on this device (set once).
 cudaError_t prepare_fused_attributes(int dtype, int smem_bytes);

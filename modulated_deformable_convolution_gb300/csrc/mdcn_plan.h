@@ -82,6 +82,7 @@ struct Plan {
     int32_t desc_size;       // bytes per sample descriptor (16, or 32 for f32)
     int32_t desc_slot_bytes; // one descriptor group: kTileM rows x kTapBlock taps
     int32_t epi_vec;         // 1: output groups of 16 bytes of consecutive pixels stay aligned and whole
+    int32_t plain;           // 1: an ordinary convolution (no offset or mask read: every offset 0, mask 1)
     int32_t epi_bytes;       // shared-memory staging of the TMA-store epilogue
     int32_t smem_bytes;      // dynamic shared memory of the fused kernel
     int32_t grid;            // persistent CTAs

@@ -156,3 +156,59 @@ def forward(x, offset, mask, weight, bias=None, stride=1, padding=0, dilation=1,
     if rc != 0:
         raise RuntimeError(f"oracle failed with code {rc}")
     return out
+
+
+def conv_output_hw(H, W, kh, kw, stride, padding, dilation):
+    """Spatial size of an ordinary convolution: floor((H + 2p - d(k-1) - 1)/s) + 1."""
+    stride, padding, dilation = _pair(stride, "stride"), _pair(padding, "padding"), _pair(dilation, "dilation")
+    Ho = (H + 2 * padding[0] - dilation[0] * (kh - 1) - 1) // stride[0] + 1
+    Wo = (W + 2 * padding[1] - dilation[1] * (kw - 1) - 1) // stride[1] + 1
+    return Ho, Wo
+
+
+def offset_mask_front_end(x, weight_om, bias_om, stride=1, padding=0, dilation=1, deformable_group=1,
+                          kernel_size=None, nthreads: int = 0):
+    """The offset/mask front end of the "pack" form of the modulated
+    deformable convolution (mmcv ModulatedDeformConv2dPack semantics, which
+    the pages name but do not spell out; reading in the design notes): an
+    ordinary convolution of x with weight_om [3*dg*kh*kw, Cin, kh, kw] and
+    bias_om [3*dg*kh*kw] (group 1, the layer's stride, padding and dilation),
+    whose first 2*dg*kh*kw output channels are the offset and whose last
+    dg*kh*kw channels, through the logistic sigmoid, are the mask.
+
+    The convolution is this oracle's own forward with zero offsets and a unit
+    mask, which the P1 pins prove equal to an ordinary convolution. Returns
+    (offset, mask) as float64 arrays."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    weight_om = np.ascontiguousarray(weight_om, dtype=np.float64)
+    bias_om = np.ascontiguousarray(bias_om, dtype=np.float64)
+    N, Cin, H, W = x.shape
+    Com, Cin_w, kh, kw = weight_om.shape
+    K = kh * kw
+    if Cin_w != Cin:
+        raise ValueError("weight_om must be [3*dg*kh*kw, Cin, kh, kw]")
+    if Com != 3 * deformable_group * K:
+        raise ValueError("weight_om must have 3*deformable_group*kh*kw output channels")
+    if bias_om.shape != (Com,):
+        raise ValueError("bias_om must be [3*dg*kh*kw]")
+    Ho, Wo = conv_output_hw(H, W, kh, kw, stride, padding, dilation)
+    if Ho < 1 or Wo < 1:
+        raise ValueError("the convolution has an empty output")
+    zero_off = np.zeros((N, 2 * K, Ho, Wo))
+    unit_mask = np.ones((N, K, Ho, Wo))
+    om = forward(x, zero_off, unit_mask, weight_om, bias_om, stride, padding, dilation, 1, 1, nthreads=nthreads)
+    c = 2 * deformable_group * K
+    offset = np.ascontiguousarray(om[:, :c])
+    mask = 1.0 / (1.0 + np.exp(-om[:, c:]))
+    return offset, np.ascontiguousarray(mask)
+
+
+def forward_pack(x, weight_om, bias_om, weight, bias=None, stride=1, padding=0, dilation=1, group=1,
+                 deformable_group=1, nthreads: int = 0):
+    """The pack form end to end: offset and mask from the front end above,
+    then this oracle's forward. Returns (out, offset, mask)."""
+    offset, mask = offset_mask_front_end(x, weight_om, bias_om, stride, padding, dilation, deformable_group,
+                                         nthreads=nthreads)
+    out = forward(x, offset, mask, weight, bias, stride, padding, dilation, group, deformable_group,
+                  nthreads=nthreads)
+    return out, offset, mask

@@ -273,3 +273,48 @@ def test_forward_host_rejects_before_any_copy(lib):
     bad.offset[1] = 5
     assert call(p, dd=bad) == _abi.MDCN_ERR_SHAPE
     lib.mdcn_destroy(h)
+
+
+def _pack_dims(N=2, Cin=8, H=10, W=12, Cout=6, kh=3, kw=3, stride=1, pad=1, dil=1, dg=1, bias=True):
+    Ho = (H + 2 * pad - dil * (kh - 1) - 1) // stride + 1
+    Wo = (W + 2 * pad - dil * (kw - 1) - 1) // stride + 1
+    return dims(N=N, Cin=Cin, H=H, W=W, Cout=Cout, kh=kh, kw=kw, Ho=Ho, Wo=Wo, dg=dg, bias=bias)
+
+
+def test_pack_workspace_size_and_shape_rule(lib):
+    h = handle(lib, stride=(2, 2), padding=(1, 1), dg=2)
+    d = _pack_dims(stride=2, pad=1, dg=2)
+    n = ctypes.c_size_t()
+    assert lib.mdcn_pack_workspace_size(h, ctypes.byref(d), _abi.MDCN_F16, ctypes.byref(n)) == 0
+    s, ws = ws_size(lib, h, d, _abi.MDCN_F16)
+    assert s == 0 and n.value >= ws
+    bad = _pack_dims(stride=2, pad=1, dg=2)
+    bad.offset[2] += 1                               # not the convolution's output height
+    bad.mask[2] += 1
+    assert lib.mdcn_pack_workspace_size(h, ctypes.byref(bad), _abi.MDCN_F16, ctypes.byref(n)) == _abi.MDCN_ERR_SHAPE
+    lib.mdcn_destroy(h)
+
+
+def test_forward_pack_rejects_before_launch(lib):
+    h = handle(lib)
+    d = _pack_dims()
+    # x, weight_om, bias_om, weight, bias, offset_out, mask_out, out, workspace
+    p = [FAKE + 256 * i for i in range(9)]
+
+    def call(q, dd=d, nbytes=1 << 30):
+        return lib.mdcn_forward_pack(h, *q, nbytes, ctypes.byref(dd), _abi.MDCN_F16, None)
+
+    for i in (0, 1, 2, 3, 5, 6, 7, 8):
+        q = list(p)
+        q[i] = None
+        assert call(q) == _abi.MDCN_ERR_NULL
+    for i in (0, 1, 2, 5, 6):
+        q = list(p)
+        q[i] = FAKE + 8
+        assert call(q) == _abi.MDCN_ERR_ALIGN
+    bad = _pack_dims()
+    bad.offset[3] = 5
+    bad.mask[3] = 5
+    assert call(p, dd=bad) == _abi.MDCN_ERR_SHAPE
+    assert call(p, nbytes=64) == _abi.MDCN_ERR_WORKSPACE
+    lib.mdcn_destroy(h)

@@ -542,3 +542,65 @@ def test_planted_slip_is_caught(oracle_mod, name, tmp_path):
                     str(cpath), "-lm"], check=True)
     lib = oracle_mod.load_library(str(so))
     assert all_pins(oracle_mod, lib), f"planted slip {name} passed every pin"
+
+
+# ---------------------------------------------------------------- the pack front end
+# (offset and mask from an ordinary convolution of x; the final sigmoid on the
+# mask channels). Pinned against torch's float64 conv2d and sigmoid, and a
+# closed form.
+
+def _pack_case(seed=7, N=2, Cin=4, H=7, W=6, Cout=5, k=(3, 3), stride=(1, 1), padding=(1, 1), dilation=(1, 1),
+               dg=2, group=1):
+    g = torch.Generator().manual_seed(seed)
+    kh, kw = k
+    K = kh * kw
+    x = torch.randn(N, Cin, H, W, generator=g, dtype=torch.float64)
+    w_om = 0.3 * torch.randn(3 * dg * K, Cin, kh, kw, generator=g, dtype=torch.float64)
+    b_om = 0.2 * torch.randn(3 * dg * K, generator=g, dtype=torch.float64)
+    w = torch.randn(Cout, Cin // group, kh, kw, generator=g, dtype=torch.float64)
+    b = torch.randn(Cout, generator=g, dtype=torch.float64)
+    return x, w_om, b_om, w, b, dict(stride=stride, padding=padding, dilation=dilation, group=group,
+                                     deformable_group=dg)
+
+
+@pytest.mark.parametrize("geom", [dict(), dict(stride=(2, 1), padding=(2, 0), dilation=(1, 2)),
+                                  dict(k=(1, 3), dg=1, padding=(0, 1))])
+def test_pack_front_end_is_conv2d_then_sigmoid(oracle_mod, geom):
+    x, w_om, b_om, w, b, a = _pack_case(**geom)
+    off, msk = oracle_mod.offset_mask_front_end(x.numpy(), w_om.numpy(), b_om.numpy(), a["stride"], a["padding"],
+                                                a["dilation"], a["deformable_group"])
+    om = torch.nn.functional.conv2d(x, w_om, b_om, a["stride"], a["padding"], a["dilation"])
+    c = off.shape[1]
+    assert c == 2 * a["deformable_group"] * w_om.shape[2] * w_om.shape[3]
+    np.testing.assert_allclose(off, om[:, :c].numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(msk, torch.sigmoid(om[:, c:]).numpy(), rtol=0, atol=1e-12)
+
+
+def test_pack_zero_front_end_is_half_conv(oracle_mod):
+    """weight_om = 0, bias_om = 0: offset 0 and mask 1/2 everywhere, so the
+    output is half an ordinary convolution plus the bias."""
+    x, w_om, b_om, w, b, a = _pack_case(seed=8)
+    out, off, msk = oracle_mod.forward_pack(x.numpy(), np.zeros_like(w_om.numpy()), np.zeros_like(b_om.numpy()),
+                                            w.numpy(), b.numpy(), **a)
+    assert np.all(off == 0) and np.all(msk == 0.5)
+    ref = 0.5 * torch.nn.functional.conv2d(x, w, None, a["stride"], a["padding"], a["dilation"], a["group"]) \
+        + b[None, :, None, None]
+    np.testing.assert_allclose(out, ref.numpy(), rtol=0, atol=1e-12)
+
+
+def test_pack_mask_channels_follow_the_offset_channels(oracle_mod):
+    """Only the mask channel of tap k of deformable group 0 is switched on
+    (bias +40, every other mask channel -40, zero offset weights): the output
+    is the convolution restricted to that tap on group 0's input channels."""
+    x, w_om, b_om, w, b, a = _pack_case(seed=9, dg=2)
+    K = 9
+    w_om0 = np.zeros_like(w_om.numpy())
+    b_om0 = np.full(b_om.shape, -40.0)
+    b_om0[: 2 * 2 * K] = 0.0                   # offsets 0
+    k = 4
+    b_om0[2 * 2 * K + k] = 40.0                # mask of (group 0, tap k) ~ 1
+    out, off, msk = oracle_mod.forward_pack(x.numpy(), w_om0, b_om0, w.numpy(), None, **a)
+    wk = torch.zeros_like(w)
+    wk[:, : w.shape[1] // 2, k // 3, k % 3] = w[:, : w.shape[1] // 2, k // 3, k % 3]
+    ref = torch.nn.functional.conv2d(x, wk, None, a["stride"], a["padding"], a["dilation"], a["group"])
+    np.testing.assert_allclose(out, ref.numpy(), rtol=0, atol=1e-12)
