@@ -395,9 +395,9 @@ def run_ours(args, case, world, rank, local, dist):
         pack_ms = statistics.mean(a.elapsed_time(c) for a, c in pt)
         fe_flops = 2 * x.shape[0] * 3 * dg * K * off.shape[2] * off.shape[3] * Cin * K
         pack = {"ms_per_call": pack_ms, "tflops": (case.flops + fe_flops) / (pack_ms * 1e-3) / 1e12,
-                "front_end_flops": fe_flops, "launches": 4,
-                "call": "mdcn_forward_pack: front-end conv (fused kernel, plain) -> offset, sigmoid(mask); "
-                        "then the deformable convolution"}
+                "front_end_flops": fe_flops, "launches": 5,
+                "call": "mdcn_forward_pack: front-end conv (prep + fused kernel, plain), split into offset and "
+                        "sigmoid(mask), then the deformable convolution (prep or weight pack + fused kernel)"}
         del pws, p_out, poff, pmsk
     except Exception as e:  # context only
         log("pack form skipped:", e)

@@ -206,9 +206,10 @@ mdcn_status mdcn_forward_prepared(mdcn_handle handle, const void* offset, const 
  * spatial size floor((H + 2p - d(k-1) - 1)/s) + 1, else MDCN_ERR_SHAPE. All
  * pointers are device pointers (16-byte aligned); the workspace is at least
  * mdcn_pack_workspace_size bytes. Asynchronous on the stream: the front end is
- * the fused kernel run as a plain convolution with a two-output epilogue,
- * then the deformable convolution reads offset_out and mask_out (reusing the
- * workspace's channels-last x when its layout is the same). */
+ * the fused kernel run as a plain convolution into the workspace, a small
+ * kernel splits its output into offset_out and sigmoid(mask) in mask_out, then
+ * the deformable convolution reads them (reusing the workspace's channels-last
+ * x when its layout is the same). */
 mdcn_status mdcn_pack_workspace_size(mdcn_handle handle, const mdcn_dims* dims, mdcn_dtype dtype, size_t* bytes);
 mdcn_status mdcn_forward_pack(mdcn_handle handle, const void* x, const void* weight_om, const void* bias_om,
                               const void* weight, const void* bias_or_null, void* offset_out, void* mask_out,

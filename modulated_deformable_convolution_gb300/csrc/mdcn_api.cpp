@@ -520,6 +520,15 @@ mdcn_status mdcn_forward_host(mdcn_handle handle, const void* x_host, const void
     return MDCN_OK;
 }
 
+// The pack form's front end uses its own workspace and, after it, the buffer
+// of its raw output om [N, 3*dg*K, Ho, Wo]; the deformable convolution then
+// reuses the whole workspace.
+static size_t pack_front_bytes(const Plan& pf, mdcn_dtype dtype) {
+    const size_t elem = dtype == MDCN_F32 ? 4 : 2;
+    return align256(pf.ws_bytes) +
+           align256(static_cast<size_t>(pf.N) * static_cast<size_t>(pf.Cout) * static_cast<size_t>(pf.P) * elem);
+}
+
 mdcn_status mdcn_pack_workspace_size(mdcn_handle handle, const mdcn_dims* dims, mdcn_dtype dtype, size_t* bytes) {
     if (!handle || !dims || !bytes) return MDCN_ERR_NULL;
     mdcn_attrs fa;
@@ -531,7 +540,8 @@ mdcn_status mdcn_pack_workspace_size(mdcn_handle handle, const mdcn_dims* dims, 
     if (s != MDCN_OK) return s;
     s = make_plan(handle->attrs, handle->tuning, dims, dtype, &pd);
     if (s != MDCN_OK) return s;
-    *bytes = pf.ws_bytes > pd.ws_bytes ? pf.ws_bytes : pd.ws_bytes;
+    const size_t front = pack_front_bytes(pf, dtype);
+    *bytes = front > pd.ws_bytes ? front : pd.ws_bytes;
     return MDCN_OK;
 }
 
@@ -552,12 +562,15 @@ mdcn_status mdcn_forward_pack(mdcn_handle handle, const void* x, const void* wei
     if (s != MDCN_OK) return s;
     s = plan_for_call(handle, dims, dtype, workspace_bytes, &pd);
     if (s != MDCN_OK) return s;
+    if (workspace_bytes < pack_front_bytes(pf, dtype)) return MDCN_ERR_WORKSPACE;
     pf.plain = 1;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const int32_t split = static_cast<int32_t>(2 * pd.dg * pd.K);
-    // 1: offset and mask from the front end (one workspace, used in turn)
+    void* om = static_cast<uint8_t*>(workspace) + align256(pf.ws_bytes);
+    // 1: the front end's raw output, then offset and sigmoid(mask) from it
     cudaError_t e = mdcn::launch_prep_both(pf, x, weight_om, nullptr, 0, nullptr, 0, workspace, st);
-    if (e == cudaSuccess) e = mdcn::launch_fused(pf, nullptr, nullptr, bias_om, offset_out, workspace, st, mask_out, split);
+    if (e == cudaSuccess) e = mdcn::launch_fused(pf, nullptr, nullptr, bias_om, om, workspace, st);
+    if (e == cudaSuccess)
+        e = mdcn::launch_split_offset_mask(pf, om, offset_out, mask_out, 2 * pd.dg * pd.K, pd.dg * pd.K, st);
     // 2: the deformable convolution; when its channels-last x has the front
     // end's layout, the copy already in the workspace is reused
     const bool same_xt = pf.Cp == pd.Cp && pf.U == pd.U && pf.UP == pd.UP && pf.off_xt == pd.off_xt &&

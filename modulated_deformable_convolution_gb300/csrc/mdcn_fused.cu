@@ -72,11 +72,6 @@ struct FusedParams {
     float* part;           // fp32 partial accumulators of split tiles: one slot per CTA
     uint32_t* split_count;  // per split tile (by its first CTA): contributors' epilogue warps done
     int32_t epi_vec;        // the plan allows 16-byte output stores and out is 16-byte aligned
-    // two outputs (split_ch > 0): output channels [0, split_ch) go to out as
-    // [N, split_ch, Ho, Wo], the rest through the logistic sigmoid to out2 as
-    // [N, Cout - split_ch, Ho, Wo] (the offset/mask front end)
-    void* out2;
-    int32_t split_ch;
     Plan pl;
 };
 
@@ -309,13 +304,16 @@ __device__ __forceinline__ void sample_rows(const Plan& pl, const T* __restrict_
 #pragma unroll 1
     for (int32_t kb0 = 0; kb0 < ntap; kb0 += kSampleTaps) {
         float v[2][3][kSampleTaps];  // [row][dh, dw, mask][tap]
+        if (pl.plain) {
 #pragma unroll
-        for (int u = 0; u < kSampleTaps; ++u) {
-            const int64_t kb = kb0 + u < ntap ? kb0 + u : kb0;
-            if (pl.plain) {
+            for (int u = 0; u < kSampleTaps; ++u) {
                 v[0][0][u] = v[0][1][u] = v[1][0][u] = v[1][1][u] = 0.f;
                 v[0][2][u] = v[1][2][u] = 1.f;
-            } else {
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < kSampleTaps; ++u) {
+                const int64_t kb = kb0 + u < ntap ? kb0 + u : kb0;
                 v[0][0][u] = to_f(ra.po[(2 * kb) * P]);
                 v[0][1][u] = to_f(ra.po[(2 * kb + 1) * P]);
                 v[0][2][u] = to_f(ra.pm[kb * P]);
@@ -349,14 +347,17 @@ __device__ __forceinline__ void sample_row_taps(const Plan& pl, const T* __restr
     const int64_t P = pl.P;
     const SampleRow<T> r = sample_row_at(pl, offset, mask, mt, gd, row, tap0);
     float v[3][kSampleTaps];
+    if (pl.plain) {
 #pragma unroll
-    for (int u = 0; u < kSampleTaps; ++u) {
-        const int32_t kb0 = kb_first + u * kb_step;
-        const int64_t kb = kb0 < ntap ? kb0 : 0;
-        if (pl.plain) {
+        for (int u = 0; u < kSampleTaps; ++u) {
             v[0][u] = v[1][u] = 0.f;
             v[2][u] = 1.f;
-        } else {
+        }
+    } else {
+#pragma unroll
+        for (int u = 0; u < kSampleTaps; ++u) {
+            const int32_t kb0 = kb_first + u * kb_step;
+            const int64_t kb = kb0 < ntap ? kb0 : 0;
             v[0][u] = to_f(r.po[(2 * kb) * P]);
             v[1][u] = to_f(r.po[(2 * kb + 1) * P]);
             v[2][u] = to_f(r.pm[kb * P]);
@@ -595,9 +596,10 @@ __device__ __forceinline__ void stage_bias(const Plan& pl, const T* bias, const 
 
 // The group of 16 / sizeof(T) consecutive output pixels whose 16-byte
 // vectors this lane stores: group lane % (32 / that) of the 32 tile rows of
-// lane quarter `quarter`: its image and the index of its first pixel.
+// lane quarter `quarter`, and the output index of its first pixel in the
+// plane of the tile's first column.
 struct OutGroup {
-    int64_t n, hw;
+    int64_t base;
     bool valid;
 };
 
@@ -607,23 +609,9 @@ __device__ __forceinline__ OutGroup out_group(const Plan& pl, const TileId& id, 
     constexpr int kGroups = 32 / kVecPx;
     const Pixel gp = tile_pixel(pl, id.mt, quarter * 32 + (lane % kGroups) * kVecPx);
     OutGroup og;
-    og.n = gp.n;
-    og.hw = gp.ho * pl.Wo + gp.wo;
+    og.base = (gp.n * pl.Cout + static_cast<int64_t>(id.g) * pl.Og + id.nt * pl.acc_cols) * pl.P + gp.ho * pl.Wo + gp.wo;
     og.valid = gp.valid;
     return og;
-}
-
-// Where output channel ch (of all Cout) of pixel hw of image n goes: out
-// [N, Cout, Ho, Wo], or with a split, out [N, split, Ho, Wo] below the split
-// and out2 [N, Cout - split, Ho, Wo] from it.
-template <typename T>
-__device__ __forceinline__ T* out_elem(const Plan& pl, const FusedParams& prm, int64_t n, int64_t ch, int64_t hw) {
-    if (prm.split_ch > 0) {
-        const int64_t cs = prm.split_ch;
-        return ch < cs ? static_cast<T*>(prm.out) + (n * cs + ch) * pl.P + hw
-                       : static_cast<T*>(prm.out2) + (n * (pl.Cout - cs) + (ch - cs)) * pl.P + hw;
-    }
-    return static_cast<T*>(prm.out) + (n * pl.Cout + ch) * pl.P + hw;
 }
 
 // 16 output channels (accumulator columns c16..c16+15) of the warp's 32 rows:
@@ -637,16 +625,10 @@ __device__ __forceinline__ void store_chunk16(const Plan& pl, const FusedParams&
                                               uint32_t bias_s, uint32_t stg) {
     const int32_t ncol0 = id.nt * pl.acc_cols;
     if (ncol0 + c16 >= pl.Og) return;
-    const int64_t ch0 = static_cast<int64_t>(id.g) * pl.Og + ncol0 + c16;  // output channel of column c16
+    T* __restrict__ out = static_cast<T*>(prm.out);
     if (prm.bias) {
 #pragma unroll
         for (int e = 0; e < 16; ++e) vals[e] += ld_shared_f32(bias_s + 4u * (c16 + e));
-    }
-    if (prm.split_ch > 0) {
-        // the second output's channels: the logistic sigmoid
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-            if (ch0 + e >= prm.split_ch) vals[e] = 1.0f / (1.0f + expf(-vals[e]));
     }
 #pragma unroll
     for (int e = 0; e < 16; ++e) st_shared_elem<T>(stg + static_cast<uint32_t>((e * 32 + lane) * sizeof(T)), vals[e]);
@@ -659,15 +641,15 @@ __device__ __forceinline__ void store_chunk16(const Plan& pl, const FusedParams&
             const int e = lane / kGroups + k * (32 / kGroups);  // channel of the chunk
             const uint32_t src = stg + static_cast<uint32_t>((e * 32 + (lane % kGroups) * kVecPx) * sizeof(T));
             if (og.valid && ncol0 + c16 + e < pl.Og)
-                st_global_v4(out_elem<T>(pl, prm, og.n, ch0 + e, og.hw), ld_shared_v4(src));
+                st_global_v4(out + og.base + static_cast<int64_t>(c16 + e) * pl.P, ld_shared_v4(src));
         }
     } else {
         const Pixel px = tile_pixel(pl, id.mt, row);
         if (px.valid) {
-            const int64_t hw = px.ho * pl.Wo + px.wo;
+            T* o = out + (px.n * pl.Cout + static_cast<int64_t>(id.g) * pl.Og + ncol0 + c16) * pl.P +
+                   px.ho * pl.Wo + px.wo;
             for (int e = 0; e < 16 && ncol0 + c16 + e < pl.Og; ++e)
-                *out_elem<T>(pl, prm, px.n, ch0 + e, hw) =
-                    ld_shared_elem<T>(stg + static_cast<uint32_t>((e * 32 + lane) * sizeof(T)));
+                o[static_cast<int64_t>(e) * pl.P] = ld_shared_elem<T>(stg + static_cast<uint32_t>((e * 32 + lane) * sizeof(T)));
         }
     }
     __syncwarp();
@@ -1198,7 +1180,7 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
 
 template <int DT>
 cudaError_t launch_fused_t(const Plan& pl, const void* offset, const void* mask, const void* bias, void* out, void* ws,
-                           cudaStream_t st, void* out2, int32_t split_ch) {
+                           cudaStream_t st) {
     using T = typename Elem<DT>::T;
     uint8_t* base = static_cast<uint8_t*>(ws);
     const T* wp = reinterpret_cast<const T*>(base + pl.off_wp);
@@ -1222,12 +1204,7 @@ cudaError_t launch_fused_t(const Plan& pl, const void* offset, const void* mask,
     prm.status = reinterpret_cast<uint32_t*>(base);
     prm.part = reinterpret_cast<float*>(base + pl.off_part);
     prm.split_count = reinterpret_cast<uint32_t*>(base + kSplitCountOffset);
-    prm.out2 = out2;
-    prm.split_ch = split_ch;
-    prm.epi_vec = pl.epi_vec && (reinterpret_cast<uintptr_t>(out) & 15u) == 0 &&
-                          (split_ch == 0 || (reinterpret_cast<uintptr_t>(out2) & 15u) == 0)
-                      ? 1
-                      : 0;
+    prm.epi_vec = pl.epi_vec && (reinterpret_cast<uintptr_t>(out) & 15u) == 0 ? 1 : 0;
     prm.pl = pl;
     // launched dependent on the prep kernel: the prologue (barriers, tensor
     // memory, the first descriptor group) overlaps its tail
@@ -1272,11 +1249,11 @@ cudaError_t prepare_fused_attributes(int dtype, int smem_bytes) {
 }
 
 cudaError_t launch_fused(const Plan& pl, const void* offset, const void* mask, const void* bias, void* out, void* ws,
-                         cudaStream_t st, void* out2, int32_t split_ch) {
+                         cudaStream_t st) {
     switch (pl.dtype) {
-        case kF32: return launch_fused_t<kF32>(pl, offset, mask, bias, out, ws, st, out2, split_ch);
-        case kF16: return launch_fused_t<kF16>(pl, offset, mask, bias, out, ws, st, out2, split_ch);
-        default: return launch_fused_t<kBF16>(pl, offset, mask, bias, out, ws, st, out2, split_ch);
+        case kF32: return launch_fused_t<kF32>(pl, offset, mask, bias, out, ws, st);
+        case kF16: return launch_fused_t<kF16>(pl, offset, mask, bias, out, ws, st);
+        default: return launch_fused_t<kBF16>(pl, offset, mask, bias, out, ws, st);
     }
 }
 

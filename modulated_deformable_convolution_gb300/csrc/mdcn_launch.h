@@ -18,12 +18,18 @@ cudaError_t launch_prep_both(const Plan& pl, const void* x, const void* weight, 
 
 // The fused sampling + gather + contraction + bias kernel (reads offset, mask
 // and the two workspace products of launch_prep_input and
-// launch_pack_weight); tiles split between CTAs are finished inside it.
-// With split_ch > 0 output channels [0, split_ch) go to out and the rest,
-// through the logistic sigmoid, to out2 (both NCHW with their own channel
-// counts). A plan with pl.plain set reads no offset or mask.
+// launch_pack_weight); tiles split between CTAs are finished inside it. A
+// plan with pl.plain set is an ordinary convolution and reads no offset or
+// mask (both may be null).
 cudaError_t launch_fused(const Plan& pl, const void* offset, const void* mask, const void* bias, void* out, void* ws,
-                         cudaStream_t st, void* out2 = nullptr, int32_t split_ch = 0);
+                         cudaStream_t st);
+
+// The pack form's split of the front end's output om [N, c_off + c_mask, P]
+// (P = pl.P, N = pl.N, dtype = pl.dtype): channels [0, c_off) copied to offset
+// [N, c_off, P], channels [c_off, c_off + c_mask) through the logistic sigmoid
+// to mask [N, c_mask, P].
+cudaError_t launch_split_offset_mask(const Plan& pl, const void* om, void* offset, void* mask, int64_t c_off,
+                                     int64_t c_mask, cudaStream_t st);
 
 // Dynamic shared memory the fused kernel may use on this device (set once).
 cudaError_t prepare_fused_attributes(int dtype, int smem_bytes);

@@ -354,6 +354,66 @@ static cudaError_t prep_both_t(const Plan& pl, const void* x, const void* weight
     return cudaGetLastError();
 }
 
+namespace {
+
+template <typename T>
+__device__ __forceinline__ T store_of(float v);
+template <>
+__device__ __forceinline__ float store_of<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ __half store_of<__half>(float v) { return __float2half_rn(v); }
+template <>
+__device__ __forceinline__ __nv_bfloat16 store_of<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+
+// Grid (x over each plane's P elements, 4 per thread; y over the planes
+// n * (c_off + c_mask) + c, looping past the grid): a plane below c_off is
+// copied to the offset, a plane from c_off goes through the logistic
+// sigmoid (fp32) into the mask.
+template <typename T>
+__global__ void __launch_bounds__(256) split_offset_mask_kernel(const T* __restrict__ om, T* __restrict__ offset,
+                                                                T* __restrict__ mask, int64_t planes, int64_t c_off,
+                                                                int64_t c_mask, int64_t P) {
+    const int64_t ct = c_off + c_mask;
+    for (int64_t pl = blockIdx.y; pl < planes; pl += gridDim.y) {
+        const int64_t n = pl / ct, c = pl - n * ct;
+        const T* src = om + pl * P;
+        T* dst = c < c_off ? offset + (n * c_off + c) * P : mask + (n * c_mask + (c - c_off)) * P;
+        const bool sig = c >= c_off;
+        for (int64_t i = (static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x) * 4; i < P;
+             i += static_cast<int64_t>(gridDim.x) * 256 * 4) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                if (i + k < P) {
+                    const T v = src[i + k];
+                    dst[i + k] = sig ? store_of<T>(1.0f / (1.0f + expf(-load_f<T>(&v)))) : v;
+                }
+            }
+        }
+    }
+}
+
+template <typename T>
+cudaError_t split_t(const Plan& pl, const void* om, void* offset, void* mask, int64_t c_off, int64_t c_mask,
+                    cudaStream_t st) {
+    const int64_t planes = pl.N * (c_off + c_mask);
+    const int64_t gx = (pl.P + 1023) / 1024;
+    const unsigned gy = static_cast<unsigned>(planes < 65535 ? planes : 65535);
+    split_offset_mask_kernel<T><<<dim3(static_cast<unsigned>(gx < 1024 ? gx : 1024), gy), 256, 0, st>>>(
+        static_cast<const T*>(om), static_cast<T*>(offset), static_cast<T*>(mask), planes, c_off, c_mask, pl.P);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_split_offset_mask(const Plan& pl, const void* om, void* offset, void* mask, int64_t c_off,
+                                     int64_t c_mask, cudaStream_t st) {
+    switch (pl.dtype) {
+        case kF32: return split_t<float>(pl, om, offset, mask, c_off, c_mask, st);
+        case kF16: return split_t<__half>(pl, om, offset, mask, c_off, c_mask, st);
+        default: return split_t<__nv_bfloat16>(pl, om, offset, mask, c_off, c_mask, st);
+    }
+}
+
 cudaError_t launch_prep_both(const Plan& pl, const void* x, const void* weight, const void* offset,
                              size_t offset_bytes, const void* mask, size_t mask_bytes, void* ws, cudaStream_t st) {
     // line counts fit 32 bits for any offset/mask below 512 GB
