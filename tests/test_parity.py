@@ -7,6 +7,7 @@ consumes the inputs already rounded to the I/O dtype, widened exactly to
 float64. Informational columns (printed): the per-element relative error
 |gpu - ref| / max(|ref|, 1e-6) (max, mean, share above 1e-5).
 """
+import ctypes
 import dataclasses
 
 import numpy as np
@@ -247,3 +248,36 @@ def test_wait_timeout_selftest_then_gpu_still_works():
     inp = make_inputs(case)
     out = gpu_out(case, inp)
     assert torch.isfinite(out).all()
+
+
+def test_rejected_calls_leave_out_untouched():
+    """Calls that fail validation on real device buffers (workspace too small,
+    a misaligned pointer, dims that break a binding) return their error and
+    launch nothing: the canary in out survives."""
+    case = CONFIGS["neck_f16"]
+    dev = torch.device("cuda", 0)
+    d = {k: (None if v is None else v.to(dev)) for k, v in make_inputs(case).items()}
+    h = mdcn.Handle(**case.attrs())
+    x, off, m, w = d["x"], d["offset"], d["mask"], d["weight"]
+    dims = mdcn.make_dims(x.shape, off.shape, m.shape, w.shape, 0)
+    nbytes = mdcn.mdcn_workspace_size(h, x, off, m, w, None)
+    ws = torch.zeros(nbytes + 64, dtype=torch.uint8, device=dev)
+    out = torch.full(mdcn.mdcn_output_dims(h, x, off, m, w, None), 7.0, dtype=x.dtype, device=dev)
+    lib = mdcn._lib()
+    vp = lambda t, add=0: ctypes.c_void_p(t.data_ptr() + add)
+    st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+    def fwd(out_add=0, ws_bytes=nbytes, dd=dims):
+        return lib.mdcn_forward(h.value, vp(x), vp(off), vp(m), vp(w), None, vp(out, out_add), vp(ws), ws_bytes,
+                                ctypes.byref(dd), mdcn._abi.MDCN_F16, st)
+
+    assert fwd(ws_bytes=nbytes - 256) == mdcn.MDCN_ERR_WORKSPACE
+    assert fwd(out_add=2) == mdcn._abi.MDCN_ERR_ALIGN
+    bad = mdcn.make_dims(x.shape, off.shape, m.shape, w.shape, 0)
+    bad.mask[1] = 4
+    assert fwd(dd=bad) == mdcn._abi.MDCN_ERR_SHAPE
+    torch.cuda.synchronize()
+    assert torch.all(out == 7.0)
+    assert fwd() == mdcn.MDCN_OK  # and the same buffers work
+    torch.cuda.synchronize()
+    assert not torch.all(out == 7.0)
