@@ -11,6 +11,12 @@ module compiles it with gcc, checks arguments the way the page's plugin does
 (section 2 shape rule, section 3 attribute ranges, section 4 dimension
 bindings) and marshals numpy float64 arrays.
 
+``backward`` gives the gradients of the same definition (the pages have no
+backward; the reading is stated in the C source), pinned in
+``tests/test_oracle_backward.py`` by finite differences of the forward,
+adjoint identities, the ordinary-convolution special case and hand-worked
+slopes.
+
 Parity status: every part of the definition is pinned by tests in
 ``tests/test_oracle.py`` (ordinary and shifted convolution, hand-computed
 bilinear values, mask and deformable-group invariants, a zero-extended
@@ -52,6 +58,8 @@ def load_library(path: str):
     i64 = ctypes.c_int64
     lib.mdcn_oracle_forward_f64.argtypes = [p, p, p, p, p, p] + [i64] * 19 + [ctypes.c_int]
     lib.mdcn_oracle_forward_f64.restype = ctypes.c_int
+    lib.mdcn_oracle_backward_f64.argtypes = [p] * 10 + [i64] * 17 + [ctypes.c_int]
+    lib.mdcn_oracle_backward_f64.restype = ctypes.c_int
     lib.mdcn_oracle_num_threads.argtypes = []
     lib.mdcn_oracle_num_threads.restype = ctypes.c_int
     return lib
@@ -212,3 +220,41 @@ def forward_pack(x, weight_om, bias_om, weight, bias=None, stride=1, padding=0, 
     out = forward(x, offset, mask, weight, bias, stride, padding, dilation, group, deformable_group,
                   nthreads=nthreads)
     return out, offset, mask
+
+
+def backward(x, offset, mask, weight, grad_out, stride=1, padding=0, dilation=1, group=1, deformable_group=1,
+             with_bias=True, nthreads: int = 0, library=None):
+    """Oracle backward: the gradients of sum(grad_out * forward(...)) with
+    respect to x, offset, mask, weight and (if ``with_bias``) the bias.
+
+    The pages describe the forward only; this is the gradient of that
+    definition (the one-sided derivative on cell edges, 0 outside the
+    sampling range; the reading is spelled out in ``mdcn_oracle.c``).
+    Returns a dict of float64 arrays with the shapes of the inputs; the bias
+    gradient is None when ``with_bias`` is false."""
+    stride, padding, dilation, group, deformable_group = check_attrs(
+        stride, padding, dilation, group, deformable_group)
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    offset = np.ascontiguousarray(offset, dtype=np.float64)
+    mask = np.ascontiguousarray(mask, dtype=np.float64)
+    weight = np.ascontiguousarray(weight, dtype=np.float64)
+    grad_out = np.ascontiguousarray(grad_out, dtype=np.float64)
+    shape = output_shape(x.shape, offset.shape, mask.shape, weight.shape, None, deformable_group, group)
+    if tuple(grad_out.shape) != tuple(shape):
+        raise ValueError(f"grad_out must have the output's shape {shape}")
+    N, Cin, H, W = x.shape
+    Cout, _, kh, kw = weight.shape
+    Ho, Wo = shape[2], shape[3]
+    g = {"x": np.zeros_like(x), "offset": np.zeros_like(offset), "mask": np.zeros_like(mask),
+         "weight": np.zeros_like(weight), "bias": np.zeros(Cout) if with_bias else None}
+    lib = library if library is not None else _load()
+    ptr = lambda arr: None if arr is None else arr.ctypes.data_as(ctypes.c_void_p)
+    rc = lib.mdcn_oracle_backward_f64(
+        ptr(x), ptr(offset), ptr(mask), ptr(weight), ptr(grad_out),
+        ptr(g["x"]), ptr(g["offset"]), ptr(g["mask"]), ptr(g["weight"]), ptr(g["bias"]),
+        N, Cin, H, W, Cout, kh, kw, Ho, Wo,
+        stride[0], stride[1], padding[0], padding[1], dilation[0], dilation[1],
+        group, deformable_group, int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"oracle backward failed with code {rc}")
+    return g

@@ -179,3 +179,233 @@ int mdcn_oracle_forward_f64(const double* x, const double* offset, const double*
     }
     return failed ? ORACLE_NO_MEMORY : ORACLE_OK;
 }
+
+/*
+ * Backward pass: the gradients of L = sum(grad_out * out) with respect to x,
+ * offset, mask, weight and bias, where out is the forward pass above. The
+ * page describes the forward only; the gradient is that of the forward's
+ * definition, read as follows (each point is pinned by a test):
+ *   - inside the open range (-1, H) x (-1, W) the sample is the bilinear
+ *     interpolation of the zero-extended image over the cell whose corner is
+ *     (floor h, floor w), so its derivatives are those of that cell's
+ *     bilinear polynomial (the one-sided derivative where h or w is an
+ *     integer); outside the open range the sample and all of its derivatives
+ *     are 0, as the forward's range test gives;
+ *   - the sample enters the output as weight * mask * sample, so with
+ *     G = sum over the group's output channels of weight * grad_out (the
+ *     gradient of the modulated column element) the chain rule gives
+ *       grad_mask   += G * sample,
+ *       grad_offset += G * mask * (d sample / dh, d sample / dw),
+ *       grad_x      += G * mask * corner weight   (in-image corners only),
+ *       grad_weight += grad_out * mask * sample,
+ *       grad_bias    = sum of grad_out over n, ho, wo.
+ * Four plain passes, each parallel over an index that owns what it writes:
+ * the modulated columns and their gradients per (n, ho); grad_x per (n, c);
+ * grad_offset and grad_mask per (n, ho); grad_weight per output channel.
+ */
+
+/* Corner weights and derivatives of one sampling point, in the cell of
+ * (floor h, floor w). inside = 0 outside the open range. */
+typedef struct {
+    int inside;
+    int64_t h0, w0;
+    double lh, lw;
+} cell_t;
+
+static cell_t cell_of(int64_t H, int64_t W, double h, double w)
+{
+    cell_t c;
+    c.inside = !(h <= -1.0 || h >= (double)H || w <= -1.0 || w >= (double)W);
+    const double h0f = floor(h), w0f = floor(w);
+    c.h0 = (int64_t)h0f;
+    c.w0 = (int64_t)w0f;
+    c.lh = h - h0f;
+    c.lw = w - w0f;
+    return c;
+}
+
+static double pixel_or_zero(const double* plane, int64_t H, int64_t W, int64_t y, int64_t xx)
+{
+    return (y < 0 || y >= H || xx < 0 || xx >= W) ? 0.0 : plane[y * W + xx];
+}
+
+/* Sample and its derivatives d/dh, d/dw at one point. */
+static void sample_and_slopes(const double* plane, int64_t H, int64_t W, double h, double w,
+                              double* v, double* dvdh, double* dvdw)
+{
+    const cell_t c = cell_of(H, W, h, w);
+    *v = 0.0;
+    *dvdh = 0.0;
+    *dvdw = 0.0;
+    if (!c.inside) return;
+    for (int dy = 0; dy < 2; ++dy) {
+        for (int dx = 0; dx < 2; ++dx) {
+            const double X = pixel_or_zero(plane, H, W, c.h0 + dy, c.w0 + dx);
+            const double wy = dy ? c.lh : 1.0 - c.lh;
+            const double wx = dx ? c.lw : 1.0 - c.lw;
+            *v += wy * wx * X;
+            *dvdh += (dy ? 1.0 : -1.0) * wx * X;
+            *dvdw += (dx ? 1.0 : -1.0) * wy * X;
+        }
+    }
+}
+
+int mdcn_oracle_backward_f64(const double* x, const double* offset, const double* mask,
+                             const double* weight, const double* grad_out,
+                             double* grad_x, double* grad_offset, double* grad_mask,
+                             double* grad_weight, double* grad_bias,
+                             int64_t N, int64_t Cin, int64_t H, int64_t W,
+                             int64_t Cout, int64_t kh, int64_t kw, int64_t Ho, int64_t Wo,
+                             int64_t stride_h, int64_t stride_w, int64_t pad_h, int64_t pad_w,
+                             int64_t dil_h, int64_t dil_w, int64_t group, int64_t deformable_group,
+                             int nthreads)
+{
+    if (!x || !offset || !mask || !weight || !grad_out || !grad_x || !grad_offset || !grad_mask || !grad_weight)
+        return ORACLE_BAD_ARG;
+    if (N < 1 || Cin < 1 || H < 1 || W < 1 || Cout < 1 || kh < 1 || kw < 1 || Ho < 1 || Wo < 1)
+        return ORACLE_BAD_ARG;
+    if (stride_h < 1 || stride_w < 1 || dil_h < 1 || dil_w < 1 || pad_h < 0 || pad_w < 0)
+        return ORACLE_BAD_ARG;
+    if (group < 1 || deformable_group < 1) return ORACLE_BAD_ARG;
+    if (Cin % group || Cout % group || Cin % deformable_group) return ORACLE_BAD_ARG;
+
+    const int64_t K = kh * kw, Cg = Cin / group, Og = Cout / group, Cd = Cin / deformable_group;
+    const int64_t P = Ho * Wo, dg = deformable_group;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    /* col[n][c][k][p] = mask * sample; gcol[n][c][k][p] = G */
+    const size_t cells = (size_t)(N * Cin * K * P);
+    double* col = (double*)malloc(cells * sizeof(double));
+    double* gcol = (double*)malloc(cells * sizeof(double));
+    if (!col || !gcol) {
+        free(col);
+        free(gcol);
+        return ORACLE_NO_MEMORY;
+    }
+#define OFF_H(n, gd, k, p) offset[((n) * 2 * dg * K + (gd) * 2 * K + 2 * (k)) * P + (p)]
+#define OFF_W(n, gd, k, p) offset[((n) * 2 * dg * K + (gd) * 2 * K + 2 * (k) + 1) * P + (p)]
+#define MASK(n, gd, k, p) mask[((n) * dg * K + (gd) * K + (k)) * P + (p)]
+
+    /* pass 1: the modulated columns and their gradients G */
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t t = 0; t < N * Ho; ++t) {
+        const int64_t n = t / Ho, ho = t % Ho;
+        for (int64_t wo = 0; wo < Wo; ++wo) {
+            const int64_t p = ho * Wo + wo;
+            for (int64_t c = 0; c < Cin; ++c) {
+                const int64_t gd = c / Cd, g = c / Cg, cl = c - g * Cg;
+                const double* plane = x + (n * Cin + c) * H * W;
+                for (int64_t i = 0; i < kh; ++i) {
+                    for (int64_t j = 0; j < kw; ++j) {
+                        const int64_t k = i * kw + j;
+                        const double h = (double)(ho * stride_h - pad_h + i * dil_h) + OFF_H(n, gd, k, p);
+                        const double w = (double)(wo * stride_w - pad_w + j * dil_w) + OFF_W(n, gd, k, p);
+                        double v, dvdh, dvdw;
+                        sample_and_slopes(plane, H, W, h, w, &v, &dvdh, &dvdw);
+                        double G = 0.0;
+                        for (int64_t o = g * Og; o < (g + 1) * Og; ++o)
+                            G += weight[(o * Cg + cl) * K + k] * grad_out[(n * Cout + o) * P + p];
+                        const size_t e = (size_t)(((n * Cin + c) * K + k) * P + p);
+                        col[e] = MASK(n, gd, k, p) * v;
+                        gcol[e] = G;
+                    }
+                }
+            }
+        }
+    }
+
+    /* pass 2: grad_x, the corner weights times mask times G, per (n, c) */
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t t = 0; t < N * Cin; ++t) {
+        const int64_t n = t / Cin, c = t % Cin, gd = c / Cd;
+        double* gplane = grad_x + (n * Cin + c) * H * W;
+        for (int64_t e = 0; e < H * W; ++e) gplane[e] = 0.0;
+        for (int64_t ho = 0; ho < Ho; ++ho) {
+            for (int64_t wo = 0; wo < Wo; ++wo) {
+                const int64_t p = ho * Wo + wo;
+                for (int64_t i = 0; i < kh; ++i) {
+                    for (int64_t j = 0; j < kw; ++j) {
+                        const int64_t k = i * kw + j;
+                        const double h = (double)(ho * stride_h - pad_h + i * dil_h) + OFF_H(n, gd, k, p);
+                        const double w = (double)(wo * stride_w - pad_w + j * dil_w) + OFF_W(n, gd, k, p);
+                        const cell_t cc = cell_of(H, W, h, w);
+                        if (!cc.inside) continue;
+                        const double gm = gcol[((n * Cin + c) * K + k) * P + p] * MASK(n, gd, k, p);
+                        for (int dy = 0; dy < 2; ++dy) {
+                            for (int dx = 0; dx < 2; ++dx) {
+                                const int64_t y = cc.h0 + dy, xx = cc.w0 + dx;
+                                if (!(y >= 0 && y < H && xx >= 0 && xx < W)) continue; /* corner off the image */
+                                const double wy = dy ? cc.lh : 1.0 - cc.lh;
+                                const double wx = dx ? cc.lw : 1.0 - cc.lw;
+                                gplane[y * W + xx] += gm * wy * wx;
+                            }
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    /* pass 3: grad_offset and grad_mask, summed over the deformable group's
+     * channels, per (n, ho) */
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t t = 0; t < N * Ho; ++t) {
+        const int64_t n = t / Ho, ho = t % Ho;
+        for (int64_t wo = 0; wo < Wo; ++wo) {
+            const int64_t p = ho * Wo + wo;
+            for (int64_t gd = 0; gd < dg; ++gd) {
+                for (int64_t i = 0; i < kh; ++i) {
+                    for (int64_t j = 0; j < kw; ++j) {
+                        const int64_t k = i * kw + j;
+                        const double h = (double)(ho * stride_h - pad_h + i * dil_h) + OFF_H(n, gd, k, p);
+                        const double w = (double)(wo * stride_w - pad_w + j * dil_w) + OFF_W(n, gd, k, p);
+                        const double m = MASK(n, gd, k, p);
+                        double s_mask = 0.0, s_h = 0.0, s_w = 0.0;
+                        for (int64_t c = gd * Cd; c < (gd + 1) * Cd; ++c) {
+                            double v, dvdh, dvdw;
+                            sample_and_slopes(x + (n * Cin + c) * H * W, H, W, h, w, &v, &dvdh, &dvdw);
+                            const double G = gcol[((n * Cin + c) * K + k) * P + p];
+                            s_mask += G * v;
+                            s_h += G * m * dvdh;
+                            s_w += G * m * dvdw;
+                        }
+                        grad_mask[((n * dg + gd) * K + k) * P + p] = s_mask;
+                        grad_offset[((n * 2 * dg + gd * 2) * K + 2 * k) * P + p] = s_h;
+                        grad_offset[((n * 2 * dg + gd * 2) * K + 2 * k + 1) * P + p] = s_w;
+                    }
+                }
+            }
+        }
+    }
+
+    /* pass 4: grad_weight per output channel, grad_bias */
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t o = 0; o < Cout; ++o) {
+        const int64_t g = o / Og;
+        for (int64_t cl = 0; cl < Cg; ++cl) {
+            const int64_t c = g * Cg + cl;
+            for (int64_t k = 0; k < K; ++k) {
+                double s = 0.0;
+                for (int64_t n = 0; n < N; ++n)
+                    for (int64_t p = 0; p < P; ++p)
+                        s += grad_out[(n * Cout + o) * P + p] * col[((n * Cin + c) * K + k) * P + p];
+                grad_weight[(o * Cg + cl) * K + k] = s;
+            }
+        }
+        if (grad_bias) {
+            double s = 0.0;
+            for (int64_t n = 0; n < N; ++n)
+                for (int64_t p = 0; p < P; ++p) s += grad_out[(n * Cout + o) * P + p];
+            grad_bias[o] = s;
+        }
+    }
+#undef OFF_H
+#undef OFF_W
+#undef MASK
+    free(col);
+    free(gcol);
+    return ORACLE_OK;
+}
