@@ -58,7 +58,7 @@ def load_library(path: str):
     i64 = ctypes.c_int64
     lib.mdcn_oracle_forward_f64.argtypes = [p, p, p, p, p, p] + [i64] * 19 + [ctypes.c_int]
     lib.mdcn_oracle_forward_f64.restype = ctypes.c_int
-    lib.mdcn_oracle_backward_f64.argtypes = [p] * 10 + [i64] * 17 + [ctypes.c_int]
+    lib.mdcn_oracle_backward_f64.argtypes = [p] * 10 + [i64] * 17 + [ctypes.c_int, ctypes.c_int]
     lib.mdcn_oracle_backward_f64.restype = ctypes.c_int
     lib.mdcn_oracle_num_threads.argtypes = []
     lib.mdcn_oracle_num_threads.restype = ctypes.c_int
@@ -223,7 +223,7 @@ def forward_pack(x, weight_om, bias_om, weight, bias=None, stride=1, padding=0, 
 
 
 def backward(x, offset, mask, weight, grad_out, stride=1, padding=0, dilation=1, group=1, deformable_group=1,
-             with_bias=True, nthreads: int = 0, library=None):
+             with_bias=True, positions: str = "f64", nthreads: int = 0, library=None):
     """Oracle backward: the gradients of sum(grad_out * forward(...)) with
     respect to x, offset, mask, weight and (if ``with_bias``) the bias.
 
@@ -231,7 +231,15 @@ def backward(x, offset, mask, weight, grad_out, stride=1, padding=0, dilation=1,
     definition (the one-sided derivative on cell edges, 0 outside the
     sampling range; the reading is spelled out in ``mdcn_oracle.c``).
     Returns a dict of float64 arrays with the shapes of the inputs; the bias
-    gradient is None when ``with_bias`` is false."""
+    gradient is None when ``with_bias`` is false.
+
+    ``positions``: "f64" forms each sampling position exactly (the gradient of
+    the forward); "f32" rounds anchor + offset to fp32 first, as the kernels
+    do, so that the cell (a floor, across which the slope jumps) is decided
+    in the kernels' precision. Only positions within half an fp32 ulp of a
+    cell edge differ."""
+    if positions not in ("f64", "f32"):
+        raise ValueError("positions must be 'f64' or 'f32'")
     stride, padding, dilation, group, deformable_group = check_attrs(
         stride, padding, dilation, group, deformable_group)
     x = np.ascontiguousarray(x, dtype=np.float64)
@@ -254,7 +262,7 @@ def backward(x, offset, mask, weight, grad_out, stride=1, padding=0, dilation=1,
         ptr(g["x"]), ptr(g["offset"]), ptr(g["mask"]), ptr(g["weight"]), ptr(g["bias"]),
         N, Cin, H, W, Cout, kh, kw, Ho, Wo,
         stride[0], stride[1], padding[0], padding[1], dilation[0], dilation[1],
-        group, deformable_group, int(nthreads))
+        group, deformable_group, int(positions == "f32"), int(nthreads))
     if rc != 0:
         raise RuntimeError(f"oracle backward failed with code {rc}")
     return g

@@ -191,6 +191,14 @@ int mdcn_oracle_forward_f64(const double* x, const double* offset, const double*
  *     bilinear polynomial (the one-sided derivative where h or w is an
  *     integer); outside the open range the sample and all of its derivatives
  *     are 0, as the forward's range test gives;
+ *   - the cell is an integer decision (floor of the position), and the slope
+ *     jumps across a cell edge. With positions_f32 = 0 the position is exact
+ *     (double): the gradient of the forward above. With positions_f32 = 1 it
+ *     is formed as the kernels form it (the integer anchor plus the offset,
+ *     rounded to fp32) before its cell and fractions are taken, so that both
+ *     sides take the cell decision in the same precision: a position within
+ *     half an fp32 ulp of an edge (e.g. anchor 38 plus offset -1.4e-6) then
+ *     lands on the edge and takes the right-hand slope;
  *   - the sample enters the output as weight * mask * sample, so with
  *     G = sum over the group's output channels of weight * grad_out (the
  *     gradient of the modulated column element) the chain rule gives
@@ -203,6 +211,14 @@ int mdcn_oracle_forward_f64(const double* x, const double* offset, const double*
  * the modulated columns and their gradients per (n, ho); grad_x per (n, c);
  * grad_offset and grad_mask per (n, ho); grad_weight per output channel.
  */
+
+/* Sampling position anchor + offset: exact, or rounded to fp32 as the
+ * kernels form it. */
+static double position(int64_t anchor, double offset, int f32)
+{
+    const double v = (double)anchor + offset;
+    return f32 ? (double)(float)v : v;
+}
 
 /* Corner weights and derivatives of one sampling point, in the cell of
  * (floor h, floor w). inside = 0 outside the open range. */
@@ -258,7 +274,7 @@ int mdcn_oracle_backward_f64(const double* x, const double* offset, const double
                              int64_t Cout, int64_t kh, int64_t kw, int64_t Ho, int64_t Wo,
                              int64_t stride_h, int64_t stride_w, int64_t pad_h, int64_t pad_w,
                              int64_t dil_h, int64_t dil_w, int64_t group, int64_t deformable_group,
-                             int nthreads)
+                             int positions_f32, int nthreads)
 {
     if (!x || !offset || !mask || !weight || !grad_out || !grad_x || !grad_offset || !grad_mask || !grad_weight)
         return ORACLE_BAD_ARG;
@@ -301,8 +317,8 @@ int mdcn_oracle_backward_f64(const double* x, const double* offset, const double
                 for (int64_t i = 0; i < kh; ++i) {
                     for (int64_t j = 0; j < kw; ++j) {
                         const int64_t k = i * kw + j;
-                        const double h = (double)(ho * stride_h - pad_h + i * dil_h) + OFF_H(n, gd, k, p);
-                        const double w = (double)(wo * stride_w - pad_w + j * dil_w) + OFF_W(n, gd, k, p);
+                        const double h = position(ho * stride_h - pad_h + i * dil_h, OFF_H(n, gd, k, p), positions_f32);
+                        const double w = position(wo * stride_w - pad_w + j * dil_w, OFF_W(n, gd, k, p), positions_f32);
                         double v, dvdh, dvdw;
                         sample_and_slopes(plane, H, W, h, w, &v, &dvdh, &dvdw);
                         double G = 0.0;
@@ -329,8 +345,8 @@ int mdcn_oracle_backward_f64(const double* x, const double* offset, const double
                 for (int64_t i = 0; i < kh; ++i) {
                     for (int64_t j = 0; j < kw; ++j) {
                         const int64_t k = i * kw + j;
-                        const double h = (double)(ho * stride_h - pad_h + i * dil_h) + OFF_H(n, gd, k, p);
-                        const double w = (double)(wo * stride_w - pad_w + j * dil_w) + OFF_W(n, gd, k, p);
+                        const double h = position(ho * stride_h - pad_h + i * dil_h, OFF_H(n, gd, k, p), positions_f32);
+                        const double w = position(wo * stride_w - pad_w + j * dil_w, OFF_W(n, gd, k, p), positions_f32);
                         const cell_t cc = cell_of(H, W, h, w);
                         if (!cc.inside) continue;
                         const double gm = gcol[((n * Cin + c) * K + k) * P + p] * MASK(n, gd, k, p);
@@ -360,8 +376,8 @@ int mdcn_oracle_backward_f64(const double* x, const double* offset, const double
                 for (int64_t i = 0; i < kh; ++i) {
                     for (int64_t j = 0; j < kw; ++j) {
                         const int64_t k = i * kw + j;
-                        const double h = (double)(ho * stride_h - pad_h + i * dil_h) + OFF_H(n, gd, k, p);
-                        const double w = (double)(wo * stride_w - pad_w + j * dil_w) + OFF_W(n, gd, k, p);
+                        const double h = position(ho * stride_h - pad_h + i * dil_h, OFF_H(n, gd, k, p), positions_f32);
+                        const double w = position(wo * stride_w - pad_w + j * dil_w, OFF_W(n, gd, k, p), positions_f32);
                         const double m = MASK(n, gd, k, p);
                         double s_mask = 0.0, s_h = 0.0, s_w = 0.0;
                         for (int64_t c = gd * Cd; c < (gd + 1) * Cd; ++c) {

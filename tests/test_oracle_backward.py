@@ -281,3 +281,53 @@ def test_planted_backward_slip_is_caught(oracle_mod, name, tmp_path):
                     str(cpath), "-lm"], check=True)
     lib = oracle_mod.load_library(str(so))
     assert backward_pins(oracle_mod, lib), f"planted slip {name} passed every pin"
+
+
+# ---------------------------------------------------------- fp32 positions (the kernels' cell decision)
+def test_b6_fp32_positions_agree_away_from_edges(oracle_mod):
+    """positions="f32" only rounds anchor + offset to fp32: away from cell
+    edges it matches finite differences of the forward to fp32 position
+    rounding, and on the hand-worked cases (positions exact in fp32) it is
+    identical to the exact gradient."""
+    rng = np.random.default_rng(600)
+    c = make_case(rng, GEOMS[1])
+    g32 = oracle_mod.backward(c["x"], c["offset"], c["mask"], c["weight"], c["grad_out"], positions="f32",
+                              **c["attrs"])
+    g64 = grads(oracle_mod, c)
+    for name in ("x", "offset", "mask", "weight", "bias"):
+        assert np.abs(g32[name] - g64[name]).max() <= 1e-5 * np.abs(g64[name]).max(), name
+    assert fd_check(oracle_mod, c, g32, "offset", range(0, c["offset"].size, 5), 0.05) < 1e-5
+    gold = golden_slopes()
+    x = np.array(gold["x"], dtype=np.float64)[None, None]
+    for case in gold["cases"]:
+        off = np.zeros((1, 2, 2, 2))
+        off[0, 0, case["ho"], case["wo"]], off[0, 1, case["ho"], case["wo"]] = case["dh"], case["dw"]
+        msk = np.full((1, 1, 2, 2), case["mask"])
+        go = np.ones((1, 1, 2, 2))
+        a = oracle_mod.backward(x, off, msk, np.ones((1, 1, 1, 1)), go, positions="f32")
+        b = oracle_mod.backward(x, off, msk, np.ones((1, 1, 1, 1)), go)
+        for name in a:
+            assert np.array_equal(a[name], b[name]), name
+
+
+def test_b7_fp32_position_on_a_cell_edge(oracle_mod):
+    """Hand-worked: x[y, 0] = y^2 on a 40 x 2 plane, 1x1 weight 1, output pixel
+    (38, 0) with offset (-1.4e-6, 0). Exactly, h = 37.9999986 lies in cell 37,
+    slope X(38) - X(37) = 1444 - 1369 = 75; in fp32, 38 - 1.4e-6 rounds to 38.0
+    (half an ulp there is 1.9e-6), the right-hand slope X(39) - X(38) = 1521 -
+    1444 = 77. Both are scaled by the mask 0.5."""
+    H, W = 40, 2
+    x = np.zeros((1, 1, H, W))
+    x[0, 0, :, 0] = np.arange(H, dtype=np.float64) ** 2
+    off = np.zeros((1, 2, H, W))
+    off[0, 0, 38, 0] = -1.4e-6
+    msk = np.full((1, 1, H, W), 0.5)
+    go = np.zeros((1, 1, H, W))
+    go[0, 0, 38, 0] = 1.0
+    g64 = oracle_mod.backward(x, off, msk, np.ones((1, 1, 1, 1)), go)
+    g32 = oracle_mod.backward(x, off, msk, np.ones((1, 1, 1, 1)), go, positions="f32")
+    assert abs(g64["offset"][0, 0, 38, 0] - 0.5 * 75.0) < 1e-9
+    assert abs(g32["offset"][0, 0, 38, 0] - 0.5 * 77.0) < 1e-12
+    assert abs(g32["mask"][0, 0, 38, 0] - 1444.0) < 1e-12  # the sample at h = 38 exactly
+    with pytest.raises(ValueError):
+        oracle_mod.backward(x, off, msk, np.ones((1, 1, 1, 1)), go, positions="f16")
