@@ -402,6 +402,37 @@ def run_ours(args, case, world, rank, local, dist):
     except Exception as e:  # context only
         log("pack form skipped:", e)
 
+    # the backward pass (gradients of sum(grad_out * y) for x, offset, mask,
+    # weight and bias), same flush rule; its flops are the two contractions
+    # (column gradients and weight gradient), twice the forward's
+    bwd = None
+    try:
+        from modulated_deformable_convolution_gb300.workloads import make_grad_out
+        go = make_grad_out(case).to(dev)
+        gb = torch.empty_like(b) if b is not None else None
+        grads = [torch.empty_like(t) for t in (x, off, m, w)]
+        bws = torch.empty(mdcn.mdcn_backward_workspace_size(h, x, off, m, w, gb), dtype=torch.uint8, device=dev)
+        for _ in range(2):
+            mdcn.mdcn_backward(h, x, off, m, w, go, *grads, gb, bws, stream)
+        bt = []
+        for _ in range(min(args.steps, 20)):
+            flush.zero_()
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            mdcn.mdcn_backward(h, x, off, m, w, go, *grads, gb, bws, stream)
+            a1.record(stream)
+            bt.append((a0, a1))
+        torch.cuda.synchronize()
+        bwd_ms = statistics.mean(a.elapsed_time(c) for a, c in bt)
+        bwd = {"ms_per_call": bwd_ms, "tflops": 2 * case.flops / (bwd_ms * 1e-3) / 1e12,
+               "launches": mdcn.mdcn_backward_launches(h, x, off, m, w, gb),
+               "call": "mdcn_backward: weight pack; per image chunk: channels-last x, column gradients (cuBLAS), "
+                       "sampling backward (grad_offset, grad_mask, grad_x reductions, columns), weight gradient "
+                       "(cuBLAS), grad_x to NCHW; weight gradient layout, bias reduction"}
+        del bws, grads
+    except Exception as e:  # context only
+        log("backward skipped:", e)
+
     if rank != 0:
         return
     flops = case.flops
@@ -448,6 +479,7 @@ def run_ours(args, case, world, rank, local, dist):
                 "single_stream": {"value": world * flops / (e2e_serial_ms * 1e-3) / 1e12,
                                   "ms_per_step": e2e_serial_ms}},
         "pack_form": pack,
+        "backward": bwd,
         "ablation_im2col_gemm": None if abl_ms is None else {"ms_per_call": abl_ms,
                                                              "tflops": flops / (abl_ms * 1e-3) / 1e12},
         "gpu_launches": plan["launches"] * args.steps,

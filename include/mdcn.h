@@ -1,6 +1,6 @@
 /*
  * mdcn.h — C ABI of the GB300 (sm_103a) modulated deformable convolution
- * (DCNv2) forward library, libmdcn.so.
+ * (DCNv2) library, libmdcn.so: the forward pass, and its gradients.
  *
  * The operation is the one described in "TensorRT plugin walkthrough:
  * modulatedDeformConvPlugin" (trdm.cn):
@@ -260,6 +260,53 @@ mdcn_status mdcn_forward_im2col_gemm(mdcn_handle handle, const void* x, const vo
                                      const void* mask, const void* weight, const void* bias_or_null,
                                      void* out, void* workspace, size_t workspace_bytes,
                                      const mdcn_dims* dims, mdcn_dtype dtype, void* stream);
+
+/* ---------------------------------------------------------------- backward
+ * The gradients of L = sum(grad_out * y) for y = mdcn_forward(x, offset,
+ * mask, weight, bias), for training. The page defines only the forward
+ * (section 5 steps 1-3); this is the gradient of that definition, read as:
+ * inside the open range (-1, H) x (-1, W) the sample is the bilinear
+ * polynomial of the cell whose corner is (floor h, floor w) over the
+ * zero-extended image, with that polynomial's slopes (the right-hand slope
+ * where h or w is an integer); outside the range the sample and its slopes
+ * are 0, as the forward's range test gives. With G[n,c,k,p] = sum over the
+ * output channels o of c's group of weight[o,c_l,k] * grad_out[n,o,p]:
+ *   grad_x[n,c,corner]          = sum of G * mask * corner weight
+ *   grad_offset[n,gd*2K+2k(+1),p] = mask * sum over c of gd: G * dv/dh (dv/dw)
+ *   grad_mask[n,gd*K+k,p]       = sum over c of gd: G * v
+ *   grad_weight[o,c_l,k]        = sum over n, p: grad_out[n,o,p] * mask * v
+ *   grad_bias[o]                = sum over n, p: grad_out[n,o,p]
+ * (v = the bilinear sample of x[n,c] at the point of tap k, pixel p). */
+
+/* Bytes of device workspace mdcn_backward needs (the tap-major weight, an
+ * fp32 weight gradient, and per chunk of images: channels-last x, an fp32
+ * grad_x accumulator, the fp32 column gradients and the modulated columns).
+ * Host only. Errors as mdcn_workspace_size. */
+mdcn_status mdcn_backward_workspace_size(mdcn_handle handle, const mdcn_dims* dims, mdcn_dtype dtype, size_t* bytes);
+
+/* Kernel launches and cuBLAS calls one mdcn_backward call makes for these
+ * dims and dtype (a diagnostic; the page has no counterpart). Host only. */
+mdcn_status mdcn_backward_launches(mdcn_handle handle, const mdcn_dims* dims, mdcn_dtype dtype, int32_t* launches);
+
+/* The backward pass. Inputs (DEVICE pointers, dense NCHW, one dtype, as for
+ * mdcn_forward): x [N,Cin,H,W], offset [N,2*dg*kh*kw,Ho,Wo], mask
+ * [N,dg*kh*kw,Ho,Wo], weight [Cout,Cin/group,kh,kw], grad_out [N,Cout,Ho,Wo].
+ * Outputs (written, same dtype and dims as the tensor they belong to):
+ * grad_x, grad_offset, grad_mask, grad_weight, and grad_bias_or_null [Cout]
+ * (NULL: not computed; dims->bias must be Cout exactly when it is given).
+ * workspace: >= mdcn_backward_workspace_size bytes, contents undefined
+ * afterwards. Every pointer 16-byte aligned. Arithmetic in fp32 (the two
+ * contractions run as cuBLAS GEMMs with fp32 accumulation, no TF32 for f32);
+ * grad_x is summed with fp32 atomic additions, so its last bits may differ
+ * from run to run; the other gradients are deterministic. Asynchronous on the
+ * stream; a call that fails validation launches nothing and writes nothing.
+ * Errors: MDCN_ERR_NULL, MDCN_ERR_SHAPE, MDCN_ERR_DTYPE, MDCN_ERR_ALIGN,
+ * MDCN_ERR_WORKSPACE, MDCN_ERR_UNSUPPORTED (a GEMM dimension beyond 2^31-1,
+ * or a coordinate beyond 2^24), MDCN_ERR_ARCH, MDCN_ERR_CUDA. */
+mdcn_status mdcn_backward(mdcn_handle handle, const void* x, const void* offset, const void* mask, const void* weight,
+                          const void* grad_out, void* grad_x, void* grad_offset, void* grad_mask, void* grad_weight,
+                          void* grad_bias_or_null, void* workspace, size_t workspace_bytes, const mdcn_dims* dims,
+                          mdcn_dtype dtype, void* stream);
 
 /* mdcn_forward without a caller-supplied workspace, for callers that cannot
  * allocate device memory on their execution path (a serving loop that reserves

@@ -1,4 +1,4 @@
-"""GB300 (sm_103a) modulated deformable convolution (DCNv2) forward.
+"""GB300 (sm_103a) modulated deformable convolution (DCNv2): forward and backward.
 
 Thin Python binding of libmdcn.so (C ABI in include/mdcn.h): the functions
 named ``mdcn_*`` here mirror the C entry points one to one and only marshal
@@ -24,7 +24,8 @@ __all__ = ["Handle", "MdcnError", "forward", "mdcn_create", "mdcn_destroy", "mdc
            "mdcn_workspace_size", "mdcn_forward", "mdcn_prepare_input", "mdcn_pack_weight",
            "mdcn_forward_prepared", "mdcn_im2col_gemm_workspace_size", "mdcn_forward_im2col_gemm",
            "mdcn_query_plan", "mdcn_query_status", "mdcn_selftest_wait_timeout", "mdcn_status_string",
-           "library_path"]
+           "library_path", "backward", "mdcn_backward_workspace_size", "mdcn_backward_launches",
+           "mdcn_backward"]
 
 _DTYPES = {torch.float32: MDCN_F32, torch.float16: MDCN_F16, torch.bfloat16: MDCN_BF16}
 
@@ -346,3 +347,53 @@ def forward(x, offset, mask, weight, bias=None, stride=1, padding=0, dilation=1,
     else:
         raise ValueError(f"unknown algo {algo!r}")
     return out
+
+
+def mdcn_backward_workspace_size(handle, x, offset, mask, weight, bias=None, dtype=None) -> int:
+    n = ctypes.c_size_t()
+    dt = _dtype(x) if dtype is None else dtype
+    _check(_lib().mdcn_backward_workspace_size(_hval(handle), ctypes.byref(_dims(x, offset, mask, weight, bias)), dt,
+                                               ctypes.byref(n)), "mdcn_backward_workspace_size")
+    return int(n.value)
+
+
+def mdcn_backward_launches(handle, x, offset, mask, weight, bias=None, dtype=None) -> int:
+    n = ctypes.c_int32()
+    dt = _dtype(x) if dtype is None else dtype
+    _check(_lib().mdcn_backward_launches(_hval(handle), ctypes.byref(_dims(x, offset, mask, weight, bias)), dt,
+                                         ctypes.byref(n)), "mdcn_backward_launches")
+    return int(n.value)
+
+
+def mdcn_backward(handle, x, offset, mask, weight, grad_out, grad_x, grad_offset, grad_mask, grad_weight, grad_bias,
+                  workspace, stream=None) -> None:
+    """mdcn_backward on torch tensors (device memory) and the current stream.
+    grad_bias may be None (no bias gradient)."""
+    _check_tensors(x, offset, mask, weight, grad_bias, grad_out)
+    for t in (grad_x, grad_offset, grad_mask, grad_weight):
+        _check_tensors(x, offset, mask, weight, None, t)
+    d = _dims(x, offset, mask, weight, grad_bias)
+    with torch.cuda.device(x.device):
+        st = _stream(x.device, stream)
+        _check(_lib().mdcn_backward(_hval(handle), _ptr(x), _ptr(offset), _ptr(mask), _ptr(weight), _ptr(grad_out),
+                                    _ptr(grad_x), _ptr(grad_offset), _ptr(grad_mask), _ptr(grad_weight),
+                                    _ptr(grad_bias), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                    ctypes.byref(d), _dtype(x), st), "mdcn_backward")
+
+
+def backward(x, offset, mask, weight, grad_out, with_bias=True, stride=1, padding=0, dilation=1, group=1,
+             deformable_group=1, workspace=None, handle=None):
+    """Gradients of sum(grad_out * forward(...)): allocates the gradient
+    tensors (and workspace) with torch and runs the library on the current
+    stream. Returns a dict with x, offset, mask, weight and bias (None when
+    ``with_bias`` is false)."""
+    h = handle if handle is not None else Handle(stride, padding, dilation, group, deformable_group)
+    Cout = weight.shape[0]
+    gb = torch.empty(Cout, dtype=x.dtype, device=x.device) if with_bias else None
+    need = mdcn_backward_workspace_size(h, x, offset, mask, weight, gb)
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    g = {"x": torch.empty_like(x), "offset": torch.empty_like(offset), "mask": torch.empty_like(mask),
+         "weight": torch.empty_like(weight), "bias": gb}
+    mdcn_backward(h, x, offset, mask, weight, grad_out, g["x"], g["offset"], g["mask"], g["weight"], gb, workspace)
+    return g

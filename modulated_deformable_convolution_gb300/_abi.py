@@ -111,6 +111,14 @@ def load(path: str = LIB_PATH):
         lib.mdcn_forward_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, ctypes.POINTER(mdcn_dims),
                                           ctypes.c_int, vp]
         lib.mdcn_forward_host.restype = st
+        lib.mdcn_backward_workspace_size.argtypes = [vp, ctypes.POINTER(mdcn_dims), ctypes.c_int,
+                                                     ctypes.POINTER(ctypes.c_size_t)]
+        lib.mdcn_backward_workspace_size.restype = st
+        lib.mdcn_backward_launches.argtypes = [vp, ctypes.POINTER(mdcn_dims), ctypes.c_int,
+                                               ctypes.POINTER(ctypes.c_int32)]
+        lib.mdcn_backward_launches.restype = st
+        lib.mdcn_backward.argtypes = [vp] * 12 + [ctypes.c_size_t, ctypes.POINTER(mdcn_dims), ctypes.c_int, vp]
+        lib.mdcn_backward.restype = st
         lib.mdcn_query_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
         lib.mdcn_query_status.restype = st
         lib.mdcn_selftest_wait_timeout.argtypes = [vp, ctypes.c_uint32, vp]

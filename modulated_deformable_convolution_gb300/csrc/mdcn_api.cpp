@@ -13,6 +13,7 @@
 #include <mutex>
 #include <new>
 
+#include "mdcn_backward.h"
 #include "mdcn_launch.h"
 #include "mdcn_plan.h"
 
@@ -358,6 +359,65 @@ mdcn_status front_end_problem(const mdcn_attrs& a, const mdcn_dims* d, mdcn_attr
     return MDCN_OK;
 }
 
+// Problem of a backward call: the forward's checks (section 2/4 bindings,
+// section 3 attributes) plus the limits of the backward's kernels and of the
+// cuBLAS dimensions (32-bit), then the chunking and workspace layout.
+constexpr size_t kBwdL2Budget = size_t(64) << 20;  // per-chunk buffers, half of the 129 MB L2
+
+mdcn_status make_bwd_plan(const mdcn_attrs& a, const mdcn_dims* d, mdcn_dtype dtype, mdcn::BwdPlan* p) {
+    if (!d || !p) return MDCN_ERR_NULL;
+    if (dtype != MDCN_F32 && dtype != MDCN_F16 && dtype != MDCN_BF16) return MDCN_ERR_DTYPE;
+    int64_t od[4];
+    mdcn_status s = check_dims(a, *d, od);
+    if (s != MDCN_OK) return s;
+    mdcn::BwdPlan b;
+    std::memset(&b, 0, sizeof(b));
+    b.N = d->x[0];
+    b.Cin = d->x[1];
+    b.H = d->x[2];
+    b.W = d->x[3];
+    b.Cout = d->weight[0];
+    b.kh = d->weight[2];
+    b.kw = d->weight[3];
+    b.Ho = d->offset[2];
+    b.Wo = d->offset[3];
+    b.sh = static_cast<int32_t>(a.stride[0]);
+    b.sw = static_cast<int32_t>(a.stride[1]);
+    b.ph = static_cast<int32_t>(a.padding[0]);
+    b.pw = static_cast<int32_t>(a.padding[1]);
+    b.dh = static_cast<int32_t>(a.dilation[0]);
+    b.dw = static_cast<int32_t>(a.dilation[1]);
+    b.group = static_cast<int32_t>(a.group);
+    b.dg = static_cast<int32_t>(a.deformable_group);
+    b.dtype = static_cast<int32_t>(dtype);
+    b.has_bias = d->bias != 0;
+    const int64_t K = b.kh * b.kw;
+    // positions are formed in fp32: keep every coordinate exactly representable
+    if (b.H >= (1 << 24) || b.W >= (1 << 24)) return MDCN_ERR_UNSUPPORTED;
+    if ((b.Ho - 1) * a.stride[0] + (b.kh - 1) * a.dilation[0] >= (1 << 24) ||
+        (b.Wo - 1) * a.stride[1] + (b.kw - 1) * a.dilation[1] >= (1 << 24))
+        return MDCN_ERR_UNSUPPORTED;
+    b.P = b.Ho * b.Wo;
+    int64_t kcg = K;
+    if (!mul_ok(kcg, b.Cin / a.group) || kcg > kI31 || b.P > kI31 || b.Cout / a.group > kI31 || K > kI31)
+        return MDCN_ERR_UNSUPPORTED;  // cuBLAS dimensions are 32-bit
+    b.K = static_cast<int32_t>(K);
+    b.Cg = static_cast<int32_t>(b.Cin / a.group);
+    b.Og = static_cast<int32_t>(b.Cout / a.group);
+    b.Cd = static_cast<int32_t>(b.Cin / a.deformable_group);
+    int64_t cols = b.P;  // column elements of one image, and its x
+    if (!mul_ok(cols, K) || !mul_ok(cols, b.Cin) || !mul_ok(cols, 32)) return MDCN_ERR_UNSUPPORTED;
+    int64_t seg = b.P;  // sampling-backward threads of one image, at most 32 lanes per point
+    if (!mul_ok(seg, b.dg) || !mul_ok(seg, K) || !mul_ok(seg, 32)) return MDCN_ERR_UNSUPPORTED;
+    mdcn::plan_backward(&b, kBwdL2Budget);
+    // one chunk's sampling-backward grid and the transposes' tile counts fit 32-bit block indices
+    int64_t thr = seg;
+    if (!mul_ok(thr, b.nb) || thr / 256 >= kI31 || (b.H * b.W / 32 + 1) * (b.Cin / 32 + 1) >= kI31)
+        return MDCN_ERR_UNSUPPORTED;
+    *p = b;
+    return MDCN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -653,6 +713,48 @@ mdcn_status mdcn_forward_im2col_gemm(mdcn_handle handle, const void* x, const vo
     if (s != MDCN_OK) return s;
     cudaError_t e = mdcn::launch_im2col_gemm(p, x, offset, mask, weight, bias_or_null, out, workspace,
                                              static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    return MDCN_OK;
+}
+
+mdcn_status mdcn_backward_workspace_size(mdcn_handle handle, const mdcn_dims* dims, mdcn_dtype dtype, size_t* bytes) {
+    if (!handle || !dims || !bytes) return MDCN_ERR_NULL;
+    mdcn::BwdPlan b;
+    mdcn_status s = make_bwd_plan(handle->attrs, dims, dtype, &b);
+    if (s != MDCN_OK) return s;
+    *bytes = b.ws_bytes;
+    return MDCN_OK;
+}
+
+mdcn_status mdcn_backward_launches(mdcn_handle handle, const mdcn_dims* dims, mdcn_dtype dtype, int32_t* launches) {
+    if (!handle || !dims || !launches) return MDCN_ERR_NULL;
+    mdcn::BwdPlan b;
+    mdcn_status s = make_bwd_plan(handle->attrs, dims, dtype, &b);
+    if (s != MDCN_OK) return s;
+    *launches = mdcn::backward_launch_count(b);
+    return MDCN_OK;
+}
+
+mdcn_status mdcn_backward(mdcn_handle handle, const void* x, const void* offset, const void* mask, const void* weight,
+                          const void* grad_out, void* grad_x, void* grad_offset, void* grad_mask, void* grad_weight,
+                          void* grad_bias_or_null, void* workspace, size_t workspace_bytes, const mdcn_dims* dims,
+                          mdcn_dtype dtype, void* stream) {
+    if (!handle || !x || !offset || !mask || !weight || !grad_out || !grad_x || !grad_offset || !grad_mask ||
+        !grad_weight || !workspace || !dims)
+        return MDCN_ERR_NULL;
+    if ((grad_bias_or_null == nullptr) != (dims->bias == 0)) return grad_bias_or_null ? MDCN_ERR_SHAPE : MDCN_ERR_NULL;
+    const void* ptrs[] = {x, offset, mask, weight, grad_out, grad_x, grad_offset, grad_mask, grad_weight, workspace};
+    for (const void* q : ptrs)
+        if (!aligned16(q)) return MDCN_ERR_ALIGN;
+    if (grad_bias_or_null && !aligned16(grad_bias_or_null)) return MDCN_ERR_ALIGN;
+    mdcn::BwdPlan b;
+    mdcn_status s = make_bwd_plan(handle->attrs, dims, dtype, &b);
+    if (s != MDCN_OK) return s;
+    if (workspace_bytes < b.ws_bytes) return MDCN_ERR_WORKSPACE;
+    s = check_device();
+    if (s != MDCN_OK) return s;
+    cudaError_t e = mdcn::launch_backward(b, x, offset, mask, weight, grad_out, grad_x, grad_offset, grad_mask,
+                                          grad_weight, grad_bias_or_null, workspace, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
     return MDCN_OK;
 }

@@ -1,0 +1,417 @@
+// Backward pass of the modulated deformable convolution: the gradients of
+// L = sum(grad_out * y) with respect to x, offset, mask, weight and bias, for
+// the forward of "TensorRT plugin walkthrough: modulatedDeformConvPlugin"
+// (section 5 steps 1-3). The page has no backward; this is the gradient of its
+// definition, with the right-hand slope on the edges of a bilinear cell and 0
+// outside the open sampling range (-1, H) x (-1, W), as its range test gives.
+//
+// With G[n, c, k, p] = sum over the output channels o of c's group of
+// weight[o, c_l, k] * grad_out[n, o, p] (the gradient of a modulated column
+// element), and v, dv/dh, dv/dw the bilinear sample and its slopes:
+//   grad_mask[n, gd*K + k, p]        = sum over c of gd: G * v
+//   grad_offset[n, gd*2K + 2k (+1), p] = mask * sum over c of gd: G * dv/dh (dv/dw)
+//   grad_x[n, c, corner]            += G * mask * corner weight
+//   grad_weight[o, c_l, k]           = sum over n, p: grad_out[n, o, p] * mask * v
+//   grad_bias[o]                     = sum over n, p: grad_out[n, o, p]
+//
+// Work per chunk of images (sized so its buffers stay in L2):
+//   1. x of the chunk -> channels-last (tiled transpose);
+//   2. G = W_g^T * grad_out per group, one cuBLAS strided-batched GEMM per
+//      group (fp32 out), laid out [n][g][p][k][c_l] so that one sampling
+//      point's channels are contiguous;
+//   3. the sampling backward: a segment of lanes per sampling point (n, p, gd,
+//      k), lanes along channels; the slope sums are reduced across the
+//      segment by shuffles (deterministic), grad_x goes by fp32 vector
+//      reductions into a channels-last accumulator, and the modulated column
+//      mask * v is written for step 4;
+//   4. grad_weight += grad_out * col^T per image, one strided-batched GEMM
+//      over the groups (fp32 accumulate in workspace);
+//   5. the fp32 grad_x accumulator -> NCHW in the I/O type.
+// Then the weight gradient to [Cout, Cg, kh, kw] and the bias reduction.
+#include <cublas_v2.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "mdcn_backward.h"
+#include "mdcn_plan.h"
+
+namespace mdcn {
+
+cublasHandle_t handle_for_current_device();  // mdcn_im2col.cu
+
+namespace {
+
+__device__ __forceinline__ float to_f(float v) { return v; }
+__device__ __forceinline__ float to_f(__half v) { return __half2float(v); }
+__device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+template <typename T>
+__device__ __forceinline__ T from_f(float v);
+template <>
+__device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ __half from_f<__half>(float v) { return __float2half_rn(v); }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+
+// VEC consecutive elements of type T as one aligned access.
+template <typename T, int VEC>
+struct alignas(sizeof(T) * VEC) Vec {
+    T v[VEC];
+};
+
+template <typename T, int VEC>
+__device__ __forceinline__ void load_f(const T* p, float (&out)[VEC]) {
+    const Vec<T, VEC> t = *reinterpret_cast<const Vec<T, VEC>*>(p);
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) out[i] = to_f(t.v[i]);
+}
+
+template <typename T, int VEC>
+__device__ __forceinline__ void store_f(T* p, const float (&in)[VEC]) {
+    Vec<T, VEC> t;
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) t.v[i] = from_f<T>(in[i]);
+    *reinterpret_cast<Vec<T, VEC>*>(p) = t;
+}
+
+// p[0..VEC) += s * w[0..VEC) as fp32 reductions (one vector reduction for VEC = 4).
+template <int VEC>
+__device__ __forceinline__ void red_add(float* p, const float (&g)[VEC], float s) {
+    if constexpr (VEC == 4) {
+        atomicAdd(reinterpret_cast<float4*>(p), make_float4(g[0] * s, g[1] * s, g[2] * s, g[3] * s));
+    } else {
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) atomicAdd(p + i, g[i] * s);
+    }
+}
+
+// out[b][c][r] = in[b][r][c] for an R x C matrix per batch entry b
+// (blockIdx.y), through a 32 x 33 shared-memory tile; blockIdx.x walks the
+// tiles, column tiles fastest.
+template <typename Tin, typename Tout>
+__global__ void __launch_bounds__(256) transpose_kernel(const Tin* __restrict__ in, Tout* __restrict__ out, int64_t R,
+                                                        int64_t C) {
+    __shared__ float tile[32][33];
+    const int64_t b = blockIdx.y;
+    const int64_t ctiles = (C + 31) / 32;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.x) / ctiles * 32;
+    const int64_t c0 = static_cast<int64_t>(blockIdx.x) % ctiles * 32;
+    const Tin* src = in + b * R * C;
+    Tout* dst = out + b * R * C;
+    for (int t = threadIdx.y; t < 32; t += 8) {
+        const int64_t r = r0 + t, c = c0 + threadIdx.x;
+        if (r < R && c < C) tile[t][threadIdx.x] = to_f(src[r * C + c]);
+    }
+    __syncthreads();
+    for (int t = threadIdx.y; t < 32; t += 8) {
+        const int64_t c = c0 + t, r = r0 + threadIdx.x;
+        if (r < R && c < C) dst[c * R + r] = from_f<Tout>(tile[threadIdx.x][t]);
+    }
+}
+
+// wt[o][k][c_l] = w[o][c_l][k]
+template <typename T>
+__global__ void __launch_bounds__(256) weight_tap_major_kernel(const T* __restrict__ w, T* __restrict__ wt,
+                                                               int64_t Cout, int64_t Cg, int64_t K) {
+    const int64_t total = Cout * Cg * K;
+    for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
+         e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t o = e / (K * Cg), r = e - o * (K * Cg);
+        const int64_t k = r / Cg, cl = r - k * Cg;
+        wt[e] = w[(o * Cg + cl) * K + k];
+    }
+}
+
+// grad_weight[o][c_l][k] = gw[o][k][c_l] in the I/O type
+template <typename T>
+__global__ void __launch_bounds__(256) weight_grad_out_kernel(const float* __restrict__ gw, T* __restrict__ gweight,
+                                                              int64_t Cout, int64_t Cg, int64_t K) {
+    const int64_t total = Cout * Cg * K;
+    for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
+         e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t o = e / (Cg * K), r = e - o * (Cg * K);
+        const int64_t cl = r / K, k = r - cl * K;
+        gweight[e] = from_f<T>(gw[(o * K + k) * Cg + cl]);
+    }
+}
+
+// grad_bias[o] = sum over n, p of grad_out[n][o][p]: one block per output
+// channel, fixed summation order.
+template <typename T>
+__global__ void __launch_bounds__(256) bias_grad_kernel(const T* __restrict__ gout, T* __restrict__ gbias, int64_t N,
+                                                        int64_t Cout, int64_t P) {
+    __shared__ float part[8];
+    const int64_t o = blockIdx.x;
+    float s = 0.f;
+    for (int64_t n = 0; n < N; ++n) {
+        const T* row = gout + (n * Cout + o) * P;
+        for (int64_t p = threadIdx.x; p < P; p += blockDim.x) s += to_f(row[p]);
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) s += __shfl_xor_sync(0xffffffffu, s, d);
+    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = s;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float t = 0.f;
+        for (int i = 0; i < 8; ++i) t += part[i];
+        gbias[o] = from_f<T>(t);
+    }
+}
+
+// The sampling backward of one chunk: a segment of `lanes` consecutive
+// threads per sampling point q = ((n*P + p)*dg + gd)*K + k (n within the
+// chunk), each lane taking VEC consecutive channels of the point's
+// deformable group per step. Reads the chunk's channels-last x and column
+// gradients; writes the modulated columns, grad_offset and grad_mask of the
+// point, and adds the corner terms into the fp32 channels-last grad_x.
+template <typename T, int VEC>
+__global__ void __launch_bounds__(256) sample_backward_kernel(const BwdPlan p, const T* __restrict__ xt,
+                                                              const T* __restrict__ offset, const T* __restrict__ mask,
+                                                              const float* __restrict__ gcol, T* __restrict__ col,
+                                                              float* __restrict__ gx, T* __restrict__ goffset,
+                                                              T* __restrict__ gmask, int64_t n0, int64_t nbc) {
+    const int lanes = p.lanes;
+    const int64_t K = p.K, P = p.P, dg = p.dg, Cin = p.Cin, Cg = p.Cg;
+    const int64_t points = nbc * P * dg * K;
+    const int64_t q = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / lanes;
+    const int sub = threadIdx.x & (lanes - 1);
+    const bool live = q < points;
+    float s_mask = 0.f, s_h = 0.f, s_w = 0.f, m = 0.f;
+    int64_t och = 0, mch = 0, pix = 0;
+    if (live) {
+        const int64_t k = q % K;
+        int64_t t = q / K;
+        const int64_t gd = t % dg;
+        t /= dg;
+        pix = t % P;
+        const int64_t n = t / P, ng = n0 + n;
+        const int64_t ho = pix / p.Wo, wo = pix - ho * p.Wo;
+        const int64_t i = k / p.kw, j = k - i * p.kw;
+        och = (ng * 2 * dg + 2 * gd) * K + 2 * k;  // the point's h-offset channel; w follows
+        mch = (ng * dg + gd) * K + k;
+        const float offh = to_f(offset[och * P + pix]);
+        const float offw = to_f(offset[(och + 1) * P + pix]);
+        m = to_f(mask[mch * P + pix]);
+        const float h = static_cast<float>(ho * p.sh - p.ph + i * p.dh) + offh;
+        const float w = static_cast<float>(wo * p.sw - p.pw + j * p.dw) + offw;
+        const bool inside = !(h <= -1.f || h >= static_cast<float>(p.H) || w <= -1.f || w >= static_cast<float>(p.W));
+        const int64_t cbeg = gd * p.Cd, cend = cbeg + p.Cd;
+        if (inside) {
+            const float h0f = floorf(h), w0f = floorf(w);
+            const int64_t y0 = static_cast<int64_t>(h0f), x0 = static_cast<int64_t>(w0f);
+            const float lh = h - h0f, lw = w - w0f, hh = 1.f - lh, hw = 1.f - lw;
+            const float w00 = hh * hw, w01 = hh * lw, w10 = lh * hw, w11 = lh * lw;
+            const bool v00 = y0 >= 0 && x0 >= 0, v01 = y0 >= 0 && x0 + 1 < p.W;
+            const bool v10 = y0 + 1 < p.H && x0 >= 0, v11 = y0 + 1 < p.H && x0 + 1 < p.W;
+            // corner (y0, x0) of image n, channels-last; only dereferenced when valid
+            const int64_t a00 = ((n * p.H + y0) * p.W + x0) * Cin;
+            const int64_t a01 = a00 + Cin, a10 = a00 + p.W * Cin, a11 = a10 + Cin;
+            for (int64_t c = cbeg + static_cast<int64_t>(sub) * VEC; c < cend; c += static_cast<int64_t>(lanes) * VEC) {
+                const int64_t g = c / Cg, cl = c - g * Cg;
+                const int64_t gi = (((n * p.group + g) * P + pix) * K + k) * Cg + cl;
+                float G[VEC], X00[VEC], X01[VEC], X10[VEC], X11[VEC], cv[VEC];
+                load_f<float, VEC>(gcol + gi, G);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) X00[e] = X01[e] = X10[e] = X11[e] = 0.f;
+                if (v00) load_f<T, VEC>(xt + a00 + c, X00);
+                if (v01) load_f<T, VEC>(xt + a01 + c, X01);
+                if (v10) load_f<T, VEC>(xt + a10 + c, X10);
+                if (v11) load_f<T, VEC>(xt + a11 + c, X11);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    const float val = w00 * X00[e] + w01 * X01[e] + w10 * X10[e] + w11 * X11[e];
+                    const float dvh = hw * (X10[e] - X00[e]) + lw * (X11[e] - X01[e]);
+                    const float dvw = hh * (X01[e] - X00[e]) + lh * (X11[e] - X10[e]);
+                    s_mask += G[e] * val;
+                    s_h += G[e] * dvh;
+                    s_w += G[e] * dvw;
+                    cv[e] = m * val;
+                }
+                store_f<T, VEC>(col + gi, cv);
+                if (v00) red_add<VEC>(gx + a00 + c, G, m * w00);
+                if (v01) red_add<VEC>(gx + a01 + c, G, m * w01);
+                if (v10) red_add<VEC>(gx + a10 + c, G, m * w10);
+                if (v11) red_add<VEC>(gx + a11 + c, G, m * w11);
+            }
+        } else {
+            float zero[VEC];
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) zero[e] = 0.f;
+            for (int64_t c = cbeg + static_cast<int64_t>(sub) * VEC; c < cend; c += static_cast<int64_t>(lanes) * VEC) {
+                const int64_t g = c / Cg, cl = c - g * Cg;
+                store_f<T, VEC>(col + (((n * p.group + g) * P + pix) * K + k) * Cg + cl, zero);
+            }
+        }
+    }
+    // segments are aligned groups of `lanes` threads inside one warp, and every
+    // thread of the warp reaches this point
+    for (int d = lanes >> 1; d > 0; d >>= 1) {
+        s_mask += __shfl_xor_sync(0xffffffffu, s_mask, d);
+        s_h += __shfl_xor_sync(0xffffffffu, s_h, d);
+        s_w += __shfl_xor_sync(0xffffffffu, s_w, d);
+    }
+    if (live && sub == 0) {
+        gmask[mch * P + pix] = from_f<T>(s_mask);
+        goffset[och * P + pix] = from_f<T>(m * s_h);
+        goffset[(och + 1) * P + pix] = from_f<T>(m * s_w);
+    }
+}
+
+template <typename T>
+constexpr cudaDataType_t blas_type();
+template <>
+constexpr cudaDataType_t blas_type<float>() { return CUDA_R_32F; }
+template <>
+constexpr cudaDataType_t blas_type<__half>() { return CUDA_R_16F; }
+template <>
+constexpr cudaDataType_t blas_type<__nv_bfloat16>() { return CUDA_R_16BF; }
+
+size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+unsigned grid_for(int64_t total) {
+    int64_t b = (total + 255) / 256;
+    return static_cast<unsigned>(b < 1 ? 1 : (b > 8192 ? 8192 : b));
+}
+
+template <typename Tin, typename Tout>
+cudaError_t transpose(const Tin* in, Tout* out, int64_t R, int64_t C, int64_t batch, cudaStream_t st) {
+    const int64_t tiles = ((R + 31) / 32) * ((C + 31) / 32);
+    transpose_kernel<Tin, Tout><<<dim3(static_cast<unsigned>(tiles), static_cast<unsigned>(batch)), dim3(32, 8), 0,
+                                  st>>>(in, out, R, C);
+    return cudaGetLastError();
+}
+
+cudaError_t blas_fail(cublasStatus_t s) {
+    return s == CUBLAS_STATUS_SUCCESS ? cudaSuccess : cudaErrorUnknown;
+}
+
+template <typename T>
+cudaError_t run_backward(const BwdPlan& p, const T* x, const T* offset, const T* mask, const T* weight,
+                         const T* grad_out, T* grad_x, T* grad_offset, T* grad_mask, T* grad_weight, T* grad_bias,
+                         void* ws, cudaStream_t st) {
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    T* wt = reinterpret_cast<T*>(base + p.off_wt);
+    float* gw = reinterpret_cast<float*>(base + p.off_gw);
+    T* xt = reinterpret_cast<T*>(base + p.off_xt);
+    float* gx = reinterpret_cast<float*>(base + p.off_gx);
+    float* gcol = reinterpret_cast<float*>(base + p.off_gcol);
+    T* col = reinterpret_cast<T*>(base + p.off_col);
+    const int64_t K = p.K, Cg = p.Cg, Og = p.Og, P = p.P, HW = p.H * p.W, KCg = K * Cg;
+    cudaError_t e;
+
+    cublasHandle_t h = handle_for_current_device();
+    if (!h) return cudaErrorNotSupported;
+    if (cublasSetStream(h, st) != CUBLAS_STATUS_SUCCESS) return cudaErrorUnknown;
+    const cublasComputeType_t ct = sizeof(T) == 4 ? CUBLAS_COMPUTE_32F_PEDANTIC : CUBLAS_COMPUTE_32F;
+    const float one = 1.0f, zero = 0.0f;
+
+    weight_tap_major_kernel<T><<<grid_for(p.Cout * KCg), 256, 0, st>>>(weight, wt, p.Cout, Cg, K);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+    for (int64_t n0 = 0; n0 < p.N; n0 += p.nb) {
+        const int64_t nbc = p.N - n0 < p.nb ? p.N - n0 : p.nb;
+        // 1. x of the chunk, channels-last
+        if ((e = transpose<T, T>(x + n0 * p.Cin * HW, xt, p.Cin, HW, nbc, st)) != cudaSuccess) return e;
+        if ((e = cudaMemsetAsync(gx, 0, static_cast<size_t>(nbc * HW * p.Cin) * sizeof(float), st)) != cudaSuccess)
+            return e;
+        // 2. column gradients, per group: (K*Cg x P) = wt_g (K*Cg x Og) * grad_out_g (Og x P), column-major views
+        for (int32_t g = 0; g < p.group; ++g) {
+            e = blas_fail(cublasGemmStridedBatchedEx(
+                h, CUBLAS_OP_N, CUBLAS_OP_T, static_cast<int>(KCg), static_cast<int>(P), static_cast<int>(Og), &one,
+                wt + g * Og * KCg, blas_type<T>(), static_cast<int>(KCg), 0,
+                grad_out + (n0 * p.Cout + g * Og) * P, blas_type<T>(), static_cast<int>(P), p.Cout * P, &zero,
+                gcol + g * P * KCg, CUDA_R_32F, static_cast<int>(KCg), p.group * P * KCg, static_cast<int>(nbc), ct,
+                CUBLAS_GEMM_DEFAULT));
+            if (e != cudaSuccess) return e;
+        }
+        // 3. sampling backward
+        {
+            const int64_t threads = nbc * P * p.dg * K * p.lanes;
+            const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
+            if (p.vec == 4)
+                sample_backward_kernel<T, 4><<<blocks, 256, 0, st>>>(p, xt, offset, mask, gcol, col, gx, grad_offset,
+                                                                     grad_mask, n0, nbc);
+            else
+                sample_backward_kernel<T, 1><<<blocks, 256, 0, st>>>(p, xt, offset, mask, gcol, col, gx, grad_offset,
+                                                                     grad_mask, n0, nbc);
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        }
+        // 4. weight gradient, per image over the groups: (K*Cg x Og) += col (K*Cg x P) * grad_out^T (P x Og)
+        for (int64_t n = 0; n < nbc; ++n) {
+            const float* beta = (n0 + n == 0) ? &zero : &one;
+            e = blas_fail(cublasGemmStridedBatchedEx(
+                h, CUBLAS_OP_N, CUBLAS_OP_N, static_cast<int>(KCg), static_cast<int>(Og), static_cast<int>(P), &one,
+                col + n * p.group * P * KCg, blas_type<T>(), static_cast<int>(KCg), P * KCg,
+                grad_out + (n0 + n) * p.Cout * P, blas_type<T>(), static_cast<int>(P), Og * P, beta, gw, CUDA_R_32F,
+                static_cast<int>(KCg), Og * KCg, p.group, ct, CUBLAS_GEMM_DEFAULT));
+            if (e != cudaSuccess) return e;
+        }
+        // 5. grad_x of the chunk to NCHW
+        if ((e = transpose<float, T>(gx, grad_x + n0 * p.Cin * HW, HW, p.Cin, nbc, st)) != cudaSuccess) return e;
+    }
+    weight_grad_out_kernel<T><<<grid_for(p.Cout * KCg), 256, 0, st>>>(gw, grad_weight, p.Cout, Cg, K);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (grad_bias) {
+        bias_grad_kernel<T><<<static_cast<unsigned>(p.Cout), 256, 0, st>>>(grad_out, grad_bias, p.N, p.Cout, P);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace
+
+void plan_backward(BwdPlan* p, size_t l2_budget) {
+    const size_t es = p->dtype == kF32 ? 4 : 2;
+    p->vec = (p->Cg % 4 == 0 && p->Cd % 4 == 0 && p->Cin % 4 == 0) ? 4 : 1;
+    const int64_t units = (p->Cd + p->vec - 1) / p->vec;
+    int lanes = 1;
+    while (lanes < 32 && lanes < units) lanes <<= 1;
+    p->lanes = lanes;
+    const size_t cols = static_cast<size_t>(p->P) * p->K * p->Cin;  // column elements of one image
+    const size_t pix = static_cast<size_t>(p->H) * p->W * p->Cin;   // x elements of one image
+    const size_t per_image = cols * (4 + es) + pix * (es + 4);
+    int64_t nb = static_cast<int64_t>(l2_budget / (per_image ? per_image : 1));
+    if (nb < 1) nb = 1;
+    if (nb > p->N) nb = p->N;
+    if (nb > 65535) nb = 65535;
+    p->nb = nb;
+    const size_t wel = static_cast<size_t>(p->Cout) * p->K * p->Cg;
+    size_t off = 0;
+    p->off_wt = off;
+    off += align256(wel * es);
+    p->off_gw = off;
+    off += align256(wel * 4);
+    p->off_xt = off;
+    off += align256(nb * pix * es);
+    p->off_gx = off;
+    off += align256(nb * pix * 4);
+    p->off_gcol = off;
+    off += align256(nb * cols * 4);
+    p->off_col = off;
+    off += align256(nb * cols * es);
+    p->ws_bytes = off;
+}
+
+int backward_launch_count(const BwdPlan& p) {
+    const int64_t chunks = (p.N + p.nb - 1) / p.nb;
+    // per chunk: transpose, memset, one GEMM per group, sampling backward, one GEMM per image, transpose
+    return static_cast<int>(1 + chunks * (4 + p.group) + p.N + 1 + (p.has_bias ? 1 : 0));
+}
+
+cudaError_t launch_backward(const BwdPlan& p, const void* x, const void* offset, const void* mask, const void* weight,
+                            const void* grad_out, void* grad_x, void* grad_offset, void* grad_mask, void* grad_weight,
+                            void* grad_bias, void* ws, cudaStream_t st) {
+#define MDCN_BWD_ARGS(T)                                                                                          \
+    p, static_cast<const T*>(x), static_cast<const T*>(offset), static_cast<const T*>(mask),                     \
+        static_cast<const T*>(weight), static_cast<const T*>(grad_out), static_cast<T*>(grad_x),                 \
+        static_cast<T*>(grad_offset), static_cast<T*>(grad_mask), static_cast<T*>(grad_weight),                  \
+        static_cast<T*>(grad_bias), ws, st
+    switch (p.dtype) {
+        case kF32: return run_backward<float>(MDCN_BWD_ARGS(float));
+        case kF16: return run_backward<__half>(MDCN_BWD_ARGS(__half));
+        default: return run_backward<__nv_bfloat16>(MDCN_BWD_ARGS(__nv_bfloat16));
+    }
+#undef MDCN_BWD_ARGS
+}
+
+}  // namespace mdcn

@@ -81,6 +81,10 @@ struct HandleCache {
     cublasHandle_t h[64] = {};
 };
 
+}  // namespace
+
+// One cuBLAS handle per device, created on first use (also used by the
+// backward pass).
 cublasHandle_t handle_for_current_device() {
     static HandleCache cache;
     int dev = 0;
@@ -93,6 +97,8 @@ cublasHandle_t handle_for_current_device() {
     }
     return cache.h[dev];
 }
+
+namespace {
 
 template <typename T>
 constexpr cudaDataType_t cuda_type();

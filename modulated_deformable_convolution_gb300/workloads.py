@@ -130,3 +130,12 @@ def make_inputs(case: Case, device="cpu"):
     dt = DTYPES[case.dtype]
     out = dict(x=x, offset=offset, mask=mask, weight=weight, bias=bias)
     return {k: (None if v is None else v.to(dt).contiguous().to(device)) for k, v in out.items()}
+
+
+def make_grad_out(case: Case, device="cpu"):
+    """The output gradient of the case for the backward pass: N(0, 1) of the
+    output's shape in the case's dtype, from its own seeded stream (seed + 1000)."""
+    g = torch.Generator().manual_seed(int(case.seed) + 1000)
+    Ho, Wo = case.out_hw
+    go = torch.randn(case.N, case.Cout, Ho, Wo, generator=g)
+    return go.to(DTYPES[case.dtype]).contiguous().to(device)
