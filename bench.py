@@ -523,6 +523,39 @@ def run_fused_only(args, case):
                       "status": s}), flush=True)
 
 
+def run_backward_only(args, case):
+    """Profiling aid: runs mdcn_backward args.backward_only times (after one
+    untimed call), each after an L2 flush, and prints the median CUDA-event
+    time per call. Used for the launch list of the backward's kernels."""
+    import modulated_deformable_convolution_gb300 as mdcn
+    from modulated_deformable_convolution_gb300.workloads import make_grad_out
+
+    dev = torch.device("cuda", 0)
+    d = {k: (None if v is None else v.to(dev)) for k, v in make_inputs(case).items()}
+    x, off, m, w, b = d["x"], d["offset"], d["mask"], d["weight"], d["bias"]
+    go = make_grad_out(case).to(dev)
+    h = mdcn.Handle(**case.attrs())
+    gb = torch.empty_like(b) if b is not None else None
+    grads = [torch.empty_like(t) for t in (x, off, m, w)]
+    ws = torch.empty(mdcn.mdcn_backward_workspace_size(h, x, off, m, w, gb), dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    st = torch.cuda.current_stream(dev)
+    mdcn.mdcn_backward(h, x, off, m, w, go, *grads, gb, ws, st)
+    torch.cuda.synchronize()
+    evs = []
+    for _ in range(args.backward_only):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        mdcn.mdcn_backward(h, x, off, m, w, go, *grads, gb, ws, st)
+        e1.record(st)
+        evs.append((e0, e1))
+    torch.cuda.synchronize()
+    us = statistics.median(a.elapsed_time(c) for a, c in evs) * 1e3
+    print(json.dumps({"workload": case.name, "backward_us": us, "tflops": 2 * case.flops / (us * 1e-6) / 1e12,
+                      "launches": mdcn.mdcn_backward_launches(h, x, off, m, w, gb)}), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -533,6 +566,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fused-only", type=int, default=0, metavar="N",
                     help="profiling aid: time N launches of the fused kernel alone")
+    ap.add_argument("--backward-only", type=int, default=0, metavar="N",
+                    help="profiling aid: time N calls of mdcn_backward alone")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
@@ -547,6 +582,11 @@ def main(argv=None):
 
             build.build()
             run_fused_only(args, case)
+        elif args.backward_only:
+            from modulated_deformable_convolution_gb300 import build
+
+            build.build()
+            run_backward_only(args, case)
         else:
             from modulated_deformable_convolution_gb300 import build
 

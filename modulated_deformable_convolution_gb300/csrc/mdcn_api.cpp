@@ -407,13 +407,11 @@ mdcn_status make_bwd_plan(const mdcn_attrs& a, const mdcn_dims* d, mdcn_dtype dt
     b.Cd = static_cast<int32_t>(b.Cin / a.deformable_group);
     int64_t cols = b.P;  // column elements of one image, and its x
     if (!mul_ok(cols, K) || !mul_ok(cols, b.Cin) || !mul_ok(cols, 32)) return MDCN_ERR_UNSUPPORTED;
-    int64_t seg = b.P;  // sampling-backward threads of one image, at most 32 lanes per point
-    if (!mul_ok(seg, b.dg) || !mul_ok(seg, K) || !mul_ok(seg, 32)) return MDCN_ERR_UNSUPPORTED;
+    // the sampling backward's grid: (pixel blocks, dg*K, images of a chunk)
+    if (static_cast<int64_t>(b.dg) * K > 65535) return MDCN_ERR_UNSUPPORTED;
     mdcn::plan_backward(&b, kBwdL2Budget);
-    // one chunk's sampling-backward grid and the transposes' tile counts fit 32-bit block indices
-    int64_t thr = seg;
-    if (!mul_ok(thr, b.nb) || thr / 256 >= kI31 || (b.H * b.W / 32 + 1) * (b.Cin / 32 + 1) >= kI31)
-        return MDCN_ERR_UNSUPPORTED;
+    // the transposes' tile counts fit 32-bit block indices
+    if ((b.H * b.W / 32 + 1) * (b.Cin / 32 + 1) >= kI31) return MDCN_ERR_UNSUPPORTED;
     *p = b;
     return MDCN_OK;
 }

@@ -158,57 +158,57 @@ __global__ void __launch_bounds__(256) bias_grad_kernel(const T* __restrict__ go
     }
 }
 
-// The sampling backward of one chunk: a segment of `lanes` consecutive
-// threads per sampling point q = ((n*P + p)*dg + gd)*K + k (n within the
-// chunk), each lane taking VEC consecutive channels of the point's
-// deformable group per step. Reads the chunk's channels-last x and column
+// The sampling backward of one chunk. Grid (pixel blocks, dg*K, images of
+// the chunk): a segment of `lanes` consecutive threads per sampling point
+// (pixel p, deformable group gd, tap k of image n), each lane taking VEC
+// consecutive channels of the deformable group per step. Per-point index
+// arithmetic is 32-bit (the planner bounds P, Cin and the coordinates);
+// element offsets are 64-bit. Reads the chunk's channels-last x and column
 // gradients; writes the modulated columns, grad_offset and grad_mask of the
 // point, and adds the corner terms into the fp32 channels-last grad_x.
 template <typename T, int VEC>
-__global__ void __launch_bounds__(256) sample_backward_kernel(const BwdPlan p, const T* __restrict__ xt,
+__global__ void __launch_bounds__(256, 4) sample_backward_kernel(const BwdPlan p, const T* __restrict__ xt,
                                                               const T* __restrict__ offset, const T* __restrict__ mask,
                                                               const float* __restrict__ gcol, T* __restrict__ col,
                                                               float* __restrict__ gx, T* __restrict__ goffset,
-                                                              T* __restrict__ gmask, int64_t n0, int64_t nbc) {
+                                                              T* __restrict__ gmask, int64_t n0) {
     const int lanes = p.lanes;
-    const int64_t K = p.K, P = p.P, dg = p.dg, Cin = p.Cin, Cg = p.Cg;
-    const int64_t points = nbc * P * dg * K;
-    const int64_t q = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / lanes;
+    const int32_t K = p.K, P = static_cast<int32_t>(p.P), Cg = p.Cg;
+    const int32_t pix = static_cast<int32_t>(blockIdx.x) * (256 / lanes) + static_cast<int32_t>(threadIdx.x) / lanes;
+    const int32_t gd = static_cast<int32_t>(blockIdx.y) / K, k = static_cast<int32_t>(blockIdx.y) - gd * K;
+    const int32_t n = static_cast<int32_t>(blockIdx.z);
     const int sub = threadIdx.x & (lanes - 1);
-    const bool live = q < points;
+    const bool live = pix < P;
+    const int64_t ng = n0 + n;
+    const int64_t och = (ng * p.dg + gd) * 2 * K + 2 * k;  // the point's h-offset channel; w follows
+    const int64_t mch = (ng * p.dg + gd) * K + k;
     float s_mask = 0.f, s_h = 0.f, s_w = 0.f, m = 0.f;
-    int64_t och = 0, mch = 0, pix = 0;
     if (live) {
-        const int64_t k = q % K;
-        int64_t t = q / K;
-        const int64_t gd = t % dg;
-        t /= dg;
-        pix = t % P;
-        const int64_t n = t / P, ng = n0 + n;
-        const int64_t ho = pix / p.Wo, wo = pix - ho * p.Wo;
-        const int64_t i = k / p.kw, j = k - i * p.kw;
-        och = (ng * 2 * dg + 2 * gd) * K + 2 * k;  // the point's h-offset channel; w follows
-        mch = (ng * dg + gd) * K + k;
+        const int32_t ho = pix / static_cast<int32_t>(p.Wo), wo = pix - ho * static_cast<int32_t>(p.Wo);
+        const int32_t i = k / static_cast<int32_t>(p.kw), j = k - i * static_cast<int32_t>(p.kw);
         const float offh = to_f(offset[och * P + pix]);
         const float offw = to_f(offset[(och + 1) * P + pix]);
         m = to_f(mask[mch * P + pix]);
         const float h = static_cast<float>(ho * p.sh - p.ph + i * p.dh) + offh;
         const float w = static_cast<float>(wo * p.sw - p.pw + j * p.dw) + offw;
         const bool inside = !(h <= -1.f || h >= static_cast<float>(p.H) || w <= -1.f || w >= static_cast<float>(p.W));
-        const int64_t cbeg = gd * p.Cd, cend = cbeg + p.Cd;
+        const int32_t cbeg = gd * p.Cd, cend = cbeg + p.Cd;
+        // column (gradient) element of channel c: ((n*group + g)*P + pix)*K*Cg + k*Cg + c_l
+        const int64_t prow = static_cast<int64_t>(n) * p.group * P + pix;
+        const int64_t kcg = static_cast<int64_t>(K) * Cg;
         if (inside) {
             const float h0f = floorf(h), w0f = floorf(w);
-            const int64_t y0 = static_cast<int64_t>(h0f), x0 = static_cast<int64_t>(w0f);
+            const int32_t y0 = static_cast<int32_t>(h0f), x0 = static_cast<int32_t>(w0f);
             const float lh = h - h0f, lw = w - w0f, hh = 1.f - lh, hw = 1.f - lw;
             const float w00 = hh * hw, w01 = hh * lw, w10 = lh * hw, w11 = lh * lw;
             const bool v00 = y0 >= 0 && x0 >= 0, v01 = y0 >= 0 && x0 + 1 < p.W;
             const bool v10 = y0 + 1 < p.H && x0 >= 0, v11 = y0 + 1 < p.H && x0 + 1 < p.W;
             // corner (y0, x0) of image n, channels-last; only dereferenced when valid
-            const int64_t a00 = ((n * p.H + y0) * p.W + x0) * Cin;
-            const int64_t a01 = a00 + Cin, a10 = a00 + p.W * Cin, a11 = a10 + Cin;
-            for (int64_t c = cbeg + static_cast<int64_t>(sub) * VEC; c < cend; c += static_cast<int64_t>(lanes) * VEC) {
-                const int64_t g = c / Cg, cl = c - g * Cg;
-                const int64_t gi = (((n * p.group + g) * P + pix) * K + k) * Cg + cl;
+            const int64_t a00 = ((static_cast<int64_t>(n) * p.H + y0) * p.W + x0) * p.Cin;
+            const int64_t a01 = a00 + p.Cin, a10 = a00 + p.W * p.Cin, a11 = a10 + p.Cin;
+            for (int32_t c = cbeg + sub * VEC; c < cend; c += lanes * VEC) {
+                const int32_t g = c / Cg, cl = c - g * Cg;
+                const int64_t gi = (prow + static_cast<int64_t>(g) * P) * kcg + k * Cg + cl;
                 float G[VEC], X00[VEC], X01[VEC], X10[VEC], X11[VEC], cv[VEC];
                 load_f<float, VEC>(gcol + gi, G);
 #pragma unroll
@@ -237,9 +237,9 @@ __global__ void __launch_bounds__(256) sample_backward_kernel(const BwdPlan p, c
             float zero[VEC];
 #pragma unroll
             for (int e = 0; e < VEC; ++e) zero[e] = 0.f;
-            for (int64_t c = cbeg + static_cast<int64_t>(sub) * VEC; c < cend; c += static_cast<int64_t>(lanes) * VEC) {
-                const int64_t g = c / Cg, cl = c - g * Cg;
-                store_f<T, VEC>(col + (((n * p.group + g) * P + pix) * K + k) * Cg + cl, zero);
+            for (int32_t c = cbeg + sub * VEC; c < cend; c += lanes * VEC) {
+                const int32_t g = c / Cg, cl = c - g * Cg;
+                store_f<T, VEC>(col + (prow + static_cast<int64_t>(g) * P) * kcg + k * Cg + cl, zero);
             }
         }
     }
@@ -326,14 +326,15 @@ cudaError_t run_backward(const BwdPlan& p, const T* x, const T* offset, const T*
         }
         // 3. sampling backward
         {
-            const int64_t threads = nbc * P * p.dg * K * p.lanes;
-            const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
+            const int64_t per_block = 256 / p.lanes;
+            const dim3 grid(static_cast<unsigned>((P + per_block - 1) / per_block), static_cast<unsigned>(p.dg * K),
+                            static_cast<unsigned>(nbc));
             if (p.vec == 4)
-                sample_backward_kernel<T, 4><<<blocks, 256, 0, st>>>(p, xt, offset, mask, gcol, col, gx, grad_offset,
-                                                                     grad_mask, n0, nbc);
+                sample_backward_kernel<T, 4><<<grid, 256, 0, st>>>(p, xt, offset, mask, gcol, col, gx, grad_offset,
+                                                                   grad_mask, n0);
             else
-                sample_backward_kernel<T, 1><<<blocks, 256, 0, st>>>(p, xt, offset, mask, gcol, col, gx, grad_offset,
-                                                                     grad_mask, n0, nbc);
+                sample_backward_kernel<T, 1><<<grid, 256, 0, st>>>(p, xt, offset, mask, gcol, col, gx, grad_offset,
+                                                                   grad_mask, n0);
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
         }
         // 4. weight gradient, per image over the groups: (K*Cg x Og) += col (K*Cg x P) * grad_out^T (P x Og)
@@ -363,9 +364,11 @@ cudaError_t run_backward(const BwdPlan& p, const T* x, const T* offset, const T*
 void plan_backward(BwdPlan* p, size_t l2_budget) {
     const size_t es = p->dtype == kF32 ? 4 : 2;
     p->vec = (p->Cg % 4 == 0 && p->Cd % 4 == 0 && p->Cin % 4 == 0) ? 4 : 1;
+    // about four steps per lane: the per-point work (position, weights,
+    // validity, the shuffle reduction) is shared by more channels
     const int64_t units = (p->Cd + p->vec - 1) / p->vec;
     int lanes = 1;
-    while (lanes < 32 && lanes < units) lanes <<= 1;
+    while (lanes < 32 && lanes * 4 < units) lanes <<= 1;
     p->lanes = lanes;
     const size_t cols = static_cast<size_t>(p->P) * p->K * p->Cin;  // column elements of one image
     const size_t pix = static_cast<size_t>(p->H) * p->W * p->Cin;   // x elements of one image
