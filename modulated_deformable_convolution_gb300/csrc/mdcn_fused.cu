@@ -655,7 +655,10 @@ __device__ __forceinline__ void store_chunk16(const Plan& pl, const FusedParams&
     __syncwarp();
 }
 
-template <int DT>
+// One kernel per (I/O type, KG = the plan's kgroups): each instance holds
+// only the gather variant it runs. The smaller binary reaches its first MMA
+// sooner: start-up is dominated by instruction fetches of cold code.
+template <int DT, int KG>
 __global__ void __launch_bounds__(kFusedThreads, 1)
     fused_kernel(const __grid_constant__ CUtensorMap tmap, const FusedParams prm) {
     using T = typename Elem<DT>::T;
@@ -909,8 +912,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         // so G k-tiles are in production at once and a stage (stages are a
         // multiple of G) always belongs to one group. Each of a group's 8/G
         // warps handles 16*G rows as 2*G row-iterations of 8 rows, the corner
-        // loads running 2 row-iterations ahead of the weighted sums. G is a
-        // compile-time constant of each of the three variants below.
+        // loads running 2 row-iterations ahead of the weighted sums. G is the
+        // kernel's compile-time KG.
         const int gw = warp - kWarpGather;
         auto gather = [&](auto g_const) {
             constexpr int G = decltype(g_const)::value;
@@ -1009,12 +1012,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                 sbase += static_cast<uint32_t>(un.k1 - un.k0);
             }
         };
-        if (pl.kgroups == 1)
-            gather(std::integral_constant<int, 1>{});
-        else if (pl.kgroups == 4)
-            gather(std::integral_constant<int, 4>{});
-        else
-            gather(std::integral_constant<int, 2>{});
+        gather(std::integral_constant<int, KG>{});
         setmaxnreg_dec<kRegsLaunch>();
     } else {
         setmaxnreg_dec<kRegsEpi>();
@@ -1218,7 +1216,9 @@ cudaError_t launch_fused_t(const Plan& pl, const void* offset, const void* mask,
     fattr[0].val.programmaticStreamSerializationAllowed = 1;
     fcfg.attrs = fattr;
     fcfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&fcfg, fused_kernel<DT>, tmap, prm);
+    void (*kern)(CUtensorMap, FusedParams) =
+        pl.kgroups == 1 ? fused_kernel<DT, 1> : (pl.kgroups == 4 ? fused_kernel<DT, 4> : fused_kernel<DT, 2>);
+    cudaError_t e = cudaLaunchKernelEx(&fcfg, kern, tmap, prm);
     if (e == cudaSuccess) e = cudaGetLastError();
     return e;
 }
@@ -1230,14 +1230,22 @@ cudaError_t launch_fused_t(const Plan& pl, const void* offset, const void* mask,
 // split, setmaxnreg, is sized for that pool) and holds no static shared
 // memory (the plan may give the whole per-CTA limit to dynamic shared
 // memory); any other build is refused.
-template <int DT>
-static cudaError_t prepare_one(int smem_bytes) {
-    cudaError_t e = cudaFuncSetAttribute(fused_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+template <int DT, int KG>
+static cudaError_t prepare_variant(int smem_bytes) {
+    cudaError_t e = cudaFuncSetAttribute(fused_kernel<DT, KG>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess) return e;
     cudaFuncAttributes attr;
-    e = cudaFuncGetAttributes(&attr, fused_kernel<DT>);
+    e = cudaFuncGetAttributes(&attr, fused_kernel<DT, KG>);
     if (e != cudaSuccess) return e;
     return attr.numRegs == kRegsLaunch && attr.sharedSizeBytes == 0 ? cudaSuccess : cudaErrorInvalidDeviceFunction;
+}
+
+template <int DT>
+static cudaError_t prepare_one(int smem_bytes) {
+    cudaError_t e = prepare_variant<DT, 1>(smem_bytes);
+    if (e == cudaSuccess) e = prepare_variant<DT, 2>(smem_bytes);
+    if (e == cudaSuccess) e = prepare_variant<DT, 4>(smem_bytes);
+    return e;
 }
 
 cudaError_t prepare_fused_attributes(int dtype, int smem_bytes) {
