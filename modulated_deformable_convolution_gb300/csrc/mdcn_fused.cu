@@ -173,12 +173,17 @@ struct TileId {
     int64_t mt;
 };
 
+// Tile indices, k-tile positions and CTA indices fit in 32 bits (the planner
+// keeps the k-tiles of all tiles below 2^31), so their divisions are 32-bit.
 __device__ __forceinline__ TileId decode_tile(const Plan& pl, int64_t t) {
     TileId id;
-    id.mt = t % pl.mtiles;
-    const int64_t r = t / pl.mtiles;
-    id.nt = static_cast<int32_t>(r % pl.ntiles_n);
-    id.g = static_cast<int32_t>(r / pl.ntiles_n);
+    const uint32_t t32 = static_cast<uint32_t>(t);
+    const uint32_t mt = static_cast<uint32_t>(pl.mtiles), nn = static_cast<uint32_t>(pl.ntiles_n);
+    const uint32_t r = t32 / mt;
+    id.mt = t32 - r * mt;
+    const uint32_t g = r / nn;
+    id.nt = static_cast<int32_t>(r - g * nn);
+    id.g = static_cast<int32_t>(g);
     return id;
 }
 
@@ -389,7 +394,7 @@ struct Unit {
 
 __device__ __forceinline__ Unit unit_at(const Plan& pl, int64_t pos, int64_t hi) {
     Unit u;
-    u.t = pos / pl.KT;
+    u.t = static_cast<uint32_t>(pos) / static_cast<uint32_t>(pl.KT);
     u.k0 = static_cast<int32_t>(pos - u.t * pl.KT);
     const int64_t end = hi - u.t * pl.KT;
     u.k1 = static_cast<int32_t>(end < pl.KT ? end : pl.KT);
@@ -437,7 +442,7 @@ __device__ __forceinline__ void cursor_init(const Plan& pl, Cursor& c, int64_t l
     c.hi = hi;
     c.live = lo < hi;
     if (!c.live) return;
-    const int64_t t = lo / pl.KT;
+    const int64_t t = static_cast<uint32_t>(lo) / static_cast<uint32_t>(pl.KT);
     int32_t k = static_cast<int32_t>(lo - t * pl.KT);
     cursor_tile(pl, c, t);
     c.gi = 0;
@@ -739,7 +744,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         Cursor c0;
         cursor_init(pl, c0, lo, hi);
         if (c0.live) {
-            const int64_t gd = (static_cast<int64_t>(c0.g) * pl.Ug + c0.ul) * pl.U / pl.Cd;
+            const int64_t gd = static_cast<uint32_t>((c0.g * pl.Ug + c0.ul) * pl.U) / static_cast<uint32_t>(pl.Cd);
             sample_row_taps<T>(pl, static_cast<const T*>(prm.offset), static_cast<const T*>(prm.mask), c0.mt, gd,
                                threadIdx.x % kTileM, c0.b * kTapBlock, c0.ntbg, threadIdx.x / kTileM, 4,
                                gbase + (d0 - sbase), static_cast<uint32_t>(pl.desc_size));
@@ -753,7 +758,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
 
     // Register split per warpgroup (launch: 128 per thread x 512 threads; the
     // host refuses to launch a build whose register count is not exactly 128):
-    // TMA/MMA/sampling 96, gather 2 x 168, epilogue 80 -> 512 x 128 in total. Each
+    // TMA/MMA/sampling 88, gather 2 x 176, epilogue 72 -> 512 x 128 in total. Each
     // warpgroup's branch starts with its own setmaxnreg, so the compiler
     // allocates each role's code within that role's budget.
     const int wg = warp >> 2;
@@ -889,7 +894,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                                                            prm.status, kSiteTmaEmpty)))
                 break;
             const int64_t unit = static_cast<int64_t>(dc.g) * pl.Ug + dc.ul;
-            const int64_t gd = (unit * pl.U) / pl.Cd;
+            const int64_t gd = static_cast<uint32_t>(unit * pl.U) / static_cast<uint32_t>(pl.Cd);
             uint8_t* ring = gbase + (d0 - sbase) + slot * dslot;
             sample_rows<T>(pl, offset, mask, dc.mt, gd, sid, dc.b * kTapBlock, dc.ntbg, ring, dsz);
             __syncwarp();
@@ -911,14 +916,18 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         // produces every G-th k-tile of the CTA's sequence (steps p, p + G, ...),
         // so G k-tiles are in production at once and a stage (stages are a
         // multiple of G) always belongs to one group. Each of a group's 8/G
-        // warps handles 16*G rows as 2*G row-iterations of 8 rows, the corner
-        // loads running 2 row-iterations ahead of the weighted sums. G is the
-        // kernel's compile-time KG.
+        // warps handles 16*G rows as 2*G row-iterations of 8 rows, with the
+        // corner loads of up to 4 row-iterations in flight (all of a k-tile's
+        // for G <= 2; 4 registered buffers, the gather warps' 176 registers).
+        // G is the kernel's compile-time KG.
         const int gw = warp - kWarpGather;
         auto gather = [&](auto g_const) {
             constexpr int G = decltype(g_const)::value;
             constexpr int wpg = kGatherWarps / G;  // warps per k-tile
             constexpr int nits = 2 * G;            // row-iterations per warp and k-tile
+            // row-iterations whose corner loads are in flight at once (one
+            // register buffer each): all of a k-tile's for G <= 2, else four
+            constexpr int kDepth = nits < 4 ? nits : 4;
             const int pair = gw / wpg;
             GatherCtx<T> cx;
             cx.lane = lane;
@@ -975,9 +984,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                         const int64_t cb = unit * UP + static_cast<int64_t>(ch) * BKc + cx.q4 * 2 * kVec;
                         const char* cbp = reinterpret_cast<const char*>(cx.xt + cb);
                         const uint32_t dtap = dbase + static_cast<uint32_t>(kb * kTileM) * cx.dsz;
-                        RowBuf rb[3];
-                        row_issue<T, kF32Path>(cx, dtap, cbp, 0, rb[0]);
-                        row_issue<T, kF32Path>(cx, dtap, cbp, 1, rb[1]);
+                        RowBuf rb[kDepth];
+#pragma unroll
+                        for (int q = 0; q < kDepth; ++q) row_issue<T, kF32Path>(cx, dtap, cbp, q, rb[q]);
                         // the stage is free once the MMAs that read it completed
                         // (tcgen05.commit); lane 0 polls, the warp follows it
                         int got = 0;
@@ -991,8 +1000,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                         const uint32_t a_s = a0 + st * a_bytes;
 #pragma unroll
                         for (int it = 0; it < nits; ++it) {
-                            if (it + 2 < nits) row_issue<T, kF32Path>(cx, dtap, cbp, it + 2, rb[(it + 2) % 3]);
-                            row_combine<T, kF32Path>(cx, a_s, it, rb[it % 3]);
+                            row_combine<T, kF32Path>(cx, a_s, it, rb[it % kDepth]);
+                            if (it + kDepth < nits)
+                                row_issue<T, kF32Path>(cx, dtap, cbp, it + kDepth, rb[it % kDepth]);
                         }
                         fence_proxy_async_smem();
                         __syncwarp();
@@ -1040,7 +1050,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                                 static_cast<uint32_t>(ab * pl.acc_cols);
             if (un.k0 != 0 || un.k1 != KT) {
                 // a split tile's tail (its head, and owner, is the CTA before)
-                const int64_t c_first = (un.t * KT) / pl.kt_per_cta;
+                const int64_t c_first = static_cast<uint32_t>(un.t * KT) / static_cast<uint32_t>(pl.kt_per_cta);
                 for (int c32 = 0; c32 < pl.acc_cols; c32 += 32)
                     write_partial32<T>(pl, prm.part, blockIdx.x, tl, c32, row);
                 tc_fence_before();
@@ -1097,13 +1107,14 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         const uint32_t tl = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                             static_cast<uint32_t>(ab * pl.acc_cols);
         const bool split = un.k0 != 0 || un.k1 != KT;
-        const int64_t c_first = split ? (un.t * KT) / pl.kt_per_cta : static_cast<int64_t>(blockIdx.x);
+        const uint32_t ktpc = static_cast<uint32_t>(pl.kt_per_cta);
+        const int64_t c_first = split ? static_cast<uint32_t>(un.t * KT) / ktpc : static_cast<int64_t>(blockIdx.x);
         if (c_first != static_cast<int64_t>(blockIdx.x)) {
             for (int c32 = 32 * member; c32 < pl.acc_cols; c32 += 128)
                 write_partial32<T>(pl, prm.part, blockIdx.x, tl, c32, row);
             count_in_split(prm.split_count + c_first, 0, kFusedThreads, threadIdx.x == 0);
         } else {
-            const int32_t m = split ? static_cast<int32_t>((un.t * KT + KT - 1) / pl.kt_per_cta - c_first) : 0;
+            const int32_t m = split ? static_cast<int32_t>(static_cast<uint32_t>(un.t * KT + KT - 1) / ktpc - c_first) : 0;
             if (prm.bias) stage_bias<T>(pl, static_cast<const T*>(prm.bias), id, bias_s, threadIdx.x, kFusedThreads);
             int ok = 1;
             if (m > 0 && threadIdx.x == 0) {

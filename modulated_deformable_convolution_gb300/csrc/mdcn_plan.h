@@ -23,9 +23,9 @@ constexpr int kFusedThreads = 32 * 16;
 // Registers per thread: at launch, and per warpgroup after setmaxnreg
 // (warpgroup 0 = TMA/MMA/sampling, 1-2 = gather, 3 = epilogue).
 constexpr int kRegsLaunch = 128;
-constexpr int kRegsCtrl = 96;
-constexpr int kRegsGather = 168;
-constexpr int kRegsEpi = 80;
+constexpr int kRegsCtrl = 88;
+constexpr int kRegsGather = 176;
+constexpr int kRegsEpi = 72;
 static_assert(kRegsCtrl + 2 * kRegsGather + kRegsEpi == 4 * kRegsLaunch, "warpgroup register split must fit");
 constexpr int kSmemLimit = 227 * 1024;
 constexpr int kMaxCtas = 160;         // persistent CTAs at most (one per SM; the workspace holds a partial slot each)

@@ -124,7 +124,7 @@ __device__ __forceinline__ void nhwc_block_body(const T* __restrict__ x, T* __re
     const int64_t oc0 = (static_cast<int64_t>(by) * 8 + cg) * kVec;  // output channel (padded)
     const int64_t p0 = ((static_cast<int64_t>(bx) * 8 + (threadIdx.x >> 5)) * 4 + pg) * kVec;
     if (oc0 >= Cp || p0 >= P) return;
-    const int32_t unit = static_cast<int32_t>(oc0 / UP);
+    const int32_t unit = static_cast<int32_t>(static_cast<uint32_t>(oc0) / static_cast<uint32_t>(UP));  // Cp < 2^21
     const int32_t within = static_cast<int32_t>(oc0) - unit * UP;
     uint4 in[kVec];
     if (within < U) {
