@@ -14,7 +14,7 @@
 //   grad_weight[o, c_l, k]           = sum over n, p: grad_out[n, o, p] * mask * v
 //   grad_bias[o]                     = sum over n, p: grad_out[n, o, p]
 //
-// Work per chunk of images (sized so its buffers stay in L2):
+// Work per chunk of images (its buffers within a fixed budget):
 //   1. x of the chunk -> channels-last (tiled transpose);
 //   2. G = W_g^T * grad_out per group, one cuBLAS strided-batched GEMM per
 //      group (fp32 out), laid out [n][g][p][k][c_l] so that one sampling
@@ -361,7 +361,7 @@ cudaError_t run_backward(const BwdPlan& p, const T* x, const T* offset, const T*
 
 }  // namespace
 
-void plan_backward(BwdPlan* p, size_t l2_budget) {
+void plan_backward(BwdPlan* p, size_t chunk_budget) {
     const size_t es = p->dtype == kF32 ? 4 : 2;
     p->vec = (p->Cg % 4 == 0 && p->Cd % 4 == 0 && p->Cin % 4 == 0) ? 4 : 1;
     // about four steps per lane: the per-point work (position, weights,
@@ -373,7 +373,7 @@ void plan_backward(BwdPlan* p, size_t l2_budget) {
     const size_t cols = static_cast<size_t>(p->P) * p->K * p->Cin;  // column elements of one image
     const size_t pix = static_cast<size_t>(p->H) * p->W * p->Cin;   // x elements of one image
     const size_t per_image = cols * (4 + es) + pix * (es + 4);
-    int64_t nb = static_cast<int64_t>(l2_budget / (per_image ? per_image : 1));
+    int64_t nb = static_cast<int64_t>(chunk_budget / (per_image ? per_image : 1));
     if (nb < 1) nb = 1;
     if (nb > p->N) nb = p->N;
     if (nb > 65535) nb = 65535;

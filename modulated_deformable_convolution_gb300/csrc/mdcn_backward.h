@@ -35,8 +35,8 @@ struct BwdPlan {
 };
 
 // Fills nb, vec, lanes and the workspace layout of a plan whose problem
-// fields are set; l2_budget = bytes of per-chunk buffers to aim for.
-void plan_backward(BwdPlan* p, size_t l2_budget);
+// fields are set; chunk_budget = bytes of per-chunk buffers to aim for.
+void plan_backward(BwdPlan* p, size_t chunk_budget);
 
 // Every launch of one backward call, on one stream.
 cudaError_t launch_backward(const BwdPlan& p, const void* x, const void* offset, const void* mask, const void* weight,

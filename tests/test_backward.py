@@ -98,7 +98,7 @@ def test_backward_sweep(oracle_mod, case):
 @pytest.mark.parametrize("name", CONFIG_ORDER)
 def test_backward_named_workloads(oracle_mod, name):
     """The five named workloads at full size, every element of every
-    gradient; neck and large-channel run in several image chunks."""
+    gradient; large-channel runs in two image chunks."""
     case = CONFIGS[name]
     inp = make_inputs(case)
     go = make_grad_out(case)
