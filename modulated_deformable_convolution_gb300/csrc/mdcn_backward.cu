@@ -24,8 +24,10 @@
 //      segment by shuffles (deterministic), grad_x goes by fp32 vector
 //      reductions into a channels-last accumulator, and the modulated column
 //      mask * v is written for step 4;
-//   4. grad_weight += grad_out * col^T per image, one strided-batched GEMM
-//      over the groups (fp32 accumulate in workspace);
+//   4. grad_weight += grad_out * col^T (fp32 accumulate in workspace): for
+//      group 1 one GEMM over the chunk's images, after grad_out is re-laid
+//      [Cout][n][P]; otherwise per image, one strided-batched GEMM over the
+//      groups;
 //   5. the fp32 grad_x accumulator -> NCHW in the I/O type.
 // Then the weight gradient to [Cout, Cg, kh, kw] and the bias reduction.
 #include <cublas_v2.h>
@@ -106,6 +108,28 @@ __global__ void __launch_bounds__(256) transpose_kernel(const Tin* __restrict__ 
     for (int t = threadIdx.y; t < 32; t += 8) {
         const int64_t c = c0 + t, r = r0 + threadIdx.x;
         if (r < R && c < C) dst[c * R + r] = from_f<Tout>(tile[threadIdx.x][t]);
+    }
+}
+
+// out[o][n][p] = in[n][o][p] for the chunk's nb images: grad_out with the
+// image index moved inside the channel index (16-byte copies along p when P
+// is a multiple of 16 / sizeof(T), else element copies).
+template <typename T>
+__global__ void __launch_bounds__(256) swap_image_channel_kernel(const T* __restrict__ in, T* __restrict__ out,
+                                                                 int64_t nb, int64_t C, int64_t P) {
+    constexpr int64_t kV = 16 / sizeof(T);
+    const bool vec = P % kV == 0;
+    const int64_t rowlen = vec ? P / kV : P;  // units per (n, o) row
+    const int64_t total = nb * C * rowlen;
+    for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
+         e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t row = e / rowlen, u = e - row * rowlen;
+        const int64_t n = row / C, o = row - n * C;
+        const int64_t dst_row = o * nb + n;
+        if (vec)
+            reinterpret_cast<uint4*>(out + dst_row * P)[u] = reinterpret_cast<const uint4*>(in + row * P)[u];
+        else
+            out[dst_row * P + u] = in[row * P + u];
     }
 }
 
@@ -206,8 +230,11 @@ __global__ void __launch_bounds__(256, 4) sample_backward_kernel(const BwdPlan p
             // corner (y0, x0) of image n, channels-last; only dereferenced when valid
             const int64_t a00 = ((static_cast<int64_t>(n) * p.H + y0) * p.W + x0) * p.Cin;
             const int64_t a01 = a00 + p.Cin, a10 = a00 + p.W * p.Cin, a11 = a10 + p.Cin;
-            for (int32_t c = cbeg + sub * VEC; c < cend; c += lanes * VEC) {
-                const int32_t g = c / Cg, cl = c - g * Cg;
+            // channel c = g * Cg + cl, advanced by the lane stride without a division per step
+            const int32_t cstep = lanes * VEC;
+            int32_t c = cbeg + sub * VEC;
+            int32_t g = c / Cg, cl = c - g * Cg;
+            for (; c < cend; c += cstep) {
                 const int64_t gi = (prow + static_cast<int64_t>(g) * P) * kcg + k * Cg + cl;
                 float G[VEC], X00[VEC], X01[VEC], X10[VEC], X11[VEC], cv[VEC];
                 load_f<float, VEC>(gcol + gi, G);
@@ -232,14 +259,18 @@ __global__ void __launch_bounds__(256, 4) sample_backward_kernel(const BwdPlan p
                 if (v01) red_add<VEC>(gx + a01 + c, G, m * w01);
                 if (v10) red_add<VEC>(gx + a10 + c, G, m * w10);
                 if (v11) red_add<VEC>(gx + a11 + c, G, m * w11);
+                for (cl += cstep; cl >= Cg; cl -= Cg) ++g;
             }
         } else {
             float zero[VEC];
 #pragma unroll
             for (int e = 0; e < VEC; ++e) zero[e] = 0.f;
-            for (int32_t c = cbeg + sub * VEC; c < cend; c += lanes * VEC) {
-                const int32_t g = c / Cg, cl = c - g * Cg;
+            const int32_t cstep = lanes * VEC;
+            int32_t c = cbeg + sub * VEC;
+            int32_t g = c / Cg, cl = c - g * Cg;
+            for (; c < cend; c += cstep) {
                 store_f<T, VEC>(col + (prow + static_cast<int64_t>(g) * P) * kcg + k * Cg + cl, zero);
+                for (cl += cstep; cl >= Cg; cl -= Cg) ++g;
             }
         }
     }
@@ -337,15 +368,31 @@ cudaError_t run_backward(const BwdPlan& p, const T* x, const T* offset, const T*
                                                                    grad_mask, n0);
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
         }
-        // 4. weight gradient, per image over the groups: (K*Cg x Og) += col (K*Cg x P) * grad_out^T (P x Og)
-        for (int64_t n = 0; n < nbc; ++n) {
-            const float* beta = (n0 + n == 0) ? &zero : &one;
-            e = blas_fail(cublasGemmStridedBatchedEx(
-                h, CUBLAS_OP_N, CUBLAS_OP_N, static_cast<int>(KCg), static_cast<int>(Og), static_cast<int>(P), &one,
-                col + n * p.group * P * KCg, blas_type<T>(), static_cast<int>(KCg), P * KCg,
-                grad_out + (n0 + n) * p.Cout * P, blas_type<T>(), static_cast<int>(P), Og * P, beta, gw, CUDA_R_32F,
-                static_cast<int>(KCg), Og * KCg, p.group, ct, CUBLAS_GEMM_DEFAULT));
+        // 4. weight gradient. Group 1: one GEMM over the chunk's images,
+        //    (K*Cg x Cout) += col (K*Cg x nbc*P) * got (nbc*P x Cout), got = grad_out as [Cout][nbc][P];
+        //    otherwise per image over the groups: (K*Cg x Og) += col (K*Cg x P) * grad_out^T (P x Og)
+        if (p.group == 1) {
+            T* got = reinterpret_cast<T*>(base + p.off_got);
+            const int64_t units = nbc * p.Cout * ((P * static_cast<int64_t>(sizeof(T))) % 16 == 0 ? P * sizeof(T) / 16 : P);
+            swap_image_channel_kernel<T><<<grid_for(units), 256, 0, st>>>(grad_out + n0 * p.Cout * P, got, nbc,
+                                                                          p.Cout, P);
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+            const float* beta = n0 == 0 ? &zero : &one;
+            e = blas_fail(cublasGemmEx(h, CUBLAS_OP_N, CUBLAS_OP_N, static_cast<int>(KCg), static_cast<int>(p.Cout),
+                                       static_cast<int>(nbc * P), &one, col, blas_type<T>(), static_cast<int>(KCg), got,
+                                       blas_type<T>(), static_cast<int>(nbc * P), beta, gw, CUDA_R_32F,
+                                       static_cast<int>(KCg), ct, CUBLAS_GEMM_DEFAULT));
             if (e != cudaSuccess) return e;
+        } else {
+            for (int64_t n = 0; n < nbc; ++n) {
+                const float* beta = (n0 + n == 0) ? &zero : &one;
+                e = blas_fail(cublasGemmStridedBatchedEx(
+                    h, CUBLAS_OP_N, CUBLAS_OP_N, static_cast<int>(KCg), static_cast<int>(Og), static_cast<int>(P), &one,
+                    col + n * p.group * P * KCg, blas_type<T>(), static_cast<int>(KCg), P * KCg,
+                    grad_out + (n0 + n) * p.Cout * P, blas_type<T>(), static_cast<int>(P), Og * P, beta, gw,
+                    CUDA_R_32F, static_cast<int>(KCg), Og * KCg, p.group, ct, CUBLAS_GEMM_DEFAULT));
+                if (e != cudaSuccess) return e;
+            }
         }
         // 5. grad_x of the chunk to NCHW
         if ((e = transpose<float, T>(gx, grad_x + n0 * p.Cin * HW, HW, p.Cin, nbc, st)) != cudaSuccess) return e;
@@ -372,7 +419,8 @@ void plan_backward(BwdPlan* p, size_t chunk_budget) {
     p->lanes = lanes;
     const size_t cols = static_cast<size_t>(p->P) * p->K * p->Cin;  // column elements of one image
     const size_t pix = static_cast<size_t>(p->H) * p->W * p->Cin;   // x elements of one image
-    const size_t per_image = cols * (4 + es) + pix * (es + 4);
+    const size_t per_image =
+        cols * (4 + es) + pix * (es + 4) + (p->group == 1 ? static_cast<size_t>(p->Cout) * p->P * es : 0);
     int64_t nb = static_cast<int64_t>(chunk_budget / (per_image ? per_image : 1));
     if (nb < 1) nb = 1;
     if (nb > p->N) nb = p->N;
@@ -392,13 +440,17 @@ void plan_backward(BwdPlan* p, size_t chunk_budget) {
     off += align256(nb * cols * 4);
     p->off_col = off;
     off += align256(nb * cols * es);
+    p->off_got = off;
+    if (p->group == 1) off += align256(static_cast<size_t>(nb) * p->Cout * p->P * es);
     p->ws_bytes = off;
 }
 
 int backward_launch_count(const BwdPlan& p) {
     const int64_t chunks = (p.N + p.nb - 1) / p.nb;
-    // per chunk: transpose, memset, one GEMM per group, sampling backward, one GEMM per image, transpose
-    return static_cast<int>(1 + chunks * (4 + p.group) + p.N + 1 + (p.has_bias ? 1 : 0));
+    // per chunk: transpose, memset, one GEMM per group, sampling backward, the weight-gradient
+    // GEMMs (group 1: a grad_out re-layout and one GEMM; else one per image), transpose
+    const int64_t wgrad = p.group == 1 ? 2 * chunks : p.N;
+    return static_cast<int>(1 + chunks * (4 + p.group) + wgrad + 1 + (p.has_bias ? 1 : 0));
 }
 
 cudaError_t launch_backward(const BwdPlan& p, const void* x, const void* offset, const void* mask, const void* weight,

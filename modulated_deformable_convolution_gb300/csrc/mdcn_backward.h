@@ -21,8 +21,9 @@ struct BwdPlan {
     // ---- sampling-backward kernel
     int32_t vec;       // channels per lane and step: 4 when Cg, Cd and Cin are multiples of 4, else 1
     int32_t lanes;     // lanes per sampling point (power of two, <= 32)
-    // ---- images per chunk: the chunk's column gradients, columns, channels-last x
-    //      and its fp32 grad_x accumulator are sized to stay in L2
+    // ---- images per chunk: the chunk's column gradients, columns, channels-last x,
+    //      fp32 grad_x accumulator (and, for group 1, grad_out as [Cout][n][P]) fit
+    //      a fixed budget
     int64_t nb;
     // ---- workspace layout (byte offsets, 256-byte aligned)
     size_t off_wt;    // weight, tap-major [group][Og][K][Cg] (dtype)
@@ -31,6 +32,8 @@ struct BwdPlan {
     size_t off_gx;    // fp32 grad_x of the chunk, channels-last [nb][H][W][Cin]
     size_t off_gcol;  // fp32 column gradients [nb][group][P][K][Cg]
     size_t off_col;   // modulated columns [nb][group][P][K][Cg] (dtype)
+    size_t off_got;   // group 1 only: grad_out of the chunk as [Cout][nb][P] (dtype), so that
+                      // the weight gradient is one GEMM over the chunk's images
     size_t ws_bytes;
 };
 
