@@ -373,7 +373,8 @@ cudaError_t run_backward(const BwdPlan& p, const T* x, const T* offset, const T*
         //    otherwise per image over the groups: (K*Cg x Og) += col (K*Cg x P) * grad_out^T (P x Og)
         if (p.group == 1) {
             T* got = reinterpret_cast<T*>(base + p.off_got);
-            const int64_t units = nbc * p.Cout * ((P * static_cast<int64_t>(sizeof(T))) % 16 == 0 ? P * sizeof(T) / 16 : P);
+            const int64_t row_units = (P * static_cast<int64_t>(sizeof(T))) % 16 == 0 ? P * sizeof(T) / 16 : P;
+            const int64_t units = nbc * p.Cout * row_units;
             swap_image_channel_kernel<T><<<grid_for(units), 256, 0, st>>>(grad_out + n0 * p.Cout * P, got, nbc,
                                                                           p.Cout, P);
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -424,6 +425,8 @@ void plan_backward(BwdPlan* p, size_t chunk_budget) {
     int64_t nb = static_cast<int64_t>(chunk_budget / (per_image ? per_image : 1));
     if (nb < 1) nb = 1;
     if (nb > p->N) nb = p->N;
+    // the group-1 weight-gradient GEMM runs over nb * P columns (a 32-bit cuBLAS dimension)
+    if (p->group == 1 && nb * p->P > 2147483647) nb = 2147483647 / p->P;
     if (nb > 65535) nb = 65535;
     p->nb = nb;
     const size_t wel = static_cast<size_t>(p->Cout) * p->K * p->Cg;
