@@ -318,3 +318,44 @@ def test_forward_pack_rejects_before_launch(lib):
     assert call(p, dd=bad) == _abi.MDCN_ERR_SHAPE
     assert call(p, nbytes=64) == _abi.MDCN_ERR_WORKSPACE
     lib.mdcn_destroy(h)
+
+
+def _meta(shape, dtype):
+    return torch.empty(shape, dtype=dtype, device="meta")
+
+
+def _bwd_problem(N, Cin, Cout, H, W, group=1, dg=1, k=3, bias=False, dtype=torch.float16):
+    K = k * k
+    t = dict(x=_meta((N, Cin, H, W), dtype), offset=_meta((N, 2 * dg * K, H, W), dtype),
+             mask=_meta((N, dg * K, H, W), dtype), weight=_meta((Cout, Cin // group, k, k), dtype),
+             bias=_meta((Cout,), dtype) if bias else None)
+    return t, mdcn.Handle(stride=1, padding=k // 2, dilation=1, group=group, deformable_group=dg)
+
+
+@pytest.mark.parametrize("N,Cin,Cout,H,group,bias,dtype", [
+    (4, 128, 128, 80, 1, False, torch.float16),   # neck: one chunk
+    (64, 128, 128, 80, 1, True, torch.float16),   # several chunks
+    (2, 256, 256, 100, 4, True, torch.float32),   # grouped: one weight-gradient GEMM per image
+    (3, 8, 6, 9, 2, False, torch.bfloat16),
+])
+def test_backward_chunks_workspace_and_launches(lib, N, Cin, Cout, H, group, bias, dtype):
+    """The backward's host plan: images go in chunks of at most 256 MB of
+    per-chunk buffers (at least one image); the workspace holds the shared
+    weight buffers plus one chunk's buffers; the launch count follows the
+    chunking (group 1: a grad_out re-layout and one weight-gradient GEMM per
+    chunk; otherwise one GEMM per image)."""
+    t, h = _bwd_problem(N, Cin, Cout, H, H, group=group, bias=bias, dtype=dtype)
+    es = torch.empty((), dtype=dtype).element_size()
+    P = H * H
+    K = 9
+    cols, pix = P * K * Cin, H * H * Cin
+    per_image = cols * (4 + es) + pix * (es + 4) + (Cout * P * es if group == 1 else 0)
+    nb = max(1, min(N, (256 << 20) // per_image))
+    chunks = -(-N // nb)
+    ws = mdcn.mdcn_backward_workspace_size(h, t["x"], t["offset"], t["mask"], t["weight"], t["bias"])
+    wel = Cout * K * (Cin // group)
+    assert ws >= wel * es + wel * 4 + nb * per_image
+    assert ws <= wel * es + wel * 4 + nb * per_image + 8 * 256
+    launches = mdcn.mdcn_backward_launches(h, t["x"], t["offset"], t["mask"], t["weight"], t["bias"])
+    wgrad = 2 * chunks if group == 1 else N
+    assert launches == 1 + chunks * (4 + group) + wgrad + 1 + (1 if bias else 0)
