@@ -280,8 +280,9 @@ mdcn_status mdcn_forward_im2col_gemm(mdcn_handle handle, const void* x, const vo
 
 /* Bytes of device workspace mdcn_backward needs (the tap-major weight, an
  * fp32 weight gradient, and per chunk of images: channels-last x, an fp32
- * grad_x accumulator, the fp32 column gradients and the modulated columns;
- * chunks hold as many images as fit in about 256 MB of these, at least one).
+ * grad_x accumulator, the fp32 column gradients, the modulated columns and,
+ * for group 1, grad_out re-laid [Cout][n][Ho*Wo]; chunks hold as many images
+ * as fit in about 256 MB of these, at least one).
  * Host only. Errors as mdcn_workspace_size. */
 mdcn_status mdcn_backward_workspace_size(mdcn_handle handle, const mdcn_dims* dims, mdcn_dtype dtype, size_t* bytes);
 
