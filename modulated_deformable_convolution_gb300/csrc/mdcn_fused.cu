@@ -293,9 +293,10 @@ __device__ __forceinline__ void write_desc(const Plan& pl, const SampleRow<T>& r
 
 // One thread writes the descriptors of tile rows row and row + 64 for taps
 // [tap0, tap0 + ntap) to dst + (kb * kTileM + row) * dsz, kb = tap - tap0;
-// the offset and mask loads of kSampleTaps taps of both rows are issued
+// the offset and mask loads of kRingTaps taps of both rows are issued
 // together.
-constexpr int kSampleTaps = 3;
+constexpr int kSampleTaps = 3;   // the prologue's taps per thread (sample_row_taps)
+constexpr int kRingTaps = 5;     // the sampling warps' taps per round (sample_rows): 30 loads in flight
 
 template <typename T>
 __device__ __forceinline__ void sample_rows(const Plan& pl, const T* __restrict__ offset, const T* __restrict__ mask,
@@ -307,17 +308,17 @@ __device__ __forceinline__ void sample_rows(const Plan& pl, const T* __restrict_
     int32_t i = tap0 / static_cast<int32_t>(pl.kw);
     int32_t j = tap0 - i * static_cast<int32_t>(pl.kw);
 #pragma unroll 1
-    for (int32_t kb0 = 0; kb0 < ntap; kb0 += kSampleTaps) {
-        float v[2][3][kSampleTaps];  // [row][dh, dw, mask][tap]
+    for (int32_t kb0 = 0; kb0 < ntap; kb0 += kRingTaps) {
+        float v[2][3][kRingTaps];  // [row][dh, dw, mask][tap]
         if (pl.plain) {
 #pragma unroll
-            for (int u = 0; u < kSampleTaps; ++u) {
+            for (int u = 0; u < kRingTaps; ++u) {
                 v[0][0][u] = v[0][1][u] = v[1][0][u] = v[1][1][u] = 0.f;
                 v[0][2][u] = v[1][2][u] = 1.f;
             }
         } else {
 #pragma unroll
-            for (int u = 0; u < kSampleTaps; ++u) {
+            for (int u = 0; u < kRingTaps; ++u) {
                 const int64_t kb = kb0 + u < ntap ? kb0 + u : kb0;
                 v[0][0][u] = to_f(ra.po[(2 * kb) * P]);
                 v[0][1][u] = to_f(ra.po[(2 * kb + 1) * P]);
@@ -328,7 +329,7 @@ __device__ __forceinline__ void sample_rows(const Plan& pl, const T* __restrict_
             }
         }
 #pragma unroll
-        for (int u = 0; u < kSampleTaps; ++u) {
+        for (int u = 0; u < kRingTaps; ++u) {
             if (kb0 + u < ntap) {
                 uint8_t* dp = dst + (static_cast<uint32_t>(kb0 + u) * kTileM + row) * dsz;
                 write_desc(pl, ra, i, j, v[0][0][u], v[0][1][u], v[0][2][u], dp);
