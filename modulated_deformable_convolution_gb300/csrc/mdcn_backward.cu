@@ -88,26 +88,37 @@ __device__ __forceinline__ void red_add(float* p, const float (&g)[VEC], float s
 }
 
 // out[b][c][r] = in[b][r][c] for an R x C matrix per batch entry b
-// (blockIdx.y), through a 32 x 33 shared-memory tile; blockIdx.x walks the
-// tiles, column tiles fastest.
+// (blockIdx.y), through a 64 x 65 shared-memory tile; blockIdx.x walks the
+// tiles, column tiles fastest. 256 threads as 64 x 4: each thread has its 16
+// loads in flight before it stores (a 32 x 32 tile per block held too few
+// bytes in flight to approach memory bandwidth).
+constexpr int kTransposeTile = 64;
+
 template <typename Tin, typename Tout>
 __global__ void __launch_bounds__(256) transpose_kernel(const Tin* __restrict__ in, Tout* __restrict__ out, int64_t R,
                                                         int64_t C) {
-    __shared__ float tile[32][33];
+    constexpr int kT = kTransposeTile, kRows = kT / 4;
+    __shared__ float tile[kT][kT + 1];
     const int64_t b = blockIdx.y;
-    const int64_t ctiles = (C + 31) / 32;
-    const int64_t r0 = static_cast<int64_t>(blockIdx.x) / ctiles * 32;
-    const int64_t c0 = static_cast<int64_t>(blockIdx.x) % ctiles * 32;
+    const int64_t ctiles = (C + kT - 1) / kT;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.x) / ctiles * kT;
+    const int64_t c0 = static_cast<int64_t>(blockIdx.x) % ctiles * kT;
     const Tin* src = in + b * R * C;
     Tout* dst = out + b * R * C;
-    for (int t = threadIdx.y; t < 32; t += 8) {
-        const int64_t r = r0 + t, c = c0 + threadIdx.x;
-        if (r < R && c < C) tile[t][threadIdx.x] = to_f(src[r * C + c]);
+    const int tx = threadIdx.x % kT, ty = threadIdx.x / kT;
+    float v[kRows];
+#pragma unroll
+    for (int k = 0; k < kRows; ++k) {
+        const int64_t r = r0 + ty + 4 * k, c = c0 + tx;
+        v[k] = r < R && c < C ? to_f(src[r * C + c]) : 0.f;
     }
+#pragma unroll
+    for (int k = 0; k < kRows; ++k) tile[ty + 4 * k][tx] = v[k];
     __syncthreads();
-    for (int t = threadIdx.y; t < 32; t += 8) {
-        const int64_t c = c0 + t, r = r0 + threadIdx.x;
-        if (r < R && c < C) dst[c * R + r] = from_f<Tout>(tile[threadIdx.x][t]);
+#pragma unroll
+    for (int k = 0; k < kRows; ++k) {
+        const int64_t c = c0 + ty + 4 * k, r = r0 + tx;
+        if (r < R && c < C) dst[c * R + r] = from_f<Tout>(tile[tx][ty + 4 * k]);
     }
 }
 
@@ -308,9 +319,9 @@ unsigned grid_for(int64_t total) {
 
 template <typename Tin, typename Tout>
 cudaError_t transpose(const Tin* in, Tout* out, int64_t R, int64_t C, int64_t batch, cudaStream_t st) {
-    const int64_t tiles = ((R + 31) / 32) * ((C + 31) / 32);
-    transpose_kernel<Tin, Tout><<<dim3(static_cast<unsigned>(tiles), static_cast<unsigned>(batch)), dim3(32, 8), 0,
-                                  st>>>(in, out, R, C);
+    const int64_t tiles = ((R + kTransposeTile - 1) / kTransposeTile) * ((C + kTransposeTile - 1) / kTransposeTile);
+    transpose_kernel<Tin, Tout><<<dim3(static_cast<unsigned>(tiles), static_cast<unsigned>(batch)), 256, 0, st>>>(
+        in, out, R, C);
     return cudaGetLastError();
 }
 
