@@ -35,7 +35,7 @@ sys.path.insert(0, ROOT)
 
 import torch  # noqa: E402
 
-from modulated_deformable_convolution_gb300.workloads import CONFIGS, make_inputs  # noqa: E402
+from modulated_deformable_convolution_gb300.workloads import CONFIG_ORDER, CONFIGS, make_inputs  # noqa: E402
 
 METRIC = "modulated deform-conv fwd TFLOP/s & µs/call at 1 GB300; % of roofline"
 UNIT = "TFLOP/s"
@@ -169,6 +169,112 @@ def profiled_traffic(workload: str):
     except Exception:
         pass
     return None
+
+
+def measure_fp32_peaks(dev, n: int = 8192, reps: int = 10):
+    """Dense fp32-input rates on this GPU, measured in this run with cuBLAS
+    through torch.matmul (n^3 GEMM, 2*n^3 flops, best of `reps`, CUDA events):
+    TF32 tensor cores allowed, and strict fp32. Returns TFLOP/s of each."""
+    a = torch.randn(n, n, device=dev)
+    b = torch.randn(n, n, device=dev)
+    out = {}
+    prev = torch.backends.cuda.matmul.allow_tf32
+    try:
+        for name, tf32 in (("tf32", True), ("fp32_strict", False)):
+            torch.backends.cuda.matmul.allow_tf32 = tf32
+            torch.matmul(a, b)
+            torch.cuda.synchronize()
+            best = float("inf")
+            for _ in range(reps if tf32 else 3):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                torch.matmul(a, b)
+                e1.record()
+                torch.cuda.synchronize()
+                best = min(best, e0.elapsed_time(e1) * 1e-3)
+            out[name] = 2.0 * n ** 3 / best / 1e12
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+    del a, b
+    torch.cuda.empty_cache()
+    return out
+
+
+def peak_for(case, peaks, peak_src, fp32_peaks):
+    """(peak TFLOP/s of the case's contraction, note). fp16/bf16: the measured
+    bf16 burst (fp16 has the same dense rate). fp32: the split-TF32 contraction
+    runs three TF32 MMAs per k-step, so a third of the TF32 rate measured in
+    this run."""
+    if case.dtype == "f32":
+        if fp32_peaks and fp32_peaks.get("tf32"):
+            return fp32_peaks["tf32"] / 3.0, "measured in this run: cuBLAS TF32 8192^3 / 3 passes (split-TF32)"
+        return peaks["bf16_tflops"] * (1.1 / 2.25) / 3.0, f"{peak_src} bf16 burst x nominal tf32/bf16 ratio / 3"
+    return peaks["bf16_tflops"], f"{peak_src} bf16 burst (fp16 has the same dense rate)"
+
+
+def time_forward(mdcn, case, dev, steps, warmup, flush):
+    """Device times of `steps` mdcn_forward calls (L2 flushed before each) and
+    of the fused kernel alone after the step-wise prep calls, on one workload.
+    Returns (step ms list, fused ms list, plan, status)."""
+    d = {k: (None if v is None else v.to(dev)) for k, v in make_inputs(case).items()}
+    x, off, m, w, b = d["x"], d["offset"], d["mask"], d["weight"], d["bias"]
+    h = mdcn.Handle(**case.attrs())
+    ws = torch.empty(mdcn.mdcn_workspace_size(h, x, off, m, w, b), dtype=torch.uint8, device=dev)
+    out = torch.empty(mdcn.mdcn_output_dims(h, x, off, m, w, b), dtype=x.dtype, device=dev)
+    st = torch.cuda.current_stream(dev)
+    plan = mdcn.mdcn_query_plan(h, x, off, m, w, b)
+    for _ in range(warmup):
+        flush.zero_()
+        mdcn.mdcn_forward(h, x, off, m, w, b, out, ws, st)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    fev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda._sleep(int(2e5) * steps)
+    for i in range(steps):
+        flush.zero_()
+        evs[i][0].record(st)
+        mdcn.mdcn_forward(h, x, off, m, w, b, out, ws, st)
+        evs[i][1].record(st)
+    torch.cuda._sleep(int(2e5) * steps)
+    for i in range(steps):
+        flush.zero_()
+        mdcn.mdcn_prepare_input(h, x, off, m, w, b, ws, st)
+        mdcn.mdcn_pack_weight(h, x, off, m, w, b, ws, st)
+        fev[i][0].record(st)
+        mdcn.mdcn_forward_prepared(h, x, off, m, w, b, out, ws, st)
+        fev[i][1].record(st)
+    torch.cuda.synchronize()
+    s, bits = mdcn.mdcn_query_status(ws)
+    return ([a.elapsed_time(c) for a, c in evs], [a.elapsed_time(c) for a, c in fev], plan,
+            "ok" if s == mdcn.MDCN_OK else f"device status {bits:#x}")
+
+
+def per_config_table(mdcn, dev, flush, peaks, peak_src, fp32_peaks, steps=20, warmup=5):
+    """Every named workload through mdcn_forward: µs per call, contraction
+    TFLOP/s, the fused kernel's time, and the roofline fractions of the step
+    and of the fused kernel. Roofline time = max(flops / tensor peak, bytes /
+    HBM bandwidth), bytes = x + offset + mask + weight + bias + output once."""
+    table = {}
+    for name in CONFIG_ORDER:
+        case = CONFIGS[name]
+        step_ms, fused_ms, plan, status = time_forward(mdcn, case, dev, steps, warmup, flush)
+        peak, note = peak_for(case, peaks, peak_src, fp32_peaks)
+        t_mma = case.flops / (peak * 1e12)
+        t_hbm = case.io_bytes / (peaks["hbm_gbs"] * 1e9)
+        roof_s = max(t_mma, t_hbm)
+        us = statistics.mean(step_ms) * 1e3
+        kus = statistics.mean(fused_ms) * 1e3
+        table[name] = {
+            "workload": describe(case), "us_per_call": us, "tflops": case.flops / (us * 1e-6) / 1e12,
+            "kernel_us": kus, "kernel_tflops": case.flops / (kus * 1e-6) / 1e12,
+            "roofline_us": roof_s * 1e6, "bound": "tensor" if t_mma >= t_hbm else "hbm",
+            "frac_step": roof_s / (us * 1e-6), "frac_kernel": roof_s / (kus * 1e-6),
+            "peak_tflops": peak, "peak_source": note, "ctas": plan["ctas"], "split": plan["split"],
+            "launches": plan["launches"], "status": status,
+        }
+        log(f"[per_config] {name}: {us:.1f} us/call, kernel {kus:.1f} us, frac kernel "
+            f"{table[name]['frac_kernel']:.3f}, {status}")
+    return table
 
 
 def cpu_oracle_time(case, inp, budget_s: float = 20.0):
@@ -433,20 +539,25 @@ def run_ours(args, case, world, rank, local, dist):
     except Exception as e:  # context only
         log("backward skipped:", e)
 
+    # every named workload (rank 0 of a single-GPU run), and the fp32 tensor
+    # peaks measured on this GPU for the fp32 workloads' denominators
+    peaks, peak_src = measured_peaks()
+    fp32_peaks = None
+    per_config = None
+    if world == 1 and not args.no_per_config:
+        try:
+            fp32_peaks = measure_fp32_peaks(dev)
+        except Exception as e:  # context only
+            log("fp32 peak measurement skipped:", e)
+        per_config = per_config_table(mdcn, dev, flush, peaks, peak_src, fp32_peaks)
+
     if rank != 0:
         return
     flops = case.flops
     value = world * flops / (ms_max * 1e-3) / 1e12
-    peaks, peak_src = measured_peaks()
     fused_mean_s = statistics.mean(fused_ms) * 1e-3
     achieved = flops / fused_mean_s / 1e12
-    if case.dtype == "f32":
-        # split-TF32: 3 tf32 passes; tf32 dense rate = bf16 rate x (1.1 / 2.25) nominal
-        peak = peaks["bf16_tflops"] * (1.1 / 2.25) / 3.0
-        peak_note = f"{peak_src} bf16 burst x tf32/bf16 nominal ratio / 3 passes"
-    else:
-        peak = peaks["bf16_tflops"]
-        peak_note = f"{peak_src} bf16 burst (fp16 has the same dense rate)"
+    peak, peak_note = peak_for(case, peaks, peak_src, fp32_peaks)
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
             "traffic": profiled_traffic(case.name),
             "kernel": "fused_kernel", "peak_source": peak_note,
@@ -484,6 +595,8 @@ def run_ours(args, case, world, rank, local, dist):
                                                              "tflops": flops / (abl_ms * 1e-3) / 1e12},
         "gpu_launches": plan["launches"] * args.steps,
         "clocks": clk,
+        "fp32_peaks_tflops": fp32_peaks,
+        "per_config": per_config,
     }
     print(json.dumps(line), flush=True)
 
@@ -564,6 +677,8 @@ def main(argv=None):
     ap.add_argument("--config", default="neck_f16", choices=sorted(CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the table of every named workload (and the fp32 peak measurement)")
     ap.add_argument("--fused-only", type=int, default=0, metavar="N",
                     help="profiling aid: time N launches of the fused kernel alone")
     ap.add_argument("--backward-only", type=int, default=0, metavar="N",

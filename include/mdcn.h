@@ -36,6 +36,12 @@
  *   - No C++ exception crosses this interface; every call returns a status.
  *   - A handle is immutable after mdcn_create and may be used from several
  *     threads at once; concurrent forwards must use distinct workspaces.
+ *   - Per-device set-up (kernel attributes, the allocation-free entry
+ *     point's scratch address, cuBLAS handles of the ablation and the
+ *     backward) is done on the first call on each device and kept for the
+ *     life of the process. cudaDeviceReset discards it on the GPU side, so
+ *     do not call the library on a device after resetting it in the same
+ *     process.
  */
 #ifndef MDCN_H
 #define MDCN_H
@@ -328,10 +334,24 @@ mdcn_status mdcn_backward(mdcn_handle handle, const void* x, const void* offset,
  *     Calls that overlap on the GPU (other streams, other threads) race on the
  *     array and must be serialised by the caller.
  *   - Otherwise identical to mdcn_forward: same arguments (minus workspace),
- *     validation, kernels and results; mdcn_query_status does not apply. */
+ *     validation (the device is checked before the array's address is looked
+ *     up, so a GPU of another architecture gets MDCN_ERR_ARCH), kernels and
+ *     results. The device status word lives in the array:
+ *     mdcn_noalloc_query_status reads it. */
 mdcn_status mdcn_forward_noalloc(mdcn_handle handle, const void* x, const void* offset, const void* mask,
                                  const void* weight, const void* bias_or_null, void* out,
                                  const mdcn_dims* dims, mdcn_dtype dtype, void* stream);
+
+/* mdcn_query_status for mdcn_forward_noalloc, whose callers never see the
+ * fixed array's address: reads the status word that the last
+ * mdcn_forward_noalloc on the current device left in the array (synchronising
+ * the stream), stores its raw bits in *device_bits (may be NULL) and clears
+ * it. Returns MDCN_ERR_TIMEOUT when a pipeline wait of that call gave up (its
+ * output is then unspecified), MDCN_OK when the word is clear, MDCN_ERR_ARCH
+ * on a device other than compute capability 10.3, MDCN_ERR_CUDA when a CUDA
+ * call fails. Like the forward, it must not overlap a noalloc forward that is
+ * still running on another stream. The source pages have no counterpart. */
+mdcn_status mdcn_noalloc_query_status(void* stream, uint32_t* device_bits);
 
 /* Reads the device status word that the last mdcn_forward on this workspace
  * left (synchronising the stream), stores its raw bits in *device_bits (may

@@ -98,6 +98,11 @@ mdcn_status check_dims(const mdcn_attrs& a, const mdcn_dims& d, int64_t out[4]) 
     return MDCN_OK;
 }
 
+// One CTA's fp32 partial accumulator of a split tile: acc_cols x 128 rows.
+size_t partial_slot_bytes(const Plan& p) {
+    return static_cast<size_t>(p.acc_cols) * mdcn::kTileM * sizeof(float);
+}
+
 mdcn_status make_plan(const mdcn_attrs& a, const mdcn_tuning& tuning, const mdcn_dims* d, mdcn_dtype dtype,
                       Plan* pl) {
     if (!d || !pl) return MDCN_ERR_NULL;
@@ -248,16 +253,37 @@ mdcn_status make_plan(const mdcn_attrs& a, const mdcn_tuning& tuning, const mdcn
                          ? 1
                          : 0;
     }
-    // stream-K: fp32 partial accumulators of split tiles, one slot per CTA
+    // stream-K: fp32 partial accumulators of split tiles, one slot per CTA.
+    // Whether any tile is split depends on the grid (the SM count), which
+    // finish_plan sets; until then the workspace size is the bound for the
+    // largest grid.
     p.total_kt = p.tiles_total;
     if (!mul_ok(p.total_kt, p.KT) || p.total_kt > kI31) return MDCN_ERR_UNSUPPORTED;  // 32-bit tile arithmetic
-    const int64_t part_bytes = static_cast<int64_t>(mdcn::kMaxCtas) * p.acc_cols * mdcn::kTileM * 4;
     p.off_xt = mdcn::kStatusBytes;
     p.off_wp = align256(p.off_xt + static_cast<size_t>(xt));
     p.off_part = align256(p.off_wp + static_cast<size_t>(wpb));
-    p.ws_bytes = align256(p.off_part + static_cast<size_t>(part_bytes));
+    p.ws_bytes = align256(p.off_part + partial_slot_bytes(p) * mdcn::kMaxCtas);
     *pl = p;
     return MDCN_OK;
+}
+
+// Finishes a plan for a device with `sms` SMs: the persistent grid, each
+// CTA's range of the k-tile sequence, and the workspace size, which holds the
+// partial-sum slots (one per CTA) only when some tile is split between CTAs.
+void finish_plan(Plan* p, const mdcn_tuning& tuning, int sms) {
+    int64_t grid = sms > 0 ? sms : 1;
+    if (grid > mdcn::kMaxCtas) grid = mdcn::kMaxCtas;
+    if (tuning.max_ctas > 0 && tuning.max_ctas < grid) grid = tuning.max_ctas;
+    if (grid > p->total_kt) grid = p->total_kt;
+    // stream-K split: equal consecutive k-tile ranges, none empty. Splitting a
+    // tile costs its other CTAs an fp32 partial write each and its owner a
+    // read of them, so ranges stay whole tiles unless the busiest CTA's share
+    // drops clearly (measured break-even: about 15% plus 4 k-tiles).
+    const int64_t split = (p->total_kt + grid - 1) / grid;
+    const int64_t whole = (p->tiles_total + grid - 1) / grid * p->KT;
+    p->kt_per_cta = split * 115 / 100 + 4 < whole ? split : whole;
+    p->grid = static_cast<int32_t>((p->total_kt + p->kt_per_cta - 1) / p->kt_per_cta);
+    p->ws_bytes = mdcn::splitk_needed(*p) ? align256(p->off_part + partial_slot_bytes(*p) * p->grid) : p->off_part;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -309,23 +335,24 @@ mdcn_status plan_for(const mdcn_attrs& attrs, const mdcn_tuning& tuning, const m
                      size_t ws_bytes, Plan* p) {
     mdcn_status s = make_plan(attrs, tuning, dims, dtype, p);
     if (s != MDCN_OK) return s;
-    if (ws_bytes < p->ws_bytes) return MDCN_ERR_WORKSPACE;
+    // below the size of any plan (no partial slots): refused before the device check
+    if (ws_bytes < p->off_part) return MDCN_ERR_WORKSPACE;
     int sms = 0;
     s = check_device(&sms);
     if (s != MDCN_OK) return s;
-    int64_t grid = sms > 0 ? sms : 1;
-    if (grid > mdcn::kMaxCtas) grid = mdcn::kMaxCtas;
-    if (tuning.max_ctas > 0 && tuning.max_ctas < grid) grid = tuning.max_ctas;
-    if (grid > p->total_kt) grid = p->total_kt;
-    // stream-K split: equal consecutive k-tile ranges, none empty. Splitting a
-    // tile costs its other CTAs an fp32 partial write each and its owner a
-    // read of them, so ranges stay whole tiles unless the busiest CTA's share
-    // drops clearly (measured break-even: about 15% plus 4 k-tiles).
-    const int64_t split = (p->total_kt + grid - 1) / grid;
-    const int64_t whole = (p->tiles_total + grid - 1) / grid * p->KT;
-    p->kt_per_cta = split * 115 / 100 + 4 < whole ? split : whole;
-    p->grid = static_cast<int32_t>((p->total_kt + p->kt_per_cta - 1) / p->kt_per_cta);
+    finish_plan(p, tuning, sms);
+    if (ws_bytes < p->ws_bytes) return MDCN_ERR_WORKSPACE;
     return MDCN_OK;
+}
+
+// Workspace bytes of a forward on the current device, or, where no usable
+// device is current, the bound for any device.
+size_t forward_ws_bytes(const mdcn_tuning& tuning, Plan p) {
+    const int last = g_last_cuda_error;  // a size query does not report the device probe's error
+    int sms = 0;
+    if (check_device(&sms) == MDCN_OK) finish_plan(&p, tuning, sms);
+    g_last_cuda_error = last;
+    return p.ws_bytes;
 }
 
 mdcn_status plan_for_call(mdcn_handle h, const mdcn_dims* dims, mdcn_dtype dtype, size_t ws_bytes, Plan* p) {
@@ -463,7 +490,7 @@ mdcn_status mdcn_workspace_size(mdcn_handle handle, const mdcn_dims* dims, mdcn_
     Plan p;
     mdcn_status s = make_plan(handle->attrs, handle->tuning, dims, dtype, &p);
     if (s != MDCN_OK) return s;
-    *bytes = p.ws_bytes;
+    *bytes = forward_ws_bytes(handle->tuning, p);
     return MDCN_OK;
 }
 
@@ -530,7 +557,7 @@ static mdcn_status host_layout(mdcn_handle h, const mdcn_dims* d, mdcn_dtype dt,
     if (!mul_ok(nout, p.N) || !mul_ok(nout, p.Cout) || !mul_ok(nout, p.Ho) || !mul_ok(nout, p.Wo))
         return MDCN_ERR_UNSUPPORTED;
     L->bytes[5] = static_cast<size_t>(nout);
-    L->bytes[6] = p.ws_bytes;
+    L->bytes[6] = forward_ws_bytes(h->tuning, p);
     size_t at = 0;
     for (int i = 0; i < 7; ++i) {
         L->off[i] = at;
@@ -602,6 +629,8 @@ mdcn_status mdcn_pack_workspace_size(mdcn_handle handle, const mdcn_dims* dims, 
     if (s != MDCN_OK) return s;
     s = make_plan(handle->attrs, handle->tuning, dims, dtype, &pd);
     if (s != MDCN_OK) return s;
+    pf.ws_bytes = forward_ws_bytes(handle->tuning, pf);
+    pd.ws_bytes = forward_ws_bytes(handle->tuning, pd);
     const size_t front = pack_front_bytes(pf, dtype);
     *bytes = front > pd.ws_bytes ? front : pd.ws_bytes;
     return MDCN_OK;

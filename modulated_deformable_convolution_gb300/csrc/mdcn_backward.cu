@@ -35,11 +35,11 @@
 #include <cuda_fp16.h>
 
 #include "mdcn_backward.h"
+#include "mdcn_launch.h"
 #include "mdcn_plan.h"
 
 namespace mdcn {
 
-cublasHandle_t handle_for_current_device();  // mdcn_im2col.cu
 
 namespace {
 
@@ -343,9 +343,9 @@ cudaError_t run_backward(const BwdPlan& p, const T* x, const T* offset, const T*
     const int64_t K = p.K, Cg = p.Cg, Og = p.Og, P = p.P, HW = p.H * p.W, KCg = K * Cg;
     cudaError_t e;
 
-    cublasHandle_t h = handle_for_current_device();
-    if (!h) return cudaErrorNotSupported;
-    if (cublasSetStream(h, st) != CUBLAS_STATUS_SUCCESS) return cudaErrorUnknown;
+    BlasLease lease;
+    if ((e = lease_blas(&lease, st, blas_workspace_in(base + p.off_blas), kBlasWorkspaceBytes)) != cudaSuccess) return e;
+    cublasHandle_t h = lease.h;
     const cublasComputeType_t ct = sizeof(T) == 4 ? CUBLAS_COMPUTE_32F_PEDANTIC : CUBLAS_COMPUTE_32F;
     const float one = 1.0f, zero = 0.0f;
 
@@ -458,6 +458,8 @@ void plan_backward(BwdPlan* p, size_t chunk_budget) {
     off += align256(nb * cols * es);
     p->off_got = off;
     if (p->group == 1) off += align256(static_cast<size_t>(nb) * p->Cout * p->P * es);
+    p->off_blas = off;
+    off += kBlasRegionBytes;
     p->ws_bytes = off;
 }
 

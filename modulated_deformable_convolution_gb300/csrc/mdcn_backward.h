@@ -34,6 +34,7 @@ struct BwdPlan {
     size_t off_col;   // modulated columns [nb][group][P][K][Cg] (dtype)
     size_t off_got;   // group 1 only: grad_out of the chunk as [Cout][nb][P] (dtype), so that
                       // the weight gradient is one GEMM over the chunk's images
+    size_t off_blas;  // the call's cuBLAS workspace region (kBlasRegionBytes)
     size_t ws_bytes;
 };
 

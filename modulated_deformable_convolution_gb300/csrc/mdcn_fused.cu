@@ -19,9 +19,10 @@
 //               128-byte-swizzled store into the A stage
 //   warps 12-15 epilogue: TMEM -> registers -> +bias -> NCHW output. A tile
 //               split between CTAs (stream-K): each CTA but the one holding
-//               its first k-tiles writes an fp32 partial sum to the workspace
-//               and counts itself in; that first CTA, which reaches the tile
-//               last, adds the partials in k order and stores the output
+//               its last k-tiles writes an fp32 partial sum to the workspace
+//               and counts itself in; that last CTA (each CTA processes its
+//               units last to first, so it reaches the tile last) adds the
+//               partials in k order and stores the output
 // Hand-offs use mbarriers; every wait is bounded (mdcn_ptx.cuh), and a wait
 // that gives up raises a CTA-wide abort that every role observes.
 #include <cuda.h>
@@ -70,7 +71,7 @@ struct FusedParams {
     void* out;
     uint32_t* status;
     float* part;           // fp32 partial accumulators of split tiles: one slot per CTA
-    uint32_t* split_count;  // per split tile (by its first CTA): contributors' epilogue warps done
+    uint32_t* split_count;  // per split tile (by its owner, the CTA of its last k-tiles): contributors in
     int32_t epi_vec;        // the plan allows 16-byte output stores and out is 16-byte aligned
     Plan pl;
 };
@@ -386,28 +387,43 @@ __device__ __forceinline__ void sample_row_taps(const Plan& pl, const T* __restr
 // position t*KT + k) and persistent CTA c takes the contiguous range
 // [c*R, min((c+1)*R, total)), R = pl.kt_per_cta. A CTA's range covers
 // "units": pieces of consecutive tiles, a whole tile or a k-range of one. A
-// tile whose k-tiles fall to several CTAs is summed from their fp32 partial
-// accumulators by the last of them to finish (see the epilogue).
+// CTA processes its units from the last to the first (k-tiles ascending
+// within each), so its first unit to finish is the piece of the tile that
+// runs past its range. A tile whose k-tiles fall to several CTAs is owned by
+// the CTA holding its last k-tiles (the highest of them): for that CTA the
+// tile is the unit processed last, while every other contributor processes
+// its piece first, writes an fp32 partial sum and counts itself in. The
+// owner waits only for CTAs of lower index, which are dispatched before it,
+// so no CTA waits for one that may not yet be resident.
 struct Unit {
     int64_t t;        // tile
     int32_t k0, k1;   // k-tile range [k0, k1) of the tile
 };
 
-__device__ __forceinline__ Unit unit_at(const Plan& pl, int64_t pos, int64_t hi) {
+// The last unit of the range [lo, end): the piece of the tile holding
+// position end - 1.
+__device__ __forceinline__ Unit unit_back(const Plan& pl, int64_t lo, int64_t end) {
     Unit u;
-    u.t = static_cast<uint32_t>(pos) / static_cast<uint32_t>(pl.KT);
-    u.k0 = static_cast<int32_t>(pos - u.t * pl.KT);
-    const int64_t end = hi - u.t * pl.KT;
-    u.k1 = static_cast<int32_t>(end < pl.KT ? end : pl.KT);
+    u.t = static_cast<uint32_t>(end - 1) / static_cast<uint32_t>(pl.KT);
+    const int64_t t0 = u.t * pl.KT;
+    u.k0 = static_cast<int32_t>(lo > t0 ? lo - t0 : 0);
+    u.k1 = static_cast<int32_t>(end - t0);
     return u;
 }
 
+// The CTA whose range holds position pos.
+__device__ __forceinline__ int64_t cta_of(const Plan& pl, int64_t pos) {
+    return static_cast<uint32_t>(pos) / static_cast<uint32_t>(pl.kt_per_cta);
+}
+
 // ---------------------------------------------------------------- gather helpers
-// Position in a CTA's k-tile sequence. A tile's k-tiles form descriptor
-// groups (unit ul, tap block b), in the order of the packed weight; each group
-// holds its chunks x taps k-tiles.
+// Position in a CTA's k-tile sequence, in processing order. A tile's k-tiles
+// form descriptor groups (unit ul, tap block b), in the order of the packed
+// weight; each group holds its chunks x taps k-tiles.
 struct Cursor {
-    int64_t pos, hi;      // position in the k-tile sequence, end of the CTA's range
+    int64_t pos;          // position in the k-tile sequence
+    int64_t ustart, uend; // the current unit [ustart, uend)
+    int64_t lo;           // start of the CTA's range
     int64_t t, mt;
     int32_t g, nt;
     int32_t gi, j;        // group, k-tile within the group
@@ -437,15 +453,13 @@ __device__ __forceinline__ void cursor_tile(const Plan& pl, Cursor& c, int64_t t
     c.mt = id.mt;
 }
 
-__device__ __forceinline__ void cursor_init(const Plan& pl, Cursor& c, int64_t lo, int64_t hi) {
-    c.gr = 0;
-    c.pos = lo;
-    c.hi = hi;
-    c.live = lo < hi;
-    if (!c.live) return;
-    const int64_t t = static_cast<uint32_t>(lo) / static_cast<uint32_t>(pl.KT);
-    int32_t k = static_cast<int32_t>(lo - t * pl.KT);
-    cursor_tile(pl, c, t);
+// Enters the unit that ends at c.uend, at its first k-tile.
+__device__ __forceinline__ void cursor_enter_unit(const Plan& pl, Cursor& c) {
+    const Unit un = unit_back(pl, c.lo, c.uend);
+    c.ustart = un.t * pl.KT + un.k0;
+    c.pos = c.ustart;
+    cursor_tile(pl, c, un.t);
+    int32_t k = un.k0;
     c.gi = 0;
     cursor_group(pl, c);
     while (k >= c.nktg) {
@@ -457,21 +471,35 @@ __device__ __forceinline__ void cursor_init(const Plan& pl, Cursor& c, int64_t l
     cursor_ktile(pl, c);
 }
 
+__device__ __forceinline__ void cursor_init(const Plan& pl, Cursor& c, int64_t lo, int64_t hi) {
+    c.gr = 0;
+    c.lo = lo;
+    c.uend = hi;
+    c.live = lo < hi;
+    if (!c.live) return;
+    cursor_enter_unit(pl, c);
+}
+
 __device__ __forceinline__ void cursor_advance(const Plan& pl, Cursor& c) {
-    if (++c.pos >= c.hi) {
-        c.live = false;
+    if (++c.pos >= c.uend) {
+        // the unit is done: on to the piece of the range before it, if any
+        if (c.ustart <= c.lo) {
+            c.live = false;
+            return;
+        }
+        c.uend = c.ustart;
+        ++c.gr;
+        cursor_enter_unit(pl, c);
         return;
     }
     if (++c.j < c.nktg) {
         cursor_ktile(pl, c);
         return;
     }
+    // the next group of the same tile (a unit never crosses a tile boundary)
     c.j = 0;
     ++c.gr;
-    if (++c.gi == pl.Ug * pl.ntb) {
-        c.gi = 0;
-        cursor_tile(pl, c, c.t + 1);
-    }
+    ++c.gi;
     cursor_group(pl, c);
     cursor_ktile(pl, c);
 }
@@ -825,9 +853,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
             const uint32_t sub_step = sub_bytes >> 4, half_step = half_bytes >> 4, alo_step = (kTileM * 128) >> 4;
             uint32_t st = 0, ph = 0, i = 0;
             bool ok = true;
-            for (int64_t pos = lo; pos < hi && ok; ++i) {
-                const Unit un = unit_at(pl, pos, hi);
-                pos = un.t * KT + un.k1;
+            for (int64_t end = hi; end > lo && ok; ++i) {
+                const Unit un = unit_back(pl, lo, end);
+                end = un.t * KT + un.k0;
                 const int ab = static_cast<int>(i % pl.nacc);
                 const uint32_t use = i / pl.nacc;
                 if (!warp_wait2(acce_bar(ab), 0u, (use & 1) ^ 1u, abort_flag, prm.status, kSiteMmaFull)) break;
@@ -953,9 +981,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
             uint32_t gr = 0;     // descriptor groups entered
             uint32_t sbase = 0;  // CTA step of the current unit's first k-tile
             bool ok = true;
-            for (int64_t pos = lo; pos < hi && ok;) {
-                const Unit un = unit_at(pl, pos, hi);
-                pos = un.t * KT + un.k1;
+            for (int64_t end = hi; end > lo && ok;) {
+                const Unit un = unit_back(pl, lo, end);
+                end = un.t * KT + un.k0;
                 const TileId id = decode_tile(pl, un.t);
                 int32_t q = 0;  // first k-tile (processing order) of the current group
                 for (int32_t gi = 0; gi < ngroups && ok && q < un.k1; ++gi) {
@@ -1034,10 +1062,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
         const int row = quarter * 32 + lane;
         uint32_t i = 0;
-        for (int64_t pos = lo; pos < hi; ++i) {
-            const Unit un = unit_at(pl, pos, hi);
-            pos = un.t * KT + un.k1;
-            if (pos >= hi) break;  // the last unit
+        for (int64_t end = hi; end > lo; ++i) {
+            const Unit un = unit_back(pl, lo, end);
+            end = un.t * KT + un.k0;
+            if (end <= lo) break;  // the last unit
             const TileId id = decode_tile(pl, un.t);
             const int ab = static_cast<int>(i % pl.nacc);
             const uint32_t use = i / pl.nacc;
@@ -1050,14 +1078,14 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
             const uint32_t tl = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                 static_cast<uint32_t>(ab * pl.acc_cols);
             if (un.k0 != 0 || un.k1 != KT) {
-                // a split tile's tail (its head, and owner, is the CTA before)
-                const int64_t c_first = static_cast<uint32_t>(un.t * KT) / static_cast<uint32_t>(pl.kt_per_cta);
+                // a split tile's first pieces: its last, and its owner, is a later CTA's
+                const int64_t c_last = cta_of(pl, un.t * KT + KT - 1);
                 for (int c32 = 0; c32 < pl.acc_cols; c32 += 32)
                     write_partial32<T>(pl, prm.part, blockIdx.x, tl, c32, row);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(acce_bar(ab));
-                count_in_split(prm.split_count + c_first, 1, kEpiWarps * 32, warp == kWarpEpi && lane == 0);
+                count_in_split(prm.split_count + c_last, 1, kEpiWarps * 32, warp == kWarpEpi && lane == 0);
                 continue;
             }
             if (prm.bias) {
@@ -1084,23 +1112,24 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
 
     // ---------------------------------------------------------------- tail
     // The pipeline has drained (the MMA warp waited for its last commit): the
-    // CTA's last unit is in tensor memory, and all 16 warps write it out,
-    // warp w taking lane quarter w % 4 and every fourth 32-column block from
-    // block w / 4. A split tile's tail (this CTA's only unit) goes to the
-    // partial slot; the head of a split tile (the owner) waits for the other
-    // contributors and adds their partials in k order from L2.
+    // CTA's last unit (the piece of the range's first tile) is in tensor
+    // memory, and all 16 warps write it out, warp w taking lane quarter w % 4
+    // and every fourth 32-column block from block w / 4. A split tile's piece
+    // other than its last goes to this CTA's partial slot; the CTA holding a
+    // split tile's last k-tiles (the owner) waits for the CTAs before it and
+    // adds their partials, in k order, and its own accumulator last.
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (lo < hi && *abort_flag == 0) {
-        int64_t pos = lo;
+        int64_t end = hi;
         uint32_t nu = 0;
         Unit un;
         do {
-            un = unit_at(pl, pos, hi);
-            pos = un.t * KT + un.k1;
+            un = unit_back(pl, lo, end);
+            end = un.t * KT + un.k0;
             ++nu;
-        } while (pos < hi);
+        } while (end > lo);
         const TileId id = decode_tile(pl, un.t);
         const int ab = static_cast<int>((nu - 1) % pl.nacc);
         const int quarter = warp & 3, member = warp >> 2;
@@ -1108,20 +1137,22 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         const uint32_t tl = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                             static_cast<uint32_t>(ab * pl.acc_cols);
         const bool split = un.k0 != 0 || un.k1 != KT;
-        const uint32_t ktpc = static_cast<uint32_t>(pl.kt_per_cta);
-        const int64_t c_first = split ? static_cast<uint32_t>(un.t * KT) / ktpc : static_cast<int64_t>(blockIdx.x);
-        if (c_first != static_cast<int64_t>(blockIdx.x)) {
+        const int64_t me = blockIdx.x;
+        const int64_t c_last = split ? cta_of(pl, un.t * KT + KT - 1) : me;
+        if (c_last != me) {
             for (int c32 = 32 * member; c32 < pl.acc_cols; c32 += 128)
-                write_partial32<T>(pl, prm.part, blockIdx.x, tl, c32, row);
-            count_in_split(prm.split_count + c_first, 0, kFusedThreads, threadIdx.x == 0);
+                write_partial32<T>(pl, prm.part, me, tl, c32, row);
+            count_in_split(prm.split_count + c_last, 0, kFusedThreads, threadIdx.x == 0);
         } else {
-            const int32_t m = split ? static_cast<int32_t>(static_cast<uint32_t>(un.t * KT + KT - 1) / ktpc - c_first) : 0;
+            // the contributors: CTAs c_first .. me - 1 (none for a whole tile)
+            const int64_t c_first = split ? cta_of(pl, un.t * KT) : me;
+            const int32_t m = static_cast<int32_t>(me - c_first);
             if (prm.bias) stage_bias<T>(pl, static_cast<const T*>(prm.bias), id, bias_s, threadIdx.x, kFusedThreads);
             int ok = 1;
             if (m > 0 && threadIdx.x == 0) {
-                ok = wait_count_bounded(prm.split_count + c_first, static_cast<uint32_t>(m), abort_flag, prm.status,
+                ok = wait_count_bounded(prm.split_count + me, static_cast<uint32_t>(m), abort_flag, prm.status,
                                         kSiteSplitWait);
-                if (ok) prm.split_count[c_first] = 0u;  // every contributor is in: zero again for the next call
+                if (ok) prm.split_count[me] = 0u;  // every contributor is in: zero again for the next call
             }
             if (__syncthreads_and(ok)) {
                 const OutGroup og = out_group<T>(pl, id, quarter, lane);
@@ -1130,8 +1161,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                 for (int c32 = 32 * member; c32 < pl.acc_cols; c32 += 128) {
                     const int nc = min(32, pl.acc_cols - c32);
                     float vals[32];
-                    tmem_ld32(tl + static_cast<uint32_t>(c32), nc == 32 ? 2 : 1, vals);
-                    for (int32_t k = 1; k <= m; ++k) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) vals[e] = 0.f;
+                    for (int32_t k = 0; k < m; ++k) {
                         // one contributor's 32 columns, all loads in flight, then added
                         const float* src = prm.part + ((c_first + k) * pl.acc_cols + c32) * kTileM + row;
                         float pv[32];
@@ -1140,6 +1172,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
 #pragma unroll
                         for (int e = 0; e < 32; ++e) vals[e] += pv[e];
                     }
+                    float own[32];
+                    tmem_ld32(tl + static_cast<uint32_t>(c32), nc == 32 ? 2 : 1, own);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) vals[e] += own[e];
                     store_chunk16<T>(pl, prm, id, og, vals, c32, row, lane, bias_s, stg);
                     if (nc > 16) store_chunk16<T>(pl, prm, id, og, vals + 16, c32 + 16, row, lane, bias_s, stg);
                 }

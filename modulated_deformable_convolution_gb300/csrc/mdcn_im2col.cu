@@ -77,25 +77,41 @@ __global__ void __launch_bounds__(256) bias_convert_kernel(const float* __restri
 }
 
 struct HandleCache {
-    std::mutex mu;
+    std::mutex create_mu;
+    std::mutex use_mu[64];
     cublasHandle_t h[64] = {};
 };
 
+HandleCache& handle_cache() {
+    static HandleCache cache;
+    return cache;
+}
+
 }  // namespace
 
-// One cuBLAS handle per device, created on first use (also used by the
-// backward pass).
-cublasHandle_t handle_for_current_device() {
-    static HandleCache cache;
+// The current device's cuBLAS handle (one per device, created on first use),
+// leased for one call: the lease holds the handle's lock until it is
+// destroyed, and binds the handle to the call's stream and to the call's own
+// workspace region. So calls from other threads neither change the stream
+// under this call's GEMMs nor share cuBLAS scratch with it on the GPU.
+cudaError_t lease_blas(BlasLease* lease, cudaStream_t st, void* blas_ws, size_t blas_ws_bytes) {
+    HandleCache& cache = handle_cache();
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    std::lock_guard<std::mutex> lock(cache.mu);
-    if (!cache.h[dev]) {
-        cublasHandle_t h = nullptr;
-        if (cublasCreate(&h) != CUBLAS_STATUS_SUCCESS) return nullptr;
-        cache.h[dev] = h;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lock(cache.create_mu);
+        if (!cache.h[dev]) {
+            cublasHandle_t h = nullptr;
+            if (cublasCreate(&h) != CUBLAS_STATUS_SUCCESS) return cudaErrorNotSupported;
+            cache.h[dev] = h;
+        }
     }
-    return cache.h[dev];
+    lease->lock = std::unique_lock<std::mutex>(cache.use_mu[dev]);
+    lease->h = cache.h[dev];
+    // cublasSetStream resets the workspace, so the workspace is set after it
+    if (cublasSetStream(lease->h, st) != CUBLAS_STATUS_SUCCESS) return cudaErrorUnknown;
+    if (cublasSetWorkspace(lease->h, blas_ws, blas_ws_bytes) != CUBLAS_STATUS_SUCCESS) return cudaErrorUnknown;
+    return cudaSuccess;
 }
 
 namespace {
@@ -110,6 +126,13 @@ template <>
 constexpr cudaDataType_t cuda_type<__nv_bfloat16>() { return CUDA_R_16BF; }
 
 size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+// Workspace of the ablation: [columns (dtype)][fp32 GEMM output][cuBLAS workspace]
+size_t im2col_blas_offset(const Plan& pl) {
+    const size_t el = pl.dtype == kF32 ? 4 : 2;
+    return align256(static_cast<size_t>(pl.N * pl.Cin * pl.K * pl.P) * el) +
+           align256(static_cast<size_t>(pl.N * pl.Cout * pl.P) * sizeof(float));
+}
 
 template <typename T>
 cudaError_t run_t(const Plan& pl, const void* x, const void* offset, const void* mask, const void* weight,
@@ -126,9 +149,10 @@ cudaError_t run_t(const Plan& pl, const void* x, const void* offset, const void*
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    cublasHandle_t h = handle_for_current_device();
-    if (!h) return cudaErrorNotSupported;
-    if (cublasSetStream(h, st) != CUBLAS_STATUS_SUCCESS) return cudaErrorUnknown;
+    BlasLease lease;
+    if (cudaError_t le = lease_blas(&lease, st, blas_workspace_in(base + im2col_blas_offset(pl)), kBlasWorkspaceBytes); le != cudaSuccess)
+        return le;
+    cublasHandle_t h = lease.h;
     const float one = 1.0f, zero = 0.0f;
     const int64_t CgK = static_cast<int64_t>(pl.Cg) * pl.K;
     const cublasComputeType_t ct = (sizeof(T) == 4) ? CUBLAS_COMPUTE_32F_PEDANTIC : CUBLAS_COMPUTE_32F;
@@ -156,11 +180,7 @@ cudaError_t run_t(const Plan& pl, const void* x, const void* offset, const void*
 
 }  // namespace
 
-size_t im2col_workspace_bytes(const Plan& pl) {
-    const size_t el = pl.dtype == kF32 ? 4 : 2;
-    return align256(static_cast<size_t>(pl.N * pl.Cin * pl.K * pl.P) * el) +
-           align256(static_cast<size_t>(pl.N * pl.Cout * pl.P) * sizeof(float));
-}
+size_t im2col_workspace_bytes(const Plan& pl) { return im2col_blas_offset(pl) + kBlasRegionBytes; }
 
 cudaError_t launch_im2col_gemm(const Plan& pl, const void* x, const void* offset, const void* mask,
                                const void* weight, const void* bias, void* out, void* ws, cudaStream_t st) {

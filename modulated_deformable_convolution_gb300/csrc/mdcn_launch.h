@@ -1,7 +1,10 @@
 // Kernel launchers of libmdcn (internal; the public interface is include/mdcn.h).
 #pragma once
 
+#include <cublas_v2.h>
 #include <cuda_runtime.h>
+
+#include <mutex>
 
 #include "mdcn_plan.h"
 
@@ -33,6 +36,24 @@ cudaError_t launch_split_offset_mask(const Plan& pl, const void* om, void* offse
 
 // Dynamic shared memory the fused kernel may use on this device (set once).
 cudaError_t prepare_fused_attributes(int dtype, int smem_bytes);
+
+// cuBLAS workspace that every call with library GEMMs (the ablation, the
+// backward) carves out of its caller's workspace; the region reserved for it
+// holds 256 bytes more, so that a 256-byte aligned start (cuBLAS's rule) fits
+// in a workspace that is only 16-byte aligned.
+constexpr size_t kBlasWorkspaceBytes = size_t(32) << 20;
+constexpr size_t kBlasRegionBytes = kBlasWorkspaceBytes + 256;
+inline void* blas_workspace_in(void* region) {
+    return reinterpret_cast<void*>((reinterpret_cast<uintptr_t>(region) + 255) & ~static_cast<uintptr_t>(255));
+}
+
+// The current device's cuBLAS handle, locked and bound to one call's stream
+// and cuBLAS workspace (256-byte aligned) until the lease is destroyed.
+struct BlasLease {
+    std::unique_lock<std::mutex> lock;
+    cublasHandle_t h = nullptr;
+};
+cudaError_t lease_blas(BlasLease* lease, cudaStream_t st, void* blas_ws, size_t blas_ws_bytes);
 
 // Ablation: deformable im2col -> cuBLAS GEMM per group -> bias/convert.
 size_t im2col_workspace_bytes(const Plan& pl);

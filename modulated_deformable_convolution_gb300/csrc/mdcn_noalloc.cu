@@ -23,25 +23,32 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 
 constexpr int kMaxDevices = 64;
 
-struct DeviceScratch {
-    std::once_flag once;
-    void* ptr = nullptr;
-    cudaError_t err = cudaSuccess;
-};
+std::mutex g_scratch_mutex;
+void* g_scratch_ptr[kMaxDevices] = {};  // set once per device, on success only
 
-DeviceScratch g_scratch[kMaxDevices];
-
-// Device address of the array on the current device. In host code the array's
-// name is only a host-side stand-in, so its device address is looked up once
-// per device, with that device current, and cached.
+// Device address of the array on the current device. The device is checked
+// first (compute capability 10.3, the only architecture the library is built
+// for), so a call on another GPU gets MDCN_ERR_ARCH, as mdcn_forward returns.
+// In host code the array's name is only a host-side stand-in, so its device
+// address is looked up with cudaGetSymbolAddress, once per device with that
+// device current, and cached; a failed look-up is not cached and is retried
+// by the next call.
 mdcn_status scratch_on_current_device(void** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MDCN_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return MDCN_ERR_UNSUPPORTED;
-    DeviceScratch& d = g_scratch[dev];
-    std::call_once(d.once, [&d] { d.err = cudaGetSymbolAddress(&d.ptr, g_noalloc_scratch); });
-    if (d.err != cudaSuccess || d.ptr == nullptr) return MDCN_ERR_CUDA;
-    *out = d.ptr;
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (g_scratch_ptr[dev] == nullptr) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return MDCN_ERR_CUDA;
+        if (major != 10 || minor != 3) return MDCN_ERR_ARCH;
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return MDCN_ERR_CUDA;
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
     return MDCN_OK;
 }
 
@@ -62,4 +69,14 @@ extern "C" mdcn_status mdcn_forward_noalloc(mdcn_handle handle, const void* x, c
     // reads from scratch is written earlier in the same call.
     return mdcn_forward(handle, x, offset, mask, weight, bias_or_null, out, scratch, kNoAllocScratchBytes, dims, dtype,
                         stream);
+}
+
+// The status word of the fixed array on the current device: what the last
+// mdcn_forward_noalloc on this device left there, read and cleared like
+// mdcn_query_status does for a caller's workspace.
+extern "C" mdcn_status mdcn_noalloc_query_status(void* stream, uint32_t* device_bits) {
+    void* scratch = nullptr;
+    const mdcn_status s = scratch_on_current_device(&scratch);
+    if (s != MDCN_OK) return s;
+    return mdcn_query_status(scratch, stream, device_bits);
 }

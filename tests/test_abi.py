@@ -341,7 +341,8 @@ def _bwd_problem(N, Cin, Cout, H, W, group=1, dg=1, k=3, bias=False, dtype=torch
 def test_backward_chunks_workspace_and_launches(lib, N, Cin, Cout, H, group, bias, dtype):
     """The backward's host plan: images go in chunks of at most 256 MB of
     per-chunk buffers (at least one image); the workspace holds the shared
-    weight buffers plus one chunk's buffers; the launch count follows the
+    weight buffers, one chunk's buffers and the call's cuBLAS workspace; the
+    launch count follows the
     chunking (group 1: a grad_out re-layout and one weight-gradient GEMM per
     chunk; otherwise one GEMM per image)."""
     t, h = _bwd_problem(N, Cin, Cout, H, H, group=group, bias=bias, dtype=dtype)
@@ -354,8 +355,9 @@ def test_backward_chunks_workspace_and_launches(lib, N, Cin, Cout, H, group, bia
     chunks = -(-N // nb)
     ws = mdcn.mdcn_backward_workspace_size(h, t["x"], t["offset"], t["mask"], t["weight"], t["bias"])
     wel = Cout * K * (Cin // group)
-    assert ws >= wel * es + wel * 4 + nb * per_image
-    assert ws <= wel * es + wel * 4 + nb * per_image + 8 * 256
+    blas = (32 << 20) + 256  # the call's own cuBLAS workspace (256-byte aligned inside the region)
+    assert ws >= wel * es + wel * 4 + nb * per_image + blas
+    assert ws <= wel * es + wel * 4 + nb * per_image + blas + 8 * 256
     launches = mdcn.mdcn_backward_launches(h, t["x"], t["offset"], t["mask"], t["weight"], t["bias"])
     wgrad = 2 * chunks if group == 1 else N
     assert launches == 1 + chunks * (4 + group) + wgrad + 1 + (1 if bias else 0)

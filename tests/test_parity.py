@@ -26,9 +26,20 @@ def np64(t):
     return None if t is None else t.detach().to("cpu", torch.float64).numpy()
 
 
+_REF_CACHE = {}
+
+
 def oracle_out(oracle_mod, case, inp, ho_range=None):
-    return oracle_mod.forward(np64(inp["x"]), np64(inp["offset"]), np64(inp["mask"]), np64(inp["weight"]),
+    """The oracle's output for a case. Full outputs of the named workloads
+    (inputs untouched) are computed once per session."""
+    key = (case.name, case.seed) if ho_range is None and case.name in CONFIGS and case == CONFIGS[case.name] else None
+    if key is not None and key in _REF_CACHE:
+        return _REF_CACHE[key]
+    ref = oracle_mod.forward(np64(inp["x"]), np64(inp["offset"]), np64(inp["mask"]), np64(inp["weight"]),
                               np64(inp["bias"]), ho_range=ho_range, **case.attrs())
+    if key is not None:
+        _REF_CACHE[key] = ref
+    return ref
 
 
 def gpu_out(case, inp, algo="fused", check_status=True, tuning=None):
@@ -66,23 +77,15 @@ def compare(gpu, ref, dtype, label):
     assert ratio <= TOL[dtype], f"{label}: {ratio:.3e} > {TOL[dtype]}"
 
 
-def sample_rows(Ho):
-    return sorted({0, 1, Ho // 2, Ho - 1})
-
-
 @pytest.mark.parametrize("name", CONFIG_ORDER)
 def test_named_workloads(oracle_mod, name):
     """The five named workloads at full size, in the launch configuration the
-    benchmark times; the oracle computes sampled output rows (first, second,
-    middle, last: every border) for all images and channels."""
+    benchmark times: every element of the output against the oracle."""
     case = CONFIGS[name]
     inp = make_inputs(case)
     gpu = np64(gpu_out(case, inp))
-    Ho, _ = case.out_hw
-    rows = sample_rows(Ho) if Ho > 4 else list(range(Ho))
-    for r in rows:
-        ref = oracle_out(oracle_mod, case, inp, ho_range=(r, r + 1))
-        compare(gpu[:, :, r], ref[:, :, r], case.dtype, f"{name} row {r}")
+    ref = oracle_out(oracle_mod, case, inp)
+    compare(gpu, ref, case.dtype, name)
 
 
 SWEEP = [
@@ -165,14 +168,13 @@ def test_tunings_agree_bitwise():
                          ids=["ctas40_whole_tiles", "ctas7", "ctas151", "linear_tiles"])
 def test_split_points_move(oracle_mod, tuning):
     """Other CTA counts and tile shapes split other tiles between CTAs (and
-    max_ctas=40 splits none on this shape): every result stays within the
-    tolerance, on rows that cross tile and split boundaries."""
+    max_ctas=40 splits none on this shape): every element stays within the
+    tolerance."""
     case = CONFIGS["neck_f16"]
     inp = make_inputs(case)
     gpu = np64(gpu_out(case, inp, tuning=tuning))
-    for r in (0, 7, 8, 40, 79):
-        ref = oracle_out(oracle_mod, case, inp, ho_range=(r, r + 1))
-        compare(gpu[:, :, r], ref[:, :, r], case.dtype, f"neck {tuning} row {r}")
+    ref = oracle_out(oracle_mod, case, inp)
+    compare(gpu, ref, case.dtype, f"neck {tuning}")
 
 
 @pytest.mark.parametrize("case", [SWEEP[0], SWEEP[1], SWEEP[2], SWEEP[3]], ids=lambda c: c.name)
@@ -187,9 +189,8 @@ def test_im2col_gemm_neck_f16(oracle_mod):
     case = CONFIGS["neck_f16"]
     inp = make_inputs(case)
     gpu = np64(gpu_out(case, inp, algo="im2col_gemm"))
-    for r in (0, 40, 79):
-        ref = oracle_out(oracle_mod, case, inp, ho_range=(r, r + 1))
-        compare(gpu[:, :, r], ref[:, :, r], case.dtype, f"im2col neck row {r}")
+    ref = oracle_out(oracle_mod, case, inp)
+    compare(gpu, ref, case.dtype, "im2col neck")
 
 
 def test_query_plan_split_choice():
