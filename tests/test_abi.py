@@ -361,3 +361,26 @@ def test_backward_chunks_workspace_and_launches(lib, N, Cin, Cout, H, group, bia
     launches = mdcn.mdcn_backward_launches(h, t["x"], t["offset"], t["mask"], t["weight"], t["bias"])
     wgrad = 2 * chunks if group == 1 else N
     assert launches == 1 + chunks * (4 + group) + wgrad + 1 + (1 if bias else 0)
+
+
+@pytest.mark.parametrize("what,d,ok", [
+    # output pixels N*Ho*Wo (Ho, Wo come from offset, independent of x): 2^31 refused, 2^31 - 1 accepted
+    ("pixels", dict(N=2, Cin=8, H=8, W=8, Cout=8, Ho=1 << 15, Wo=1 << 15), False),
+    ("pixels", dict(N=(1 << 31) - 1, Cin=8, H=1, W=1, Cout=8, Ho=1, Wo=1), True),
+    # input pixels N*H*W of the channels-last copy
+    ("x pixels", dict(N=2, Cin=8, H=1 << 15, W=1 << 15, Cout=8, Ho=4, Wo=4), False),
+    # k-tiles of all tiles: 256 groups x (2^19 tiles of 128 pixels) x 16 k-tiles (4x4 taps, 64 channels)
+    ("k-tiles", dict(N=1, Cin=16384, H=8, W=8, Cout=4096, Ho=8192, Wo=8192, kh=4, kw=4, group=256), False),
+    ("k-tiles", dict(N=1, Cin=16384, H=8, W=8, Cout=4096, Ho=8184, Wo=8192, kh=4, kw=4, group=256), True),
+])
+def test_32bit_limits_at_2_pow_31(lib, what, d, ok):
+    """The kernels index pixels, tiles and k-tiles with 32-bit integers; the
+    planner refuses (MDCN_ERR_UNSUPPORTED, before anything runs) every call
+    whose count of output pixels, input pixels or k-tiles reaches 2^31, and
+    accepts the same shapes just below it."""
+    group = d.pop("group", 1)
+    h = handle(lib, padding=(0, 0), group=group)
+    dd = dims(bias=False, group=group, **d)
+    s, n = ws_size(lib, h, dd, _abi.MDCN_F16)
+    assert s == (_abi.MDCN_OK if ok else _abi.MDCN_ERR_UNSUPPORTED), (what, s)
+    lib.mdcn_destroy(h)
