@@ -101,16 +101,23 @@ mdcn_status mdcn_create(const mdcn_attrs* attrs, mdcn_handle* out);
 
 /* Optional overrides of the fused kernel's automatic execution plan, for
  * benchmarking and tuning. Results are bitwise identical for every stages and
- * kgroups setting; tile_mode and max_ctas move the points where output tiles
- * are split between CTAs, which changes the order of some fp32 additions. A zero
- * (or -1 for tile_mode) keeps the automatic choice. */
+ * kgroups setting with the same a_operand; a_operand changes which channels
+ * share each tensor-core K-step (the rounding of the fp32 sums), tile_mode and
+ * max_ctas move the points where output tiles are split between CTAs, which
+ * changes the order of some fp32 additions. A zero (or -1 for tile_mode)
+ * keeps the automatic choice. */
 typedef struct mdcn_tuning {
-    int32_t stages;    /* shared-memory pipeline stages: 2, 4, 6 or 8 (0: automatic) */
+    int32_t stages;    /* pipeline stages: 2, 4, 6 or 8 (0: automatic) */
     int32_t tile_mode; /* pixel tile: 0 = 128 consecutive pixels of N*Ho*Wo, 1 = 8x16 block of one image,
                           -1 = automatic */
     int32_t max_ctas;  /* cap on persistent CTAs (0: one per SM) */
     int32_t kgroups;   /* k-tiles the gather warps produce at once: 1, 2 or 4, dividing the stage count
                           (0: automatic) */
+    int32_t a_operand; /* where the modulated columns (the MMA's A operand) are staged: 1 = shared memory,
+                          2 = tensor memory (float16/bfloat16 with kgroups 2 only; the accumulators and
+                          32 columns per stage must fit the 512 tensor-memory columns, with one
+                          accumulator if two do not fit), 0 = automatic (tensor memory where it fits
+                          beside two accumulators) */
 } mdcn_tuning;
 
 /* mdcn_create with plan overrides (tuning may be NULL = automatic). Errors as
@@ -149,6 +156,7 @@ typedef struct mdcn_plan_info {
     int32_t stages, kgroups, tile_mode;
     int32_t launches;       /* kernels one mdcn_forward launches: prep (1, or 2 when x needs the staged
                                transpose) and the fused kernel */
+    int32_t a_operand;      /* 1: A stages in shared memory, 2: in tensor memory */
 } mdcn_plan_info;
 
 /* Errors as mdcn_workspace_size, plus MDCN_ERR_ARCH / MDCN_ERR_CUDA from the
@@ -157,13 +165,15 @@ mdcn_status mdcn_query_plan(mdcn_handle handle, const mdcn_dims* dims, mdcn_dtyp
 
 /* The forward pass (section 5, steps 1-3) as one fused implicit-GEMM kernel:
  * producer warps compute each sampling point from offset and mask, gather
- * and modulate the columns straight into shared memory, tcgen05 tensor-core
- * MMAs accumulate in tensor memory, the epilogue adds the bias and writes
- * NCHW. The im2col column matrix never reaches device memory. Persistent CTAs
- * (one per SM) take equal consecutive ranges of the k-tiles of all output
- * tiles (stream-K). A tile split between CTAs is finished by the CTA holding
- * its first k-tiles, which reaches it last: it adds the other CTAs' fp32
- * partial sums, in k order, before its epilogue. One small kernel runs
+ * and modulate the columns straight into the tensor core's operand stages
+ * (tensor memory, or shared memory where the plan keeps them there), tcgen05
+ * tensor-core MMAs accumulate in tensor memory, the epilogue adds the bias
+ * and writes NCHW. The im2col column matrix never reaches device memory.
+ * Persistent CTAs (one per SM) take equal consecutive ranges of the k-tiles
+ * of all output tiles (stream-K). A tile split between CTAs is finished by
+ * the CTA holding its last k-tiles, which processes its ranges last to first
+ * and so reaches it last: it adds the other CTAs' fp32 partial sums, in k
+ * order, before its epilogue. One small kernel runs
  * first, into workspace: x to channels-last and the weight repack (two
  * launches for shapes whose transpose needs the staged kernel).
  *   x [N,Cin,H,W], offset [N,2*dg*kh*kw,Ho,Wo], mask [N,dg*kh*kw,Ho,Wo],

@@ -176,9 +176,6 @@ mdcn_status make_plan(const mdcn_attrs& a, const mdcn_tuning& tuning, const mdcn
     }
     p.acc_cols = p.nsub * p.BNs;
     p.nacc = 2 * p.acc_cols <= 512 ? 2 : 1;
-    int32_t cols = 32;
-    while (cols < p.nacc * p.acc_cols) cols <<= 1;
-    p.tmem_cols = cols;
 
     // pixel tiles: 8 x 16 blocks of one image when they waste (almost) no rows,
     // else 128 consecutive pixels of N*Ho*Wo
@@ -210,6 +207,33 @@ mdcn_status make_plan(const mdcn_attrs& a, const mdcn_tuning& tuning, const mdcn
     }
     p.epi_bytes = mdcn::kEpiWarps * 16 * 32 * static_cast<int32_t>(elem);
     const int32_t fixed = 1024 + 2 * p.desc_slot_bytes + p.epi_bytes + mdcn::kBiasBytes + 512;
+    // automatic: 2 k-tiles in production at once, which hides the gather's
+    // latency while the contraction of a k-tile is short; 1 (all 8 warps on
+    // one k-tile) when the accumulator is wider than 256 columns and each
+    // k-tile's contraction takes about as long as its gather (measured on
+    // the named workloads)
+    p.kgroups = tuning.kgroups > 0 ? tuning.kgroups : (p.acc_cols > 256 ? 1 : 2);
+    // A stages in tensor memory (32 columns each, after the accumulators):
+    // 16-bit types whose gather warps form 2 groups (each warp then writes the
+    // tile rows of its own tensor-memory lane quarter). Automatic where they fit
+    // beside the accumulators; a request for them drops to one accumulator if
+    // two leave no room.
+    {
+        const int32_t st_req = tuning.stages > 0 ? tuning.stages : 4;
+        const int32_t room = 512 - 32 * st_req;
+        int32_t a_tmem = 0;
+        if (tuning.a_operand != 1 && elem == 2 && p.kgroups == 2) {
+            if (p.nacc * p.acc_cols <= room) {
+                a_tmem = 1;
+            } else if (tuning.a_operand == 2 && p.acc_cols <= room) {
+                p.nacc = 1;
+                a_tmem = 1;
+            }
+        }
+        if (tuning.a_operand == 2 && !a_tmem) return MDCN_ERR_UNSUPPORTED;
+        p.a_tmem = a_tmem;
+        if (a_tmem) p.a_bytes = 0;  // no A stages in shared memory
+    }
     const int32_t per_stage = p.a_bytes + p.b_bytes;
     // stages: 2, 4, 6 or 8; the gather produces kgroups k-tiles at once (1, 2
     // or 4, dividing the stage count)
@@ -217,14 +241,16 @@ mdcn_status make_plan(const mdcn_attrs& a, const mdcn_tuning& tuning, const mdcn
     int32_t stages = tuning.stages > 0 ? tuning.stages : (max_stages >= 4 ? 4 : 2);
     if (stages < 2 || stages > 8 || (stages & 1) || stages > max_stages) return MDCN_ERR_UNSUPPORTED;
     p.stages = stages;
-    // automatic: 2 k-tiles in production at once, which hides the gather's
-    // latency while the contraction of a k-tile is short; 1 (all 8 warps on
-    // one k-tile) when the accumulator is wider than 256 columns and each
-    // k-tile's contraction takes about as long as its gather (measured on
-    // the named workloads)
-    p.kgroups = tuning.kgroups > 0 ? tuning.kgroups : (p.acc_cols > 256 ? 1 : 2);
     if (stages % p.kgroups != 0) return MDCN_ERR_UNSUPPORTED;
     p.smem_bytes = fixed + stages * per_stage;
+    p.a_col0 = p.nacc * p.acc_cols;
+    {
+        const int32_t used = p.a_col0 + (p.a_tmem ? 32 * stages : 0);
+        if (used > 512) return MDCN_ERR_UNSUPPORTED;
+        int32_t cols = 32;
+        while (cols < used) cols <<= 1;
+        p.tmem_cols = cols;
+    }
     p.grid = 0;  // set at launch from the SM count
 
     // workspace: [status word, split-tile counters: 1 KB][x channels-last][packed weight][partials]
@@ -454,11 +480,12 @@ extern "C" {
 mdcn_status mdcn_create_tuned(const mdcn_attrs* attrs, const mdcn_tuning* tuning, mdcn_handle* out) {
     if (!attrs || !out) return MDCN_ERR_NULL;
     if (!attrs_valid(*attrs)) return MDCN_ERR_ATTR;
-    mdcn_tuning tu{0, -1, 0, 0};
+    mdcn_tuning tu{0, -1, 0, 0, 0};
     if (tuning) {
         tu = *tuning;
         if (tu.stages < 0 || tu.stages == 1 || tu.stages > 8 || tu.tile_mode < -1 || tu.tile_mode > 1 ||
-            tu.max_ctas < 0 || !(tu.kgroups == 0 || tu.kgroups == 1 || tu.kgroups == 2 || tu.kgroups == 4))
+            tu.max_ctas < 0 || !(tu.kgroups == 0 || tu.kgroups == 1 || tu.kgroups == 2 || tu.kgroups == 4) ||
+            tu.a_operand < 0 || tu.a_operand > 2)
             return MDCN_ERR_ATTR;
     }
     mdcn_handle h = new (std::nothrow) mdcn_handle_;
@@ -510,6 +537,7 @@ mdcn_status mdcn_query_plan(mdcn_handle handle, const mdcn_dims* dims, mdcn_dtyp
     info->kgroups = p.kgroups;
     info->tile_mode = p.tile_mode;
     info->launches = p.xt_block ? 2 : 3;
+    info->a_operand = p.a_tmem ? 2 : 1;
     return MDCN_OK;
 }
 

@@ -564,19 +564,38 @@ __device__ __forceinline__ void row_issue(const GatherCtx<T>& cx, uint32_t dtap,
     }
 }
 
-// Weighted sum of the 4 corners of row-iteration it into the A stage a_s.
-template <typename T, bool kF32Path>
-__device__ __forceinline__ void row_combine(const GatherCtx<T>& cx, uint32_t a_s, int it, const RowBuf& rb) {
-    // rows of a row-iteration are 8 apart in 128-byte lines: row & 7 == rsub
-    const uint32_t o0 = cx.row_sts + static_cast<uint32_t>(it) * 1024u, o1 = o0 ^ 16u;
+// 16-bit: the lane's 8 blended channel pairs of a row (pair m = channels
+// 16*q4 + 2m, + 1 of the k-tile), m = 4*hv + j for the corner loads' half hv
+// and word j.
+template <typename T>
+__device__ __forceinline__ void blend_row16(const RowBuf& rb, uint32_t (&v)[8]) {
     const uint4 w = rb.w;
+    T* tag = nullptr;
 #pragma unroll
     for (int hv = 0; hv < 2; ++hv) {
         const uint4 a = rb.v[0][hv], b = rb.v[1][hv], c = rb.v[2][hv], d = rb.v[3][hv];
-        const uint32_t o = hv ? o1 : o0;
-        if constexpr (kF32Path) {
-            const float w00 = __uint_as_float(w.x), w01 = __uint_as_float(w.y);
-            const float w10 = __uint_as_float(w.z), w11 = __uint_as_float(w.w);
+        v[4 * hv + 0] = blend(w.z, w.w, a.x, b.x, c.x, d.x, tag);
+        v[4 * hv + 1] = blend(w.z, w.w, a.y, b.y, c.y, d.y, tag);
+        v[4 * hv + 2] = blend(w.z, w.w, a.z, b.z, c.z, d.z, tag);
+        v[4 * hv + 3] = blend(w.z, w.w, a.w, b.w, c.w, d.w, tag);
+    }
+}
+
+// Weighted sum of the 4 corners of row-iteration it into the A stage a_s:
+// the lane's 32 bytes are 16-byte chunks 2*q4 and 2*q4 + 1 of its row
+// (128-byte swizzle; channels in their natural order). Rows of a
+// row-iteration are 8 apart in 128-byte lines: row & 7 == rsub.
+template <typename T, bool kF32Path>
+__device__ __forceinline__ void row_combine(const GatherCtx<T>& cx, uint32_t a_s, int it, const RowBuf& rb) {
+    const uint32_t o0 = cx.row_sts + static_cast<uint32_t>(it) * 1024u, o1 = o0 ^ 16u;
+    if constexpr (kF32Path) {
+        const uint4 w = rb.w;
+        const float w00 = __uint_as_float(w.x), w01 = __uint_as_float(w.y);
+        const float w10 = __uint_as_float(w.z), w11 = __uint_as_float(w.w);
+#pragma unroll
+        for (int hv = 0; hv < 2; ++hv) {
+            const uint4 a = rb.v[0][hv], b = rb.v[1][hv], c = rb.v[2][hv], d = rb.v[3][hv];
+            const uint32_t o = hv ? o1 : o0;
             const float s0 = blend_f32(w00, w01, w10, w11, a.x, b.x, c.x, d.x);
             const float s1 = blend_f32(w00, w01, w10, w11, a.y, b.y, c.y, d.y);
             const float s2 = blend_f32(w00, w01, w10, w11, a.z, b.z, c.z, d.z);
@@ -585,12 +604,34 @@ __device__ __forceinline__ void row_combine(const GatherCtx<T>& cx, uint32_t a_s
             sts128(a_s + o, __float_as_uint(h0), __float_as_uint(h1), __float_as_uint(h2), __float_as_uint(h3));
             sts128(a_s + kTileM * 128 + o, __float_as_uint(s0 - h0), __float_as_uint(s1 - h1),
                    __float_as_uint(s2 - h2), __float_as_uint(s3 - h3));
-        } else {
-            T* tag = nullptr;
-            sts128(a_s + o, blend(w.z, w.w, a.x, b.x, c.x, d.x, tag), blend(w.z, w.w, a.y, b.y, c.y, d.y, tag),
-                   blend(w.z, w.w, a.z, b.z, c.z, d.z, tag), blend(w.z, w.w, a.w, b.w, c.w, d.w, tag));
         }
+    } else {
+        uint32_t v[8];
+        blend_row16<T>(rb, v);
+        sts128(a_s + o0, v[0], v[1], v[2], v[3]);
+        sts128(a_s + o1, v[4], v[5], v[6], v[7]);
     }
+}
+
+// 16-bit, A in tensor memory: row-iterations it (rows r) and it + 1 (rows
+// r + 8) of the lane, one 16-row block, stored with one 16x256b.x4 fragment
+// at ta (lane = the block's first row, column = the stage's first). Fragment
+// register 4k + h (h < 2: row r, else r + 8) goes to column 8k + 2*q4 + h % 2;
+// it holds pair 2k + h % 2, so that column holds channels whose K position
+// the tensor-memory K order (kperm16, which the packed weight follows) gives.
+template <typename T>
+__device__ __forceinline__ void rows_to_tmem(uint32_t ta, const RowBuf& ra, const RowBuf& rb) {
+    uint32_t va[8], vb[8], r[16];
+    blend_row16<T>(ra, va);
+    blend_row16<T>(rb, vb);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        r[4 * k + 0] = va[2 * k];
+        r[4 * k + 1] = va[2 * k + 1];
+        r[4 * k + 2] = vb[2 * k];
+        r[4 * k + 3] = vb[2 * k + 1];
+    }
+    tmem_st_16x256b_x4(ta, r);
 }
 
 // ---------------------------------------------------------------- epilogue helpers
@@ -689,14 +730,18 @@ __device__ __forceinline__ void store_chunk16(const Plan& pl, const FusedParams&
     __syncwarp();
 }
 
-// One kernel per (I/O type, KG = the plan's kgroups): each instance holds
-// only the gather variant it runs. The smaller binary reaches its first MMA
-// sooner: start-up is dominated by instruction fetches of cold code.
-template <int DT, int KG>
+// One kernel per (I/O type, KG = the plan's kgroups, AT = A stages in tensor
+// memory): each instance holds only the gather variant it runs. The smaller
+// binary reaches its first MMA sooner: start-up is dominated by instruction
+// fetches of cold code.
+template <int DT, int KG, bool AT>
 __global__ void __launch_bounds__(kFusedThreads, 1)
     fused_kernel(const __grid_constant__ CUtensorMap tmap, const FusedParams prm) {
     using T = typename Elem<DT>::T;
     constexpr bool kF32Path = (DT == kF32);
+    // tensor-memory A stages: each of a group's 4 warps writes the 32 tile rows
+    // of its own lane quarter (warp % 4), two 16-row fragments per k-tile
+    static_assert(!AT || (!kF32Path && KG == 2), "A in tensor memory: 16-bit types, two k-groups");
     const Plan& pl = prm.pl;
 
     extern __shared__ uint8_t smem_raw[];
@@ -870,6 +915,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                     tc_fence_after();
                     const uint64_t ad = adesc0 + st * a_step;
                     const uint64_t bd = bdesc0 + st * b_step;
+                    // A in tensor memory: stage st at column a_col0 + 32*st, 8 columns per K-step
+                    const uint32_t at = tmem_base + static_cast<uint32_t>(pl.a_col0) + 32u * st;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {  // 4 MMA K-steps of 32 bytes per 128-byte k-tile
                         const uint32_t accum = (kt > un.k0 || kk > 0) ? 1u : 0u;
@@ -879,7 +926,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                                 const uint32_t d = dacc + static_cast<uint32_t>(j * pl.BNs);
                                 const uint64_t adesc = ad + 2u * kk;
                                 const uint64_t bdesc = bd + j * sub_step + 2u * kk;
-                                if constexpr (kF32Path) {
+                                if constexpr (AT) {
+                                    mma_f16_ts_elect(d, at + 8u * kk, bdesc, idesc, accum);
+                                } else if constexpr (kF32Path) {
                                     mma_tf32_elect(d, adesc, bdesc, idesc, accum);
                                     mma_tf32_elect(d, adesc, bdesc + half_step, idesc, 1u);
                                     mma_tf32_elect(d, adesc + alo_step, bdesc, idesc, 1u);
@@ -1026,14 +1075,28 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                             ok = false;
                             break;
                         }
-                        const uint32_t a_s = a0 + st * a_bytes;
+                        if constexpr (AT) {
+                            // after the MMAs that read the stage: 16-row fragments
+                            // (row-iterations 2p, 2p + 1) into the warp's lane quarter
+                            static_assert(nits == kDepth && nits % 2 == 0, "every row-iteration loaded up front");
+                            tc_fence_after();
+                            const uint32_t ta = tmem_base + (static_cast<uint32_t>(cx.row0) << 16) +
+                                                static_cast<uint32_t>(pl.a_col0) + 32u * st;
 #pragma unroll
-                        for (int it = 0; it < nits; ++it) {
-                            row_combine<T, kF32Path>(cx, a_s, it, rb[it % kDepth]);
-                            if (it + kDepth < nits)
-                                row_issue<T, kF32Path>(cx, dtap, cbp, it + kDepth, rb[it % kDepth]);
+                            for (int pr = 0; pr < nits / 2; ++pr)
+                                rows_to_tmem<T>(ta + ((16u * pr) << 16), rb[2 * pr], rb[2 * pr + 1]);
+                            tmem_wait_st();
+                            tc_fence_before();
+                        } else {
+                            const uint32_t a_s = a0 + st * a_bytes;
+#pragma unroll
+                            for (int it = 0; it < nits; ++it) {
+                                row_combine<T, kF32Path>(cx, a_s, it, rb[it % kDepth]);
+                                if (it + kDepth < nits)
+                                    row_issue<T, kF32Path>(cx, dtap, cbp, it + kDepth, rb[it % kDepth]);
+                            }
+                            fence_proxy_async_smem();
                         }
-                        fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(full_bar(st));
                         st += G;
@@ -1265,7 +1328,13 @@ cudaError_t launch_fused_t(const Plan& pl, const void* offset, const void* mask,
     fcfg.attrs = fattr;
     fcfg.numAttrs = 1;
     void (*kern)(CUtensorMap, FusedParams) =
-        pl.kgroups == 1 ? fused_kernel<DT, 1> : (pl.kgroups == 4 ? fused_kernel<DT, 4> : fused_kernel<DT, 2>);
+        pl.kgroups == 1 ? fused_kernel<DT, 1, false>
+                        : (pl.kgroups == 4 ? fused_kernel<DT, 4, false> : fused_kernel<DT, 2, false>);
+    if constexpr (DT != kF32) {
+        if (pl.a_tmem) kern = fused_kernel<DT, 2, true>;
+    } else {
+        if (pl.a_tmem) return cudaErrorInvalidValue;  // the planner never stages fp32 A in tensor memory
+    }
     cudaError_t e = cudaLaunchKernelEx(&fcfg, kern, tmap, prm);
     if (e == cudaSuccess) e = cudaGetLastError();
     return e;
@@ -1278,21 +1347,24 @@ cudaError_t launch_fused_t(const Plan& pl, const void* offset, const void* mask,
 // split, setmaxnreg, is sized for that pool) and holds no static shared
 // memory (the plan may give the whole per-CTA limit to dynamic shared
 // memory); any other build is refused.
-template <int DT, int KG>
+template <int DT, int KG, bool AT>
 static cudaError_t prepare_variant(int smem_bytes) {
-    cudaError_t e = cudaFuncSetAttribute(fused_kernel<DT, KG>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    cudaError_t e =
+        cudaFuncSetAttribute(fused_kernel<DT, KG, AT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess) return e;
     cudaFuncAttributes attr;
-    e = cudaFuncGetAttributes(&attr, fused_kernel<DT, KG>);
+    e = cudaFuncGetAttributes(&attr, fused_kernel<DT, KG, AT>);
     if (e != cudaSuccess) return e;
     return attr.numRegs == kRegsLaunch && attr.sharedSizeBytes == 0 ? cudaSuccess : cudaErrorInvalidDeviceFunction;
 }
 
 template <int DT>
 static cudaError_t prepare_one(int smem_bytes) {
-    cudaError_t e = prepare_variant<DT, 1>(smem_bytes);
-    if (e == cudaSuccess) e = prepare_variant<DT, 2>(smem_bytes);
-    if (e == cudaSuccess) e = prepare_variant<DT, 4>(smem_bytes);
+    cudaError_t e = prepare_variant<DT, 1, false>(smem_bytes);
+    if (e == cudaSuccess) e = prepare_variant<DT, 2, false>(smem_bytes);
+    if (e == cudaSuccess) e = prepare_variant<DT, 4, false>(smem_bytes);
+    if constexpr (DT != kF32)
+        if (e == cudaSuccess) e = prepare_variant<DT, 2, true>(smem_bytes);
     return e;
 }
 

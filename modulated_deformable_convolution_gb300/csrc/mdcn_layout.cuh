@@ -27,6 +27,19 @@ struct KTile {
     int32_t ntb; // taps in this block
 };
 
+// Order of the 64 channels of a 16-bit k-tile along the contraction index
+// when the A stages live in tensor memory. The gather's four lanes of a tile
+// row hold 16 consecutive channels each (lane q: channels 16q .. 16q+15, as 8
+// pairs) and write them with the 16x256b tensor-memory store, whose fragment
+// gives thread q of a row the 32-bit columns 8a + 2q and 8a + 2q + 1 (a = 0..3).
+// So channel 16q + 4a + 2b + e sits at K position 16a + 4q + 2b + e (the
+// two-bit fields q and a swapped), and the packed weight follows the same
+// order, which leaves the contraction unchanged. The map is its own inverse.
+// Shared-memory A stages keep the natural order.
+__host__ __device__ __forceinline__ int32_t kperm16(int32_t ci) {
+    return (ci & ~0x3c) | ((ci & 0x30) >> 2) | ((ci & 0x0c) << 2);
+}
+
 __host__ __device__ __forceinline__ KTile decode_ktile(int32_t kt, int32_t K, int32_t nch) {
     KTile t;
     const int32_t per_unit = K * nch;

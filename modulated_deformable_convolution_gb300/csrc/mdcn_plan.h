@@ -75,6 +75,10 @@ struct Plan {
     int32_t acc_cols;        // TMEM columns of one accumulator = nsub * BNs
     int32_t nacc;            // accumulators in TMEM (2: epilogue overlaps the next tile)
     int32_t tmem_cols;
+    int32_t a_tmem;          // 1: the A stages (modulated columns) live in tensor memory, written by the
+                             //    gather with tcgen05.st and read by the MMA from there (16-bit types, 2
+                             //    k-groups); 0: 128-byte-swizzled shared-memory stages
+    int32_t a_col0;          // tensor-memory column of A stage 0 (after the accumulators); stage s at + 32*s
     int32_t stages;          // 2, 4, 6 or 8
     int32_t kgroups;         // k-tiles produced concurrently by the gather warps (1, 2 or 4; divides stages)
     int32_t a_bytes;         // one A stage (both tf32 halves for f32)

@@ -202,7 +202,9 @@ __device__ __forceinline__ void pack_weight_body(const T* __restrict__ weight, T
     const int32_t ci = static_cast<int32_t>(threadIdx.x) % pl.BKc;
     if (kt >= pl.KT) return;
     const KTile t = decode_ktile(kt, pl.K, pl.nch);
-    const int32_t within = t.ch * pl.BKc + ci;  // channel within the unit
+    // channel within the unit held at K position ci of the k-tile (A stages in
+    // tensor memory: the order of the gather's fragments, kperm16)
+    const int32_t within = t.ch * pl.BKc + (pl.a_tmem ? kperm16(ci) : ci);
     const int64_t cl = static_cast<int64_t>(t.ul) * pl.U + within;  // channel within the group
     // kRows rows per iteration: their loads are in flight together
     constexpr int kRows = pack_rows<T>();

@@ -310,6 +310,19 @@ __device__ __forceinline__ void mma_f16_elect(uint32_t d_tmem, uint64_t adesc, u
         : "memory");
 }
 
+// The same with the A operand in tensor memory (a_tmem: lane = row of A,
+// 32-bit column c = K elements 2c and 2c + 1 of the instruction's 16).
+__device__ __forceinline__ void mma_f16_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 __device__ __forceinline__ void mma_tf32_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                                uint32_t accumulate) {
     asm volatile(
@@ -415,6 +428,22 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, int n, float (&v)[64])
 #pragma unroll
     for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
+
+// 16 lanes x 256 bits, repeated over 4 consecutive 8-column blocks: thread t
+// writes r[4k], r[4k+1] to lane (taddr.lane + t/4), columns taddr.col + 8k +
+// 2(t%4) and + 1, and r[4k+2], r[4k+3] to lane (taddr.lane + 8 + t/4), the
+// same columns. taddr.lane must lie in the warp's lane quarter.
+__device__ __forceinline__ void tmem_st_16x256b_x4(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.16x256b.x4.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+          "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+// Waits until this thread's tensor-memory stores have completed.
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // 256-bit read-only global load (32-byte aligned address).
 __device__ __forceinline__ void ldg256(const void* p, uint4& a, uint4& b) {

@@ -69,9 +69,9 @@ def test_create_rejects_out_of_range_attrs(lib, bad):
 
 
 @pytest.mark.parametrize("tuning,ok", [
-    ((0, -1, 0, 0), True), ((4, 1, 8, 4), True), ((2, 0, 0, 1), True), ((6, -1, 0, 2), True),
-    ((0, -1, 0, 3), False), ((0, -1, 0, 8), False), ((1, -1, 0, 0), False), ((10, -1, 0, 0), False),
-    ((0, 2, 0, 0), False), ((0, -1, -1, 0), False),
+    ((0, -1, 0, 0, 0), True), ((4, 1, 8, 4, 1), True), ((2, 0, 0, 1, 0), True), ((6, -1, 0, 2, 2), True),
+    ((0, -1, 0, 3, 0), False), ((0, -1, 0, 8, 0), False), ((1, -1, 0, 0, 0), False), ((10, -1, 0, 0, 0), False),
+    ((0, 2, 0, 0, 0), False), ((0, -1, -1, 0, 0), False), ((0, -1, 0, 0, 3), False), ((0, -1, 0, 0, -1), False),
 ])
 def test_create_tuned_validates(lib, tuning, ok):
     h = ctypes.c_void_p()

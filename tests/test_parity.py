@@ -143,6 +143,13 @@ TUNED = [
     # fp32, 10 tiles of 9 k-tiles over 4 CTAs: 23 k-tiles each, tiles split at three points
     (Case("f32_split4", "f32", N=1, Cin=64, Cout=48, H=24, W=24, group=2, deformable_group=2, bias=True, seed=48,
           offset_dist=("normal", 2.0)), dict(max_ctas=4)),
+    # A stages in tensor memory: bf16, 2 groups x 2 deformable groups, 8 stages, tiles split over 5 CTAs
+    (Case("bf16_tmemA_g2_split", "bf16", N=2, Cin=64, Cout=96, H=20, W=24, group=2, deformable_group=2, bias=True,
+          seed=49, offset_dist=("normal", 2.0)), dict(a_operand=2, stages=8, max_ctas=5)),
+    # A stages in tensor memory with one accumulator (Cout = 256 leaves no room for two), linear tiles, f16
+    (Case("f16_tmemA_cout256", "f16", N=1, Cin=128, Cout=256, H=13, W=27, bias=True, seed=50), dict(a_operand=2)),
+    # the same shape with A in shared memory
+    (Case("f16_smemA_cout256", "f16", N=1, Cin=128, Cout=256, H=13, W=27, bias=True, seed=50), dict(a_operand=1)),
 ]
 
 
@@ -155,13 +162,35 @@ def test_tuned_plans(oracle_mod, case, tuning):
 
 
 def test_tunings_agree_bitwise():
-    """The stage count and the number of k-tiles produced at once do not change
-    which sums are formed nor their order: outputs are bitwise equal."""
+    """With the A stages in one place (shared or tensor memory), the stage count
+    and the number of k-tiles produced at once do not change which sums are
+    formed nor their order: outputs are bitwise equal."""
     case = CONFIGS["neck_f16"]
     inp = make_inputs(case)
-    ref = gpu_out(case, inp)
-    for tuning in (dict(stages=2), dict(stages=4, kgroups=4), dict(stages=4, kgroups=1), dict(stages=2, kgroups=1)):
-        assert torch.equal(gpu_out(case, inp, tuning=tuning), ref), tuning
+    smem = gpu_out(case, inp, tuning=dict(a_operand=1))
+    for tuning in (dict(a_operand=1, stages=2), dict(stages=4, kgroups=4), dict(stages=4, kgroups=1),
+                   dict(stages=2, kgroups=1)):
+        assert torch.equal(gpu_out(case, inp, tuning=tuning), smem), tuning
+    tmem = gpu_out(case, inp)
+    for tuning in (dict(stages=2), dict(a_operand=2, stages=8), dict(stages=6)):
+        assert torch.equal(gpu_out(case, inp, tuning=tuning), tmem), tuning
+
+
+@pytest.mark.parametrize("name", ["neck_f16", "multidg_bf16"])
+def test_a_operand_places_agree(oracle_mod, name):
+    """A in tensor memory (one accumulator where two do not fit beside the
+    stages) and in shared memory: both within the tolerance of the oracle on
+    every element, and within a few fp32 roundings of each other."""
+    case = CONFIGS[name]
+    inp = make_inputs(case)
+    ref = oracle_out(oracle_mod, case, inp)
+    outs = [np64(gpu_out(case, inp, tuning=dict(a_operand=a))) for a in (1, 2)]
+    for a, g in zip((1, 2), outs):
+        compare(g, ref, case.dtype, f"{name} a_operand={a}")
+    # the two differ only in fp32 rounding inside the accumulation, which can
+    # move an output by at most one unit in the last place of its 16-bit type
+    ulp = {"f16": 2.0 ** -10, "bf16": 2.0 ** -7}[case.dtype]
+    assert np.abs(outs[0] - outs[1]).max() <= ulp * np.abs(outs[0]).max()
 
 
 @pytest.mark.parametrize("tuning", [dict(max_ctas=40), dict(max_ctas=7), dict(max_ctas=151), dict(tile_mode=0)],
@@ -199,12 +228,13 @@ def test_query_plan_split_choice():
     split would not pay (largec: 2 tiles of 72 k-tiles per CTA)."""
     dev = torch.device("cuda", 0)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    for name, split in (("neck_f16", 1), ("largec_f16", 0)):
+    for name, split, a_operand in (("neck_f16", 1, 2), ("largec_f16", 0, 1), ("multidg_bf16", 1, 1)):
         case = CONFIGS[name]
         d = {k: (None if v is None else v.to(dev)) for k, v in make_inputs(case).items()}
         h = mdcn.Handle(**case.attrs())
         plan = mdcn.mdcn_query_plan(h, d["x"], d["offset"], d["mask"], d["weight"], d["bias"])
         assert plan["split"] == split, (name, plan)
+        assert plan["a_operand"] == a_operand, (name, plan)
         assert plan["launches"] == 2  # one prep launch (transpose + pack), the fused kernel
         assert plan["ctas"] <= sms and plan["ctas"] * plan["ktiles_per_cta"] >= plan["tiles"] * plan["ktiles_per_tile"]
         if not split:
