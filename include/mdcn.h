@@ -116,8 +116,10 @@ typedef struct mdcn_tuning {
     int32_t a_operand; /* where the modulated columns (the MMA's A operand) are staged: 1 = shared memory,
                           2 = tensor memory (float16/bfloat16 with kgroups 2 only; the accumulators and
                           32 columns per stage must fit the 512 tensor-memory columns, with one
-                          accumulator if two do not fit), 0 = automatic (tensor memory where it fits
-                          beside two accumulators) */
+                          accumulator if two do not fit), 0 = automatic (tensor memory wherever it
+                          is allowed) */
+    int32_t ntile;     /* most output channels one tile holds: a multiple of 16 up to 512 (0: automatic).
+                          Narrower tiles gather each pixel's columns once per tile of its group */
 } mdcn_tuning;
 
 /* mdcn_create with plan overrides (tuning may be NULL = automatic). Errors as

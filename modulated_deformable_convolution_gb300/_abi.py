@@ -37,7 +37,7 @@ class mdcn_attrs(ctypes.Structure):
 
 class mdcn_tuning(ctypes.Structure):
     _fields_ = [("stages", ctypes.c_int32), ("tile_mode", ctypes.c_int32), ("max_ctas", ctypes.c_int32),
-                ("kgroups", ctypes.c_int32), ("a_operand", ctypes.c_int32)]
+                ("kgroups", ctypes.c_int32), ("a_operand", ctypes.c_int32), ("ntile", ctypes.c_int32)]
 
 
 class mdcn_plan_info(ctypes.Structure):

@@ -69,9 +69,11 @@ def test_create_rejects_out_of_range_attrs(lib, bad):
 
 
 @pytest.mark.parametrize("tuning,ok", [
-    ((0, -1, 0, 0, 0), True), ((4, 1, 8, 4, 1), True), ((2, 0, 0, 1, 0), True), ((6, -1, 0, 2, 2), True),
-    ((0, -1, 0, 3, 0), False), ((0, -1, 0, 8, 0), False), ((1, -1, 0, 0, 0), False), ((10, -1, 0, 0, 0), False),
-    ((0, 2, 0, 0, 0), False), ((0, -1, -1, 0, 0), False), ((0, -1, 0, 0, 3), False), ((0, -1, 0, 0, -1), False),
+    ((0, -1, 0, 0, 0, 0), True), ((4, 1, 8, 4, 1, 256), True), ((2, 0, 0, 1, 0, 16), True),
+    ((6, -1, 0, 2, 2, 512), True), ((0, -1, 0, 3, 0, 0), False), ((0, -1, 0, 8, 0, 0), False),
+    ((1, -1, 0, 0, 0, 0), False), ((10, -1, 0, 0, 0, 0), False), ((0, 2, 0, 0, 0, 0), False),
+    ((0, -1, -1, 0, 0, 0), False), ((0, -1, 0, 0, 3, 0), False), ((0, -1, 0, 0, -1, 0), False),
+    ((0, -1, 0, 0, 0, 24), False), ((0, -1, 0, 0, 0, 528), False), ((0, -1, 0, 0, 0, -16), False),
 ])
 def test_create_tuned_validates(lib, tuning, ok):
     h = ctypes.c_void_p()

@@ -179,8 +179,8 @@ def test_tunings_agree_bitwise():
 @pytest.mark.parametrize("name", ["neck_f16", "multidg_bf16"])
 def test_a_operand_places_agree(oracle_mod, name):
     """A in tensor memory (one accumulator where two do not fit beside the
-    stages) and in shared memory: both within the tolerance of the oracle on
-    every element, and within a few fp32 roundings of each other."""
+    stages, as on multi-dg) and in shared memory: both within the tolerance of
+    the oracle on every element, and within one rounding of each other."""
     case = CONFIGS[name]
     inp = make_inputs(case)
     ref = oracle_out(oracle_mod, case, inp)
@@ -228,7 +228,7 @@ def test_query_plan_split_choice():
     split would not pay (largec: 2 tiles of 72 k-tiles per CTA)."""
     dev = torch.device("cuda", 0)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    for name, split, a_operand in (("neck_f16", 1, 2), ("largec_f16", 0, 1), ("multidg_bf16", 1, 1)):
+    for name, split, a_operand in (("neck_f16", 1, 2), ("largec_f16", 0, 1), ("multidg_bf16", 1, 2)):
         case = CONFIGS[name]
         d = {k: (None if v is None else v.to(dev)) for k, v in make_inputs(case).items()}
         h = mdcn.Handle(**case.attrs())
