@@ -296,16 +296,18 @@ mdcn_status mdcn_forward_im2col_gemm(mdcn_handle handle, const void* x, const vo
  *   grad_bias[o]                = sum over n, p: grad_out[n,o,p]
  * (v = the bilinear sample of x[n,c] at the point of tap k, pixel p). */
 
-/* Bytes of device workspace mdcn_backward needs (the tap-major weight, an
- * fp32 weight gradient, and per chunk of images: channels-last x, an fp32
- * grad_x accumulator, the fp32 column gradients, the modulated columns and,
- * for group 1, grad_out re-laid [Cout][n][Ho*Wo]; chunks hold as many images
- * as fit in about 256 MB of these, at least one).
+/* Bytes of device workspace mdcn_backward needs (a status word, the
+ * tap-major weight, an fp32 weight gradient, and per chunk of images:
+ * channels-last x, an fp32 grad_x accumulator, the fp32 column gradients and
+ * the modulated columns; chunks hold as many images as fit in about 256 MB of
+ * these, at least one; then, where the contractions run on the tensor cores,
+ * the fp32 slices of the split weight-gradient contraction, else, for group
+ * 1, grad_out re-laid [Cout][n][Ho*Wo] and a 32 MB cuBLAS workspace).
  * Host only. Errors as mdcn_workspace_size. */
 mdcn_status mdcn_backward_workspace_size(mdcn_handle handle, const mdcn_dims* dims, mdcn_dtype dtype, size_t* bytes);
 
-/* Kernel launches and cuBLAS calls one mdcn_backward call makes for these
- * dims and dtype (a diagnostic; the page has no counterpart). Host only. */
+/* Kernel launches, memsets and cuBLAS calls one mdcn_backward call makes for
+ * these dims and dtype (a diagnostic; the page has no counterpart). Host only. */
 mdcn_status mdcn_backward_launches(mdcn_handle handle, const mdcn_dims* dims, mdcn_dtype dtype, int32_t* launches);
 
 /* The backward pass. Inputs (DEVICE pointers, dense NCHW, one dtype, as for
@@ -315,11 +317,18 @@ mdcn_status mdcn_backward_launches(mdcn_handle handle, const mdcn_dims* dims, md
  * grad_x, grad_offset, grad_mask, grad_weight, and grad_bias_or_null [Cout]
  * (NULL: not computed; dims->bias must be Cout exactly when it is given).
  * workspace: >= mdcn_backward_workspace_size bytes, contents undefined
- * afterwards. Every pointer 16-byte aligned. Arithmetic in fp32 (the two
- * contractions run as cuBLAS GEMMs with fp32 accumulation, no TF32 for f32);
- * grad_x is summed with fp32 atomic additions, so its last bits may differ
- * from run to run; the other gradients are deterministic. Asynchronous on the
- * stream; a call that fails validation launches nothing and writes nothing.
+ * afterwards; its first word is the call's device status word, which
+ * mdcn_query_status reads (a bounded wait of the tensor-core GEMMs that gave
+ * up sets it). Every pointer 16-byte aligned. Arithmetic in fp32: for
+ * float16 and bfloat16 the two contractions (the column gradients W^T *
+ * grad_out, and the weight gradient grad_out * columns^T) run on this
+ * library's tcgen05 tensor-core GEMM with fp32 accumulation, where Ho*Wo and
+ * (Cin/group)*kh*kw are multiples of 8 (TMA's 16-byte row rule), else, and
+ * for float32 (fp32 products, no TF32), as cuBLAS GEMMs. grad_x is summed
+ * with fp32 atomic additions, so its last bits may differ from run to run;
+ * the other gradients are deterministic (the split weight-gradient
+ * contraction is summed in a fixed order). Asynchronous on the stream; a call
+ * that fails validation launches nothing and writes nothing.
  * Errors: MDCN_ERR_NULL, MDCN_ERR_SHAPE, MDCN_ERR_DTYPE, MDCN_ERR_ALIGN,
  * MDCN_ERR_WORKSPACE, MDCN_ERR_UNSUPPORTED (a GEMM dimension beyond 2^31-1,
  * or a coordinate beyond 2^24), MDCN_ERR_ARCH, MDCN_ERR_CUDA. */

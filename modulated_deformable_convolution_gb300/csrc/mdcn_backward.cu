@@ -16,17 +16,22 @@
 //
 // Work per chunk of images (its buffers within a fixed budget):
 //   1. x of the chunk -> channels-last (tiled transpose);
-//   2. G = W_g^T * grad_out per group, one cuBLAS strided-batched GEMM per
-//      group (fp32 out), laid out [n][g][p][k][c_l] so that one sampling
-//      point's channels are contiguous;
+//   2. G = W_g^T * grad_out per group (fp32 out), laid out [n][g][p][k][c_l]
+//      so that one sampling point's channels are contiguous: for float16 and
+//      bfloat16 the tcgen05 GEMM of mdcn_gemm.cu (grad_out and the tap-major
+//      weight read as MN-major operands, straight from their layouts), for
+//      float32 one cuBLAS strided-batched GEMM per group (fp32 products);
 //   3. the sampling backward: a segment of lanes per sampling point (n, p, gd,
 //      k), lanes along channels; the slope sums are reduced across the
 //      segment by shuffles (deterministic), grad_x goes by fp32 vector
 //      reductions into a channels-last accumulator, and the modulated column
 //      mask * v is written for step 4;
 //   4. grad_weight += grad_out * col^T (fp32 accumulate in workspace): for
+//      float16 / bfloat16 one tcgen05 GEMM over the chunk's images and all
+//      groups (the contraction over images and pixels split between CTAs,
+//      fp32 reductions into the zeroed accumulator); for float32, cuBLAS: for
 //      group 1 one GEMM over the chunk's images, after grad_out is re-laid
-//      [Cout][n][P]; otherwise per image, one strided-batched GEMM over the
+//      [Cout][n][P], otherwise per image one strided-batched GEMM over the
 //      groups;
 //   5. the fp32 grad_x accumulator -> NCHW in the I/O type.
 // Then the weight gradient to [Cout, Cg, kh, kw] and the bias reduction.
@@ -35,6 +40,7 @@
 #include <cuda_fp16.h>
 
 #include "mdcn_backward.h"
+#include "mdcn_gemm.h"
 #include "mdcn_launch.h"
 #include "mdcn_plan.h"
 
@@ -147,7 +153,9 @@ __global__ void __launch_bounds__(256) swap_image_channel_kernel(const T* __rest
 // wt[o][k][c_l] = w[o][c_l][k]
 template <typename T>
 __global__ void __launch_bounds__(256) weight_tap_major_kernel(const T* __restrict__ w, T* __restrict__ wt,
-                                                               int64_t Cout, int64_t Cg, int64_t K) {
+                                                               int64_t Cout, int64_t Cg, int64_t K,
+                                                               uint32_t* __restrict__ status) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) *status = 0u;  // the call's device status word
     const int64_t total = Cout * Cg * K;
     for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
          e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -329,6 +337,81 @@ cudaError_t blas_fail(cublasStatus_t s) {
     return s == CUBLAS_STATUS_SUCCESS ? cudaSuccess : cudaErrorUnknown;
 }
 
+// The column-gradient GEMM of one group for a chunk of nbc images on the
+// tensor cores, computed as its transpose so that each epilogue warp writes
+// 128 contiguous bytes per column: gcol[n][g][p][kc] (m = kc, n = p) = sum
+// over o of wt[g][o][kc] * grad_out[n][g*Og + o][p]; A = wt (m = kc
+// contiguous: MN-major, shared by the images), B = grad_out (n = p
+// contiguous: MN-major, one per image), K = the group's Og output channels.
+template <typename T>
+cudaError_t column_grad_tc(const BwdPlan& p, const T* grad_out_chunk, const T* wt, float* gcol, int64_t nbc, int32_t g,
+                           uint32_t* status, cudaStream_t st) {
+    const int64_t es = sizeof(T), P = p.P, Og = p.Og, KCg = static_cast<int64_t>(p.K) * p.Cg;
+    GemmOperand a{wt + static_cast<int64_t>(g) * Og * KCg, {KCg, Og, 1, 1}, {KCg * es, Og * KCg * es, Og * KCg * es}};
+    GemmOperand b{grad_out_chunk + static_cast<int64_t>(g) * Og * P, {P, Og, 1, nbc},
+                  {P * es, Og * P * es, p.Cout * P * es}};
+    GemmArgs ga{};
+    ga.M = static_cast<int32_t>(KCg);
+    ga.N = static_cast<int32_t>(P);
+    ga.kt_inner = static_cast<int32_t>((Og + 63) / 64);
+    ga.kbatch = 1;
+    ga.atomic = 0;
+    ga.D = gcol + static_cast<int64_t>(g) * P * KCg;
+    ga.ldm = 1;
+    ga.ldn = KCg;
+    ga.ldz = static_cast<int64_t>(p.group) * P * KCg;
+    ga.status = status;
+    // two stages (65 KB of shared memory): three CTAs per SM, so that one CTA's
+    // stores overlap the others' loads; the contraction is only Og long
+    ga.stages = 2;
+    ga.a_z = 0;  // batch = image: the weight shared, grad_out per image
+    ga.b_z = 1;
+    return launch_tc_gemm(p.dtype, a, true, b, true, 128, ga, static_cast<int>(nbc), 1, st);
+}
+
+// The weight-gradient GEMM of a chunk of nbc images, every group at once on
+// the tensor cores, as its transpose: part[s][g][o][kc] (m = kc, n = o) = the
+// sum over split s's share of the chunk's images and pixels of
+// col[n][g][p][kc] * grad_out[n][g*Og + o][p]; A = col (m = kc contiguous:
+// MN-major), B = grad_out (K-major in p). The contraction (images x pixels)
+// is split between p.wsplits CTAs per tile, each writing its own fp32 slice;
+// reduce_splits_kernel adds the slices in order (deterministic).
+template <typename T>
+cudaError_t weight_grad_tc(const BwdPlan& p, const T* grad_out_chunk, const T* col, float* part, int64_t nbc,
+                           uint32_t* status, cudaStream_t st, int* splits_used) {
+    const int64_t es = sizeof(T), P = p.P, Og = p.Og, KCg = static_cast<int64_t>(p.K) * p.Cg, G = p.group;
+    GemmOperand a{col, {KCg, P, nbc, G}, {KCg * es, G * P * KCg * es, P * KCg * es}};
+    GemmOperand b{grad_out_chunk, {P, Og, nbc, G}, {P * es, p.Cout * P * es, Og * P * es}};
+    GemmArgs ga{};
+    ga.M = static_cast<int32_t>(KCg);
+    ga.N = static_cast<int32_t>(Og);
+    ga.kt_inner = static_cast<int32_t>((P + 63) / 64);
+    ga.kbatch = static_cast<int32_t>(nbc);
+    ga.atomic = 0;
+    ga.D = part;
+    ga.ldm = 1;
+    ga.ldn = KCg;
+    ga.ldz = Og * KCg;
+    ga.lds = G * Og * KCg;
+    ga.status = status;
+    ga.stages = 6;
+    ga.a_z = 1;  // batch = group: both operands per group
+    ga.b_z = 1;
+    const int bn = Og > 128 ? 256 : 128;
+    return launch_tc_gemm(p.dtype, a, true, b, false, bn, ga, static_cast<int>(G), p.wsplits, st, splits_used);
+}
+
+// gw[i] (+)= sum over s < splits of part[s][i], in order of s (first chunk: =).
+__global__ void __launch_bounds__(256) reduce_splits_kernel(const float* __restrict__ part, float* __restrict__ gw,
+                                                            int64_t count, int32_t splits, int32_t first) {
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < count;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        float acc = first ? 0.f : gw[i];
+        for (int32_t s = 0; s < splits; ++s) acc += part[s * count + i];
+        gw[i] = acc;
+    }
+}
+
 template <typename T>
 cudaError_t run_backward(const BwdPlan& p, const T* x, const T* offset, const T* mask, const T* weight,
                          const T* grad_out, T* grad_x, T* grad_offset, T* grad_mask, T* grad_weight, T* grad_bias,
@@ -343,13 +426,19 @@ cudaError_t run_backward(const BwdPlan& p, const T* x, const T* offset, const T*
     const int64_t K = p.K, Cg = p.Cg, Og = p.Og, P = p.P, HW = p.H * p.W, KCg = K * Cg;
     cudaError_t e;
 
+    uint32_t* status = reinterpret_cast<uint32_t*>(base + p.off_status);
+    const bool tc = backward_uses_tc(p);
     BlasLease lease;
-    if ((e = lease_blas(&lease, st, blas_workspace_in(base + p.off_blas), kBlasWorkspaceBytes)) != cudaSuccess) return e;
-    cublasHandle_t h = lease.h;
+    cublasHandle_t h = nullptr;
+    if (!tc) {
+        if ((e = lease_blas(&lease, st, blas_workspace_in(base + p.off_blas), kBlasWorkspaceBytes)) != cudaSuccess)
+            return e;
+        h = lease.h;
+    }
     const cublasComputeType_t ct = sizeof(T) == 4 ? CUBLAS_COMPUTE_32F_PEDANTIC : CUBLAS_COMPUTE_32F;
     const float one = 1.0f, zero = 0.0f;
 
-    weight_tap_major_kernel<T><<<grid_for(p.Cout * KCg), 256, 0, st>>>(weight, wt, p.Cout, Cg, K);
+    weight_tap_major_kernel<T><<<grid_for(p.Cout * KCg), 256, 0, st>>>(weight, wt, p.Cout, Cg, K, status);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
     for (int64_t n0 = 0; n0 < p.N; n0 += p.nb) {
@@ -360,6 +449,12 @@ cudaError_t run_backward(const BwdPlan& p, const T* x, const T* offset, const T*
             return e;
         // 2. column gradients, per group: (K*Cg x P) = wt_g (K*Cg x Og) * grad_out_g (Og x P), column-major views
         for (int32_t g = 0; g < p.group; ++g) {
+            if (tc) {
+                if ((e = column_grad_tc<T>(p, grad_out + n0 * p.Cout * P, wt, gcol, nbc, g, status, st)) !=
+                    cudaSuccess)
+                    return e;
+                continue;
+            }
             e = blas_fail(cublasGemmStridedBatchedEx(
                 h, CUBLAS_OP_N, CUBLAS_OP_T, static_cast<int>(KCg), static_cast<int>(P), static_cast<int>(Og), &one,
                 wt + g * Og * KCg, blas_type<T>(), static_cast<int>(KCg), 0,
@@ -384,7 +479,16 @@ cudaError_t run_backward(const BwdPlan& p, const T* x, const T* offset, const T*
         // 4. weight gradient. Group 1: one GEMM over the chunk's images,
         //    (K*Cg x Cout) += col (K*Cg x nbc*P) * got (nbc*P x Cout), got = grad_out as [Cout][nbc][P];
         //    otherwise per image over the groups: (K*Cg x Og) += col (K*Cg x P) * grad_out^T (P x Og)
-        if (p.group == 1) {
+        if (tc) {
+            float* part = reinterpret_cast<float*>(base + p.off_wpart);
+            int used = 0;
+            if ((e = weight_grad_tc<T>(p, grad_out + n0 * p.Cout * P, col, part, nbc, status, st, &used)) !=
+                cudaSuccess)
+                return e;
+            reduce_splits_kernel<<<grid_for(p.Cout * KCg), 256, 0, st>>>(part, gw, p.Cout * KCg, used,
+                                                                       n0 == 0 ? 1 : 0);
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        } else if (p.group == 1) {
             T* got = reinterpret_cast<T*>(base + p.off_got);
             const int64_t row_units = (P * static_cast<int64_t>(sizeof(T))) % 16 == 0 ? P * sizeof(T) / 16 : P;
             const int64_t units = nbc * p.Cout * row_units;
@@ -433,17 +537,21 @@ void plan_backward(BwdPlan* p, size_t chunk_budget) {
     p->lanes = lanes;
     const size_t cols = static_cast<size_t>(p->P) * p->K * p->Cin;  // column elements of one image
     const size_t pix = static_cast<size_t>(p->H) * p->W * p->Cin;   // x elements of one image
-    const size_t per_image =
-        cols * (4 + es) + pix * (es + 4) + (p->group == 1 ? static_cast<size_t>(p->Cout) * p->P * es : 0);
+    const bool tc = backward_uses_tc(*p);
+    // the cuBLAS path's group-1 weight gradient wants grad_out re-laid [Cout][nb][P]
+    const bool got = p->group == 1 && !tc;
+    const size_t per_image = cols * (4 + es) + pix * (es + 4) + (got ? static_cast<size_t>(p->Cout) * p->P * es : 0);
     int64_t nb = static_cast<int64_t>(chunk_budget / (per_image ? per_image : 1));
     if (nb < 1) nb = 1;
     if (nb > p->N) nb = p->N;
-    // the group-1 weight-gradient GEMM runs over nb * P columns (a 32-bit cuBLAS dimension)
-    if (p->group == 1 && nb * p->P > 2147483647) nb = 2147483647 / p->P;
+    // the cuBLAS group-1 weight-gradient GEMM runs over nb * P columns (a 32-bit dimension)
+    if (got && nb * p->P > 2147483647) nb = 2147483647 / p->P;
     if (nb > 65535) nb = 65535;
     p->nb = nb;
     const size_t wel = static_cast<size_t>(p->Cout) * p->K * p->Cg;
     size_t off = 0;
+    p->off_status = off;
+    off += 256;
     p->off_wt = off;
     off += align256(wel * es);
     p->off_gw = off;
@@ -457,17 +565,40 @@ void plan_backward(BwdPlan* p, size_t chunk_budget) {
     p->off_col = off;
     off += align256(nb * cols * es);
     p->off_got = off;
-    if (p->group == 1) off += align256(static_cast<size_t>(nb) * p->Cout * p->P * es);
+    if (got) off += align256(static_cast<size_t>(nb) * p->Cout * p->P * es);
     p->off_blas = off;
-    off += kBlasRegionBytes;
+    if (!tc) off += kBlasRegionBytes;
+    // tensor-core weight gradient: the contraction of each 128 x 128 output tile
+    // split between about 160 / tiles CTAs, one fp32 slice each
+    p->wsplits = 1;
+    p->off_wpart = off;
+    if (tc) {
+        const int64_t KCg = static_cast<int64_t>(p->K) * p->Cg;
+        const int64_t bn = p->Og > 128 ? 256 : 128;  // weight_grad_tc's tile width along Og
+        const int64_t tiles = ((KCg + 127) / 128) * ((p->Og + bn - 1) / bn) * p->group;
+        const int64_t kt_total = ((p->P + 63) / 64) * nb;
+        int64_t sp = 160 / tiles;
+        if (sp > kt_total) sp = kt_total;
+        if (sp < 1) sp = 1;
+        p->wsplits = static_cast<int32_t>(sp);
+        off += align256(static_cast<size_t>(sp) * wel * 4);
+    }
     p->ws_bytes = off;
+}
+
+bool backward_uses_tc(const BwdPlan& p) {
+    // 16-bit I/O whose operand rows meet TMA's 16-byte rule: P and K*Cg
+    // multiples of 8 elements (the caller's pointers are 16-byte aligned)
+    const int64_t KCg = static_cast<int64_t>(p.K) * p.Cg;
+    return p.dtype != kF32 && p.P % 8 == 0 && KCg % 8 == 0 && p.P < (int64_t(1) << 31) && KCg < (int64_t(1) << 31);
 }
 
 int backward_launch_count(const BwdPlan& p) {
     const int64_t chunks = (p.N + p.nb - 1) / p.nb;
     // per chunk: transpose, memset, one GEMM per group, sampling backward, the weight-gradient
-    // GEMMs (group 1: a grad_out re-layout and one GEMM; else one per image), transpose
-    const int64_t wgrad = p.group == 1 ? 2 * chunks : p.N;
+    // GEMMs (tensor-core path: one GEMM and the in-order sum of its split slices per chunk;
+    // cuBLAS path, group 1: a grad_out re-layout and one GEMM; else one per image), transpose
+    const int64_t wgrad = backward_uses_tc(p) ? 2 * chunks : (p.group == 1 ? 2 * chunks : p.N);
     return static_cast<int>(1 + chunks * (4 + p.group) + wgrad + 1 + (p.has_bias ? 1 : 0));
 }
 

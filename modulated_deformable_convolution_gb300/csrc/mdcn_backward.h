@@ -26,15 +26,18 @@ struct BwdPlan {
     //      a fixed budget
     int64_t nb;
     // ---- workspace layout (byte offsets, 256-byte aligned)
+    size_t off_status; // the call's device status word (bounded waits of the tensor-core GEMMs)
     size_t off_wt;    // weight, tap-major [group][Og][K][Cg] (dtype)
     size_t off_gw;    // fp32 weight gradient, same layout
     size_t off_xt;    // x of the chunk, channels-last [nb][H][W][Cin] (dtype)
     size_t off_gx;    // fp32 grad_x of the chunk, channels-last [nb][H][W][Cin]
     size_t off_gcol;  // fp32 column gradients [nb][group][P][K][Cg]
     size_t off_col;   // modulated columns [nb][group][P][K][Cg] (dtype)
-    size_t off_got;   // group 1 only: grad_out of the chunk as [Cout][nb][P] (dtype), so that
-                      // the weight gradient is one GEMM over the chunk's images
-    size_t off_blas;  // the call's cuBLAS workspace region (kBlasRegionBytes)
+    size_t off_got;   // float32, group 1 only: grad_out of the chunk as [Cout][nb][P] (dtype), so
+                      // that the cuBLAS weight gradient is one GEMM over the chunk's images
+    size_t off_blas;  // the call's cuBLAS workspace region (kBlasRegionBytes; float32 only)
+    size_t off_wpart; // tensor-core path: fp32 weight-gradient slices [wsplits][Cout][K*Cg]
+    int32_t wsplits;  // CTAs sharing one weight-gradient tile's contraction (tensor-core path)
     size_t ws_bytes;
 };
 
@@ -49,5 +52,9 @@ cudaError_t launch_backward(const BwdPlan& p, const void* x, const void* offset,
 
 // Kernel launches (and cuBLAS calls) one backward call makes.
 int backward_launch_count(const BwdPlan& p);
+
+// True when the call's contractions run on the tcgen05 GEMM (float16 and
+// bfloat16 with P and K*Cg multiples of 8); false: cuBLAS (float32 products).
+bool backward_uses_tc(const BwdPlan& p);
 
 }  // namespace mdcn

@@ -338,30 +338,41 @@ def _bwd_problem(N, Cin, Cout, H, W, group=1, dg=1, k=3, bias=False, dtype=torch
     (4, 128, 128, 80, 1, False, torch.float16),   # neck: one chunk
     (64, 128, 128, 80, 1, True, torch.float16),   # several chunks
     (2, 256, 256, 100, 4, True, torch.float32),   # grouped: one weight-gradient GEMM per image
-    (3, 8, 6, 9, 2, False, torch.bfloat16),
+    (3, 8, 6, 9, 2, False, torch.bfloat16),       # P = 81: rows break the 16-byte rule, cuBLAS
+    (2, 64, 32, 16, 2, True, torch.bfloat16),     # grouped, tensor-core GEMMs
 ])
 def test_backward_chunks_workspace_and_launches(lib, N, Cin, Cout, H, group, bias, dtype):
     """The backward's host plan: images go in chunks of at most 256 MB of
-    per-chunk buffers (at least one image); the workspace holds the shared
-    weight buffers, one chunk's buffers and the call's cuBLAS workspace; the
-    launch count follows the
-    chunking (group 1: a grad_out re-layout and one weight-gradient GEMM per
+    per-chunk buffers (at least one image); the workspace holds the status
+    word, the shared weight buffers, one chunk's buffers and, where the
+    contractions run on cuBLAS (float32, or rows that break TMA's 16-byte
+    rule), the call's cuBLAS workspace; the launch count follows the chunking
+    (tensor-core path: one weight-gradient GEMM per chunk and the in-order sum
+    of its split slices; cuBLAS, group 1: a grad_out re-layout and one GEMM per
     chunk; otherwise one GEMM per image)."""
     t, h = _bwd_problem(N, Cin, Cout, H, H, group=group, bias=bias, dtype=dtype)
     es = torch.empty((), dtype=dtype).element_size()
     P = H * H
     K = 9
+    KCg = K * (Cin // group)
+    tc = dtype != torch.float32 and P % 8 == 0 and KCg % 8 == 0
+    got = group == 1 and not tc
     cols, pix = P * K * Cin, H * H * Cin
-    per_image = cols * (4 + es) + pix * (es + 4) + (Cout * P * es if group == 1 else 0)
+    per_image = cols * (4 + es) + pix * (es + 4) + (Cout * P * es if got else 0)
     nb = max(1, min(N, (256 << 20) // per_image))
     chunks = -(-N // nb)
     ws = mdcn.mdcn_backward_workspace_size(h, t["x"], t["offset"], t["mask"], t["weight"], t["bias"])
-    wel = Cout * K * (Cin // group)
-    blas = (32 << 20) + 256  # the call's own cuBLAS workspace (256-byte aligned inside the region)
-    assert ws >= wel * es + wel * 4 + nb * per_image + blas
-    assert ws <= wel * es + wel * 4 + nb * per_image + blas + 8 * 256
+    wel = Cout * KCg
+    blas = 0 if tc else (32 << 20) + 256  # the call's own cuBLAS workspace (256-byte aligned inside the region)
+    # tensor-core weight gradient: one fp32 slice per CTA sharing a 128 x 128 tile's contraction
+    Og = Cout // group
+    tiles = -(-KCg // 128) * -(-Og // (256 if Og > 128 else 128)) * group
+    wsplits = max(1, min(160 // tiles, -(-P // 64) * nb)) if tc else 0
+    slices = wsplits * wel * 4
+    assert ws >= 256 + wel * es + wel * 4 + nb * per_image + blas + slices
+    assert ws <= 256 + wel * es + wel * 4 + nb * per_image + blas + slices + 9 * 256
     launches = mdcn.mdcn_backward_launches(h, t["x"], t["offset"], t["mask"], t["weight"], t["bias"])
-    wgrad = 2 * chunks if group == 1 else N
+    wgrad = 2 * chunks if tc else (2 * chunks if got else N)
     assert launches == 1 + chunks * (4 + group) + wgrad + 1 + (1 if bias else 0)
 
 

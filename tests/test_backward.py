@@ -39,6 +39,8 @@ def gpu_backward(case, inp, go, poison=True):
     mdcn.mdcn_backward(h, d["x"], d["offset"], d["mask"], d["weight"], god, g["x"], g["offset"], g["mask"],
                        g["weight"], gb, ws)
     torch.cuda.synchronize()
+    s, bits = mdcn.mdcn_query_status(ws)  # no bounded wait of the tensor-core GEMMs gave up
+    assert s == mdcn.MDCN_OK, f"device status {bits:#x}"
     g["bias"] = gb
     return {k: np64(v) for k, v in g.items()}
 
