@@ -636,6 +636,43 @@ def run_fused_only(args, case):
                       "status": s}), flush=True)
 
 
+def run_prep_vs_copy(args, case):
+    """Profiling aid: args.prep_vs_copy rounds of, each after an L2 flush, a
+    plain elementwise copy of x (PyTorch), the channels-last transpose alone,
+    the weight pack alone and one mdcn_forward (prep + fused kernel); prints
+    the mean CUDA-event time of each. Used for the ncu launch list that puts
+    the prep beside a copy of the same bytes."""
+    import modulated_deformable_convolution_gb300 as mdcn
+
+    dev = torch.device("cuda", 0)
+    d = {k: (None if v is None else v.to(dev)) for k, v in make_inputs(case).items()}
+    a = (d["x"], d["offset"], d["mask"], d["weight"], d["bias"])
+    h = mdcn.Handle(**case.attrs())
+    ws = torch.empty(mdcn.mdcn_workspace_size(h, *a), dtype=torch.uint8, device=dev)
+    out = torch.empty(mdcn.mdcn_output_dims(h, *a), dtype=a[0].dtype, device=dev)
+    y = torch.empty_like(d["x"])
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    st = torch.cuda.current_stream(dev)
+    steps = {
+        "copy_x": lambda: torch.add(d["x"], 0, out=y),
+        "prepare_input": lambda: mdcn.mdcn_prepare_input(h, *a, ws, st),
+        "pack_weight": lambda: mdcn.mdcn_pack_weight(h, *a, ws, st),
+        "forward": lambda: mdcn.mdcn_forward(h, *a, out, ws),
+    }
+    evs = {k: [] for k in steps}
+    for _ in range(args.prep_vs_copy):
+        for k, fn in steps.items():
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            fn()
+            e1.record(st)
+            evs[k].append((e0, e1))
+    torch.cuda.synchronize()
+    print(json.dumps({"workload": case.name, **{k + "_us": statistics.mean(x.elapsed_time(y) for x, y in v) * 1e3
+                                               for k, v in evs.items()}}), flush=True)
+
+
 def run_backward_only(args, case):
     """Profiling aid: runs mdcn_backward args.backward_only times (after one
     untimed call), each after an L2 flush, and prints the median CUDA-event
@@ -683,6 +720,8 @@ def main(argv=None):
                     help="profiling aid: time N launches of the fused kernel alone")
     ap.add_argument("--backward-only", type=int, default=0, metavar="N",
                     help="profiling aid: time N calls of mdcn_backward alone")
+    ap.add_argument("--prep-vs-copy", type=int, default=0, metavar="N",
+                    help="profiling aid: N rounds of a plain copy of x, the prep kernels and one forward")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
@@ -702,6 +741,11 @@ def main(argv=None):
 
             build.build()
             run_backward_only(args, case)
+        elif args.prep_vs_copy:
+            from modulated_deformable_convolution_gb300 import build
+
+            build.build()
+            run_prep_vs_copy(args, case)
         else:
             from modulated_deformable_convolution_gb300 import build
 
