@@ -361,12 +361,14 @@ cudaError_t column_grad_tc(const BwdPlan& p, const T* grad_out_chunk, const T* w
     ga.ldn = KCg;
     ga.ldz = static_cast<int64_t>(p.group) * P * KCg;
     ga.status = status;
-    // two stages (65 KB of shared memory): three CTAs per SM, so that one CTA's
-    // stores overlap the others' loads; the contraction is only Og long
-    ga.stages = 2;
+    // a short contraction (Og <= 128): 128-wide tiles, two stages, two CTAs per
+    // SM; a longer one: 256-wide tiles (fewer operand re-reads per output byte),
+    // four stages, one CTA per SM
+    const int bn = Og > 128 ? 256 : 128;
+    ga.stages = bn == 256 ? 4 : 2;
     ga.a_z = 0;  // batch = image: the weight shared, grad_out per image
     ga.b_z = 1;
-    return launch_tc_gemm(p.dtype, a, true, b, true, 128, ga, static_cast<int>(nbc), 1, st);
+    return launch_tc_gemm(p.dtype, a, true, b, true, bn, ga, static_cast<int>(nbc), 1, st);
 }
 
 // The weight-gradient GEMM of a chunk of nbc images, every group at once on
@@ -401,14 +403,23 @@ cudaError_t weight_grad_tc(const BwdPlan& p, const T* grad_out_chunk, const T* c
     return launch_tc_gemm(p.dtype, a, true, b, false, bn, ga, static_cast<int>(G), p.wsplits, st, splits_used);
 }
 
-// gw[i] (+)= sum over s < splits of part[s][i], in order of s (first chunk: =).
+// gw[i] (+)= sum over s < splits of part[s][i], in order of s (first chunk: =),
+// four consecutive elements per thread (count is a multiple of 4 on the
+// tensor-core path: K*Cg is a multiple of 8).
 __global__ void __launch_bounds__(256) reduce_splits_kernel(const float* __restrict__ part, float* __restrict__ gw,
                                                             int64_t count, int32_t splits, int32_t first) {
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < count;
+    const int64_t n4 = count / 4;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        float acc = first ? 0.f : gw[i];
-        for (int32_t s = 0; s < splits; ++s) acc += part[s * count + i];
-        gw[i] = acc;
+        float4 acc = first ? make_float4(0.f, 0.f, 0.f, 0.f) : reinterpret_cast<const float4*>(gw)[i];
+        for (int32_t s = 0; s < splits; ++s) {
+            const float4 v = reinterpret_cast<const float4*>(part + s * count)[i];
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+        reinterpret_cast<float4*>(gw)[i] = acc;
     }
 }
 
@@ -485,8 +496,8 @@ cudaError_t run_backward(const BwdPlan& p, const T* x, const T* offset, const T*
             if ((e = weight_grad_tc<T>(p, grad_out + n0 * p.Cout * P, col, part, nbc, status, st, &used)) !=
                 cudaSuccess)
                 return e;
-            reduce_splits_kernel<<<grid_for(p.Cout * KCg), 256, 0, st>>>(part, gw, p.Cout * KCg, used,
-                                                                       n0 == 0 ? 1 : 0);
+            reduce_splits_kernel<<<grid_for(p.Cout * KCg / 4), 256, 0, st>>>(part, gw, p.Cout * KCg, used,
+                                                                           n0 == 0 ? 1 : 0);
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
         } else if (p.group == 1) {
             T* got = reinterpret_cast<T*>(base + p.off_got);

@@ -31,7 +31,8 @@ struct GemmArgs {
     int32_t stages;        // pipeline stages (2..6)
     int32_t a_z, b_z;      // 1: the operand's dims[3] is the batch z; 0: the operand is shared by every batch
     // set by launch_tc_gemm
-    int32_t fmt, mt, nt, kt_split;
+    int32_t fmt, mt, nt, kt_split, splits;
+    int64_t items;         // work items: mt * nt * splits * batches
 };
 
 // True when the operand meets TMA's rules (16-byte aligned base and strides).
