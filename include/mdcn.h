@@ -120,6 +120,13 @@ typedef struct mdcn_tuning {
                           is allowed) */
     int32_t ntile;     /* most output channels one tile holds: a multiple of 16 up to 512 (0: automatic).
                           Narrower tiles gather each pixel's columns once per tile of its group */
+    int32_t path;      /* 1 = the fused implicit-GEMM kernel on the tensor cores; 2 = the direct kernel
+                          on the CUDA cores (one thread per output pixel and up to 16 groups, fp32
+                          sums, x read in NCHW; groups of at most 32 output channels, the fp32
+                          weights of a thread's groups within 96 KB);
+                          0 = automatic: direct where (Cin/group) * (Cout/group) <= 16, e.g.
+                          depthwise, where the implicit GEMM would pad each channel unit to a 128-byte
+                          k-tile and each group's outputs to 16 MMA columns */
 } mdcn_tuning;
 
 /* mdcn_create with plan overrides (tuning may be NULL = automatic). Errors as
@@ -143,7 +150,8 @@ mdcn_status mdcn_output_dims(mdcn_handle handle, const mdcn_dims* dims, int64_t 
 
 /* Bytes of device workspace mdcn_forward needs for these dims and dtype
  * (a status word, the channels-last copy of x, the repacked weight, and the
- * fp32 partial sums of output tiles split between CTAs). Host only. */
+ * fp32 partial sums of output tiles split between CTAs; a direct plan, see
+ * mdcn_tuning.path, needs the 1 KB header only). Host only. */
 mdcn_status mdcn_workspace_size(mdcn_handle handle, const mdcn_dims* dims, mdcn_dtype dtype,
                                 size_t* bytes);
 
@@ -157,8 +165,9 @@ typedef struct mdcn_plan_info {
     int32_t split;          /* 1 when some tile is split between CTAs (summed inside the fused kernel) */
     int32_t stages, kgroups, tile_mode;
     int32_t launches;       /* kernels one mdcn_forward launches: prep (1, or 2 when x needs the staged
-                               transpose) and the fused kernel */
-    int32_t a_operand;      /* 1: A stages in shared memory, 2: in tensor memory */
+                               transpose) and the fused kernel; 1 for a direct plan */
+    int32_t a_operand;      /* 1: A stages in shared memory, 2: in tensor memory (0: direct plan) */
+    int32_t path;           /* 1: fused implicit GEMM, 2: direct kernel (the tile fields above are then 0) */
 } mdcn_plan_info;
 
 /* Errors as mdcn_workspace_size, plus MDCN_ERR_ARCH / MDCN_ERR_CUDA from the
@@ -193,7 +202,9 @@ mdcn_status mdcn_forward(mdcn_handle handle, const void* x, const void* offset, 
 /* The three steps of mdcn_forward as separate calls, for callers that pack a
  * constant weight once or time the steps on their own. Same argument rules
  * and workspace as mdcn_forward; x and weight are read only by the step that
- * names them. Run on one stream, with one workspace, and
+ * names them. Plans of the fused kernel only: for a direct plan (see
+ * mdcn_tuning.path; mdcn_query_plan tells) each returns MDCN_ERR_UNSUPPORTED
+ * and launches nothing. Run on one stream, with one workspace, and
  * mdcn_forward_prepared after the other two:
  *   mdcn_prepare_input:    x -> channels-last copy in workspace; clears the
  *                          workspace status word;

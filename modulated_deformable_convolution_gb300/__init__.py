@@ -67,7 +67,7 @@ def _pair(v):
 
 def mdcn_create(stride=1, padding=0, dilation=1, group=1, deformable_group=1, tuning=None):
     """mdcn_create (or mdcn_create_tuned when ``tuning`` is a dict with keys
-    stages, tile_mode, max_ctas, kgroups, a_operand, ntile): returns the opaque handle
+    stages, tile_mode, max_ctas, kgroups, a_operand, ntile, path): returns the opaque handle
     (an int) or raises MdcnError."""
     a = _abi.mdcn_attrs()
     a.stride[:] = _pair(stride)
@@ -81,7 +81,8 @@ def mdcn_create(stride=1, padding=0, dilation=1, group=1, deformable_group=1, tu
     else:
         t = _abi.mdcn_tuning(int(tuning.get("stages", 0)), int(tuning.get("tile_mode", -1)),
                              int(tuning.get("max_ctas", 0)), int(tuning.get("kgroups", 0)),
-                             int(tuning.get("a_operand", 0)), int(tuning.get("ntile", 0)))
+                             int(tuning.get("a_operand", 0)), int(tuning.get("ntile", 0)),
+                             int(tuning.get("path", 0)))
         _check(_lib().mdcn_create_tuned(ctypes.byref(a), ctypes.byref(t), ctypes.byref(h)), "mdcn_create_tuned")
     return h.value
 

@@ -37,13 +37,15 @@ class mdcn_attrs(ctypes.Structure):
 
 class mdcn_tuning(ctypes.Structure):
     _fields_ = [("stages", ctypes.c_int32), ("tile_mode", ctypes.c_int32), ("max_ctas", ctypes.c_int32),
-                ("kgroups", ctypes.c_int32), ("a_operand", ctypes.c_int32), ("ntile", ctypes.c_int32)]
+                ("kgroups", ctypes.c_int32), ("a_operand", ctypes.c_int32), ("ntile", ctypes.c_int32),
+                ("path", ctypes.c_int32)]
 
 
 class mdcn_plan_info(ctypes.Structure):
     _fields_ = [("tiles", i64), ("ktiles_per_tile", i64), ("ktiles_per_cta", i64), ("ctas", ctypes.c_int32),
                 ("split", ctypes.c_int32), ("stages", ctypes.c_int32), ("kgroups", ctypes.c_int32),
-                ("tile_mode", ctypes.c_int32), ("launches", ctypes.c_int32), ("a_operand", ctypes.c_int32)]
+                ("tile_mode", ctypes.c_int32), ("launches", ctypes.c_int32), ("a_operand", ctypes.c_int32),
+                ("path", ctypes.c_int32)]
 
 
 class mdcn_dims(ctypes.Structure):

@@ -22,7 +22,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmdcn.so")
 
-CU_SOURCES = ["mdcn_fused.cu", "mdcn_prep.cu", "mdcn_im2col.cu", "mdcn_noalloc.cu", "mdcn_backward.cu", "mdcn_gemm.cu"]
+CU_SOURCES = ["mdcn_fused.cu", "mdcn_prep.cu", "mdcn_im2col.cu", "mdcn_noalloc.cu", "mdcn_backward.cu", "mdcn_gemm.cu",
+              "mdcn_direct.cu"]
 CPP_SOURCES = ["mdcn_api.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

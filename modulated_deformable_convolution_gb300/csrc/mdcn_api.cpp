@@ -147,6 +147,25 @@ mdcn_status make_plan(const mdcn_attrs& a, const mdcn_tuning& tuning, const mdcn
     p.NP = p.N * p.P;
     if (p.NP > kI31) return MDCN_ERR_UNSUPPORTED;  // 32-bit pixel arithmetic in the kernels
 
+    // The direct CUDA-core kernel where each output sums over few products per
+    // tap (Cin/group x Cout/group <= 16, e.g. depthwise): the implicit GEMM would
+    // pad each channel unit to a 128-byte k-tile and each group's outputs to 16
+    // MMA columns (measured: a depthwise 128-channel 80x80 layer 1343 us fused,
+    // ~250 us direct; groups of 8 x 8 channels are faster fused, 158 against
+    // 258 us). It needs no workspace beyond the status word.
+    {
+        const bool fits = Og <= mdcn::kDirectMaxOg &&
+                          mdcn::direct_groups_per_thread(Og) * Og * Cg * K * 4 <= mdcn::kDirectMaxSmem &&
+                          p.group <= 65535 && p.N <= 65535;
+        if (tuning.path == 2 && !fits) return MDCN_ERR_UNSUPPORTED;
+        if (fits && (tuning.path == 2 || (tuning.path == 0 && Cg * Og <= 16))) {
+            p.direct = 1;
+            p.off_xt = p.off_wp = p.off_part = p.ws_bytes = mdcn::kStatusBytes;
+            *pl = p;
+            return MDCN_OK;
+        }
+    }
+
     const int64_t elem = dtype == MDCN_F32 ? 4 : 2;
     p.BKc = static_cast<int32_t>(128 / elem);
     const int64_t U = gcd64(Cg, Cd);
@@ -295,6 +314,7 @@ mdcn_status make_plan(const mdcn_attrs& a, const mdcn_tuning& tuning, const mdcn
 // CTA's range of the k-tile sequence, and the workspace size, which holds the
 // partial-sum slots (one per CTA) only when some tile is split between CTAs.
 void finish_plan(Plan* p, const mdcn_tuning& tuning, int sms) {
+    if (p->direct) return;  // no persistent grid, no partial sums
     int64_t grid = sms > 0 ? sms : 1;
     if (grid > mdcn::kMaxCtas) grid = mdcn::kMaxCtas;
     if (tuning.max_ctas > 0 && tuning.max_ctas < grid) grid = tuning.max_ctas;
@@ -478,12 +498,13 @@ extern "C" {
 mdcn_status mdcn_create_tuned(const mdcn_attrs* attrs, const mdcn_tuning* tuning, mdcn_handle* out) {
     if (!attrs || !out) return MDCN_ERR_NULL;
     if (!attrs_valid(*attrs)) return MDCN_ERR_ATTR;
-    mdcn_tuning tu{0, -1, 0, 0, 0, 0};
+    mdcn_tuning tu{0, -1, 0, 0, 0, 0, 0};
     if (tuning) {
         tu = *tuning;
         if (tu.stages < 0 || tu.stages == 1 || tu.stages > 8 || tu.tile_mode < -1 || tu.tile_mode > 1 ||
             tu.max_ctas < 0 || !(tu.kgroups == 0 || tu.kgroups == 1 || tu.kgroups == 2 || tu.kgroups == 4) ||
-            tu.a_operand < 0 || tu.a_operand > 2 || tu.ntile < 0 || tu.ntile > 512 || tu.ntile % 16 != 0)
+            tu.a_operand < 0 || tu.a_operand > 2 || tu.ntile < 0 || tu.ntile > 512 || tu.ntile % 16 != 0 ||
+            tu.path < 0 || tu.path > 2)
             return MDCN_ERR_ATTR;
     }
     mdcn_handle h = new (std::nothrow) mdcn_handle_;
@@ -534,8 +555,9 @@ mdcn_status mdcn_query_plan(mdcn_handle handle, const mdcn_dims* dims, mdcn_dtyp
     info->stages = p.stages;
     info->kgroups = p.kgroups;
     info->tile_mode = p.tile_mode;
-    info->launches = p.xt_block ? 2 : 3;
-    info->a_operand = p.a_tmem ? 2 : 1;
+    info->launches = p.direct ? 1 : (p.xt_block ? 2 : 3);
+    info->a_operand = p.direct ? 0 : (p.a_tmem ? 2 : 1);
+    info->path = p.direct ? 2 : 1;
     return MDCN_OK;
 }
 
@@ -548,6 +570,10 @@ mdcn_status mdcn_forward(mdcn_handle handle, const void* x, const void* offset, 
     s = plan_for_call(handle, dims, dtype, workspace_bytes, &p);
     if (s != MDCN_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (p.direct) {
+        const cudaError_t e = mdcn::launch_direct(p, x, offset, mask, weight, bias_or_null, out, workspace, st);
+        return e == cudaSuccess ? MDCN_OK : cuda_fail(e);
+    }
     const size_t elem = dtype == MDCN_F32 ? 4 : 2;
     const size_t plane = static_cast<size_t>(p.N) * static_cast<size_t>(p.P) * elem;
     cudaError_t e = mdcn::launch_prep_both(p, x, weight, offset, plane * 2 * p.dg * p.K, mask, plane * p.dg * p.K,
@@ -684,21 +710,31 @@ mdcn_status mdcn_forward_pack(mdcn_handle handle, const void* x, const void* wei
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     void* om = static_cast<uint8_t*>(workspace) + align256(pf.ws_bytes);
     // 1: the front end's raw output, then offset and sigmoid(mask) from it
-    cudaError_t e = mdcn::launch_prep_both(pf, x, weight_om, nullptr, 0, nullptr, 0, workspace, st);
-    if (e == cudaSuccess) e = mdcn::launch_fused(pf, nullptr, nullptr, bias_om, om, workspace, st);
+    cudaError_t e;
+    if (pf.direct) {
+        e = mdcn::launch_direct(pf, x, nullptr, nullptr, weight_om, bias_om, om, workspace, st);
+    } else {
+        e = mdcn::launch_prep_both(pf, x, weight_om, nullptr, 0, nullptr, 0, workspace, st);
+        if (e == cudaSuccess) e = mdcn::launch_fused(pf, nullptr, nullptr, bias_om, om, workspace, st);
+    }
     if (e == cudaSuccess)
         e = mdcn::launch_split_offset_mask(pf, om, offset_out, mask_out, 2 * pd.dg * pd.K, pd.dg * pd.K, st);
     // 2: the deformable convolution; when its channels-last x has the front
     // end's layout, the copy already in the workspace is reused
-    const bool same_xt = pf.Cp == pd.Cp && pf.U == pd.U && pf.UP == pd.UP && pf.off_xt == pd.off_xt &&
-                         pf.off_wp == pd.off_wp;
+    const bool same_xt = !pf.direct && !pd.direct && pf.Cp == pd.Cp && pf.U == pd.U && pf.UP == pd.UP &&
+                         pf.off_xt == pd.off_xt && pf.off_wp == pd.off_wp && pf.a_tmem == pd.a_tmem;
     const size_t elem = dtype == MDCN_F32 ? 4 : 2;
     const size_t plane = static_cast<size_t>(pd.N) * static_cast<size_t>(pd.P) * elem;
-    if (e == cudaSuccess)
-        e = same_xt ? mdcn::launch_pack_weight(pd, weight, workspace, st)
-                    : mdcn::launch_prep_both(pd, x, weight, offset_out, plane * 2 * pd.dg * pd.K, mask_out,
-                                             plane * pd.dg * pd.K, workspace, st);
-    if (e == cudaSuccess) e = mdcn::launch_fused(pd, offset_out, mask_out, bias_or_null, out, workspace, st);
+    if (pd.direct) {
+        if (e == cudaSuccess)
+            e = mdcn::launch_direct(pd, x, offset_out, mask_out, weight, bias_or_null, out, workspace, st);
+    } else {
+        if (e == cudaSuccess)
+            e = same_xt ? mdcn::launch_pack_weight(pd, weight, workspace, st)
+                        : mdcn::launch_prep_both(pd, x, weight, offset_out, plane * 2 * pd.dg * pd.K, mask_out,
+                                                 plane * pd.dg * pd.K, workspace, st);
+        if (e == cudaSuccess) e = mdcn::launch_fused(pd, offset_out, mask_out, bias_or_null, out, workspace, st);
+    }
     if (e != cudaSuccess) return cuda_fail(e);
     return MDCN_OK;
 }
@@ -710,6 +746,7 @@ mdcn_status mdcn_prepare_input(mdcn_handle handle, const void* x, void* workspac
     Plan p;
     mdcn_status s = plan_for_call(handle, dims, dtype, workspace_bytes, &p);
     if (s != MDCN_OK) return s;
+    if (p.direct) return MDCN_ERR_UNSUPPORTED;  // a direct plan runs whole, in mdcn_forward
     cudaError_t e = mdcn::launch_prep_input(p, x, workspace, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
     return MDCN_OK;
@@ -722,6 +759,7 @@ mdcn_status mdcn_pack_weight(mdcn_handle handle, const void* weight, void* works
     Plan p;
     mdcn_status s = plan_for_call(handle, dims, dtype, workspace_bytes, &p);
     if (s != MDCN_OK) return s;
+    if (p.direct) return MDCN_ERR_UNSUPPORTED;  // a direct plan runs whole, in mdcn_forward
     cudaError_t e = mdcn::launch_pack_weight(p, weight, workspace, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
     return MDCN_OK;
@@ -738,6 +776,7 @@ mdcn_status mdcn_forward_prepared(mdcn_handle handle, const void* offset, const 
     Plan p;
     mdcn_status s = plan_for_call(handle, dims, dtype, workspace_bytes, &p);
     if (s != MDCN_OK) return s;
+    if (p.direct) return MDCN_ERR_UNSUPPORTED;  // a direct plan runs whole, in mdcn_forward
     cudaError_t e = mdcn::launch_fused(p, offset, mask, bias_or_null, out, workspace, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
     return MDCN_OK;

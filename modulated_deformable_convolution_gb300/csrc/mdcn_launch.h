@@ -27,6 +27,21 @@ cudaError_t launch_prep_both(const Plan& pl, const void* x, const void* weight, 
 cudaError_t launch_fused(const Plan& pl, const void* offset, const void* mask, const void* bias, void* out, void* ws,
                          cudaStream_t st);
 
+// The direct CUDA-core forward (mdcn_direct.cu) of plans with pl.direct: one
+// launch, x read in NCHW, no workspace beyond the status word (which it
+// clears). Groups of at most kDirectMaxOg output channels; a thread takes
+// direct_groups_per_thread(Og) groups, whose fp32 weights (that many times
+// Og * Cg * K * 4 bytes) must fit kDirectMaxSmem.
+constexpr int kDirectMaxOg = 32;
+constexpr int64_t kDirectMaxSmem = 96 * 1024;
+inline int direct_og_bucket(int64_t og) { return og <= 1 ? 1 : (og <= 4 ? 4 : (og <= 16 ? 16 : kDirectMaxOg)); }
+inline int direct_groups_per_thread(int64_t og) {
+    const int b = direct_og_bucket(og);
+    return b >= 16 ? 1 : 16 / b;
+}
+cudaError_t launch_direct(const Plan& pl, const void* x, const void* offset, const void* mask, const void* weight,
+                          const void* bias, void* out, void* ws, cudaStream_t st);
+
 // The pack form's split of the front end's output om [N, c_off + c_mask, P]
 // (P = pl.P, N = pl.N, dtype = pl.dtype): channels [0, c_off) copied to offset
 // [N, c_off, P], channels [c_off, c_off + c_mask) through the logistic sigmoid

@@ -75,6 +75,8 @@ struct Plan {
     int32_t acc_cols;        // TMEM columns of one accumulator = nsub * BNs
     int32_t nacc;            // accumulators in TMEM (2: epilogue overlaps the next tile)
     int32_t tmem_cols;
+    int32_t direct;          // 1: the direct CUDA-core kernel (little contraction per output, e.g.
+                             //    depthwise); none of the fused-path fields below is set
     int32_t a_tmem;          // 1: the A stages (modulated columns) live in tensor memory, written by the
                              //    gather with tcgen05.st and read by the MMA from there (16-bit types, 2
                              //    k-groups); 0: 128-byte-swizzled shared-memory stages

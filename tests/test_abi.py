@@ -69,11 +69,12 @@ def test_create_rejects_out_of_range_attrs(lib, bad):
 
 
 @pytest.mark.parametrize("tuning,ok", [
-    ((0, -1, 0, 0, 0, 0), True), ((4, 1, 8, 4, 1, 256), True), ((2, 0, 0, 1, 0, 16), True),
-    ((6, -1, 0, 2, 2, 512), True), ((0, -1, 0, 3, 0, 0), False), ((0, -1, 0, 8, 0, 0), False),
-    ((1, -1, 0, 0, 0, 0), False), ((10, -1, 0, 0, 0, 0), False), ((0, 2, 0, 0, 0, 0), False),
-    ((0, -1, -1, 0, 0, 0), False), ((0, -1, 0, 0, 3, 0), False), ((0, -1, 0, 0, -1, 0), False),
-    ((0, -1, 0, 0, 0, 24), False), ((0, -1, 0, 0, 0, 528), False), ((0, -1, 0, 0, 0, -16), False),
+    ((0, -1, 0, 0, 0, 0, 0), True), ((4, 1, 8, 4, 1, 256, 1), True), ((2, 0, 0, 1, 0, 16, 2), True),
+    ((6, -1, 0, 2, 2, 512, 0), True), ((0, -1, 0, 3, 0, 0, 0), False), ((0, -1, 0, 8, 0, 0, 0), False),
+    ((1, -1, 0, 0, 0, 0, 0), False), ((10, -1, 0, 0, 0, 0, 0), False), ((0, 2, 0, 0, 0, 0, 0), False),
+    ((0, -1, -1, 0, 0, 0, 0), False), ((0, -1, 0, 0, 3, 0, 0), False), ((0, -1, 0, 0, -1, 0, 0), False),
+    ((0, -1, 0, 0, 0, 24, 0), False), ((0, -1, 0, 0, 0, 528, 0), False), ((0, -1, 0, 0, 0, -16, 0), False),
+    ((0, -1, 0, 0, 0, 0, 3), False), ((0, -1, 0, 0, 0, 0, -1), False),
 ])
 def test_create_tuned_validates(lib, tuning, ok):
     h = ctypes.c_void_p()
@@ -380,8 +381,9 @@ def test_backward_chunks_workspace_and_launches(lib, N, Cin, Cout, H, group, bia
     # output pixels N*Ho*Wo (Ho, Wo come from offset, independent of x): 2^31 refused, 2^31 - 1 accepted
     ("pixels", dict(N=2, Cin=8, H=8, W=8, Cout=8, Ho=1 << 15, Wo=1 << 15), False),
     ("pixels", dict(N=(1 << 31) - 1, Cin=8, H=1, W=1, Cout=8, Ho=1, Wo=1), True),
-    # input pixels N*H*W of the channels-last copy
-    ("x pixels", dict(N=2, Cin=8, H=1 << 15, W=1 << 15, Cout=8, Ho=4, Wo=4), False),
+    # input pixels N*H*W of the fused path's channels-last copy (Cout = 16: (Cin/group) * (Cout/group)
+    # above 64, so not a direct plan, which reads x in place with 64-bit indices)
+    ("x pixels", dict(N=2, Cin=8, H=1 << 15, W=1 << 15, Cout=16, Ho=4, Wo=4), False),
     # k-tiles of all tiles: 256 groups x (2^19 tiles of 128 pixels) x 16 k-tiles (4x4 taps, 64 channels)
     ("k-tiles", dict(N=1, Cin=16384, H=8, W=8, Cout=4096, Ho=8192, Wo=8192, kh=4, kw=4, group=256), False),
     ("k-tiles", dict(N=1, Cin=16384, H=8, W=8, Cout=4096, Ho=8184, Wo=8192, kh=4, kw=4, group=256), True),

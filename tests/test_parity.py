@@ -312,3 +312,65 @@ def test_rejected_calls_leave_out_untouched():
     assert fwd() == mdcn.MDCN_OK  # and the same buffers work
     torch.cuda.synchronize()
     assert not torch.all(out == 7.0)
+
+
+# Shapes with little contraction per output, for the direct CUDA-core kernel:
+# depthwise with a channel multiplier, small groups, the largest direct group
+# (32 outputs), strides, dilations, 5x3 taps, far offsets. Each runs on both
+# paths (tuning path=2 and path=1).
+DIRECT = [
+    Case("f16_dw_mult2_dg8", "f16", N=2, Cin=32, Cout=64, H=23, W=19, group=32, deformable_group=8, bias=True,
+         seed=70, offset_dist=("normal", 2.0)),
+    Case("bf16_g8_s2d2", "bf16", N=2, Cin=64, Cout=64, H=30, W=30, stride=(2, 2), padding=(2, 2), dilation=(2, 2),
+         group=8, deformable_group=4, bias=True, seed=71, offset_dist=("uniform", -4.0, 4.0)),
+    Case("f32_g4_k5x3_far", "f32", N=1, Cin=16, Cout=16, H=17, W=21, kh=5, kw=3, padding=(2, 1), group=4,
+         deformable_group=2, bias=False, seed=72, offset_dist=("uniform", -6.0, 6.0), mask_dist="uniform"),
+    Case("f16_og32_cg2", "f16", N=1, Cin=4, Cout=64, H=12, W=12, group=2, deformable_group=2, bias=True, seed=73),
+]
+
+
+@pytest.mark.parametrize("case", DIRECT, ids=[c.name for c in DIRECT])
+def test_direct_path(oracle_mod, case):
+    """The direct kernel (one launch) and the fused kernel, each forced on the
+    same shape, both meet the tolerance on every element; the automatic plan is
+    direct exactly where (Cin/group) * (Cout/group) <= 16."""
+    dev = torch.device("cuda", 0)
+    inp = make_inputs(case)
+    d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+    for tuning, path in ((None, 2 if (case.Cin // case.group) * (case.Cout // case.group) <= 16 else 1),
+                         (dict(path=2), 2), (dict(path=1), 1)):
+        h = mdcn.Handle(**case.attrs(), tuning=tuning)
+        plan = mdcn.mdcn_query_plan(h, d["x"], d["offset"], d["mask"], d["weight"], d["bias"])
+        assert plan["path"] == path and (path == 1 or plan["launches"] == 1), (tuning, plan)
+    ref = oracle_out(oracle_mod, case, inp)
+    compare(np64(gpu_out(case, inp, tuning=dict(path=2))), ref, case.dtype, case.name + " direct")
+    compare(np64(gpu_out(case, inp, tuning=dict(path=1))), ref, case.dtype, case.name + " fused")
+
+
+@pytest.mark.parametrize("case", SWEEP, ids=[c.name for c in SWEEP])
+def test_sweep_fused_forced(oracle_mod, case):
+    """Every sweep shape on the fused kernel, whichever path the planner picks
+    for it (the small ones plan as direct)."""
+    inp = make_inputs(case)
+    compare(np64(gpu_out(case, inp, tuning=dict(path=1))), oracle_out(oracle_mod, case, inp), case.dtype,
+            case.name + " fused")
+
+
+def test_direct_neck_depthwise_vs_forced_direct():
+    """A neck-sized depthwise layer (128 channels, one deformable group):
+    automatic (direct) and forced-direct plans give the same bits; the step-wise
+    calls refuse a direct plan and launch nothing."""
+    case = dataclasses.replace(CONFIGS["neck_f16"], name="neck_dw", group=128, seed=74)
+    inp = make_inputs(case)
+    a = gpu_out(case, inp)
+    b = gpu_out(case, inp, tuning=dict(path=2))
+    assert torch.equal(a, b)
+    dev = torch.device("cuda", 0)
+    d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+    h = mdcn.Handle(**case.attrs())
+    ws = torch.empty(mdcn.mdcn_workspace_size(h, d["x"], d["offset"], d["mask"], d["weight"], None),
+                     dtype=torch.uint8, device=dev)
+    assert ws.numel() == 1024  # the status word's header only
+    with pytest.raises(mdcn.MdcnError) as e:
+        mdcn.mdcn_prepare_input(h, d["x"], d["offset"], d["mask"], d["weight"], None, ws, torch.cuda.current_stream())
+    assert e.value.status == mdcn._abi.MDCN_ERR_UNSUPPORTED
