@@ -35,7 +35,7 @@ sys.path.insert(0, ROOT)
 
 import torch  # noqa: E402
 
-from modulated_deformable_convolution_gb300.workloads import CONFIG_ORDER, CONFIGS, make_inputs  # noqa: E402
+from modulated_deformable_convolution_gb300.workloads import CONFIG_ORDER, CONFIGS, EXTRA_ORDER, make_inputs  # noqa: E402
 
 METRIC = "modulated deform-conv fwd TFLOP/s & µs/call at 1 GB300; % of roofline"
 UNIT = "TFLOP/s"
@@ -261,7 +261,7 @@ def per_config_table(mdcn, dev, flush, peaks, peak_src, fp32_peaks, steps=20, wa
     and of the fused kernel. Roofline time = max(flops / tensor peak, bytes /
     HBM bandwidth), bytes = x + offset + mask + weight + bias + output once."""
     table = {}
-    for name in CONFIG_ORDER:
+    for name in CONFIG_ORDER + EXTRA_ORDER:
         case = CONFIGS[name]
         step_ms, fused_ms, plan, status = time_forward(mdcn, case, dev, steps, warmup, flush)
         peak, note = peak_for(case, peaks, peak_src, fp32_peaks)

@@ -102,6 +102,12 @@ CONFIGS = {
 }
 CONFIG_ORDER = ["tiny_f32", "neck_f16", "multidg_bf16", "grouped_f32", "largec_f16"]
 
+# Context beside the named workloads: the neck shape as a depthwise layer (one
+# group per channel, one deformable group), the case for the direct kernel.
+CONFIGS["depthwise_f16"] = Case("depthwise_f16", "f16", N=4, Cin=128, Cout=128, H=80, W=80, group=128, bias=False,
+                                seed=5, offset_dist=("normal", 1.5))
+EXTRA_ORDER = ["depthwise_f16"]
+
 
 def make_inputs(case: Case, device="cpu"):
     """Draw the case's inputs. Returns a dict of tensors in the case's dtype:
