@@ -87,12 +87,54 @@ SWEEP = [
     Case("b_f32_cin3", "f32", N=2, Cin=3, Cout=5, H=8, W=8, bias=True, seed=68, offset_dist=("normal", 1.0)),
     Case("b_f16_cd6_g3", "f16", N=2, Cin=18, Cout=9, H=10, W=7, group=3, deformable_group=3, bias=False, seed=69,
          offset_dist=("normal", 1.0)),
+    # the tensor-core GEMMs (P and K*Cg multiples of 8): pixels not a multiple of 128, K*Cg = 4.5 tiles,
+    # Og < 64 (one zero-padded contraction chunk)
+    Case("b_f16_tc_ragged", "f16", N=3, Cin=64, Cout=48, H=12, W=10, deformable_group=2, bias=True, seed=71,
+         offset_dist=("normal", 1.5)),
+    # groups with several deformable groups each
+    Case("b_bf16_tc_g2_dg4", "bf16", N=2, Cin=128, Cout=96, H=20, W=20, group=2, deformable_group=4, bias=True,
+         seed=72, offset_dist=("normal", 2.0)),
+    # Cd = 16, strided 5x3 taps
+    Case("b_f16_tc_cd16_s2_k5x3", "f16", N=2, Cin=64, Cout=40, H=16, W=16, kh=5, kw=3, stride=(2, 2),
+         padding=(2, 1), deformable_group=4, bias=False, seed=77, offset_dist=("normal", 1.5)),
+    # Cd = 8 (lanes of 2 per sampling point)
+    Case("b_f16_tc_cd8_s2_k5x3", "f16", N=2, Cin=32, Cout=40, H=16, W=16, kh=5, kw=3, stride=(2, 2),
+         padding=(2, 1), deformable_group=4, bias=False, seed=73, offset_dist=("normal", 1.5)),
+    # Og = 256 (four 64-wide contraction chunks), Cd = 128, dilated, border-heavy offsets
+    Case("b_f16_tc_og256_dil2", "f16", N=1, Cin=128, Cout=256, H=24, W=24, padding=(2, 2), dilation=(2, 2),
+         bias=False, seed=74, offset_dist=("uniform", -4.0, 4.0), mask_dist="uniform"),
+    # Cd = 4: one lane per sampling point
+    Case("b_bf16_tc_cd4", "bf16", N=2, Cin=8, Cout=8, H=8, W=8, deformable_group=2, bias=True, seed=75,
+         offset_dist=("normal", 1.0)),
+    # a deformable group of 32 channels over two groups of 16
+    Case("b_f16_tc_g4_dg2", "f16", N=2, Cin=64, Cout=64, H=16, W=16, group=4, deformable_group=2,
+         bias=True, seed=76, offset_dist=("normal", 1.5)),
 ]
+
+# Two image chunks (about 140 MB of per-chunk buffers per image: one image per chunk).
+CHUNKED = Case("b_f16_tc_chunks", "f16", N=2, Cin=16, Cout=16, H=384, W=384, bias=False, seed=70,
+               offset_dist=("normal", 1.5))
 
 
 @pytest.mark.parametrize("case", SWEEP, ids=[c.name for c in SWEEP])
 def test_backward_sweep(oracle_mod, case):
     inp = make_inputs(case)
+    go = make_grad_out(case)
+    compare_all(gpu_backward(case, inp, go), oracle_backward(oracle_mod, case, inp, go), case.dtype, case.name)
+
+
+def test_backward_two_chunks(oracle_mod):
+    """Images in two chunks (each chunk's channels-last x, columns and grad_x
+    buffers reused), every element of every gradient."""
+    case = CHUNKED
+    inp = make_inputs(case)
+    h = mdcn.Handle(**case.attrs())
+    dev = torch.device("cuda", 0)
+    d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+    launches = mdcn.mdcn_backward_launches(h, d["x"], d["offset"], d["mask"], d["weight"], None)
+    # weight re-layout; per chunk: transpose, memset, column-gradient GEMM, sampling, weight-gradient
+    # GEMM and its split sum, transpose; the weight gradient's layout
+    assert launches == 1 + 2 * 7 + 1
     go = make_grad_out(case)
     compare_all(gpu_backward(case, inp, go), oracle_backward(oracle_mod, case, inp, go), case.dtype, case.name)
 
