@@ -128,6 +128,65 @@ __global__ void __launch_bounds__(256) transpose_kernel(const Tin* __restrict__ 
     }
 }
 
+// The same transposes with 16-byte accesses on both sides (R and C multiples
+// of 16 / sizeof of each side's type): a 64 x 64 tile per block, loaded as
+// 16-byte vectors along the input rows and stored as 16-byte vectors along
+// the output rows, through a 64 x 65 fp32 tile. With zero != nullptr (same
+// layout as out, fp32) the block also clears its tile of zero: the chunk's
+// grad_x accumulator, cleared while x is transposed.
+template <typename Tin, typename Tout>
+__global__ void __launch_bounds__(256) transpose_vec_kernel(const Tin* __restrict__ in, Tout* __restrict__ out,
+                                                            float* __restrict__ zero, int64_t R, int64_t C) {
+    constexpr int kT = kTransposeTile;
+    constexpr int kVi = 16 / sizeof(Tin), kVo = 16 / sizeof(Tout);
+    __shared__ float tile[kT][kT + 1];
+    const int64_t b = blockIdx.y;
+    const int64_t ctiles = (C + kT - 1) / kT;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.x) / ctiles * kT;
+    const int64_t c0 = static_cast<int64_t>(blockIdx.x) % ctiles * kT;
+    const Tin* src = in + b * R * C;
+    Tout* dst = out + b * R * C;
+    // load: the tile's rows as kT / kVi vectors each
+    constexpr int kVrow = kT / kVi, kLoads = kT * kVrow / 256;
+    Vec<Tin, kVi> v[kLoads];
+#pragma unroll
+    for (int k = 0; k < kLoads; ++k) {
+        const int idx = threadIdx.x + 256 * k;
+        const int64_t r = r0 + idx / kVrow, c = c0 + (idx % kVrow) * kVi;
+        if (r < R && c < C) {
+            v[k] = *reinterpret_cast<const Vec<Tin, kVi>*>(src + r * C + c);
+        } else {
+#pragma unroll
+            for (int e = 0; e < kVi; ++e) v[k].v[e] = Tin(0);
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < kLoads; ++k) {
+        const int idx = threadIdx.x + 256 * k;
+#pragma unroll
+        for (int e = 0; e < kVi; ++e) tile[idx / kVrow][(idx % kVrow) * kVi + e] = to_f(v[k].v[e]);
+    }
+    __syncthreads();
+    // store: output row c0 + cc holds the tile's column cc, kT / kVo vectors each
+    constexpr int kVcol = kT / kVo, kStores = kT * kVcol / 256;
+#pragma unroll
+    for (int k = 0; k < kStores; ++k) {
+        const int cc = threadIdx.x % kT, vi = threadIdx.x / kT + (256 / kT) * k;
+        const int64_t c = c0 + cc, r = r0 + vi * kVo;
+        if (c < C && r < R) {
+            float w[kVo];
+#pragma unroll
+            for (int e = 0; e < kVo; ++e) w[e] = tile[vi * kVo + e][cc];
+            store_f<Tout, kVo>(dst + c * R + r, w);
+            if (zero) {
+#pragma unroll
+                for (int e = 0; e < kVo; e += 4)
+                    *reinterpret_cast<float4*>(zero + b * R * C + c * R + r + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+    }
+}
+
 // out[o][n][p] = in[n][o][p] for the chunk's nb images: grad_out with the
 // image index moved inside the channel index (16-byte copies along p when P
 // is a multiple of 16 / sizeof(T), else element copies).
@@ -325,11 +384,23 @@ unsigned grid_for(int64_t total) {
     return static_cast<unsigned>(b < 1 ? 1 : (b > 8192 ? 8192 : b));
 }
 
+// out[b] = in[b]^T (R x C per batch entry); with zero != nullptr also clears zero[b] (fp32, out's layout),
+// then returning whether it did (the element kernel leaves it to the caller).
 template <typename Tin, typename Tout>
-cudaError_t transpose(const Tin* in, Tout* out, int64_t R, int64_t C, int64_t batch, cudaStream_t st) {
+cudaError_t transpose(const Tin* in, Tout* out, int64_t R, int64_t C, int64_t batch, cudaStream_t st,
+                      float* zero = nullptr, bool* zeroed = nullptr) {
     const int64_t tiles = ((R + kTransposeTile - 1) / kTransposeTile) * ((C + kTransposeTile - 1) / kTransposeTile);
-    transpose_kernel<Tin, Tout><<<dim3(static_cast<unsigned>(tiles), static_cast<unsigned>(batch)), 256, 0, st>>>(
-        in, out, R, C);
+    const dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(batch));
+    constexpr int64_t kVi = 16 / sizeof(Tin), kVo = 16 / sizeof(Tout);
+    // 16-byte vectors where a side is 16-bit (float32 on both sides is as fast element-wise, measured)
+    // and the rows of both sides are whole vectors (the caller's buffers are 16-byte aligned)
+    const bool vec = (sizeof(Tin) == 2 || sizeof(Tout) == 2) && C % kVi == 0 && R % kVo == 0 && (!zero || R % 4 == 0);
+    if (vec) {
+        transpose_vec_kernel<Tin, Tout><<<grid, 256, 0, st>>>(in, out, zero, R, C);
+    } else {
+        transpose_kernel<Tin, Tout><<<grid, 256, 0, st>>>(in, out, R, C);
+    }
+    if (zeroed) *zeroed = vec && zero;
     return cudaGetLastError();
 }
 
@@ -454,9 +525,16 @@ cudaError_t run_backward(const BwdPlan& p, const T* x, const T* offset, const T*
 
     for (int64_t n0 = 0; n0 < p.N; n0 += p.nb) {
         const int64_t nbc = p.N - n0 < p.nb ? p.N - n0 : p.nb;
-        // 1. x of the chunk, channels-last
-        if ((e = transpose<T, T>(x + n0 * p.Cin * HW, xt, p.Cin, HW, nbc, st)) != cudaSuccess) return e;
-        if ((e = cudaMemsetAsync(gx, 0, static_cast<size_t>(nbc * HW * p.Cin) * sizeof(float), st)) != cudaSuccess)
+        // 1. x of the chunk, channels-last, and the chunk's grad_x accumulator cleared (by the
+        //    transpose where it takes 16-byte vectors, else by a memset)
+        const bool clear = backward_clears_in_transpose(p);
+        bool zeroed = false;
+        if ((e = transpose<T, T>(x + n0 * p.Cin * HW, xt, p.Cin, HW, nbc, st, clear ? gx : nullptr, &zeroed)) !=
+            cudaSuccess)
+            return e;
+        if (clear != zeroed) return cudaErrorInvalidValue;  // the two tests of the vector path agree
+        if (!zeroed &&
+            (e = cudaMemsetAsync(gx, 0, static_cast<size_t>(nbc * HW * p.Cin) * sizeof(float), st)) != cudaSuccess)
             return e;
         // 2. column gradients, per group: (K*Cg x P) = wt_g (K*Cg x Og) * grad_out_g (Og x P), column-major views
         for (int32_t g = 0; g < p.group; ++g) {
@@ -604,13 +682,20 @@ bool backward_uses_tc(const BwdPlan& p) {
     return p.dtype != kF32 && p.P % 8 == 0 && KCg % 8 == 0 && p.P < (int64_t(1) << 31) && KCg < (int64_t(1) << 31);
 }
 
+bool backward_clears_in_transpose(const BwdPlan& p) {
+    // the x transpose takes 16-byte vectors on both sides: 16-bit I/O, H*W and Cin multiples of 8
+    return p.dtype != kF32 && (p.H * p.W) % 8 == 0 && p.Cin % 8 == 0;
+}
+
 int backward_launch_count(const BwdPlan& p) {
     const int64_t chunks = (p.N + p.nb - 1) / p.nb;
-    // per chunk: transpose, memset, one GEMM per group, sampling backward, the weight-gradient
-    // GEMMs (tensor-core path: one GEMM and the in-order sum of its split slices per chunk;
-    // cuBLAS path, group 1: a grad_out re-layout and one GEMM; else one per image), transpose
+    // per chunk: transpose (with a memset of grad_x unless the transpose clears it), one GEMM per
+    // group, sampling backward, the weight-gradient GEMMs (tensor-core path: one GEMM and the
+    // in-order sum of its split slices per chunk; cuBLAS path, group 1: a grad_out re-layout and
+    // one GEMM; else one per image), transpose
     const int64_t wgrad = backward_uses_tc(p) ? 2 * chunks : (p.group == 1 ? 2 * chunks : p.N);
-    return static_cast<int>(1 + chunks * (4 + p.group) + wgrad + 1 + (p.has_bias ? 1 : 0));
+    const int64_t per_chunk = (backward_clears_in_transpose(p) ? 3 : 4) + p.group;
+    return static_cast<int>(1 + chunks * per_chunk + wgrad + 1 + (p.has_bias ? 1 : 0));
 }
 
 cudaError_t launch_backward(const BwdPlan& p, const void* x, const void* offset, const void* mask, const void* weight,

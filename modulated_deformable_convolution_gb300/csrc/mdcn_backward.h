@@ -50,6 +50,11 @@ cudaError_t launch_backward(const BwdPlan& p, const void* x, const void* offset,
                             const void* grad_out, void* grad_x, void* grad_offset, void* grad_mask, void* grad_weight,
                             void* grad_bias, void* ws, cudaStream_t st);
 
+// True when the x transpose of each chunk also clears its grad_x accumulator
+// (16-byte vectors: 16-bit I/O, H*W and Cin multiples of 8), so no memset is
+// launched.
+bool backward_clears_in_transpose(const BwdPlan& p);
+
 // Kernel launches (and cuBLAS calls) one backward call makes.
 int backward_launch_count(const BwdPlan& p);
 

@@ -132,9 +132,9 @@ def test_backward_two_chunks(oracle_mod):
     dev = torch.device("cuda", 0)
     d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
     launches = mdcn.mdcn_backward_launches(h, d["x"], d["offset"], d["mask"], d["weight"], None)
-    # weight re-layout; per chunk: transpose, memset, column-gradient GEMM, sampling, weight-gradient
-    # GEMM and its split sum, transpose; the weight gradient's layout
-    assert launches == 1 + 2 * 7 + 1
+    # weight re-layout; per chunk: transpose (clearing grad_x), column-gradient GEMM, sampling,
+    # weight-gradient GEMM and its split sum, transpose; the weight gradient's layout
+    assert launches == 1 + 2 * 6 + 1
     go = make_grad_out(case)
     compare_all(gpu_backward(case, inp, go), oracle_backward(oracle_mod, case, inp, go), case.dtype, case.name)
 
