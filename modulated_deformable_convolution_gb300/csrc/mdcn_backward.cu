@@ -36,6 +36,8 @@
 //   5. the fp32 grad_x accumulator -> NCHW in the I/O type.
 // Then the weight gradient to [Cout, Cg, kh, kw] and the bias reduction.
 #include <cublas_v2.h>
+
+#include <algorithm>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -234,6 +236,80 @@ __global__ void __launch_bounds__(256) weight_grad_out_kernel(const float* __res
         const int64_t o = e / (Cg * K), r = e - o * (Cg * K);
         const int64_t cl = r / K, k = r - cl * K;
         gweight[e] = from_f<T>(gw[(o * K + k) * Cg + cl]);
+    }
+}
+
+// The two weight re-layouts one output channel per block, through shared
+// memory (Cg*K elements): both the read of one layout and the write of the
+// other are contiguous. wt[o][k][c_l] = w[o][c_l][k]; the block of o = 0
+// also clears the call's device status word.
+template <typename T>
+__global__ void __launch_bounds__(256) weight_tap_major_block_kernel(const T* __restrict__ w, T* __restrict__ wt,
+                                                                     int32_t Cg, int32_t K,
+                                                                     uint32_t* __restrict__ status) {
+    extern __shared__ float wsm[];  // [c_l][k], pitch K + 1
+    if (blockIdx.x == 0 && threadIdx.x == 0) *status = 0u;
+    const int64_t o = blockIdx.x;
+    const int32_t n = Cg * K;
+    const T* src = w + o * n;
+    T* dst = wt + o * n;
+    for (int32_t e = threadIdx.x; e < n; e += blockDim.x) {
+        const int32_t cl = e / K, k = e - cl * K;
+        wsm[cl * (K + 1) + k] = to_f(src[e]);
+    }
+    __syncthreads();
+    for (int32_t e = threadIdx.x; e < n; e += blockDim.x) {
+        const int32_t k = e / Cg, cl = e - k * Cg;
+        dst[e] = from_f<T>(wsm[cl * (K + 1) + k]);
+    }
+}
+
+// grad_weight[o][c_l][k] = gw[o][k][c_l] in the I/O type, one output channel per block.
+template <typename T>
+__global__ void __launch_bounds__(256) weight_grad_out_block_kernel(const float* __restrict__ gw,
+                                                                    T* __restrict__ gweight, int32_t Cg, int32_t K) {
+    extern __shared__ float wsm[];  // [k][c_l], pitch Cg + 1
+    const int64_t o = blockIdx.x;
+    const int32_t n = Cg * K;
+    const float* src = gw + o * n;
+    T* dst = gweight + o * n;
+    for (int32_t e = threadIdx.x; e < n; e += blockDim.x) {
+        const int32_t k = e / Cg, cl = e - k * Cg;
+        wsm[k * (Cg + 1) + cl] = src[e];
+    }
+    __syncthreads();
+    for (int32_t e = threadIdx.x; e < n; e += blockDim.x) {
+        const int32_t cl = e / K, k = e - cl * K;
+        dst[e] = from_f<T>(wsm[k * (Cg + 1) + cl]);
+    }
+}
+
+// grad_bias[o] with 16-byte loads (P a multiple of 16 / sizeof(T)): one block
+// per output channel; each thread sums its vectors in order, then a fixed
+// tree over the block.
+template <typename T>
+__global__ void __launch_bounds__(256) bias_grad_vec_kernel(const T* __restrict__ gout, T* __restrict__ gbias,
+                                                            int64_t N, int64_t Cout, int64_t P) {
+    constexpr int kV = 16 / sizeof(T);
+    __shared__ float part[8];
+    const int64_t o = blockIdx.x;
+    const int64_t pv = P / kV;
+    float s = 0.f;
+    for (int64_t i = threadIdx.x; i < N * pv; i += blockDim.x) {
+        const int64_t n = i / pv, v = i - n * pv;
+        float x[kV];
+        load_f<T, kV>(gout + (n * Cout + o) * P + v * kV, x);
+#pragma unroll
+        for (int e = 0; e < kV; ++e) s += x[e];
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) s += __shfl_xor_sync(0xffffffffu, s, d);
+    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = s;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float t = 0.f;
+        for (int i = 0; i < 8; ++i) t += part[i];
+        gbias[o] = from_f<T>(t);
     }
 }
 
@@ -520,7 +596,16 @@ cudaError_t run_backward(const BwdPlan& p, const T* x, const T* offset, const T*
     const cublasComputeType_t ct = sizeof(T) == 4 ? CUBLAS_COMPUTE_32F_PEDANTIC : CUBLAS_COMPUTE_32F;
     const float one = 1.0f, zero = 0.0f;
 
-    weight_tap_major_kernel<T><<<grid_for(p.Cout * KCg), 256, 0, st>>>(weight, wt, p.Cout, Cg, K, status);
+    // one output channel per block through shared memory where its Cg*K weights (padded by a row)
+    // fit 48 KB as fp32
+    const int64_t wfl = KCg + std::max(Cg, K);
+    const bool wblock = wfl <= 12288 && p.Cout <= 2147483647;
+    const size_t wsmem = static_cast<size_t>(wfl) * sizeof(float);
+    if (wblock)
+        weight_tap_major_block_kernel<T><<<static_cast<unsigned>(p.Cout), 256, wsmem, st>>>(
+            weight, wt, static_cast<int32_t>(Cg), static_cast<int32_t>(K), status);
+    else
+        weight_tap_major_kernel<T><<<grid_for(p.Cout * KCg), 256, 0, st>>>(weight, wt, p.Cout, Cg, K, status);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
     for (int64_t n0 = 0; n0 < p.N; n0 += p.nb) {
@@ -604,10 +689,18 @@ cudaError_t run_backward(const BwdPlan& p, const T* x, const T* offset, const T*
         // 5. grad_x of the chunk to NCHW
         if ((e = transpose<float, T>(gx, grad_x + n0 * p.Cin * HW, HW, p.Cin, nbc, st)) != cudaSuccess) return e;
     }
-    weight_grad_out_kernel<T><<<grid_for(p.Cout * KCg), 256, 0, st>>>(gw, grad_weight, p.Cout, Cg, K);
+    if (wblock)
+        weight_grad_out_block_kernel<T><<<static_cast<unsigned>(p.Cout), 256, wsmem, st>>>(
+            gw, grad_weight, static_cast<int32_t>(Cg), static_cast<int32_t>(K));
+    else
+        weight_grad_out_kernel<T><<<grid_for(p.Cout * KCg), 256, 0, st>>>(gw, grad_weight, p.Cout, Cg, K);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (grad_bias) {
-        bias_grad_kernel<T><<<static_cast<unsigned>(p.Cout), 256, 0, st>>>(grad_out, grad_bias, p.N, p.Cout, P);
+        if (P % (16 / static_cast<int64_t>(sizeof(T))) == 0)
+            bias_grad_vec_kernel<T><<<static_cast<unsigned>(p.Cout), 256, 0, st>>>(grad_out, grad_bias, p.N, p.Cout,
+                                                                                    P);
+        else
+            bias_grad_kernel<T><<<static_cast<unsigned>(p.Cout), 256, 0, st>>>(grad_out, grad_bias, p.N, p.Cout, P);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;
