@@ -253,9 +253,22 @@ __global__ void __launch_bounds__(256) weight_tap_major_block_kernel(const T* __
     const int32_t n = Cg * K;
     const T* src = w + o * n;
     T* dst = wt + o * n;
-    for (int32_t e = threadIdx.x; e < n; e += blockDim.x) {
-        const int32_t cl = e / K, k = e - cl * K;
-        wsm[cl * (K + 1) + k] = to_f(src[e]);
+    // 8 loads per thread in flight per round
+    for (int32_t base = 0; base < n; base += 8 * 256) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int32_t e = base + 256 * u + static_cast<int32_t>(threadIdx.x);
+            v[u] = e < n ? to_f(src[e]) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int32_t e = base + 256 * u + static_cast<int32_t>(threadIdx.x);
+            if (e < n) {
+                const int32_t cl = e / K, k = e - cl * K;
+                wsm[cl * (K + 1) + k] = v[u];
+            }
+        }
     }
     __syncthreads();
     for (int32_t e = threadIdx.x; e < n; e += blockDim.x) {
@@ -273,9 +286,22 @@ __global__ void __launch_bounds__(256) weight_grad_out_block_kernel(const float*
     const int32_t n = Cg * K;
     const float* src = gw + o * n;
     T* dst = gweight + o * n;
-    for (int32_t e = threadIdx.x; e < n; e += blockDim.x) {
-        const int32_t k = e / Cg, cl = e - k * Cg;
-        wsm[k * (Cg + 1) + cl] = src[e];
+    // 8 loads per thread in flight per round
+    for (int32_t base = 0; base < n; base += 8 * 256) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int32_t e = base + 256 * u + static_cast<int32_t>(threadIdx.x);
+            v[u] = e < n ? src[e] : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int32_t e = base + 256 * u + static_cast<int32_t>(threadIdx.x);
+            if (e < n) {
+                const int32_t k = e / Cg, cl = e - k * Cg;
+                wsm[k * (Cg + 1) + cl] = v[u];
+            }
+        }
     }
     __syncthreads();
     for (int32_t e = threadIdx.x; e < n; e += blockDim.x) {
