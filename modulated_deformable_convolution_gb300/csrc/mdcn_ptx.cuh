@@ -30,12 +30,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ uint64_t globaltimer_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -47,11 +41,6 @@ __device__ __forceinline__ void fence_mbarrier_init() {
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
@@ -214,15 +203,6 @@ __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
-// 2-D tiled load of one box into shared memory; completion is signalled as
-// transaction bytes on the mbarrier. c0 is the innermost coordinate.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int32_t c0, int32_t c1, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(bar)
-        : "memory");
-}
-
 __device__ __forceinline__ void prefetch_l2(const void* p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
@@ -267,33 +247,6 @@ __host__ __device__ constexpr uint32_t make_idesc(uint32_t ab_format, uint32_t M
            | ((M >> 4) << 24);        // M >> 4
 }
 
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                        uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                         uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Arrives on the mbarrier once every tcgen05 operation issued so far by this
-// thread has completed.
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
-}
-
 // Warp-wide forms of the issue instructions: the whole (converged) warp
 // executes them, computing every operand alike, and the lane elect.sync picks
 // (the lowest one, so always the same lane) issues. Operands computed by a
@@ -323,6 +276,7 @@ __device__ __forceinline__ void mma_f16_ts_elect(uint32_t d_tmem, uint32_t a_tme
         : "memory");
 }
 
+// kind::tf32: A and B fp32 in shared memory, read as tf32.
 __device__ __forceinline__ void mma_tf32_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                                uint32_t accumulate) {
     asm volatile(
@@ -334,6 +288,8 @@ __device__ __forceinline__ void mma_tf32_elect(uint32_t d_tmem, uint64_t adesc, 
         : "memory");
 }
 
+// Arrives on the mbarrier once every tcgen05 operation the CTA issued so far
+// has completed.
 __device__ __forceinline__ void mma_commit_elect(uint32_t bar) {
     asm volatile(
         "{\n\t.reg .pred e;\n\t"
@@ -343,6 +299,7 @@ __device__ __forceinline__ void mma_commit_elect(uint32_t bar) {
         : "memory");
 }
 
+// One arrival that also expects `bytes` of asynchronous copies on the barrier.
 __device__ __forceinline__ void mbar_arrive_expect_tx_elect(uint32_t bar, uint32_t bytes) {
     asm volatile(
         "{\n\t.reg .pred e;\n\t"
@@ -352,6 +309,8 @@ __device__ __forceinline__ void mbar_arrive_expect_tx_elect(uint32_t bar, uint32
         : "memory");
 }
 
+// 2-D tiled load of one box into shared memory; completion is signalled on the
+// mbarrier as transferred bytes.
 __device__ __forceinline__ void tma_load_2d_elect(uint32_t dst, const void* tmap, int32_t c0, int32_t c1,
                                                   uint32_t bar) {
     asm volatile(
@@ -403,32 +362,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, int n, float (&v)[32])
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Up to 4 x (32 lanes x 16 columns) TMEM loads issued back to back, one wait:
-// v[16*k + c] = column (taddr.col + 16*k + c) of this thread's lane, k < n.
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, int n, float (&v)[64]) {
-    uint32_t r[64];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        if (k < n) {
-            asm volatile(
-                "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-                "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-                : "=r"(r[16 * k + 0]), "=r"(r[16 * k + 1]), "=r"(r[16 * k + 2]), "=r"(r[16 * k + 3]),
-                  "=r"(r[16 * k + 4]), "=r"(r[16 * k + 5]), "=r"(r[16 * k + 6]), "=r"(r[16 * k + 7]),
-                  "=r"(r[16 * k + 8]), "=r"(r[16 * k + 9]), "=r"(r[16 * k + 10]), "=r"(r[16 * k + 11]),
-                  "=r"(r[16 * k + 12]), "=r"(r[16 * k + 13]), "=r"(r[16 * k + 14]), "=r"(r[16 * k + 15])
-                : "r"(taddr + 16u * k)
-                : "memory");
-        } else {
-#pragma unroll
-            for (int c = 0; c < 16; ++c) r[16 * k + c] = 0u;
-        }
-    }
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
-}
-
 // 16 lanes x 256 bits, repeated over 4 consecutive 8-column blocks: thread t
 // writes r[4k], r[4k+1] to lane (taddr.lane + t/4), columns taddr.col + 8k +
 // 2(t%4) and + 1, and r[4k+2], r[4k+3] to lane (taddr.lane + 8 + t/4), the
@@ -450,10 +383,6 @@ __device__ __forceinline__ void ldg256(const void* p, uint4& a, uint4& b) {
     asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                  : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
                  : "l"(p));
-}
-
-__device__ __forceinline__ void prefetch_l1(const void* p) {
-    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
 }
 
 // Round-to-nearest (ties away) fp32 -> tf32, returned as an fp32 bit pattern
