@@ -126,7 +126,12 @@ typedef struct mdcn_tuning {
                           weights of a thread's groups within 96 KB);
                           0 = automatic: direct where (Cin/group) * (Cout/group) <= 16, e.g.
                           depthwise, where the implicit GEMM would pad each channel unit to a 128-byte
-                          k-tile and each group's outputs to 16 MMA columns */
+                          k-tile and each group's outputs to 16 MMA columns; for a depthwise layer
+                          (one input and one output channel per group) with Cin and Cin/dg multiples
+                          of 4 and at most 49 taps, its channels-last form: x copied to
+                          [N*H*W + 1][Cin] in the workspace first, then each lane reads a sampling
+                          point's corners for 4 channels at once (2 launches; the same fp32 sums in
+                          the same order, so the same bits). Forcing path 2 keeps x in NCHW */
 } mdcn_tuning;
 
 /* mdcn_create with plan overrides (tuning may be NULL = automatic). Errors as
@@ -151,7 +156,9 @@ mdcn_status mdcn_output_dims(mdcn_handle handle, const mdcn_dims* dims, int64_t 
 /* Bytes of device workspace mdcn_forward needs for these dims and dtype
  * (a status word, the channels-last copy of x, the repacked weight, and the
  * fp32 partial sums of output tiles split between CTAs; a direct plan, see
- * mdcn_tuning.path, needs the 1 KB header only). Host only. */
+ * mdcn_tuning.path, needs the 1 KB header only, plus x channels-last,
+ * (N*H*W + 1) * Cin elements, for its depthwise channels-last form). Host
+ * only. */
 mdcn_status mdcn_workspace_size(mdcn_handle handle, const mdcn_dims* dims, mdcn_dtype dtype,
                                 size_t* bytes);
 
@@ -165,7 +172,8 @@ typedef struct mdcn_plan_info {
     int32_t split;          /* 1 when some tile is split between CTAs (summed inside the fused kernel) */
     int32_t stages, kgroups, tile_mode;
     int32_t launches;       /* kernels one mdcn_forward launches: prep (1, or 2 when x needs the staged
-                               transpose) and the fused kernel; 1 for a direct plan */
+                               transpose) and the fused kernel; 1 for a direct plan, 2 for its
+                               depthwise channels-last form */
     int32_t a_operand;      /* 1: A stages in shared memory, 2: in tensor memory (0: direct plan) */
     int32_t path;           /* 1: fused implicit GEMM, 2: direct kernel (the tile fields above are then 0) */
 } mdcn_plan_info;

@@ -161,6 +161,18 @@ mdcn_status make_plan(const mdcn_attrs& a, const mdcn_tuning& tuning, const mdcn
         if (fits && (tuning.path == 2 || (tuning.path == 0 && Cg * Og <= 16))) {
             p.direct = 1;
             p.off_xt = p.off_wp = p.off_part = p.ws_bytes = mdcn::kStatusBytes;
+            // depthwise with deformable groups of whole 4-channel chunks: the
+            // channels-last form, on a copy of x [N*H*W + 1][Cin] in the workspace
+            const int64_t elem_b = dtype == MDCN_F32 ? 4 : 2;
+            int64_t xt_bytes = p.N * p.H;  // N <= 65535, H < 2^24
+            bool xt_ok = mul_ok(xt_bytes, p.W);
+            xt_bytes += 1;  // the zero pixel
+            xt_ok = xt_ok && mul_ok(xt_bytes, p.Cin) && mul_ok(xt_bytes, elem_b);
+            if (Cg == 1 && Og == 1 && p.Cin % 4 == 0 && Cd % 4 == 0 && K <= mdcn::kDirectClMaxTaps &&
+                p.Cin <= 65535ll * 128 && xt_ok && tuning.path != 2) {
+                p.direct_cl = 1;
+                p.ws_bytes = align256(p.off_xt + static_cast<size_t>(xt_bytes));
+            }
             *pl = p;
             return MDCN_OK;
         }
@@ -555,7 +567,7 @@ mdcn_status mdcn_query_plan(mdcn_handle handle, const mdcn_dims* dims, mdcn_dtyp
     info->stages = p.stages;
     info->kgroups = p.kgroups;
     info->tile_mode = p.tile_mode;
-    info->launches = p.direct ? 1 : (p.xt_block ? 2 : 3);
+    info->launches = p.direct ? (p.direct_cl ? 2 : 1) : (p.xt_block ? 2 : 3);
     info->a_operand = p.direct ? 0 : (p.a_tmem ? 2 : 1);
     info->path = p.direct ? 2 : 1;
     return MDCN_OK;

@@ -35,6 +35,15 @@ __device__ __forceinline__ void stf(float* p, float v) { *p = v; }
 __device__ __forceinline__ void stf(__half* p, float v) { *p = __float2half_rn(v); }
 __device__ __forceinline__ void stf(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 
+// Four consecutive channels of one channels-last pixel, as one aligned access.
+template <typename T>
+struct alignas(4 * sizeof(T)) ClVec {
+    T v[4];
+};
+__device__ __forceinline__ float cl_elem(const ClVec<float>& a, int e) { return a.v[e]; }
+__device__ __forceinline__ float cl_elem(const ClVec<__half>& a, int e) { return __half2float(a.v[e]); }
+__device__ __forceinline__ float cl_elem(const ClVec<__nv_bfloat16>& a, int e) { return __bfloat162float(a.v[e]); }
+
 constexpr int kDirectThreads = 128;
 constexpr int kDirectTaps = 3;  // taps whose sampling points a thread holds at once
 
@@ -209,10 +218,321 @@ cudaError_t launch_direct_t(const Plan& pl, const void* x, const void* offset, c
     return launch_direct_og<T, kDirectMaxOg>(pl, x, offset, mask, weight, bias, out, status, st);
 }
 
+// ---------------------------------------------------------------- depthwise, channels-last
+// For depthwise layers (one input and one output channel per group) whose
+// deformable groups hold whole 4-channel chunks: x is first made
+// channels-last, so that one sampling point's 4 corners are read for 4
+// channels at a time (8 bytes for 16-bit types) by each lane, and a warp
+// reads a corner's 128 channels as 256 contiguous bytes instead of 128
+// scattered 2-byte loads from the channel planes. (Measured on the neck
+// shape as a depthwise layer, 128 channels, one deformable group.)
+
+// x [N][C][H*W] -> xt [N*H*W + 1][C]; the last pixel is all zeros (read for
+// corners outside the image). 64 x 64 tiles through shared memory; block 0
+// also clears the call's status word.
+template <typename T>
+__global__ void __launch_bounds__(256) nhwc_zero_pixel_kernel(const T* __restrict__ x, T* __restrict__ xt,
+                                                              uint32_t* __restrict__ status, int64_t C, int64_t HW,
+                                                              int64_t NHW) {
+    __shared__ float tile[64][65];
+    if (blockIdx.x == 0 && blockIdx.y == 0) {
+        if (threadIdx.x == 0 && status) *status = 0u;
+        for (int64_t i = threadIdx.x; i < C; i += 256) stf(xt + NHW * C + i, 0.f);
+    }
+    const int64_t n = blockIdx.y;
+    const int64_t ptiles = (HW + 63) / 64;
+    const int64_t c0 = static_cast<int64_t>(blockIdx.x) / ptiles * 64;
+    const int64_t p0 = static_cast<int64_t>(blockIdx.x) % ptiles * 64;
+    const int tx = threadIdx.x % 64, ty = threadIdx.x / 64;
+    float v[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        const int64_t c = c0 + ty + 4 * k, pp = p0 + tx;
+        v[k] = c < C && pp < HW ? ldf(x + (n * C + c) * HW + pp) : 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < 16; ++k) tile[ty + 4 * k][tx] = v[k];
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        const int64_t pp = p0 + ty + 4 * k, c = c0 + tx;
+        if (pp < HW && c < C) stf(xt + (n * HW + pp) * C + c, tile[tx][ty + 4 * k]);
+    }
+}
+
+constexpr int kClPix = 32;      // output pixels per block (4 per warp)
+constexpr int kClChannels = 128;  // channels per block: 4 per lane
+
+// Lane l of every warp takes channels cbase + 4l .. + 3 (one deformable group:
+// one sampling point per tap) of the block's pixels, one pixel at a time, its
+// taps in blocks of kDirectTaps with every offset, mask and corner load of a
+// block in flight at once; the 4 channels' sums stay in fp32 registers, then
+// go through a shared-memory tile so that the NCHW output is written along
+// pixels.
+template <typename T>
+__global__ void __launch_bounds__(256) direct_cl_kernel(const T* __restrict__ xt, const T* __restrict__ offset,
+                                                        const T* __restrict__ mask, const T* __restrict__ weight,
+                                                        const T* __restrict__ bias, T* __restrict__ out, const Plan pl) {
+    extern __shared__ float csm[];  // weights [K][128], then the output tile [128][kClPix + 1]
+    const int32_t K = pl.K, C = static_cast<int32_t>(pl.Cin);
+    float* wsm = csm;
+    float* osm = csm + K * kClChannels;
+    const int64_t n = blockIdx.z;
+    const int32_t cbase = static_cast<int32_t>(blockIdx.y) * kClChannels;
+    const int64_t p0 = static_cast<int64_t>(blockIdx.x) * kClPix;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int32_t i = threadIdx.x; i < K * kClChannels; i += 256) {
+        const int32_t k = i / kClChannels, c = cbase + (i - k * kClChannels);
+        wsm[i] = c < C ? ldf(weight + static_cast<int64_t>(c) * K + k) : 0.f;
+    }
+    __syncthreads();
+    const int32_t c = cbase + 4 * lane;
+    const bool cval = c < C;  // C is a multiple of 4: the lane's 4 channels all exist, or none
+    const int64_t gd = cval ? c / pl.Cd : 0;
+    const int64_t P = pl.P, H = pl.H, W = pl.W;
+    const int64_t zpix = pl.N * H * W;  // the all-zero pixel
+    const float Hf = static_cast<float>(H), Wf = static_cast<float>(W);
+    for (int j = warp; j < kClPix; j += 8) {
+        const int64_t p = p0 + j;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        if (p < P && cval) {
+            const int64_t ho = p / pl.Wo, wo = p - ho * pl.Wo;
+            const float hbase = static_cast<float>(ho * pl.sh - pl.ph), wbase = static_cast<float>(wo * pl.sw - pl.pw);
+            for (int32_t k0 = 0; k0 < K; k0 += kDirectTaps) {
+                const int32_t nk = min(kDirectTaps, K - k0);
+                float dh[kDirectTaps], dw[kDirectTaps], mv[kDirectTaps];
+#pragma unroll
+                for (int t = 0; t < kDirectTaps; ++t) {
+                    dh[t] = dw[t] = 0.f;
+                    mv[t] = t < nk ? 1.f : 0.f;  // an ordinary convolution (pl.plain) reads no offset or mask
+                    if (t < nk && !pl.plain) {
+                        const int64_t ob = ((n * pl.dg + gd) * 2 * K + 2 * (k0 + t)) * P + p;
+                        dh[t] = ldf(offset + ob);
+                        dw[t] = ldf(offset + ob + P);
+                        mv[t] = ldf(mask + ((n * pl.dg + gd) * K + k0 + t) * P + p);
+                    }
+                }
+                int64_t pix[kDirectTaps][4];
+                float wq[kDirectTaps][4];
+#pragma unroll
+                for (int t = 0; t < kDirectTaps; ++t) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        pix[t][q] = zpix;
+                        wq[t][q] = 0.f;
+                    }
+                    const int32_t k = k0 + t;
+                    const int32_t i = k / static_cast<int32_t>(pl.kw), jj = k - i * static_cast<int32_t>(pl.kw);
+                    const float hf = hbase + static_cast<float>(i * pl.dh) + dh[t];
+                    const float wf = wbase + static_cast<float>(jj * pl.dw) + dw[t];
+                    if (t < nk && hf > -1.0f && hf < Hf && wf > -1.0f && wf < Wf) {
+                        const float h0f = floorf(hf), w0f = floorf(wf);
+                        const float lh = hf - h0f, lw = wf - w0f, hh = 1.0f - lh, hw = 1.0f - lw;
+                        const int64_t y0 = static_cast<int64_t>(h0f), x0 = static_cast<int64_t>(w0f);
+                        const int64_t b = (n * H + y0) * W + x0;
+                        if (y0 >= 0 && x0 >= 0) pix[t][0] = b;
+                        if (y0 >= 0 && x0 + 1 < W) pix[t][1] = b + 1;
+                        if (y0 + 1 < H && x0 >= 0) pix[t][2] = b + W;
+                        if (y0 + 1 < H && x0 + 1 < W) pix[t][3] = b + W + 1;
+                        wq[t][0] = hh * hw * mv[t];
+                        wq[t][1] = hh * lw * mv[t];
+                        wq[t][2] = lh * hw * mv[t];
+                        wq[t][3] = lh * lw * mv[t];
+                    }
+                }
+                ClVec<T> X[kDirectTaps][4];
+#pragma unroll
+                for (int t = 0; t < kDirectTaps; ++t)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) X[t][q] = *reinterpret_cast<const ClVec<T>*>(xt + pix[t][q] * C + c);
+#pragma unroll
+                for (int t = 0; t < kDirectTaps; ++t) {
+                    if (t < nk) {
+                        const float* wk = wsm + (k0 + t) * kClChannels + 4 * lane;
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            float v = wq[t][0] * cl_elem(X[t][0], e);
+                            v = fmaf(wq[t][1], cl_elem(X[t][1], e), v);
+                            v = fmaf(wq[t][2], cl_elem(X[t][2], e), v);
+                            v = fmaf(wq[t][3], cl_elem(X[t][3], e), v);
+                            acc[e] = fmaf(wk[e], v, acc[e]);
+                        }
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) osm[(4 * lane + e) * (kClPix + 1) + j] = acc[e];
+    }
+    __syncthreads();
+    // the output along pixels: warp w writes channels w, w + 8, ... of the block's 32 pixels
+    const int64_t p = p0 + lane;
+    for (int cc = warp; cc < kClChannels; cc += 8) {
+        const int32_t co = cbase + cc;
+        if (co < C && p < P) {
+            const float b = bias ? ldf(bias + co) : 0.f;
+            stf(out + (n * C + co) * P + p, osm[cc * (kClPix + 1) + lane] + b);
+        }
+    }
+}
+
+// The same for 16-bit types, at most 9 taps, one deformable group per block of
+// 128 channels (so every lane of a warp samples the same points) and fewer
+// than 2^31 pixels of x (32-bit pixel indices): a pixel's
+// 3K offset and mask values are one load per lane (lane t the value t), shared
+// by shuffles, and the next pixel's are loaded while this one is gathered;
+// every corner load of all its taps (4K per lane) is in flight at once.
+template <typename T>
+__global__ void __launch_bounds__(256, 2) direct_cl9_kernel(const T* __restrict__ xt, const T* __restrict__ offset,
+                                                         const T* __restrict__ mask, const T* __restrict__ weight,
+                                                         const T* __restrict__ bias, T* __restrict__ out,
+                                                         const Plan pl) {
+    static_assert(sizeof(T) == 2, "16-bit types");
+    extern __shared__ float csm[];  // weights [K][128], then the output tile [128][kClPix + 1]
+    const int32_t K = pl.K, C = static_cast<int32_t>(pl.Cin);
+    float* wsm = csm;
+    float* osm = csm + K * kClChannels;
+    const int64_t n = blockIdx.z;
+    const int32_t cbase = static_cast<int32_t>(blockIdx.y) * kClChannels;
+    const int64_t p0 = static_cast<int64_t>(blockIdx.x) * kClPix;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int32_t i = threadIdx.x; i < K * kClChannels; i += 256) {
+        const int32_t k = i / kClChannels, c = cbase + (i - k * kClChannels);
+        wsm[i] = c < C ? ldf(weight + static_cast<int64_t>(c) * K + k) : 0.f;
+    }
+    __syncthreads();
+    const int32_t c = cbase + 4 * lane;
+    const bool cval = c < C;
+    const int64_t gd = cbase / pl.Cd;  // one deformable group for the whole block
+    const int64_t P = pl.P, H = pl.H, W = pl.W;
+    // pixel indices of the channels-last copy in 32 bits (its N*H*W + 1 pixels are below 2^31)
+    const int32_t zpix32 = static_cast<int32_t>(pl.N * H * W), H32 = static_cast<int32_t>(H),
+                  W32 = static_cast<int32_t>(W), img = static_cast<int32_t>(n * H);
+    const float Hf = static_cast<float>(H), Wf = static_cast<float>(W);
+    const int64_t obase = (n * pl.dg + gd) * 2 * K * P, mbase = (n * pl.dg + gd) * K * P;
+    // lane t's offset / mask value of pixel p (t < 2K: offset channel t, 2K <= t < 3K: mask of tap t - 2K)
+    auto om_load = [&](int64_t p) -> float {
+        if (p >= P || pl.plain) return 0.f;
+        if (lane < 2 * K) return ldf(offset + obase + lane * P + p);
+        if (lane < 3 * K) return ldf(mask + mbase + (lane - 2 * K) * P + p);
+        return 0.f;
+    };
+    float ov = om_load(p0 + warp);
+    for (int j = warp; j < kClPix; j += 8) {
+        const int64_t p = p0 + j;
+        const float ov_next = om_load(p + 8);  // in flight while this pixel is gathered
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        if (p < P) {  // warp-uniform
+            const int64_t ho = p / pl.Wo, wo = p - ho * pl.Wo;
+            const float hbase = static_cast<float>(ho * pl.sh - pl.ph), wbase = static_cast<float>(wo * pl.sw - pl.pw);
+            ClVec<T> X[9][4];
+            float lhv[9], lwv[9], mvv[9];  // the taps' cell fractions and mask (mask 0: outside)
+#pragma unroll
+            for (int t = 0; t < 9; ++t) {
+                const float dh = __shfl_sync(0xffffffffu, ov, 2 * t), dw = __shfl_sync(0xffffffffu, ov, 2 * t + 1);
+                const float mv = pl.plain ? 1.f : __shfl_sync(0xffffffffu, ov, (2 * K + t) & 31);
+                int32_t pix[4] = {zpix32, zpix32, zpix32, zpix32};
+                lhv[t] = lwv[t] = mvv[t] = 0.f;
+                const int32_t i = t / static_cast<int32_t>(pl.kw), jj = t - i * static_cast<int32_t>(pl.kw);
+                const float hf = hbase + static_cast<float>(i * pl.dh) + dh;
+                const float wf = wbase + static_cast<float>(jj * pl.dw) + dw;
+                if (t < K && hf > -1.0f && hf < Hf && wf > -1.0f && wf < Wf) {
+                    const float h0f = floorf(hf), w0f = floorf(wf);
+                    lhv[t] = hf - h0f;
+                    lwv[t] = wf - w0f;
+                    mvv[t] = mv;
+                    const int32_t y0 = static_cast<int32_t>(h0f), x0 = static_cast<int32_t>(w0f);
+                    const int32_t b = (img + y0) * W32 + x0;
+                    if (y0 >= 0 && x0 >= 0) pix[0] = b;
+                    if (y0 >= 0 && x0 + 1 < W32) pix[1] = b + 1;
+                    if (y0 + 1 < H32 && x0 >= 0) pix[2] = b + W32;
+                    if (y0 + 1 < H32 && x0 + 1 < W32) pix[3] = b + W32 + 1;
+                }
+                if (cval) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        X[t][q] = *reinterpret_cast<const ClVec<T>*>(xt + static_cast<int64_t>(pix[q]) * C + c);
+                }
+            }
+            if (cval) {
+#pragma unroll
+                for (int t = 0; t < 9; ++t) {
+                    if (t < K) {
+                        const float lh = lhv[t], lw = lwv[t], hh = 1.0f - lh, hw = 1.0f - lw;
+                        const float wq0 = hh * hw * mvv[t], wq1 = hh * lw * mvv[t], wq2 = lh * hw * mvv[t],
+                                    wq3 = lh * lw * mvv[t];
+                        const float* wk = wsm + t * kClChannels + 4 * lane;
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            float v = wq0 * cl_elem(X[t][0], e);
+                            v = fmaf(wq1, cl_elem(X[t][1], e), v);
+                            v = fmaf(wq2, cl_elem(X[t][2], e), v);
+                            v = fmaf(wq3, cl_elem(X[t][3], e), v);
+                            acc[e] = fmaf(wk[e], v, acc[e]);
+                        }
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) osm[(4 * lane + e) * (kClPix + 1) + j] = acc[e];
+        ov = ov_next;
+    }
+    __syncthreads();
+    const int64_t p = p0 + lane;
+    for (int cc = warp; cc < kClChannels; cc += 8) {
+        const int32_t co = cbase + cc;
+        if (co < C && p < P) {
+            const float b = bias ? ldf(bias + co) : 0.f;
+            stf(out + (n * C + co) * P + p, osm[cc * (kClPix + 1) + lane] + b);
+        }
+    }
+}
+
+template <typename T>
+cudaError_t launch_direct_cl_t(const Plan& pl, const void* x, const void* offset, const void* mask,
+                               const void* weight, const void* bias, void* out, void* ws, cudaStream_t st) {
+    uint32_t* status = static_cast<uint32_t*>(ws);
+    T* xt = reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + pl.off_xt);
+    const int64_t HW = pl.H * pl.W, NHW = pl.N * HW;
+    const int64_t tiles = ((HW + 63) / 64) * ((pl.Cin + 63) / 64);
+    nhwc_zero_pixel_kernel<T><<<dim3(static_cast<unsigned>(tiles), static_cast<unsigned>(pl.N)), 256, 0, st>>>(
+        static_cast<const T*>(x), xt, status, pl.Cin, HW, NHW);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const size_t smem = (static_cast<size_t>(pl.K) * kClChannels + kClChannels * (kClPix + 1)) * sizeof(float);
+    const dim3 grid(static_cast<unsigned>((pl.P + kClPix - 1) / kClPix),
+                    static_cast<unsigned>((pl.Cin + kClChannels - 1) / kClChannels), static_cast<unsigned>(pl.N));
+    // one deformable group per 128-channel block: the warp-shared sampling points
+    const bool shared_points = pl.dg == 1 || pl.Cd % kClChannels == 0;
+    if constexpr (sizeof(T) == 2) {
+        if (shared_points && pl.K <= 9 && pl.N * pl.H * pl.W < 2147483647ll) {
+            direct_cl9_kernel<T><<<grid, 256, smem, st>>>(xt, static_cast<const T*>(offset),
+                                                          static_cast<const T*>(mask), static_cast<const T*>(weight),
+                                                          static_cast<const T*>(bias), static_cast<T*>(out), pl);
+            return cudaGetLastError();
+        }
+    }
+    direct_cl_kernel<T><<<grid, 256, smem, st>>>(xt, static_cast<const T*>(offset), static_cast<const T*>(mask),
+                                                 static_cast<const T*>(weight), static_cast<const T*>(bias),
+                                                 static_cast<T*>(out), pl);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_direct(const Plan& pl, const void* x, const void* offset, const void* mask, const void* weight,
                           const void* bias, void* out, void* ws, cudaStream_t st) {
+    if (pl.direct_cl) {
+        if (pl.Cg != 1 || pl.Og != 1 || pl.Cin % 4 != 0 || pl.Cd % 4 != 0 || pl.K > kDirectClMaxTaps ||
+            pl.N > 65535 || pl.Cin > 65535ll * 128 || (pl.P + kClPix - 1) / kClPix > 2147483647ll)
+            return cudaErrorInvalidValue;
+        switch (pl.dtype) {
+            case kF32: return launch_direct_cl_t<float>(pl, x, offset, mask, weight, bias, out, ws, st);
+            case kF16: return launch_direct_cl_t<__half>(pl, x, offset, mask, weight, bias, out, ws, st);
+            default: return launch_direct_cl_t<__nv_bfloat16>(pl, x, offset, mask, weight, bias, out, ws, st);
+        }
+    }
     if (pl.Og > kDirectMaxOg || pl.P > 2147483647ll * kDirectThreads || pl.group > 65535 || pl.N > 65535 ||
         direct_groups_per_thread(pl.Og) * static_cast<int64_t>(pl.Og) * pl.Cg * pl.K * 4 > kDirectMaxSmem)
         return cudaErrorInvalidValue;

@@ -33,6 +33,9 @@ cudaError_t launch_fused(const Plan& pl, const void* offset, const void* mask, c
 // direct_groups_per_thread(Og) groups, whose fp32 weights (that many times
 // Og * Cg * K * 4 bytes) must fit kDirectMaxSmem.
 constexpr int kDirectMaxOg = 32;
+// The depthwise channels-last variant (Plan::direct_cl): its weights [K][128]
+// and output tile [128][33] in fp32 shared memory stay under 48 KB.
+constexpr int kDirectClMaxTaps = 49;
 constexpr int64_t kDirectMaxSmem = 96 * 1024;
 inline int direct_og_bucket(int64_t og) { return og <= 1 ? 1 : (og <= 4 ? 4 : (og <= 16 ? 16 : kDirectMaxOg)); }
 inline int direct_groups_per_thread(int64_t og) {

@@ -77,6 +77,8 @@ struct Plan {
     int32_t tmem_cols;
     int32_t direct;          // 1: the direct CUDA-core kernel (little contraction per output, e.g.
                              //    depthwise); none of the fused-path fields below is set
+    int32_t direct_cl;       // 1 (with direct): its depthwise form on a channels-last copy of x at
+                             //    off_xt, [N*H*W + 1][Cin] (the last pixel zero)
     int32_t a_tmem;          // 1: the A stages (modulated columns) live in tensor memory, written by the
                              //    gather with tcgen05.st and read by the MMA from there (16-bit types, 2
                              //    k-groups); 0: 128-byte-swizzled shared-memory stages

@@ -356,10 +356,52 @@ def test_sweep_fused_forced(oracle_mod, case):
             case.name + " fused")
 
 
+# Depthwise layers (one input and one output channel per group) whose
+# deformable groups hold whole 4-channel chunks: the automatic plan is the
+# direct kernel's channels-last form (a copy of x, then the kernel: two
+# launches); forced path=2 keeps the plain direct kernel on x in place.
+DIRECT_CL = [
+    Case("f16_dw_dg1", "f16", N=2, Cin=64, Cout=64, H=20, W=21, group=64, bias=True, seed=75,
+         offset_dist=("normal", 1.5)),
+    Case("bf16_dw_dg16_s2", "bf16", N=2, Cin=64, Cout=64, H=19, W=17, stride=(2, 2), group=64,
+         deformable_group=16, bias=False, seed=76, offset_dist=("normal", 2.0)),
+    Case("f32_dw_k5x3_far", "f32", N=1, Cin=8, Cout=8, H=13, W=15, kh=5, kw=3, padding=(2, 1), group=8,
+         deformable_group=2, bias=True, seed=77, offset_dist=("uniform", -6.0, 6.0), mask_dist="uniform"),
+    # 132 channels: a second block of channels with one lane group in it; 63 pixels per image
+    Case("f16_dw_c132_dil2", "f16", N=3, Cin=132, Cout=132, H=7, W=9, padding=(2, 2), dilation=(2, 2),
+         group=132, deformable_group=33, bias=True, seed=78, Ho=7, Wo=9),
+]
+
+
+@pytest.mark.parametrize("case", DIRECT_CL, ids=[c.name for c in DIRECT_CL])
+def test_direct_channels_last(oracle_mod, case):
+    """The depthwise channels-last form (automatic plan: two launches, x
+    copied channels-last into the workspace after the status header) and the
+    plain direct kernel (forced, one launch) both meet the tolerance on every
+    element, and give the same bits: the same fp32 sums in the same order."""
+    dev = torch.device("cuda", 0)
+    inp = make_inputs(case)
+    d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+    h = mdcn.Handle(**case.attrs())
+    plan = mdcn.mdcn_query_plan(h, d["x"], d["offset"], d["mask"], d["weight"], d["bias"])
+    assert plan["path"] == 2 and plan["launches"] == 2, plan
+    es = torch.empty((), dtype=d["x"].dtype).element_size()
+    need = mdcn.mdcn_workspace_size(h, d["x"], d["offset"], d["mask"], d["weight"], d["bias"])
+    assert need >= 1024 + (case.N * case.H * case.W + 1) * case.Cin * es
+    hp = mdcn.Handle(**case.attrs(), tuning=dict(path=2))
+    assert mdcn.mdcn_query_plan(hp, d["x"], d["offset"], d["mask"], d["weight"], d["bias"])["launches"] == 1
+    ref = oracle_out(oracle_mod, case, inp)
+    a = gpu_out(case, inp)
+    b = gpu_out(case, inp, tuning=dict(path=2))
+    compare(np64(a), ref, case.dtype, case.name + " channels-last")
+    compare(np64(b), ref, case.dtype, case.name + " direct")
+    assert torch.equal(a, b)
+
+
 def test_direct_neck_depthwise_vs_forced_direct():
     """A neck-sized depthwise layer (128 channels, one deformable group):
-    automatic (direct) and forced-direct plans give the same bits; the step-wise
-    calls refuse a direct plan and launch nothing."""
+    automatic (the channels-last form) and forced-direct plans give the same
+    bits; the step-wise calls refuse a direct plan and launch nothing."""
     case = dataclasses.replace(CONFIGS["neck_f16"], name="neck_dw", group=128, seed=74)
     inp = make_inputs(case)
     a = gpu_out(case, inp)
@@ -370,7 +412,10 @@ def test_direct_neck_depthwise_vs_forced_direct():
     h = mdcn.Handle(**case.attrs())
     ws = torch.empty(mdcn.mdcn_workspace_size(h, d["x"], d["offset"], d["mask"], d["weight"], None),
                      dtype=torch.uint8, device=dev)
-    assert ws.numel() == 1024  # the status word's header only
+    # the status header, then x channels-last with one zero pixel
+    assert ws.numel() == 1024 + (4 * 80 * 80 + 1) * 128 * 2
+    hp = mdcn.Handle(**case.attrs(), tuning=dict(path=2))
+    assert mdcn.mdcn_workspace_size(hp, d["x"], d["offset"], d["mask"], d["weight"], None) == 1024
     with pytest.raises(mdcn.MdcnError) as e:
         mdcn.mdcn_prepare_input(h, d["x"], d["offset"], d["mask"], d["weight"], None, ws, torch.cuda.current_stream())
     assert e.value.status == mdcn._abi.MDCN_ERR_UNSUPPORTED
