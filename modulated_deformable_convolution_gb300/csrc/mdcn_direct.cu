@@ -16,6 +16,10 @@
 // each input channel of the group, and accumulates weight x sample into the
 // group's output channels (fp32 registers; the sample is not rounded to the
 // I/O type). The group's weights are staged in shared memory as fp32.
+//
+// Depthwise layers (one input and one output channel per group) take a
+// channels-last form of the same sums, below: x copied to [N*H*W + 1][Cin]
+// first, then 4 channels of a pixel per lane.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
