@@ -267,6 +267,32 @@ __global__ void __launch_bounds__(256) nhwc_zero_pixel_kernel(const T* __restric
 constexpr int kClPix = 32;      // output pixels per block (4 per warp)
 constexpr int kClChannels = 128;  // channels per block: 4 per lane
 
+// The block's weights, wsm[k][cc] = weight[cbase + cc][k] in fp32 (0 past Cin).
+template <typename T>
+__device__ __forceinline__ void cl_stage_weights(const T* __restrict__ weight, float* wsm, int32_t K, int32_t C,
+                                                 int32_t cbase) {
+    for (int32_t i = threadIdx.x; i < K * kClChannels; i += 256) {
+        const int32_t k = i / kClChannels, c = cbase + (i - k * kClChannels);
+        wsm[i] = c < C ? ldf(weight + static_cast<int64_t>(c) * K + k) : 0.f;
+    }
+}
+
+// The block's output tile osm[cc][j] (+ bias) to NCHW, along pixels: warp w
+// writes channels w, w + 8, ... of the block's kClPix pixels.
+template <typename T>
+__device__ __forceinline__ void cl_store_tile(const float* osm, const T* __restrict__ bias, T* __restrict__ out,
+                                              int64_t n, int32_t C, int32_t cbase, int64_t p0, int64_t P) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t p = p0 + lane;
+    for (int cc = warp; cc < kClChannels; cc += 8) {
+        const int32_t co = cbase + cc;
+        if (co < C && p < P) {
+            const float b = bias ? ldf(bias + co) : 0.f;
+            stf(out + (n * C + co) * P + p, osm[cc * (kClPix + 1) + lane] + b);
+        }
+    }
+}
+
 // Lane l of every warp takes channels cbase + 4l .. + 3 (one deformable group:
 // one sampling point per tap) of the block's pixels, one pixel at a time, its
 // taps in blocks of kDirectTaps with every offset, mask and corner load of a
@@ -285,10 +311,7 @@ __global__ void __launch_bounds__(256) direct_cl_kernel(const T* __restrict__ xt
     const int32_t cbase = static_cast<int32_t>(blockIdx.y) * kClChannels;
     const int64_t p0 = static_cast<int64_t>(blockIdx.x) * kClPix;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int32_t i = threadIdx.x; i < K * kClChannels; i += 256) {
-        const int32_t k = i / kClChannels, c = cbase + (i - k * kClChannels);
-        wsm[i] = c < C ? ldf(weight + static_cast<int64_t>(c) * K + k) : 0.f;
-    }
+    cl_stage_weights(weight, wsm, K, C, cbase);
     __syncthreads();
     const int32_t c = cbase + 4 * lane;
     const bool cval = c < C;  // C is a multiple of 4: the lane's 4 channels all exist, or none
@@ -369,15 +392,7 @@ __global__ void __launch_bounds__(256) direct_cl_kernel(const T* __restrict__ xt
         for (int e = 0; e < 4; ++e) osm[(4 * lane + e) * (kClPix + 1) + j] = acc[e];
     }
     __syncthreads();
-    // the output along pixels: warp w writes channels w, w + 8, ... of the block's 32 pixels
-    const int64_t p = p0 + lane;
-    for (int cc = warp; cc < kClChannels; cc += 8) {
-        const int32_t co = cbase + cc;
-        if (co < C && p < P) {
-            const float b = bias ? ldf(bias + co) : 0.f;
-            stf(out + (n * C + co) * P + p, osm[cc * (kClPix + 1) + lane] + b);
-        }
-    }
+    cl_store_tile(osm, bias, out, n, C, cbase, p0, P);
 }
 
 // The same for 16-bit types, at most 9 taps, one deformable group per block of
@@ -400,10 +415,7 @@ __global__ void __launch_bounds__(256, 2) direct_cl9_kernel(const T* __restrict_
     const int32_t cbase = static_cast<int32_t>(blockIdx.y) * kClChannels;
     const int64_t p0 = static_cast<int64_t>(blockIdx.x) * kClPix;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int32_t i = threadIdx.x; i < K * kClChannels; i += 256) {
-        const int32_t k = i / kClChannels, c = cbase + (i - k * kClChannels);
-        wsm[i] = c < C ? ldf(weight + static_cast<int64_t>(c) * K + k) : 0.f;
-    }
+    cl_stage_weights(weight, wsm, K, C, cbase);
     __syncthreads();
     const int32_t c = cbase + 4 * lane;
     const bool cval = c < C;
@@ -483,14 +495,7 @@ __global__ void __launch_bounds__(256, 2) direct_cl9_kernel(const T* __restrict_
         ov = ov_next;
     }
     __syncthreads();
-    const int64_t p = p0 + lane;
-    for (int cc = warp; cc < kClChannels; cc += 8) {
-        const int32_t co = cbase + cc;
-        if (co < C && p < P) {
-            const float b = bias ? ldf(bias + co) : 0.f;
-            stf(out + (n * C + co) * P + p, osm[cc * (kClPix + 1) + lane] + b);
-        }
-    }
+    cl_store_tile(osm, bias, out, n, C, cbase, p0, P);
 }
 
 template <typename T>
