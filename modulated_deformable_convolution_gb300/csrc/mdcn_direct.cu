@@ -397,7 +397,7 @@ __global__ void __launch_bounds__(256) direct_cl_kernel(const T* __restrict__ xt
 
 // The same for 16-bit types, at most 9 taps, one deformable group per block of
 // 128 channels (so every lane of a warp samples the same points) and fewer
-// than 2^31 pixels of x (32-bit pixel indices): a pixel's
+// than 2^31 elements in the channels-last copy (32-bit offsets): a pixel's
 // 3K offset and mask values are one load per lane (lane t the value t), shared
 // by shuffles, and the next pixel's are loaded while this one is gathered;
 // every corner load of all its taps (4K per lane) is in flight at once.
@@ -407,15 +407,22 @@ __global__ void __launch_bounds__(256, 2) direct_cl9_kernel(const T* __restrict_
                                                          const T* __restrict__ bias, T* __restrict__ out,
                                                          const Plan pl) {
     static_assert(sizeof(T) == 2, "16-bit types");
-    extern __shared__ float csm[];  // weights [K][128], then the output tile [128][kClPix + 1]
+    // weights [K][128], the output tile [128][kClPix + 1], then the taps' displacements (h, then w)
+    extern __shared__ float csm[];
     const int32_t K = pl.K, C = static_cast<int32_t>(pl.Cin);
     float* wsm = csm;
     float* osm = csm + K * kClChannels;
+    float* tsm = osm + kClChannels * (kClPix + 1);
     const int64_t n = blockIdx.z;
     const int32_t cbase = static_cast<int32_t>(blockIdx.y) * kClChannels;
     const int64_t p0 = static_cast<int64_t>(blockIdx.x) * kClPix;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     cl_stage_weights(weight, wsm, K, C, cbase);
+    if (threadIdx.x < K) {  // tap t = i * kw + j: displacement (i * dh, j * dw), once per block
+        const int32_t t = threadIdx.x, i = t / static_cast<int32_t>(pl.kw), jj = t - i * static_cast<int32_t>(pl.kw);
+        tsm[t] = static_cast<float>(i * pl.dh);
+        tsm[kDirectClMaxTaps + t] = static_cast<float>(jj * pl.dw);
+    }
     __syncthreads();
     const int32_t c = cbase + 4 * lane;
     const bool cval = c < C;
@@ -439,7 +446,9 @@ __global__ void __launch_bounds__(256, 2) direct_cl9_kernel(const T* __restrict_
         const float ov_next = om_load(p + 8);  // in flight while this pixel is gathered
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         if (p < P) {  // warp-uniform
-            const int64_t ho = p / pl.Wo, wo = p - ho * pl.Wo;
+            // 32-bit position arithmetic: pixels below 2^31, coordinates below 2^24
+            const int32_t p32 = static_cast<int32_t>(p), Wo32 = static_cast<int32_t>(pl.Wo);
+            const int32_t ho = p32 / Wo32, wo = p32 - ho * Wo32;
             const float hbase = static_cast<float>(ho * pl.sh - pl.ph), wbase = static_cast<float>(wo * pl.sw - pl.pw);
             ClVec<T> X[9][4];
             float lhv[9], lwv[9], mvv[9];  // the taps' cell fractions and mask (mask 0: outside)
@@ -449,9 +458,8 @@ __global__ void __launch_bounds__(256, 2) direct_cl9_kernel(const T* __restrict_
                 const float mv = pl.plain ? 1.f : __shfl_sync(0xffffffffu, ov, (2 * K + t) & 31);
                 int32_t pix[4] = {zpix32, zpix32, zpix32, zpix32};
                 lhv[t] = lwv[t] = mvv[t] = 0.f;
-                const int32_t i = t / static_cast<int32_t>(pl.kw), jj = t - i * static_cast<int32_t>(pl.kw);
-                const float hf = hbase + static_cast<float>(i * pl.dh) + dh;
-                const float wf = wbase + static_cast<float>(jj * pl.dw) + dw;
+                const float hf = hbase + tsm[t] + dh;
+                const float wf = wbase + tsm[kDirectClMaxTaps + t] + dw;
                 if (t < K && hf > -1.0f && hf < Hf && wf > -1.0f && wf < Wf) {
                     const float h0f = floorf(hf), w0f = floorf(wf);
                     lhv[t] = hf - h0f;
@@ -464,10 +472,9 @@ __global__ void __launch_bounds__(256, 2) direct_cl9_kernel(const T* __restrict_
                     if (y0 + 1 < H32 && x0 >= 0) pix[2] = b + W32;
                     if (y0 + 1 < H32 && x0 + 1 < W32) pix[3] = b + W32 + 1;
                 }
-                if (cval) {
+                if (cval) {  // element offsets in 32 bits: (N*H*W + 1) * Cin below 2^31
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        X[t][q] = *reinterpret_cast<const ClVec<T>*>(xt + static_cast<int64_t>(pix[q]) * C + c);
+                    for (int q = 0; q < 4; ++q) X[t][q] = *reinterpret_cast<const ClVec<T>*>(xt + (pix[q] * C + c));
                 }
             }
             if (cval) {
@@ -477,7 +484,8 @@ __global__ void __launch_bounds__(256, 2) direct_cl9_kernel(const T* __restrict_
                         const float lh = lhv[t], lw = lwv[t], hh = 1.0f - lh, hw = 1.0f - lw;
                         const float wq0 = hh * hw * mvv[t], wq1 = hh * lw * mvv[t], wq2 = lh * hw * mvv[t],
                                     wq3 = lh * lw * mvv[t];
-                        const float* wk = wsm + t * kClChannels + 4 * lane;
+                        const float4 w4 = *reinterpret_cast<const float4*>(wsm + t * kClChannels + 4 * lane);
+                        const float wk[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             float v = wq0 * cl_elem(X[t][0], e);
@@ -515,8 +523,9 @@ cudaError_t launch_direct_cl_t(const Plan& pl, const void* x, const void* offset
     // one deformable group per 128-channel block: the warp-shared sampling points
     const bool shared_points = pl.dg == 1 || pl.Cd % kClChannels == 0;
     if constexpr (sizeof(T) == 2) {
-        if (shared_points && pl.K <= 9 && pl.N * pl.H * pl.W < 2147483647ll) {
-            direct_cl9_kernel<T><<<grid, 256, smem, st>>>(xt, static_cast<const T*>(offset),
+        if (shared_points && pl.K <= 9 && (pl.N * pl.H * pl.W + 1) * pl.Cin < 2147483647ll) {
+            const size_t smem9 = smem + 2 * kDirectClMaxTaps * sizeof(float);
+            direct_cl9_kernel<T><<<grid, 256, smem9, st>>>(xt, static_cast<const T*>(offset),
                                                           static_cast<const T*>(mask), static_cast<const T*>(weight),
                                                           static_cast<const T*>(bias), static_cast<T*>(out), pl);
             return cudaGetLastError();
