@@ -49,6 +49,9 @@ CASES = [
              dilation=(2, 2), group=2, dg=2, seed=3),
     PackCase("f16_1x5_odd", torch.float16, 1, 16, 24, 9, 13, k=(1, 5), padding=(0, 2), dg=2, bias=False, seed=4),
     PackCase("f16_neck_shape", torch.float16, 4, 128, 128, 80, 80, seed=5),
+    # depthwise deformable convolutions: the direct kernel's channels-last form after the front end
+    PackCase("f16_depthwise", torch.float16, 2, 64, 64, 20, 20, group=64, seed=6),
+    PackCase("bf16_depthwise_dg16", torch.bfloat16, 1, 64, 64, 15, 17, group=64, dg=16, seed=7),
 ]
 
 
