@@ -67,7 +67,7 @@ def _call_noalloc(f, h, d, out):
              ctypes.byref(dims), dt, stream)
 
 
-@pytest.mark.parametrize("name", ["neck_f16", "tiny_f32", "multidg_bf16", "largec_f16"])
+@pytest.mark.parametrize("name", ["neck_f16", "tiny_f32", "multidg_bf16", "largec_f16", "depthwise_f16"])
 def test_noalloc_matches_forward_on_two_calls(name):
     f = _noalloc_fn()
     case, d = _inputs(name)
