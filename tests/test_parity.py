@@ -367,6 +367,9 @@ DIRECT_CL = [
          deformable_group=16, bias=False, seed=76, offset_dist=("normal", 2.0)),
     Case("f32_dw_k5x3_far", "f32", N=1, Cin=8, Cout=8, H=13, W=15, kh=5, kw=3, padding=(2, 1), group=8,
          deformable_group=2, bias=True, seed=77, offset_dist=("uniform", -6.0, 6.0), mask_dist="uniform"),
+    # bfloat16 with one deformable group (the shared-points kernel), 96 channels: lanes 24-31 idle
+    Case("bf16_dw_dg1_c96", "bf16", N=2, Cin=96, Cout=96, H=14, W=18, group=96, bias=True, seed=79,
+         offset_dist=("normal", 2.0)),
     # 132 channels: a second block of channels with one lane group in it; 63 pixels per image
     Case("f16_dw_c132_dil2", "f16", N=3, Cin=132, Cout=132, H=7, W=9, padding=(2, 2), dilation=(2, 2),
          group=132, deformable_group=33, bias=True, seed=78, Ho=7, Wo=9),
